@@ -1,0 +1,425 @@
+"""Benchmark of the fused ZeRO step on one GB300 (N simulated ranks in one HBM).
+
+    python bench.py [--gpus G] [--steps K] [--warmup W] [--workload NAME]
+                    [--impl ours|reference] [--no-cpu-baseline]
+
+A step is one fused ZeRO step (reduce-scatter-mean + AdamW + all-gather) over
+the whole parameter vector of the workload, with the inputs resident in HBM.
+Prints ONE JSON line (rank 0). Under torchrun with G > 1 every rank runs an
+independent replica of the workload on its own GPU (weak scaling, no
+collective on the data path); the timed region is bracketed by barriers and
+the slowest rank's time is reported.
+
+--impl reference times the CPU oracle (fp32-mirror numpy, as it stands) on a
+bounded sample of the same workload on the host cores.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+from zero_sharded_optimizer_gb300 import inputs  # noqa: E402
+
+METRIC = "ZeRO step params/s at N ranks on 1 GB300; achieved HBM GB/s vs peak"
+UNIT = "params/s"
+DEFAULT_WORKLOAD = "fp32_25m"
+KERNEL_SRC = os.path.join(ROOT, "zero_sharded_optimizer_gb300", "csrc", "zero_kernels.cu")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+L2_BYTES = 129 * 10 ** 6
+
+
+def bytes_per_param(wl) -> int:
+    """Algorithmic HBM bytes per parameter of one fused step (the mean
+    gradient is never stored): fp32 reads N grads + p + m + v and writes m, v
+    and N replicas: 8N+20; mixed reads N bf16 grads + master, m, v and writes
+    master, m, v and N bf16 replicas: 4N+24."""
+    if wl.precision == inputs.BF16_MIXED:
+        return 4 * wl.N + 24
+    return 8 * wl.N + 20
+
+
+def default_steps(wl) -> int:
+    # about two seconds of timed work, so the clock sampler sees the load
+    per_step_s = wl.n * bytes_per_param(wl) / 6.0e12
+    return int(min(20000, max(20, round(2.0 / max(per_step_s, 1e-6)))))
+
+
+def load_peaks() -> tuple[float, str]:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def kernel_source_hash() -> str:
+    with open(KERNEL_SRC, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def traffic_per_launch(workload: str):
+    """DRAM bytes per launch from the committed ncu summary, or None when absent
+    or taken on a different kernel source."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            entry = json.load(f).get(workload)
+    except Exception:
+        return None
+    if not entry or entry.get("kernel_source_sha256_16") != kernel_source_hash():
+        return None
+    return entry.get("dram_bytes_per_launch")
+
+
+def config_of(wl, extra=None) -> dict:
+    step_bytes = wl.n * bytes_per_param(wl)
+    cfg = {
+        "workload": wl.name,
+        "n_params": wl.n,
+        "ranks_simulated": wl.N,
+        "state": "bf16 params/grads + fp32 master/m/v" if wl.precision else "fp32 params/grads/m/v",
+        "optimizer": f"AdamW lr={wl.lr} betas=({wl.beta1},{wl.beta2}) eps={wl.eps} "
+                     f"wd={wl.weight_decay}",
+        "shards": "np.array_split",
+        "bytes_per_step": step_bytes,
+        "l2": f"inputs larger than L2 ({step_bytes / 1e9:.2f} GB touched per step vs 129 MB L2)"
+              if step_bytes > L2_BYTES else "L2-resident",
+    }
+    if wl.bucket_bytes:
+        cfg["bucket_bytes"] = wl.bucket_bytes
+    if extra:
+        cfg.update(extra)
+    return cfg
+
+
+def max_over_ranks(values, device, world: int):
+    """Element-wise maximum of `values` over all ranks (the slowest rank decides)."""
+    if world <= 1:
+        return [float(x) for x in values]
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x) for x in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.tolist()]
+
+
+def whole_job_rate(units_per_rank: int, world: int, ms_per_step: float) -> float:
+    """Units processed by all ranks per second, over the slowest rank's time."""
+    return world * units_per_rank / (ms_per_step / 1e3)
+
+
+# ------------------------------------------------------------------- clocks --
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.path = None
+        try:
+            import torch
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            target = ["-i", uuid if uuid.startswith("GPU-") else f"GPU-{uuid}"]
+        except Exception:
+            target = []
+        fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", *target], stdout=self.out, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"],
+                    "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.out.close()
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                    power.append(float(parts[3]))
+                except ValueError:
+                    continue
+                for name, val in zip(names, parts[5:9]):
+                    if val.lower() == "active":
+                        reasons.add(name)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------ cpu baseline --
+
+def oracle_sample_rate(wl, seconds: float, sample_n: int | None = None, steps: int | None = None):
+    """Time the fp32-mirror oracle's ZeRO step on a sample of the workload.
+
+    The sample is `sample_n` consecutive parameters with all N ranks (the step
+    is elementwise, so any slice is a faithful sub-problem). Returns
+    (params per second, steps run, sample size, seconds)."""
+    import oracle
+    rng = np.random.default_rng(0)
+    k = sample_n or min(wl.n, 1 << 20)
+    mixed = wl.precision == inputs.BF16_MIXED
+    init = rng.normal(0, 0.02 if wl.param_init == "normal" else 0.5, k).astype(np.float32)
+    reps = [oracle.f32_to_bf16_rne(init) if mixed else init.copy() for _ in range(wl.N)]
+    grads = [rng.normal(0, wl.grad_std, k).astype(np.float32) for _ in range(wl.N)]
+    if mixed:
+        grads = [oracle.f32_to_bf16_rne(g) for g in grads]
+    states = oracle.init_states(k, wl.N, wl.precision, master_init=init, mode="fp32")
+    hp = dict(lr=wl.lr, beta1=wl.beta1, beta2=wl.beta2, eps=wl.eps, weight_decay=wl.weight_decay,
+              precision=wl.precision, mode="fp32")
+    t0 = time.perf_counter()
+    t = 0
+    while True:
+        t += 1
+        reps, states = oracle.zero_step(reps, grads, states, t, **hp)
+        el = time.perf_counter() - t0
+        if (steps is not None and t >= steps) or (steps is None and el >= seconds):
+            break
+    return k * t / el, t, k, el
+
+
+def cpu_baseline(wl, seconds: float = 12.0) -> dict:
+    rate, steps, k, el = oracle_sample_rate(wl, seconds)
+    return {"value": rate, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{steps} oracle steps (fp32-mirror numpy, one thread) on {k:,} consecutive "
+                      f"parameters x {wl.N} ranks of {wl.name}; {el:.1f} s"}
+
+
+# --------------------------------------------------------------- GPU arm --
+
+def run_gpu(args, wl, rank: int, world: int, local_rank: int) -> dict | None:
+    import torch
+    import torch.distributed as dist
+
+    from zero_sharded_optimizer_gb300 import abi
+    from zero_sharded_optimizer_gb300.optimizer import ZeroOptimizer
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    K, W = args.steps, args.warmup
+    n, N = wl.n, wl.N
+    mixed = wl.precision == inputs.BF16_MIXED
+    init = inputs.init_params_fp32(n, wl, seed=rank, device=dev)
+    reps = inputs.make_replicas(init, N, wl.precision)
+    grads = inputs.make_grads(n, N, wl.precision, device=dev)
+    inputs.fill_grads(grads, wl, step=1, seed=rank)
+    opt = ZeroOptimizer(n, N, wl.precision, lr=wl.lr, betas=(wl.beta1, wl.beta2), eps=wl.eps,
+                        weight_decay=wl.weight_decay, master_init=init if mixed else None)
+    del init
+    bucketed = wl.bucket_bytes > 0
+    launches_per_step = len(opt.bucket_ranges(wl.bucket_bytes)) if bucketed else 1
+    stream = torch.cuda.current_stream()
+
+    def one_step():
+        if bucketed:
+            opt.step_bucketed(reps, grads, None, stream, wl.bucket_bytes)
+        else:
+            opt.step(reps, grads)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(W):
+        one_step()
+    barrier()
+
+    sampler = ClockSampler(local_rank) if rank == 0 else None
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    t_begin = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    barrier()
+    t_begin.record(stream)
+    for k in range(K):
+        starts[k].record(stream)
+        one_step()
+        ends[k].record(stream)
+    t_end.record(stream)
+    barrier()
+    clocks = sampler.stop() if sampler else None
+    ms_total = t_begin.elapsed_time(t_end)
+    kernel_ms = sum(s.elapsed_time(e) for s, e in zip(starts, ends)) / K
+    ms_step = ms_total / K
+
+    ms_step, kernel_ms = max_over_ranks([ms_step, kernel_ms], dev, world)
+
+    # ---- end to end through the public API: host gradients in, parameters out
+    K_e = max(3, min(K, 30))
+    host_grads = [g.cpu().pin_memory() for g in grads]
+    host_out = torch.empty(n, dtype=reps[0].dtype).pin_memory()
+    for _ in range(2):
+        opt.step(reps, host_grads)
+        host_out.copy_(reps[0], non_blocking=True)
+    barrier()
+    e_begin = torch.cuda.Event(enable_timing=True)
+    e_end = torch.cuda.Event(enable_timing=True)
+    e_begin.record(stream)
+    for _ in range(K_e):
+        opt.step(reps, host_grads)
+        host_out.copy_(reps[0], non_blocking=True)
+    e_end.record(stream)
+    barrier()
+    e_ms = max_over_ranks([e_begin.elapsed_time(e_end) / K_e], dev, world)[0]
+    es = 2 if mixed else 4
+    e2e = {"value": whole_job_rate(n, world, e_ms), "unit": UNIT,
+           "h2d_bytes_per_step": N * n * es, "d2h_bytes_per_step": n * es,
+           "ms_per_step": e_ms, "steps": K_e,
+           "path": "ZeroOptimizer.step with pinned host gradients (H2D into device staging on "
+                   "the step's stream), then D2H of one updated replica"}
+
+    if rank != 0:
+        return None
+    peak, peak_kind = load_peaks()
+    step_bytes = n * bytes_per_param(wl)
+    achieved = step_bytes / (kernel_ms / 1e3) / 1e9
+    traffic = traffic_per_launch(wl.name)
+    if traffic is not None and bucketed:
+        traffic = None
+    line = {
+        "metric": METRIC,
+        "value": whole_job_rate(n, world, ms_step),
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": K,
+        "warmup": W,
+        "ms_per_step": ms_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic (seeded device draws; inputs resident in HBM)",
+        "config": config_of(wl, {"parallelism": f"{N} simulated ranks per GPU; "
+                                                f"{world} independent GPU replica(s)"}),
+        "hbm_gbs": step_bytes / (ms_step / 1e3) / 1e9,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs, copy "
+                                    f"bandwidth)" if peak_kind == "measured" else "fallback",
+                     "algorithmic_bytes_per_launch": step_bytes // launches_per_step,
+                     "kernel": "zero_step_kernel",
+                     "kernel_ms": kernel_ms / launches_per_step},
+        "gpu_launches": K * launches_per_step,
+        "clocks": clocks,
+        "e2e": e2e,
+    }
+    if args.cpu_baseline and world == 1:
+        line["cpu_baseline"] = cpu_baseline(wl)
+    return line
+
+
+# ---------------------------------------------------------- reference arm --
+
+def run_reference(args, wl, world: int) -> dict:
+    K, W = args.steps, args.warmup
+    # calibrate, then size each step's sample so the whole run stays near a minute
+    rate, _, _, _ = oracle_sample_rate(wl, 0.0, sample_n=min(wl.n, 1 << 18), steps=3)
+    budget_s = 60.0
+    k = int(min(wl.n, max(4096, rate * budget_s / max(K + W, 1))))
+    if W:
+        oracle_sample_rate(wl, 0.0, sample_n=k, steps=W)
+    rate, steps, k, el = oracle_sample_rate(wl, 0.0, sample_n=k, steps=K)
+    ms = el / steps * 1e3
+    sample = (f"each step: the fp32-mirror oracle (numpy, one thread) on {k:,} consecutive "
+              f"parameters x {wl.N} ranks of {wl.name}")
+    return {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": rate,
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": K,
+        "warmup": W,
+        "ms_per_step": ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic (seeded numpy draws)",
+        "config": config_of(wl, {"parallelism": f"{wl.N} simulated ranks; host cores"}),
+        "cpu_baseline": {"value": rate, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": rate, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+# -------------------------------------------------------------------- main --
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawTextHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(inputs.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    args = ap.parse_args(argv)
+    wl = inputs.WORKLOADS[args.workload]
+    if args.steps is None:
+        args.steps = default_steps(wl)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if world != args.gpus:
+        print(f"warning: --gpus {args.gpus} but WORLD_SIZE={world}; using {world}",
+              file=sys.stderr)
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args, wl, world)), flush=True)
+        return 0
+
+    import torch
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    try:
+        line = run_gpu(args, wl, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+    if line is not None:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

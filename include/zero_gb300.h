@@ -1,0 +1,217 @@
+/*
+ * zero_gb300.h -- C ABI of libzero_gb300.so: one ZeRO step over N simulated
+ * data-parallel ranks whose buffers all live in the memory of one GPU.
+ *
+ * The step (the "ZeRO-Sharded Adam Step" problem page, section "The step"):
+ *   1. reduce-scatter: rank i receives the mean over the N ranks' local
+ *      gradients, for the indices of its shard only;
+ *   2. rank i runs Adam/AdamW on its shard with its own m and v (and its fp32
+ *      master weights in mixed precision);
+ *   3. all-gather: every rank's parameter replica receives all updated shards.
+ * Shard i is np.array_split(np.arange(n), N)[i] (same page, "The shards").
+ * The three steps run fused in one pass over memory; the mean gradient is
+ * never stored.
+ *
+ * Conventions for every call:
+ *  - Return value: ZERO_OK (0) or a negative ZERO_E* code. zero_strerror()
+ *    names a code; zero_last_error() gives the calling thread's last message.
+ *  - Sizes are int64_t element counts; byte counts are uint64_t.
+ *  - `params`, `grads`: HOST arrays of N DEVICE pointers, each to n elements
+ *    (float for ZERO_FP32, bf16 bit patterns (uint16) for ZERO_BF16_MIXED),
+ *    at least naturally aligned. Buffers sharing one 16-byte phase (the usual
+ *    case: separate allocations) take the 16-byte vector path; any other
+ *    layout is still correct, on a slower 4-/2-byte path.
+ *  - The caller owns every device buffer. The library never allocates device
+ *    memory; zero_init_states allocates only a small host handle.
+ *  - Device work is queued on the caller's stream (zero_stream_t is a
+ *    cudaStream_t; NULL is the legacy default stream) and runs
+ *    asynchronously; argument errors are reported before anything is queued.
+ *  - Calls on distinct state handles may come from different host threads.
+ */
+#ifndef ZERO_GB300_H
+#define ZERO_GB300_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *zero_stream_t; /* same type as cudaStream_t */
+typedef struct CUevent_st *zero_event_t;   /* same type as cudaEvent_t */
+
+/* Storage precision of the training state. */
+enum {
+  ZERO_FP32 = 0,       /* fp32 params and grads, fp32 m, v: 4+4+8 bytes/param */
+  ZERO_BF16_MIXED = 1, /* bf16 params and grads, fp32 master, m, v: 2+2+12    */
+  ZERO_FP64_EMU = 2    /* float64 course-emulation bookkeeping (memory only)  */
+};
+
+/* Status codes. */
+enum {
+  ZERO_OK = 0,
+  ZERO_EINVAL = -1,    /* bad n, N, stage, precision, t, hyperparameter, range or NULL */
+  ZERO_EALIGN = -2,    /* a pointer is not aligned to its element size */
+  ZERO_ECUDA = -3,     /* a CUDA runtime call or kernel launch failed */
+  ZERO_ETIMEDOUT = -4, /* zero_step_bucketed: work not finished by the deadline */
+  ZERO_ENOMEM = -5     /* host allocation of a state handle failed */
+};
+
+#define ZERO_MAX_RANKS 64
+
+typedef struct zero_states zero_states_t;
+
+/* ---------------------------------------------------------------- shards -- */
+
+/* Shard offsets a_0..a_N of [0, n) over N ranks, written to the host array
+ * bounds[N+1]: a_i = i*q + min(i, r) with q = n / N, r = n % N, i.e. the
+ * pieces of np.array_split(np.arange(n), N) ("ZeRO-Sharded Adam Step",
+ * "The shards"). n < N is legal and gives empty shards.
+ * Errors: EINVAL if n < 0, N < 1, or bounds is NULL. */
+int zero_shard_bounds(int64_t n, int32_t N, int64_t *bounds);
+
+/* ----------------------------------------------------------------- state -- */
+
+/* Build the optimizer state of all N ranks ("ZeRO-Sharded Adam Step", "What to
+ * implement": init_states gives every worker zero m and v of its shard's
+ * size). State is stored flat in global index order: rank i's m, v (and
+ * master) are elements [a_i, a_{i+1}) of the caller's n-element device
+ * buffers m, v, master, so a shard is a pure index range.
+ *   m, v        : device float[n], zeroed here (queued on `stream`).
+ *   master      : ZERO_BF16_MIXED only: device float[n], set to master_init;
+ *                 must be NULL for ZERO_FP32.
+ *   master_init : ZERO_BF16_MIXED only: device float[n], the fp32 initial
+ *                 weights (the replicas are expected to hold their bf16
+ *                 round-to-nearest-even); NULL for ZERO_FP32.
+ *   out         : receives a host handle; release it with zero_free_states.
+ * The handle records the buffers; they must outlive it.
+ * Errors: EINVAL (n < 0, N outside [1, ZERO_MAX_RANKS], precision not FP32 or
+ * BF16_MIXED, NULL or extra pointer), EALIGN, ECUDA, ENOMEM. */
+int zero_init_states(int64_t n, int32_t N, int32_t precision, float *m, float *v,
+                     float *master, const float *master_init, zero_stream_t stream,
+                     zero_states_t **out);
+
+/* Release a handle (the caller's device buffers are untouched). NULL is a no-op. */
+int zero_free_states(zero_states_t *st);
+
+/* n, N and precision of a handle (any output pointer may be NULL). */
+int zero_states_info(const zero_states_t *st, int64_t *n, int32_t *N, int32_t *precision);
+
+/* Rank `rank`'s shard [lo, hi) and its views into m, v, master (master is NULL
+ * in fp32). Errors: EINVAL for a NULL handle or a rank outside [0, N). */
+int zero_state_view(const zero_states_t *st, int32_t rank, int64_t *lo, int64_t *hi,
+                    float **m, float **v, float **master);
+
+/* ------------------------------------------------------------------ step -- */
+
+/* One ZeRO step at step number t (1-based) over all n parameters.
+ * For every index j, with a the owner rank of j:
+ *   g   = (((g_0[j] + g_1[j]) + ...) + g_{N-1}[j]) / N      fp32, rank order
+ *   p   = params[a][j] (fp32) or master[j] (mixed)
+ *   p   = p * fl(1 - lr*wd)                                  decoupled decay
+ *   m   = fl(b1)*m + fl(1-b1)*g;   v = fl(b2)*v + fl(1-b2)*(g*g)
+ *   p   = p - fl(lr/(1-b1^t)) * (m / (sqrt(v)/fl(sqrt(1-b2^t)) + fl(eps)))
+ *   params[r][j] = p for every r (mixed: master[j] = p, params[r][j] = bf16 RNE(p))
+ * Every operation is one IEEE fp32 operation (no contraction); fl(.) is a
+ * constant formed in double on the host and rounded to float once. wd = 0 is
+ * plain Adam. The Adam formula is not printed on the pages; this is the
+ * reading of "Data parallelism and ZeRO stages 1 to 3", section 3 (m_hat = g,
+ * sqrt(v_hat) = |g| at t = 1) with PyTorch-style decoupled decay.
+ * params and grads must not overlap one another or the state buffers.
+ * Errors: EINVAL (NULL pointer or entry, t < 1, betas outside [0,1),
+ * non-finite or negative lr/eps, non-finite wd), EALIGN, ECUDA. */
+int zero_step(void *const *params, const void *const *grads, zero_states_t *st, int64_t t,
+              double lr, double beta1, double beta2, double eps, double weight_decay,
+              zero_stream_t stream);
+
+/* zero_step restricted to the indices [lo, hi) (0 <= lo <= hi <= n): the update
+ * is elementwise, so the steps of a partition of [0, n) equal one full step
+ * bit for bit. Errors: as zero_step, plus EINVAL for a bad range. */
+int zero_step_range(void *const *params, const void *const *grads, zero_states_t *st,
+                    int64_t t, double lr, double beta1, double beta2, double eps,
+                    double weight_decay, int64_t lo, int64_t hi, zero_stream_t stream);
+
+/* --------------------------------------------------------------- buckets -- */
+
+/* Gradient buckets ("ZeRO One: Sharding the Optimizer", section "Bucketing":
+ * buckets of bucket_cap_mb * 1024 * 1024 bytes filled in backward order).
+ * A bucket holds B = bucket_bytes / element_size consecutive elements of each
+ * rank's gradient (element_size 4 for ZERO_FP32, 2 for ZERO_BF16_MIXED);
+ * bucket k (k = 0 first ready) covers [max(0, n-(k+1)B), n-kB).
+ * zero_bucket_count: *count = ceil(n / B). zero_bucket_range: bucket k's range.
+ * Errors: EINVAL (n < 0, B < 1, bad precision, k outside [0, count), NULL). */
+int zero_bucket_count(int64_t n, int32_t precision, int64_t bucket_bytes, int64_t *count);
+int zero_bucket_range(int64_t n, int32_t precision, int64_t bucket_bytes, int64_t k,
+                      int64_t *lo, int64_t *hi);
+
+/* One bucket as soon as it is ready: queue on `side` a wait for `ready` (may
+ * be NULL) and then the step on bucket k's range. `ready` must already have
+ * been recorded by the producer when this is called (CUDA stream-wait
+ * semantics). Errors: as zero_step_range, plus EINVAL for a bad k. */
+int zero_step_bucket(void *const *params, const void *const *grads, zero_states_t *st,
+                     int64_t t, double lr, double beta1, double beta2, double eps,
+                     double weight_decay, int64_t bucket_bytes, int64_t k, zero_event_t ready,
+                     zero_stream_t side);
+
+/* The whole step, bucket by bucket, in arrival order: for k = 0..count-1 queue
+ * on `side` a wait for ready[k] and the step on bucket k. `ready` holds
+ * n_ready == count events (already recorded by the producer), or is NULL with
+ * n_ready == 0 (no waits). `done` (may be NULL) is recorded on `side` after
+ * the last bucket. With timeout_ms >= 0 the call then waits on the host, up
+ * to timeout_ms milliseconds, for `done` (or for `side` when done is NULL)
+ * and returns ZERO_ETIMEDOUT if the work is still running; the queued work
+ * is not cancelled and completes later. With timeout_ms < 0 it returns after
+ * queueing. The result equals zero_step bit for bit.
+ * Errors: as zero_step, EINVAL for a bad bucket size or event count,
+ * ETIMEDOUT. */
+int zero_step_bucketed(void *const *params, const void *const *grads, zero_states_t *st,
+                       int64_t t, double lr, double beta1, double beta2, double eps,
+                       double weight_decay, int64_t bucket_bytes, const zero_event_t *ready,
+                       int64_t n_ready, zero_stream_t side, zero_event_t done,
+                       int64_t timeout_ms);
+
+/* ------------------------------------------------------------------- DDP -- */
+
+/* DDP all_reduce(op="mean") in place ("Data parallelism and ZeRO stages 1 to 3",
+ * section 2, "DDP": every rank gets the averaged gradient with identical
+ * bits): grads[r][j] = (((g_0[j] + g_1[j]) + ...) + g_{N-1}[j]) / N for every
+ * r, summed in fp32 in rank order; bf16 buffers receive the RNE of the fp32
+ * mean. precision: ZERO_FP32 (float) or ZERO_BF16_MIXED (bf16).
+ * Errors: EINVAL (n < 0, N outside [1, ZERO_MAX_RANKS], NULL, bad precision),
+ * EALIGN, ECUDA. */
+int ddp_allreduce_mean(void *const *grads, int64_t n, int32_t N, int32_t precision,
+                       zero_stream_t stream);
+
+/* ---------------------------------------------------------------- memory -- */
+
+/* Model-state bytes per rank after a step, by stage: 0 = plain DDP, 1 = shard
+ * the optimizer state, 2 = also the gradients, 3 = also the parameters
+ * ("Data Parallelism & ZeRO", "ZeRO, stage by stage"; "Data parallelism and
+ * ZeRO optimization", ZeRO-1/2/3 memory formulas). With per-parameter bytes
+ * (P, G, K) = (4, 4, 8) for ZERO_FP32 and (2, 2, 12) for ZERO_BF16_MIXED, and
+ * s the rank's shard size: params = P*(stage 3 ? s : n), grads =
+ * G*(stage >= 2 ? s : n), optimizer = K*(stage >= 1 ? s : n). ZERO_FP64_EMU
+ * reproduces the float64 bookkeeping table of "Data parallelism and ZeRO stages
+ * 1 to 3", section 3 (stage 1 keeps the full averaged gradient plus the
+ * chunk's; stages 1-2 hold m, v and a master chunk; stage 3 holds m, v).
+ * zero_memory_breakdown writes {params, grads, optimizer} for `rank`;
+ * zero_memory_bytes writes the total of rank 0, which holds the largest shard
+ * (16n, 4n+12n/N, 2n+14n/N, 16n/N in mixed precision when N divides n).
+ * Errors: EINVAL (n < 0, N < 1, stage outside 0..3, bad precision or rank,
+ * NULL output, or a total that overflows 64 bits). */
+int zero_memory_bytes(int64_t n, int32_t N, int32_t stage, int32_t precision, uint64_t *out);
+int zero_memory_breakdown(int64_t n, int32_t N, int32_t stage, int32_t precision,
+                          int32_t rank, uint64_t out[3]);
+
+/* ---------------------------------------------------------------- errors -- */
+
+/* Static description of a status code (never NULL). */
+const char *zero_strerror(int code);
+/* The calling thread's most recent error message ("" if none). */
+const char *zero_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ZERO_GB300_H */

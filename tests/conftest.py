@@ -1,5 +1,8 @@
 import os
+import shutil
 import sys
+
+import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 if ROOT not in sys.path:
@@ -8,3 +11,22 @@ if ROOT not in sys.path:
 
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a) and the built library")
+
+
+@pytest.fixture(scope="session")
+def abi():
+    """The C-ABI binding, building the library first when it is missing or stale."""
+    from zero_sharded_optimizer_gb300 import build as b
+    if shutil.which("nvcc") is None and not os.path.exists(b.LIB):
+        pytest.skip("nvcc not available and library not built")
+    b.build()
+    from zero_sharded_optimizer_gb300 import abi as a
+    return a
+
+
+@pytest.fixture(scope="session")
+def cuda(abi):
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    return torch.device("cuda:0")

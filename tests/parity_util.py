@@ -1,0 +1,59 @@
+"""Comparison helpers for the GPU-vs-oracle parity tests.
+
+Tolerances (written here once, used by every parity test):
+  * fp32 parameters, m, v, master: |gpu - oracle| <= 1e-6 + 1e-5 * |oracle|
+    against the fp32-mirror oracle;
+  * bf16 replicas: within one bf16 ulp of the round-to-nearest-even of the
+    oracle's fp32 master;
+  * shard bounds, memory bytes, bucket plans: bit-exact (checked elsewhere).
+"""
+
+import numpy as np
+
+import oracle
+
+ABS_TOL = 1e-6
+REL_TOL = 1e-5
+
+
+def assert_fp32_close(got, ref, what=""):
+    got = np.asarray(got, np.float32).astype(np.float64)
+    ref = np.asarray(ref, np.float32).astype(np.float64)
+    assert got.shape == ref.shape, (what, got.shape, ref.shape)
+    both_nan = np.isnan(got) & np.isnan(ref)
+    bad = ~both_nan & ~(np.abs(got - ref) <= ABS_TOL + REL_TOL * np.abs(ref))
+    if bad.any():
+        i = int(np.flatnonzero(bad)[0])
+        raise AssertionError(f"{what}: {int(bad.sum())} of {got.size} outside tolerance; "
+                             f"first at {i}: gpu={got[i]!r} oracle={ref[i]!r}")
+
+
+def bf16_ulp(x):
+    """Spacing of bf16 numbers at |x| (8 significant bits)."""
+    a = np.abs(np.asarray(x, np.float64))
+    e = np.floor(np.log2(np.maximum(a, 2.0 ** -126)))
+    return np.exp2(e - 7)
+
+
+def assert_bf16_within_one_ulp(got_bits, ref_master_fp32, what=""):
+    ref_bits = oracle.f32_to_bf16_rne(np.asarray(ref_master_fp32, np.float32))
+    got = oracle.bf16_to_f32(got_bits).astype(np.float64)
+    ref = oracle.bf16_to_f32(ref_bits).astype(np.float64)
+    bad = ~(np.abs(got - ref) <= bf16_ulp(np.maximum(np.abs(got), np.abs(ref))))
+    if bad.any():
+        i = int(np.flatnonzero(bad)[0])
+        raise AssertionError(f"{what}: {int(bad.sum())} bf16 values beyond 1 ulp; first at {i}: "
+                             f"gpu={got[i]!r} oracle RNE={ref[i]!r}")
+
+
+def exact_fraction(got, ref):
+    got = np.asarray(got)
+    ref = np.asarray(ref)
+    if got.size == 0:
+        return 1.0
+    return float(np.mean(got.view(np.uint32 if got.dtype == np.float32 else got.dtype) ==
+                         ref.view(np.uint32 if ref.dtype == np.float32 else ref.dtype)))
+
+
+def flat(states, key):
+    return np.concatenate([s[key] for s in states]) if states else np.zeros(0, np.float32)

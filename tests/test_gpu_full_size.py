@@ -1,0 +1,103 @@
+"""Parity at the workloads' full sizes, in the benchmark's launch configuration.
+
+Inputs are generated on the device (seeded). Before each step the sampled
+indices' inputs are copied back; after it, their outputs. The oracle computes
+the sampled outputs one by one (the step is elementwise, so a sample is an
+exact sub-problem), and the replicas are checked bitwise equal on the device
+over all n. Samples: random indices plus every shard and bucket edge and both
+ends of the vector.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from parity_util import assert_bf16_within_one_ulp, assert_fp32_close
+from zero_sharded_optimizer_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+
+def sample_indices(n, N, bucket_ranges=(), k=1 << 15, seed=0):
+    rng = np.random.default_rng(seed)
+    idx = set(rng.integers(0, n, k).tolist())
+    edges = set(oracle.shard_bounds(n, N)) | {0, n}
+    for lo, hi in bucket_ranges:
+        edges |= {lo, hi}
+    for e in edges:
+        idx |= {e + d for d in range(-9, 9) if 0 <= e + d < n}
+    return np.array(sorted(idx), dtype=np.int64)
+
+
+def oracle_on_sample(wl, t, g_s, p_s, m_s, v_s, master_s):
+    """The oracle's step on the sampled sub-problem (k indices, N ranks)."""
+    N, k = wl.N, len(m_s)
+    b = oracle.shard_bounds(k, N)
+    states = []
+    for i in range(N):
+        st = {"m": m_s[b[i]:b[i + 1]].copy(), "v": v_s[b[i]:b[i + 1]].copy()}
+        if master_s is not None:
+            st["master"] = master_s[b[i]:b[i + 1]].copy()
+        states.append(st)
+    reps, new = oracle.zero_step([p_s] * N, g_s, states, t, lr=wl.lr, beta1=wl.beta1,
+                                 beta2=wl.beta2, eps=wl.eps, weight_decay=wl.weight_decay,
+                                 precision=wl.precision, mode="fp32")
+    cat = lambda key: np.concatenate([s[key] for s in new])  # noqa: E731
+    return reps[0], cat("m"), cat("v"), (cat("master") if master_s is not None else None)
+
+
+@pytest.mark.parametrize("name", ["fp32_25m", "gpt2_small", "fp32_320m", "mixed_1p3b"])
+def test_full_size_sampled(abi, cuda, name):
+    from zero_sharded_optimizer_gb300.optimizer import ZeroOptimizer
+    wl = inputs.WORKLOADS[name]
+    n, N = wl.n, wl.N
+    mixed = wl.precision == inputs.BF16_MIXED
+    init = inputs.init_params_fp32(n, wl, seed=0, device=cuda)
+    reps = inputs.make_replicas(init, N, wl.precision)
+    grads = inputs.make_grads(n, N, wl.precision, device=cuda)
+    opt = ZeroOptimizer(n, N, wl.precision, lr=wl.lr, betas=(wl.beta1, wl.beta2), eps=wl.eps,
+                        weight_decay=wl.weight_decay, master_init=init if mixed else None)
+    del init
+    ranges = opt.bucket_ranges(wl.bucket_bytes) if wl.bucket_bytes else []
+    idx = sample_indices(n, N, ranges, seed=len(name))
+    idx_d = torch.from_numpy(idx).to(cuda)
+    take = lambda x: inputs.to_numpy_storage(x[idx_d])  # noqa: E731
+    producer, side = torch.cuda.Stream(), torch.cuda.Stream()
+    for t in range(1, wl.steps + 1):
+        p_before = take(opt.master) if mixed else take(reps[0])
+        m_before, v_before = take(opt.m), take(opt.v)
+        if wl.bucket_bytes:
+            # gradients arrive bucket by bucket, in reverse index order
+            ready = []
+            producer.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(producer):
+                for lo, hi in ranges:
+                    inputs.fill_grads(grads, wl, step=t, lo=lo, hi=hi)
+                    ev = torch.cuda.Event()
+                    ev.record(producer)
+                    ready.append(ev)
+            side.wait_stream(torch.cuda.current_stream())
+            opt.step_bucketed(reps, grads, ready, side, wl.bucket_bytes, timeout_ms=600_000)
+        else:
+            inputs.fill_grads(grads, wl, step=t)
+            opt.step(reps, grads)
+        torch.cuda.synchronize()
+        g_s = [take(g) for g in grads]
+        ref_p, ref_m, ref_v, ref_master = oracle_on_sample(
+            wl, t, g_s, p_before, m_before, v_before, p_before if mixed else None)
+        assert_fp32_close(take(opt.m), ref_m, f"{name} t={t} m")
+        assert_fp32_close(take(opt.v), ref_v, f"{name} t={t} v")
+        if mixed:
+            assert_fp32_close(take(opt.master), ref_master, f"{name} t={t} master")
+            for r in range(N):
+                assert_bf16_within_one_ulp(take(reps[r]), ref_master, f"{name} t={t} rep {r}")
+        else:
+            for r in range(N):
+                assert_fp32_close(take(reps[r]), ref_p, f"{name} t={t} rep {r}")
+        for r in range(1, N):
+            assert torch.equal(reps[r], reps[0])
+        if wl.zero_frac:
+            # the shared zero mask leaves ~1% of indices with an exact zero mean
+            zeros = np.all(np.stack([inputs.to_numpy_storage(g[idx_d]) for g in grads]) == 0, 0)
+            assert 0.003 < zeros.mean() < 0.03

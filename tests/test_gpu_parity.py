@@ -1,0 +1,398 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle.
+
+Inputs are seeded numpy draws copied to the device; the oracle sees the same
+bytes. Sizes span many vector units, several CTAs and ragged heads/tails;
+offset views exercise the unaligned and mixed-phase paths. Tolerances are in
+parity_util.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from parity_util import (assert_bf16_within_one_ulp, assert_fp32_close, exact_fraction, flat)
+from zero_sharded_optimizer_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+HP = dict(lr=3e-3, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.01)
+
+
+def to_dev(host, dtype, device, offset=0):
+    """Device view of `host` (float32, or bf16 bits as uint16) starting `offset`
+    elements into a padded allocation."""
+    n = host.shape[0]
+    buf = torch.zeros(n + 16, dtype=dtype, device=device)
+    view = buf[offset:offset + n]
+    if dtype == torch.bfloat16:
+        src = torch.from_numpy(host.view(np.int16).copy()).view(torch.bfloat16)
+    else:
+        src = torch.from_numpy(host.copy())
+    view.copy_(src)
+    return view
+
+
+def host_of(t):
+    return inputs.to_numpy_storage(t)
+
+
+class Case:
+    """One problem: device buffers, oracle state, and a step that checks both."""
+
+    def __init__(self, abi, device, n, N, prec, seed=0, rep_off=None, grad_off=None,
+                 state_off=0, hp=None):
+        self.abi, self.device, self.n, self.N, self.prec = abi, device, n, N, prec
+        self.hp = dict(HP if hp is None else hp)
+        self.rng = np.random.default_rng(seed)
+        self.mixed = prec == oracle.BF16_MIXED
+        self.dt = torch.bfloat16 if self.mixed else torch.float32
+        rep_off = rep_off or [0] * N
+        self.grad_off = grad_off or [0] * N
+        init = self.rng.normal(0, 0.5, n).astype(np.float32)
+        if self.mixed:
+            rep_host = oracle.f32_to_bf16_rne(init)    # replicas hold RNE(init)
+        else:
+            rep_host = init
+        self.reps = [to_dev(rep_host, self.dt, device, rep_off[r]) for r in range(N)]
+        self.grads = [to_dev(np.zeros(n, np.uint16 if self.mixed else np.float32), self.dt,
+                             device, self.grad_off[r]) for r in range(N)]
+        f32 = dict(dtype=torch.float32, device=device)
+        self.m = torch.full((n + 16,), 7.0, **f32)[state_off:state_off + n]
+        self.v = torch.full((n + 16,), 7.0, **f32)[state_off:state_off + n]
+        self.master = None
+        master_init = None
+        if self.mixed:
+            self.master = torch.zeros(n + 16, **f32)[state_off:state_off + n]
+            master_init = to_dev(init, torch.float32, device, state_off)
+        self.st = abi.zero_init_states(n, N, prec, self.m, self.v, self.master, master_init)
+        self.o_reps = [rep_host.copy() for _ in range(N)]
+        self.o_states = oracle.init_states(n, N, prec, master_init=init, mode="fp32")
+        self.t = 0
+
+    def new_grads(self, scale=1.0):
+        hs = []
+        for r in range(self.N):
+            g = (self.rng.normal(0, scale, self.n)).astype(np.float32)
+            if self.mixed:
+                g = oracle.f32_to_bf16_rne(g)
+            hs.append(g)
+            self.grads[r].copy_(to_dev(g, self.dt, self.device))
+        return hs
+
+    def oracle_step(self, host_grads):
+        self.t += 1
+        self.o_reps, self.o_states = oracle.zero_step(
+            self.o_reps, host_grads, self.o_states, self.t, precision=self.prec, mode="fp32",
+            **self.hp)
+
+    def gpu_step(self):
+        self.abi.zero_step(self.reps, self.grads, self.st, self.t, **self.hp)
+
+    def step(self, scale=1.0):
+        hg = self.new_grads(scale)
+        self.oracle_step(hg)
+        self.gpu_step()
+        torch.cuda.synchronize()
+
+    def compare(self, exact=False):
+        om, ov = flat(self.o_states, "m"), flat(self.o_states, "v")
+        gm, gv = host_of(self.m), host_of(self.v)
+        assert_fp32_close(gm, om, "m")
+        assert_fp32_close(gv, ov, "v")
+        if self.mixed:
+            omaster = flat(self.o_states, "master")
+            assert_fp32_close(host_of(self.master), omaster, "master")
+            for r in range(self.N):
+                assert_bf16_within_one_ulp(host_of(self.reps[r]), omaster, f"replica {r}")
+        else:
+            for r in range(self.N):
+                assert_fp32_close(host_of(self.reps[r]), self.o_reps[r], f"replica {r}")
+        # all replicas bitwise equal to each other (the all-gather)
+        r0 = host_of(self.reps[0])
+        for r in range(1, self.N):
+            assert np.array_equal(host_of(self.reps[r]), r0)
+        if exact:
+            assert exact_fraction(gm, om) == 1.0
+            assert exact_fraction(gv, ov) == 1.0
+            assert np.array_equal(r0, self.o_reps[0])
+            if self.mixed:
+                assert exact_fraction(host_of(self.master), flat(self.o_states, "master")) == 1.0
+
+
+GRID = [(1, 1), (5, 2), (7, 3), (33, 4), (4099, 5), (4099, 8), (100_003, 1), (100_003, 2),
+        (100_003, 3), (100_003, 4), (100_003, 8), (65_537, 13), (1_000_003, 4), (1_000_003, 8)]
+
+
+@pytest.mark.parametrize("prec", [oracle.FP32, oracle.BF16_MIXED])
+@pytest.mark.parametrize("n,N", GRID)
+def test_step_parity_grid(abi, cuda, n, N, prec):
+    c = Case(abi, cuda, n, N, prec, seed=n * 31 + N)
+    for _ in range(3):
+        c.step()
+        c.compare(exact=True)
+
+
+def test_tiny_adam_workload(abi, cuda):
+    """n=10,007 fp32 params, N=2, U(-1,1) params and N(0,1) grads from
+    default_rng(0), Adam lr=1e-2 (0.9, 0.999), eps=1e-8, wd=0, t=1..5: every
+    element of every output."""
+    wl = inputs.WORKLOADS["tiny_adam"]
+    params, grads = inputs.tiny_adam_numpy(wl.n, wl.N, wl.steps, seed=0)
+    hp = dict(lr=wl.lr, beta1=wl.beta1, beta2=wl.beta2, eps=wl.eps, weight_decay=wl.weight_decay)
+    reps = [torch.from_numpy(params.copy()).to(cuda) for _ in range(wl.N)]
+    gdev = [torch.empty(wl.n, dtype=torch.float32, device=cuda) for _ in range(wl.N)]
+    m = torch.empty(wl.n, dtype=torch.float32, device=cuda)
+    v = torch.empty_like(m)
+    st = abi.zero_init_states(wl.n, wl.N, abi.ZERO_FP32, m, v)
+    o_reps = [params.copy() for _ in range(wl.N)]
+    o_st = oracle.init_states(wl.n, wl.N)
+    assert abi.zero_shard_bounds(wl.n, wl.N) == [0, 5004, 10007]
+    for t in range(1, wl.steps + 1):
+        for r in range(wl.N):
+            gdev[r].copy_(torch.from_numpy(grads[t - 1][r]))
+        abi.zero_step(reps, gdev, st, t, **hp)
+        o_reps, o_st = oracle.zero_step(o_reps, grads[t - 1], o_st, t, mode="fp32", **hp)
+        torch.cuda.synchronize()
+        for r in range(wl.N):
+            assert_fp32_close(host_of(reps[r]), o_reps[r], f"t={t} replica {r}")
+            assert np.array_equal(host_of(reps[r]), o_reps[r])
+        assert np.array_equal(host_of(m), flat(o_st, "m"))
+        assert np.array_equal(host_of(v), flat(o_st, "v"))
+
+
+@pytest.mark.parametrize("prec", [oracle.FP32, oracle.BF16_MIXED])
+@pytest.mark.parametrize("layout", ["shifted", "mixed_phase", "per_rank"])
+def test_unaligned_layouts(abi, cuda, prec, layout):
+    n, N = 50_011, 4
+    if layout == "shifted":        # every buffer shifted by the same amount: vector path + head
+        kw = dict(rep_off=[3] * N, grad_off=[3] * N, state_off=3)
+    elif layout == "mixed_phase":  # phases differ: scalar path
+        kw = dict(rep_off=[1, 2, 3, 0], grad_off=[0, 0, 0, 1], state_off=0)
+    else:
+        kw = dict(rep_off=[5] * N, grad_off=[5] * N, state_off=1)
+    c = Case(abi, cuda, n, N, prec, seed=7, **kw)
+    for _ in range(2):
+        c.step()
+        c.compare(exact=True)
+
+
+def test_hyperparameters_honoured(abi, cuda):
+    for hp in [dict(lr=0.1, beta1=0.5, beta2=0.6, eps=1e-3, weight_decay=0.0),
+               dict(lr=1e-4, beta1=0.0, beta2=0.0, eps=0.0, weight_decay=0.3),
+               dict(lr=0.0, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.5)]:
+        c = Case(abi, cuda, 9_999, 3, oracle.FP32, seed=3, hp=hp)
+        for _ in range(3):
+            c.step()
+            c.compare(exact=True)
+
+
+def test_tiny_and_zero_gradients(abi, cuda):
+    # gradients ~1e-7 (the eps term matters) and exact zeros (no movement)
+    c = Case(abi, cuda, 20_000, 4, oracle.FP32, seed=4)
+    c.step(scale=1e-7)
+    c.compare(exact=True)
+    before = host_of(c.reps[0]).copy()
+    for g in c.grads:
+        g.zero_()
+    c.oracle_step([np.zeros(c.n, np.float32)] * c.N)
+    c.gpu_step()
+    torch.cuda.synchronize()
+    c.compare(exact=True)
+    assert not np.array_equal(host_of(c.reps[0]), before)   # decay still applies
+
+
+def test_empty_and_degenerate(abi, cuda):
+    for n, N in [(0, 1), (0, 4), (3, 5), (1, 64), (1000, 64)]:
+        for prec in (oracle.FP32, oracle.BF16_MIXED):
+            c = Case(abi, cuda, n, N, prec, seed=n + N)
+            c.step()
+            c.compare(exact=True)
+    with pytest.raises(abi.ZeroError):
+        Case(abi, cuda, 10, 65, oracle.FP32)
+
+
+def test_state_views_and_init(abi, cuda):
+    n, N = 10_007, 3
+    c = Case(abi, cuda, n, N, oracle.BF16_MIXED, seed=5)
+    torch.cuda.synchronize()
+    assert np.all(host_of(c.m) == 0) and np.all(host_of(c.v) == 0)
+    b = abi.zero_shard_bounds(n, N)
+    for r in range(N):
+        view = c.st.view(r)
+        assert (view["lo"], view["hi"]) == (b[r], b[r + 1])
+        assert view["m"] == c.m.data_ptr() + 4 * b[r]
+        assert view["v"] == c.v.data_ptr() + 4 * b[r]
+        assert view["master"] == c.master.data_ptr() + 4 * b[r]
+    assert c.st.info() == (n, N, oracle.BF16_MIXED)
+
+
+@pytest.mark.parametrize("prec", [oracle.FP32, oracle.BF16_MIXED])
+def test_range_partition_is_bitwise_full_step(abi, cuda, prec):
+    n, N = 200_003, 4
+    a = Case(abi, cuda, n, N, prec, seed=9)
+    b = Case(abi, cuda, n, N, prec, seed=9)
+    cuts = [0, 1, 17, 4096, 99_999, 100_001, 150_000, n]
+    for t in range(1, 3):
+        hg = a.new_grads()
+        for r in range(N):
+            b.grads[r].copy_(a.grads[r])
+        a.t = b.t = t
+        a.gpu_step()
+        for lo, hi in zip(cuts, cuts[1:]):
+            abi.zero_step_range(b.reps, b.grads, b.st, t, HP["lr"], HP["beta1"], HP["beta2"],
+                                HP["eps"], HP["weight_decay"], lo, hi)
+        torch.cuda.synchronize()
+        for x, y in [(a.m, b.m), (a.v, b.v)] + list(zip(a.reps, b.reps)):
+            assert torch.equal(x, y)
+    with pytest.raises(abi.ZeroError):
+        abi.zero_step_range(b.reps, b.grads, b.st, 1, 1e-3, 0.9, 0.9, 1e-8, 0.0, 5, n + 1)
+
+
+@pytest.mark.parametrize("prec", [oracle.FP32, oracle.BF16_MIXED])
+def test_bucketed_equals_monolithic(abi, cuda, prec):
+    n, N = 300_007, 8
+    bucket_bytes = 24_574          # not a multiple of 16 bytes: bucket edges off the vector grid
+    a = Case(abi, cuda, n, N, prec, seed=11)
+    b = Case(abi, cuda, n, N, prec, seed=11)
+    es = 2 if prec == oracle.BF16_MIXED else 4
+    ranges = [abi.zero_bucket_range(n, prec, bucket_bytes, k)
+              for k in range(abi.zero_bucket_count(n, prec, bucket_bytes))]
+    assert ranges == oracle.bucket_bounds(n, es, bucket_bytes)
+    producer = torch.cuda.Stream()
+    side = torch.cuda.Stream()
+    for t in range(1, 4):
+        a.new_grads()
+        a.t = b.t = t
+        a.gpu_step()
+        # the producer writes each bucket (reverse index order), then marks it ready
+        ready = []
+        producer.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(producer):
+            for lo, hi in ranges:
+                for r in range(N):
+                    b.grads[r][lo:hi].copy_(a.grads[r][lo:hi])
+                ev = torch.cuda.Event()
+                ev.record(producer)
+                ready.append(ev)
+        side.wait_stream(torch.cuda.current_stream())
+        done = torch.cuda.Event()
+        abi.zero_step_bucketed(b.reps, b.grads, b.st, t, HP["lr"], HP["beta1"], HP["beta2"],
+                               HP["eps"], HP["weight_decay"], bucket_bytes, ready, side, done,
+                               timeout_ms=60_000)
+        torch.cuda.synchronize()
+        for x, y in [(a.m, b.m), (a.v, b.v)] + list(zip(a.reps, b.reps)):
+            assert torch.equal(x, y)
+    # one bucket at a time, hook style
+    c = Case(abi, cuda, n, N, prec, seed=12)
+    d = Case(abi, cuda, n, N, prec, seed=12)
+    c.new_grads()
+    for r in range(N):
+        d.grads[r].copy_(c.grads[r])
+    c.t = 1
+    c.gpu_step()
+    for k in range(len(ranges)):
+        ev = torch.cuda.Event()
+        ev.record()
+        abi.zero_step_bucket(d.reps, d.grads, d.st, 1, HP["lr"], HP["beta1"], HP["beta2"],
+                             HP["eps"], HP["weight_decay"], bucket_bytes, k, ev, side)
+    torch.cuda.synchronize()
+    for x, y in [(c.m, d.m), (c.v, d.v)] + list(zip(c.reps, d.reps)):
+        assert torch.equal(x, y)
+
+
+def test_bucketed_deadline_reports_timeout(abi, cuda):
+    """A producer that is late: the host deadline passes, the call returns
+    ZERO_ETIMEDOUT, and the queued work still completes correctly."""
+    n, N = 100_000, 2
+    bucket_bytes = 4 * 50_000
+    a = Case(abi, cuda, n, N, oracle.FP32, seed=13)
+    b = Case(abi, cuda, n, N, oracle.FP32, seed=13)
+    a.new_grads()
+    for r in range(N):
+        b.grads[r].copy_(a.grads[r])
+    torch.cuda.synchronize()
+    a.t = b.t = 1
+    a.gpu_step()
+    producer = torch.cuda.Stream()
+    side = torch.cuda.Stream()
+    ready = []
+    with torch.cuda.stream(producer):
+        torch.cuda._sleep(400_000_000)          # a bounded busy kernel (~0.2 s)
+        for _ in range(2):
+            ev = torch.cuda.Event()
+            ev.record(producer)
+            ready.append(ev)
+    with pytest.raises(abi.ZeroError) as e:
+        abi.zero_step_bucketed(b.reps, b.grads, b.st, 1, HP["lr"], HP["beta1"], HP["beta2"],
+                               HP["eps"], HP["weight_decay"], bucket_bytes, ready, side, None,
+                               timeout_ms=5)
+    assert e.value.code == abi.ZERO_ETIMEDOUT
+    torch.cuda.synchronize()
+    for x, y in [(a.m, b.m), (a.v, b.v)] + list(zip(a.reps, b.reps)):
+        assert torch.equal(x, y)
+
+
+@pytest.mark.parametrize("prec", [oracle.FP32, oracle.BF16_MIXED])
+@pytest.mark.parametrize("n,N", [(1, 1), (9, 2), (4099, 3), (100_003, 4), (100_003, 8),
+                                 (65_537, 13)])
+def test_ddp_allreduce_mean(abi, cuda, n, N, prec):
+    rng = np.random.default_rng(n + N)
+    mixed = prec == oracle.BF16_MIXED
+    dt = torch.bfloat16 if mixed else torch.float32
+    hs = []
+    for _ in range(N):
+        g = rng.normal(0, 1, n).astype(np.float32)
+        hs.append(oracle.f32_to_bf16_rne(g) if mixed else g)
+    dev = [to_dev(h, dt, cuda, offset=1 if n % 2 else 0) for h in hs]
+    abi.ddp_allreduce_mean(dev, prec)
+    torch.cuda.synchronize()
+    ref = oracle.allreduce_mean(hs, precision=prec, mode="fp32")
+    for r in range(N):
+        assert np.array_equal(host_of(dev[r]), ref[r])
+
+
+def test_checkpoint_resume_is_bitwise(abi, cuda):
+    from zero_sharded_optimizer_gb300.optimizer import ZeroOptimizer
+    n, N = 123_457, 4
+    rng = np.random.default_rng(21)
+    init = torch.from_numpy(rng.normal(0, 0.02, n).astype(np.float32)).to(cuda)
+    gs = [[torch.from_numpy(rng.normal(0, 1e-3, n).astype(np.float32)).to(cuda).to(torch.bfloat16)
+           for _ in range(N)] for _ in range(6)]
+    kw = dict(precision=abi.ZERO_BF16_MIXED, lr=6e-4, betas=(0.9, 0.999), weight_decay=0.1,
+              master_init=init)
+    ref = ZeroOptimizer(n, N, **kw)
+    ref_p = [init.to(torch.bfloat16) for _ in range(N)]
+    for g in gs:
+        ref.step(ref_p, g)
+    a = ZeroOptimizer(n, N, **kw)
+    a_p = [init.to(torch.bfloat16) for _ in range(N)]
+    for g in gs[:3]:
+        a.step(a_p, g)
+    ckpt = a.state_dict()
+    ckpt_p = [p.clone() for p in a_p]
+    b = ZeroOptimizer(n, N, **kw)
+    b.load_state_dict(ckpt)
+    for g in gs[3:]:
+        b.step(ckpt_p, g)
+    torch.cuda.synchronize()
+    assert b.t == ref.t == 6
+    assert torch.equal(b.master, ref.master) and torch.equal(b.m, ref.m)
+    assert all(torch.equal(x, y) for x, y in zip(ckpt_p, ref_p))
+
+
+def test_optimizer_host_gradients_match_device(abi, cuda):
+    from zero_sharded_optimizer_gb300.optimizer import ZeroOptimizer
+    n, N = 77_777, 4
+    rng = np.random.default_rng(22)
+    p0 = torch.from_numpy(rng.normal(0, 0.02, n).astype(np.float32))
+    host = [torch.from_numpy(rng.normal(0, 1e-3, n).astype(np.float32)).pin_memory()
+            for _ in range(N)]
+    a = ZeroOptimizer(n, N, lr=1e-3, weight_decay=0.01)
+    b = ZeroOptimizer(n, N, lr=1e-3, weight_decay=0.01)
+    pa = [p0.to(cuda) for _ in range(N)]
+    pb = [p0.to(cuda) for _ in range(N)]
+    a.step(pa, host)
+    b.step(pb, [h.to(cuda) for h in host])
+    torch.cuda.synchronize()
+    assert all(torch.equal(x, y) for x, y in zip(pa, pb))

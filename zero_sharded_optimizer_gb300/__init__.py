@@ -9,14 +9,11 @@ the C-ABI library ``libzero_gb300.so`` (declared in ``include/zero_gb300.h``).
 raises at import when the library has not been built.
 """
 
-__all__ = ["abi", "inputs"]
+__all__ = ["abi", "inputs", "optimizer"]
 
 
 def __getattr__(name):
-    if name == "abi":
-        from . import abi
-        return abi
-    if name == "inputs":
-        from . import inputs
-        return inputs
+    if name in __all__:
+        import importlib
+        return importlib.import_module(f"{__name__}.{name}")
     raise AttributeError(name)

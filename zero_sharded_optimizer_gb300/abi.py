@@ -1,0 +1,291 @@
+"""Thin ctypes binding over libzero_gb300.so (declared in include/zero_gb300.h).
+
+Same names as the C entry points; this module only marshals arguments
+(tensor data pointers, stream and event handles, sizes) and turns status codes
+into exceptions. Every step of the computation runs in the library's CUDA
+kernels. Importing this module raises if the library has not been built --
+there is no fallback path.
+
+PyTorch provides device memory, streams and events here; tensors passed to the
+step must be contiguous CUDA tensors of the precision's storage type (float32,
+or bfloat16 in mixed precision).
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libzero_gb300.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(
+        f"{LIB_PATH} is missing: build it first (python -c 'import __graft_entry__ as g; g.build()' "
+        "or python zero_sharded_optimizer_gb300/build.py)")
+
+_lib = ctypes.CDLL(LIB_PATH)
+
+ZERO_FP32 = 0
+ZERO_BF16_MIXED = 1
+ZERO_FP64_EMU = 2
+
+ZERO_OK = 0
+ZERO_EINVAL = -1
+ZERO_EALIGN = -2
+ZERO_ECUDA = -3
+ZERO_ETIMEDOUT = -4
+ZERO_ENOMEM = -5
+ZERO_MAX_RANKS = 64
+
+_i64 = ctypes.c_int64
+_i32 = ctypes.c_int32
+_u64 = ctypes.c_uint64
+_dbl = ctypes.c_double
+_vp = ctypes.c_void_p
+_P = ctypes.POINTER
+
+# Every symbol the header declares, with its signature.
+_SIGNATURES = {
+    "zero_shard_bounds": (ctypes.c_int, [_i64, _i32, _P(_i64)]),
+    "zero_init_states": (ctypes.c_int, [_i64, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _P(_vp)]),
+    "zero_free_states": (ctypes.c_int, [_vp]),
+    "zero_states_info": (ctypes.c_int, [_vp, _P(_i64), _P(_i32), _P(_i32)]),
+    "zero_state_view": (ctypes.c_int, [_vp, _i32, _P(_i64), _P(_i64), _P(_vp), _P(_vp), _P(_vp)]),
+    "zero_step": (ctypes.c_int, [_P(_vp), _P(_vp), _vp, _i64, _dbl, _dbl, _dbl, _dbl, _dbl, _vp]),
+    "zero_step_range": (ctypes.c_int, [_P(_vp), _P(_vp), _vp, _i64, _dbl, _dbl, _dbl, _dbl, _dbl,
+                                       _i64, _i64, _vp]),
+    "zero_bucket_count": (ctypes.c_int, [_i64, _i32, _i64, _P(_i64)]),
+    "zero_bucket_range": (ctypes.c_int, [_i64, _i32, _i64, _i64, _P(_i64), _P(_i64)]),
+    "zero_step_bucket": (ctypes.c_int, [_P(_vp), _P(_vp), _vp, _i64, _dbl, _dbl, _dbl, _dbl, _dbl,
+                                        _i64, _i64, _vp, _vp]),
+    "zero_step_bucketed": (ctypes.c_int, [_P(_vp), _P(_vp), _vp, _i64, _dbl, _dbl, _dbl, _dbl,
+                                          _dbl, _i64, _P(_vp), _i64, _vp, _vp, _i64]),
+    "ddp_allreduce_mean": (ctypes.c_int, [_P(_vp), _i64, _i32, _i32, _vp]),
+    "zero_memory_bytes": (ctypes.c_int, [_i64, _i32, _i32, _i32, _P(_u64)]),
+    "zero_memory_breakdown": (ctypes.c_int, [_i64, _i32, _i32, _i32, _i32, _P(_u64)]),
+    "zero_strerror": (ctypes.c_char_p, [ctypes.c_int]),
+    "zero_last_error": (ctypes.c_char_p, []),
+}
+
+for _name, (_res, _args) in _SIGNATURES.items():
+    _f = getattr(_lib, _name)
+    _f.restype = _res
+    _f.argtypes = _args
+
+
+class ZeroError(RuntimeError):
+    """A non-zero status from the library, with its code and message."""
+
+    def __init__(self, code: int, func: str):
+        self.code = code
+        msg = _lib.zero_last_error().decode(errors="replace")
+        super().__init__(f"{func}: {zero_strerror(code)} ({code}): {msg}")
+
+
+def _check(code: int, func: str) -> None:
+    if code != ZERO_OK:
+        raise ZeroError(code, func)
+
+
+def zero_strerror(code: int) -> str:
+    return _lib.zero_strerror(code).decode()
+
+
+# --------------------------------------------------------------- marshalling --
+
+def _storage_dtype(precision: int):
+    if precision == ZERO_FP32:
+        return torch.float32
+    if precision == ZERO_BF16_MIXED:
+        return torch.bfloat16
+    raise ValueError(f"no tensor storage type for precision {precision}")
+
+
+def _ptr_array(tensors, n: int, dtype, what: str):
+    arr = (_vp * len(tensors))()
+    for i, t in enumerate(tensors):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda:
+            raise TypeError(f"{what}[{i}] must be a CUDA tensor")
+        if t.dtype != dtype:
+            raise TypeError(f"{what}[{i}] has dtype {t.dtype}, expected {dtype}")
+        if not t.is_contiguous() or t.numel() < n:
+            raise ValueError(f"{what}[{i}] must be contiguous with at least {n} elements")
+        arr[i] = t.data_ptr()
+    return arr
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _event(ev) -> int | None:
+    if ev is None:
+        return None
+    if isinstance(ev, torch.cuda.Event):
+        h = ev.cuda_event
+        if not h:
+            raise ValueError("event has never been recorded")
+        return h
+    return int(ev)
+
+
+# ----------------------------------------------------------------- host calls --
+
+def zero_shard_bounds(n: int, N: int) -> list[int]:
+    out = (_i64 * (max(N, 0) + 1))()
+    _check(_lib.zero_shard_bounds(n, N, out), "zero_shard_bounds")
+    return list(out)
+
+
+def zero_memory_bytes(n: int, N: int, stage: int, precision: int) -> int:
+    out = _u64()
+    _check(_lib.zero_memory_bytes(n, N, stage, precision, ctypes.byref(out)), "zero_memory_bytes")
+    return out.value
+
+
+def zero_memory_breakdown(n: int, N: int, stage: int, precision: int, rank: int) -> tuple:
+    out = (_u64 * 3)()
+    _check(_lib.zero_memory_breakdown(n, N, stage, precision, rank, out), "zero_memory_breakdown")
+    return tuple(out)
+
+
+def zero_bucket_count(n: int, precision: int, bucket_bytes: int) -> int:
+    out = _i64()
+    _check(_lib.zero_bucket_count(n, precision, bucket_bytes, ctypes.byref(out)),
+           "zero_bucket_count")
+    return out.value
+
+
+def zero_bucket_range(n: int, precision: int, bucket_bytes: int, k: int) -> tuple:
+    lo, hi = _i64(), _i64()
+    _check(_lib.zero_bucket_range(n, precision, bucket_bytes, k, ctypes.byref(lo),
+                                  ctypes.byref(hi)), "zero_bucket_range")
+    return lo.value, hi.value
+
+
+# ------------------------------------------------------------------- state --
+
+class ZeroStates:
+    """Owner of a zero_states_t handle; keeps the state tensors alive."""
+
+    def __init__(self, handle: int, n: int, N: int, precision: int, tensors: dict):
+        self.handle = handle
+        self.n = n
+        self.N = N
+        self.precision = precision
+        self.tensors = tensors
+
+    def view(self, rank: int) -> dict:
+        lo, hi = _i64(), _i64()
+        m, v, master = _vp(), _vp(), _vp()
+        _check(_lib.zero_state_view(self.handle, rank, ctypes.byref(lo), ctypes.byref(hi),
+                                    ctypes.byref(m), ctypes.byref(v), ctypes.byref(master)),
+               "zero_state_view")
+        return {"lo": lo.value, "hi": hi.value, "m": m.value, "v": v.value,
+                "master": master.value}
+
+    def info(self) -> tuple:
+        n, N, p = _i64(), _i32(), _i32()
+        _check(_lib.zero_states_info(self.handle, ctypes.byref(n), ctypes.byref(N),
+                                     ctypes.byref(p)), "zero_states_info")
+        return n.value, N.value, p.value
+
+    def close(self):
+        if self.handle:
+            _lib.zero_free_states(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def zero_init_states(n: int, N: int, precision: int, m, v, master=None, master_init=None,
+                     stream=None) -> ZeroStates:
+    """m, v (and master, master_init in mixed precision): contiguous float32 CUDA
+    tensors of n elements. Returns the state handle."""
+    def ptr(t, what):
+        if t is None:
+            return None
+        if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dtype != torch.float32:
+            raise TypeError(f"{what} must be a float32 CUDA tensor")
+        if not t.is_contiguous() or t.numel() < n:
+            raise ValueError(f"{what} must be contiguous with at least {n} elements")
+        return t.data_ptr()
+    h = _vp()
+    _check(_lib.zero_init_states(n, N, precision, ptr(m, "m"), ptr(v, "v"), ptr(master, "master"),
+                                 ptr(master_init, "master_init"), _stream(stream), ctypes.byref(h)),
+           "zero_init_states")
+    return ZeroStates(h.value, n, N, precision, {"m": m, "v": v, "master": master})
+
+
+# -------------------------------------------------------------------- step --
+
+def _step_ptrs(params, grads, st: ZeroStates):
+    if len(params) != st.N or len(grads) != st.N:
+        raise ValueError(f"need {st.N} params and {st.N} grads")
+    dt = _storage_dtype(st.precision)
+    return _ptr_array(params, st.n, dt, "params"), _ptr_array(grads, st.n, dt, "grads")
+
+
+def zero_step(params, grads, st: ZeroStates, t: int, lr: float, beta1: float = 0.9,
+              beta2: float = 0.999, eps: float = 1e-8, weight_decay: float = 0.0, stream=None):
+    pp, gp = _step_ptrs(params, grads, st)
+    _check(_lib.zero_step(pp, gp, st.handle, t, lr, beta1, beta2, eps, weight_decay,
+                          _stream(stream)), "zero_step")
+
+
+def zero_step_range(params, grads, st: ZeroStates, t: int, lr: float, beta1: float, beta2: float,
+                    eps: float, weight_decay: float, lo: int, hi: int, stream=None):
+    pp, gp = _step_ptrs(params, grads, st)
+    _check(_lib.zero_step_range(pp, gp, st.handle, t, lr, beta1, beta2, eps, weight_decay, lo, hi,
+                                _stream(stream)), "zero_step_range")
+
+
+def zero_step_bucket(params, grads, st: ZeroStates, t: int, lr: float, beta1: float, beta2: float,
+                     eps: float, weight_decay: float, bucket_bytes: int, k: int, ready=None,
+                     side=None):
+    pp, gp = _step_ptrs(params, grads, st)
+    _check(_lib.zero_step_bucket(pp, gp, st.handle, t, lr, beta1, beta2, eps, weight_decay,
+                                 bucket_bytes, k, _event(ready), _stream(side)), "zero_step_bucket")
+
+
+def zero_step_bucketed(params, grads, st: ZeroStates, t: int, lr: float, beta1: float,
+                       beta2: float, eps: float, weight_decay: float, bucket_bytes: int,
+                       ready=None, side=None, done=None, timeout_ms: int = -1):
+    """Raises ZeroError with code ZERO_ETIMEDOUT when the deadline passes."""
+    pp, gp = _step_ptrs(params, grads, st)
+    if ready is None:
+        arr, count = None, 0
+    else:
+        arr = (_vp * len(ready))(*[_event(e) for e in ready])
+        count = len(ready)
+    _check(_lib.zero_step_bucketed(pp, gp, st.handle, t, lr, beta1, beta2, eps, weight_decay,
+                                   bucket_bytes, arr, count, _stream(side), _event(done),
+                                   timeout_ms), "zero_step_bucketed")
+
+
+def ddp_allreduce_mean(grads, precision: int, n: int | None = None, stream=None):
+    n = grads[0].numel() if n is None else n
+    gp = _ptr_array(grads, n, _storage_dtype(precision), "grads")
+    _check(_lib.ddp_allreduce_mean(gp, n, len(grads), precision, _stream(stream)),
+           "ddp_allreduce_mean")
+
+
+def raw_call(name: str, *args) -> int:
+    """Call an entry point with raw ctypes arguments and return its status
+    (for callers that manage pointers themselves)."""
+    return getattr(_lib, name)(*args)
+
+
+def declared_symbols() -> list[str]:
+    return sorted(_SIGNATURES)

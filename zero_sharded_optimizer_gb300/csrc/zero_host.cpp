@@ -1,0 +1,502 @@
+// Host side of libzero_gb300.so: argument checking, the shard planner, memory
+// accounting, per-step constants, the bucket streamer, and error reporting.
+// Device work is delegated to the launchers in zero_kernels.cu.
+//
+// Built with -ffp-contract=off so that the per-step constants are formed with
+// separately rounded double operations.
+
+#include <algorithm>
+#include <chrono>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+#include <thread>
+#include <vector>
+
+#include "zero_internal.h"
+
+struct zero_states {
+  int64_t n;
+  int32_t N;
+  int32_t precision;
+  float* m;
+  float* v;
+  float* master;
+  int64_t bounds[ZERO_MAX_RANKS + 1];
+};
+
+namespace {
+
+thread_local char g_last_error[512] = "";
+
+int fail(int code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+  va_end(ap);
+  return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  return fail(ZERO_ECUDA, "%s: %s (%s)", what, cudaGetErrorString(e), cudaGetErrorName(e));
+}
+
+bool valid_ranks(int32_t N) { return N >= 1 && N <= ZERO_MAX_RANKS; }
+
+// Shard offsets of np.array_split(np.arange(n), N): a_i = i*q + min(i, r).
+void shard_bounds(int64_t n, int32_t N, int64_t* b) {
+  const int64_t q = n / N, r = n % N;
+  for (int32_t i = 0; i <= N; ++i) b[i] = i * q + std::min<int64_t>(i, r);
+}
+
+// ----------------------------------------------------------- alignment plan --
+
+// Element phase of a pointer within a 16-byte line, or -1 if it is not aligned
+// to its element size.
+int phase_of(const void* p, int elem) {
+  const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+  if (a % elem) return -1;
+  return int((a / elem) % (16 / elem));
+}
+
+zk::Split make_split(int64_t lo, int64_t hi, bool vector_ok, int phase, int V) {
+  zk::Split s{lo, hi - lo, 0, 0};
+  if (!vector_ok) return s;
+  const int64_t len = hi - lo;
+  int64_t head = (V - (phase + lo % V) % V) % V;
+  if (head > len) head = len;
+  s.head = head;
+  s.nvec = (len - head) / V;
+  s.tail = len - head - s.nvec * V;
+  return s;
+}
+
+struct Range {
+  uintptr_t lo, hi;
+  const char* what;
+};
+
+// Every buffer must be disjoint from every other one.
+int check_disjoint(std::vector<Range>& rs) {
+  std::sort(rs.begin(), rs.end(), [](const Range& a, const Range& b) { return a.lo < b.lo; });
+  for (size_t i = 1; i < rs.size(); ++i) {
+    if (rs[i].lo < rs[i - 1].hi)
+      return fail(ZERO_EINVAL, "buffers overlap (%s and %s)", rs[i - 1].what, rs[i].what);
+  }
+  return ZERO_OK;
+}
+
+// ------------------------------------------------------- step preparation --
+
+int adam_consts(int64_t t, double lr, double beta1, double beta2, double eps, double wd,
+                zk::AdamConsts* c) {
+  if (t < 1) return fail(ZERO_EINVAL, "step number t=%lld must be >= 1", (long long)t);
+  if (!(beta1 >= 0.0 && beta1 < 1.0) || !(beta2 >= 0.0 && beta2 < 1.0))
+    return fail(ZERO_EINVAL, "betas must lie in [0, 1) (got %g, %g)", beta1, beta2);
+  if (!std::isfinite(lr) || lr < 0.0) return fail(ZERO_EINVAL, "lr must be finite and >= 0");
+  if (!std::isfinite(eps) || eps < 0.0) return fail(ZERO_EINVAL, "eps must be finite and >= 0");
+  if (!std::isfinite(wd)) return fail(ZERO_EINVAL, "weight_decay must be finite");
+  const double td = double(t);
+  const double bc1 = 1.0 - std::pow(beta1, td);
+  const double bc2 = 1.0 - std::pow(beta2, td);
+  c->decay = float(1.0 - lr * wd);
+  c->b1 = float(beta1);
+  c->omb1 = float(1.0 - beta1);
+  c->b2 = float(beta2);
+  c->omb2 = float(1.0 - beta2);
+  c->step = float(lr / bc1);
+  c->bc2s = float(std::sqrt(bc2));
+  c->eps = float(eps);
+  if (!(c->bc2s > 0.0f)) return fail(ZERO_EINVAL, "1 - beta2^t rounds to zero");
+  return ZERO_OK;
+}
+
+// Checks the buffers of a step and fills everything in StepArgs except the
+// split and the constants.
+int prepare_step(void* const* params, const void* const* grads, const zero_states* st,
+                 zk::StepArgs* a, bool* vector_ok, int* phase) {
+  if (!st) return fail(ZERO_EINVAL, "state handle is NULL");
+  if (!params || !grads) return fail(ZERO_EINVAL, "params/grads array is NULL");
+  const int32_t N = st->N;
+  const bool mixed = st->precision == ZERO_BF16_MIXED;
+  const int es = mixed ? 2 : 4;
+  std::memset(a, 0, sizeof(*a));
+  a->N = N;
+  a->fN = float(N);
+  a->m = st->m;
+  a->v = st->v;
+  a->master = st->master;
+  std::memcpy(a->bounds, st->bounds, sizeof(int64_t) * (N + 1));
+  std::vector<Range> rs;
+  rs.reserve(2 * N + 3);
+  const uintptr_t pbytes = uintptr_t(st->n) * es, sbytes = uintptr_t(st->n) * 4;
+  int ph16 = -2, ph32 = -2;
+  bool same = true;
+  auto note = [&](const void* p, int elem, int* ph) {
+    const int q = phase_of(p, elem);
+    if (q < 0) return false;
+    if (*ph == -2) *ph = q;
+    else if (*ph != q) same = false;
+    return true;
+  };
+  for (int32_t r = 0; r < N; ++r) {
+    if (!params[r] || !grads[r]) return fail(ZERO_EINVAL, "params[%d] or grads[%d] is NULL", r, r);
+    a->reps[r] = params[r];
+    a->grads[r] = grads[r];
+    int* ph = mixed ? &ph16 : &ph32;
+    if (!note(params[r], es, ph) || !note(grads[r], es, ph))
+      return fail(ZERO_EALIGN, "params[%d]/grads[%d] not aligned to %d bytes", r, r, es);
+    if (st->n > 0) {
+      rs.push_back({uintptr_t(params[r]), uintptr_t(params[r]) + pbytes, "a parameter replica"});
+      rs.push_back({uintptr_t(grads[r]), uintptr_t(grads[r]) + pbytes, "a gradient"});
+    }
+  }
+  const float* sbufs[3] = {st->m, st->v, st->master};
+  for (int k = 0; k < (mixed ? 3 : 2); ++k) {
+    if (!note(sbufs[k], 4, &ph32)) return fail(ZERO_EALIGN, "state buffer not 4-byte aligned");
+    if (st->n > 0) rs.push_back({uintptr_t(sbufs[k]), uintptr_t(sbufs[k]) + sbytes, "a state buffer"});
+  }
+  if (int e = check_disjoint(rs)) return e;
+  if (mixed) {
+    // 8-element units: bf16 buffers 16-byte aligned at j = -ph16 (mod 8), fp32
+    // buffers at j = -ph32 (mod 4); both hold when ph16 = ph32 (mod 4).
+    *vector_ok = same && (ph16 % 4) == ph32;
+    *phase = ph16;
+  } else {
+    *vector_ok = same;
+    *phase = ph32;
+  }
+  return ZERO_OK;
+}
+
+int launch_range(zk::StepArgs& a, const zero_states* st, bool vector_ok, int phase, int64_t lo,
+                 int64_t hi, cudaStream_t s) {
+  if (hi <= lo) return ZERO_OK;
+  const bool mixed = st->precision == ZERO_BF16_MIXED;
+  a.sp = make_split(lo, hi, vector_ok, phase, mixed ? 8 : 4);
+  cudaError_t e = zk::launch_step(a, mixed, s);
+  if (e != cudaSuccess) return cuda_fail(e, "zero_step kernel launch");
+  return ZERO_OK;
+}
+
+int bucket_elems(int32_t precision, int64_t bucket_bytes, int64_t* B) {
+  int es;
+  if (precision == ZERO_FP32) es = 4;
+  else if (precision == ZERO_BF16_MIXED) es = 2;
+  else return fail(ZERO_EINVAL, "bucket plan needs precision FP32 or BF16_MIXED");
+  if (bucket_bytes < es) return fail(ZERO_EINVAL, "bucket of %lld bytes holds no element",
+                                     (long long)bucket_bytes);
+  *B = bucket_bytes / es;
+  return ZERO_OK;
+}
+
+int64_t bucket_count_of(int64_t n, int64_t B) { return n == 0 ? 0 : (n + B - 1) / B; }
+
+void bucket_range_of(int64_t n, int64_t B, int64_t k, int64_t* lo, int64_t* hi) {
+  *hi = n - k * B;
+  *lo = std::max<int64_t>(0, *hi - B);
+}
+
+// Checked a*b + c for the memory totals.
+bool mul_add(uint64_t a, uint64_t b, uint64_t* acc) {
+  if (a != 0 && b > UINT64_MAX / a) return false;
+  const uint64_t p = a * b;
+  if (*acc > UINT64_MAX - p) return false;
+  *acc += p;
+  return true;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* zero_strerror(int code) {
+  switch (code) {
+    case ZERO_OK: return "ok";
+    case ZERO_EINVAL: return "invalid argument";
+    case ZERO_EALIGN: return "misaligned pointer";
+    case ZERO_ECUDA: return "CUDA runtime error";
+    case ZERO_ETIMEDOUT: return "timed out";
+    case ZERO_ENOMEM: return "out of host memory";
+    default: return "unknown status code";
+  }
+}
+
+const char* zero_last_error(void) { return g_last_error; }
+
+int zero_shard_bounds(int64_t n, int32_t N, int64_t* bounds) {
+  if (n < 0) return fail(ZERO_EINVAL, "n=%lld must be >= 0", (long long)n);
+  if (N < 1) return fail(ZERO_EINVAL, "N=%d must be >= 1", N);
+  if (!bounds) return fail(ZERO_EINVAL, "bounds is NULL");
+  shard_bounds(n, N, bounds);
+  return ZERO_OK;
+}
+
+int zero_memory_breakdown(int64_t n, int32_t N, int32_t stage, int32_t precision, int32_t rank,
+                          uint64_t out[3]) {
+  if (n < 0 || N < 1) return fail(ZERO_EINVAL, "need n >= 0 and N >= 1");
+  if (stage < 0 || stage > 3) return fail(ZERO_EINVAL, "stage %d outside 0..3", stage);
+  if (rank < 0 || rank >= N) return fail(ZERO_EINVAL, "rank %d outside [0, %d)", rank, N);
+  if (!out) return fail(ZERO_EINVAL, "out is NULL");
+  const int64_t q = n / N, r = n % N;
+  const uint64_t s = uint64_t(q + (rank < r ? 1 : 0));  // this rank's shard size
+  const uint64_t un = uint64_t(n);
+  uint64_t p = 0, g = 0, o = 0;
+  bool ok = true;
+  if (precision == ZERO_FP64_EMU) {
+    // The course's float64 bookkeeping: 8-byte values; stage 1 keeps the full
+    // averaged .grad plus the chunk's; stages 1-2 hold m, v and a master chunk;
+    // stage 3's chunk is the parameter storage; one process holds m, v of all n.
+    ok &= mul_add(8, stage == 3 ? s : un, &p);
+    if (stage == 0) ok &= mul_add(8, un, &g);
+    else if (stage == 1) ok &= mul_add(8, un, &g) && mul_add(8, s, &g);
+    else ok &= mul_add(8, s, &g);
+    if (stage == 0) ok &= mul_add(16, un, &o);
+    else if (stage == 3) ok &= mul_add(16, s, &o);
+    else ok &= mul_add(24, s, &o);
+  } else if (precision == ZERO_FP32 || precision == ZERO_BF16_MIXED) {
+    const uint64_t P = precision == ZERO_FP32 ? 4 : 2;
+    const uint64_t G = P;
+    const uint64_t K = precision == ZERO_FP32 ? 8 : 12;
+    ok &= mul_add(P, stage == 3 ? s : un, &p);
+    ok &= mul_add(G, stage >= 2 ? s : un, &g);
+    ok &= mul_add(K, stage >= 1 ? s : un, &o);
+  } else {
+    return fail(ZERO_EINVAL, "unknown precision %d", precision);
+  }
+  if (!ok) return fail(ZERO_EINVAL, "byte count overflows 64 bits");
+  out[0] = p;
+  out[1] = g;
+  out[2] = o;
+  return ZERO_OK;
+}
+
+int zero_memory_bytes(int64_t n, int32_t N, int32_t stage, int32_t precision, uint64_t* out) {
+  if (!out) return fail(ZERO_EINVAL, "out is NULL");
+  uint64_t b[3];
+  if (int e = zero_memory_breakdown(n, N, stage, precision, 0, b)) return e;
+  uint64_t total = 0;
+  for (uint64_t x : b) {
+    if (total > UINT64_MAX - x) return fail(ZERO_EINVAL, "byte count overflows 64 bits");
+    total += x;
+  }
+  *out = total;
+  return ZERO_OK;
+}
+
+int zero_init_states(int64_t n, int32_t N, int32_t precision, float* m, float* v, float* master,
+                     const float* master_init, zero_stream_t stream, zero_states_t** out) {
+  if (!out) return fail(ZERO_EINVAL, "out is NULL");
+  *out = nullptr;
+  if (n < 0) return fail(ZERO_EINVAL, "n=%lld must be >= 0", (long long)n);
+  if (!valid_ranks(N)) return fail(ZERO_EINVAL, "N=%d outside [1, %d]", N, ZERO_MAX_RANKS);
+  if (precision != ZERO_FP32 && precision != ZERO_BF16_MIXED)
+    return fail(ZERO_EINVAL, "state precision must be FP32 or BF16_MIXED");
+  if (!m || !v) return fail(ZERO_EINVAL, "m or v is NULL");
+  const bool mixed = precision == ZERO_BF16_MIXED;
+  if (mixed && (!master || !master_init))
+    return fail(ZERO_EINVAL, "mixed precision needs master and master_init");
+  if (!mixed && (master || master_init))
+    return fail(ZERO_EINVAL, "fp32 state takes no master buffer");
+  int ph = -2;
+  bool same = true;
+  const float* bufs[4] = {m, v, master, master_init};
+  std::vector<Range> rs;
+  for (int k = 0; k < (mixed ? 4 : 2); ++k) {
+    const int q = phase_of(bufs[k], 4);
+    if (q < 0) return fail(ZERO_EALIGN, "state buffer not 4-byte aligned");
+    if (ph == -2) ph = q;
+    else if (ph != q) same = false;
+    if (n > 0) rs.push_back({uintptr_t(bufs[k]), uintptr_t(bufs[k]) + uintptr_t(n) * 4, "a state buffer"});
+  }
+  if (int e = check_disjoint(rs)) return e;
+  zero_states* st = new (std::nothrow) zero_states;
+  if (!st) return fail(ZERO_ENOMEM, "cannot allocate the state handle");
+  st->n = n;
+  st->N = N;
+  st->precision = precision;
+  st->m = m;
+  st->v = v;
+  st->master = master;
+  shard_bounds(n, N, st->bounds);
+  if (n > 0) {
+    zk::InitArgs ia{m, v, master, master_init, make_split(0, n, same, ph, 4)};
+    cudaError_t e = zk::launch_init(ia, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) {
+      delete st;
+      return cuda_fail(e, "state init kernel launch");
+    }
+  }
+  *out = st;
+  return ZERO_OK;
+}
+
+int zero_free_states(zero_states_t* st) {
+  delete st;
+  return ZERO_OK;
+}
+
+int zero_states_info(const zero_states_t* st, int64_t* n, int32_t* N, int32_t* precision) {
+  if (!st) return fail(ZERO_EINVAL, "state handle is NULL");
+  if (n) *n = st->n;
+  if (N) *N = st->N;
+  if (precision) *precision = st->precision;
+  return ZERO_OK;
+}
+
+int zero_state_view(const zero_states_t* st, int32_t rank, int64_t* lo, int64_t* hi, float** m,
+                    float** v, float** master) {
+  if (!st) return fail(ZERO_EINVAL, "state handle is NULL");
+  if (rank < 0 || rank >= st->N) return fail(ZERO_EINVAL, "rank %d outside [0, %d)", rank, st->N);
+  const int64_t a = st->bounds[rank], b = st->bounds[rank + 1];
+  if (lo) *lo = a;
+  if (hi) *hi = b;
+  if (m) *m = st->m + a;
+  if (v) *v = st->v + a;
+  if (master) *master = st->master ? st->master + a : nullptr;
+  return ZERO_OK;
+}
+
+int zero_step_range(void* const* params, const void* const* grads, zero_states_t* st, int64_t t,
+                    double lr, double beta1, double beta2, double eps, double weight_decay,
+                    int64_t lo, int64_t hi, zero_stream_t stream) {
+  zk::StepArgs a;
+  bool vec = false;
+  int phase = 0;
+  if (int e = prepare_step(params, grads, st, &a, &vec, &phase)) return e;
+  if (lo < 0 || hi < lo || hi > st->n)
+    return fail(ZERO_EINVAL, "range [%lld, %lld) outside [0, %lld)", (long long)lo, (long long)hi,
+                (long long)st->n);
+  if (int e = adam_consts(t, lr, beta1, beta2, eps, weight_decay, &a.c)) return e;
+  return launch_range(a, st, vec, phase, lo, hi, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int zero_step(void* const* params, const void* const* grads, zero_states_t* st, int64_t t,
+              double lr, double beta1, double beta2, double eps, double weight_decay,
+              zero_stream_t stream) {
+  if (!st) return fail(ZERO_EINVAL, "state handle is NULL");
+  return zero_step_range(params, grads, st, t, lr, beta1, beta2, eps, weight_decay, 0, st->n,
+                         stream);
+}
+
+int zero_bucket_count(int64_t n, int32_t precision, int64_t bucket_bytes, int64_t* count) {
+  if (!count) return fail(ZERO_EINVAL, "count is NULL");
+  if (n < 0) return fail(ZERO_EINVAL, "n=%lld must be >= 0", (long long)n);
+  int64_t B;
+  if (int e = bucket_elems(precision, bucket_bytes, &B)) return e;
+  *count = bucket_count_of(n, B);
+  return ZERO_OK;
+}
+
+int zero_bucket_range(int64_t n, int32_t precision, int64_t bucket_bytes, int64_t k, int64_t* lo,
+                      int64_t* hi) {
+  if (!lo || !hi) return fail(ZERO_EINVAL, "lo/hi is NULL");
+  if (n < 0) return fail(ZERO_EINVAL, "n=%lld must be >= 0", (long long)n);
+  int64_t B;
+  if (int e = bucket_elems(precision, bucket_bytes, &B)) return e;
+  if (k < 0 || k >= bucket_count_of(n, B))
+    return fail(ZERO_EINVAL, "bucket %lld outside [0, %lld)", (long long)k,
+                (long long)bucket_count_of(n, B));
+  bucket_range_of(n, B, k, lo, hi);
+  return ZERO_OK;
+}
+
+int zero_step_bucket(void* const* params, const void* const* grads, zero_states_t* st, int64_t t,
+                     double lr, double beta1, double beta2, double eps, double weight_decay,
+                     int64_t bucket_bytes, int64_t k, zero_event_t ready, zero_stream_t side) {
+  if (!st) return fail(ZERO_EINVAL, "state handle is NULL");
+  int64_t lo, hi;
+  if (int e = zero_bucket_range(st->n, st->precision, bucket_bytes, k, &lo, &hi)) return e;
+  zk::StepArgs a;
+  bool vec = false;
+  int phase = 0;
+  if (int e = prepare_step(params, grads, st, &a, &vec, &phase)) return e;
+  if (int e = adam_consts(t, lr, beta1, beta2, eps, weight_decay, &a.c)) return e;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(side);
+  if (ready) {
+    cudaError_t ce = cudaStreamWaitEvent(s, reinterpret_cast<cudaEvent_t>(ready), 0);
+    if (ce != cudaSuccess) return cuda_fail(ce, "cudaStreamWaitEvent");
+  }
+  return launch_range(a, st, vec, phase, lo, hi, s);
+}
+
+int zero_step_bucketed(void* const* params, const void* const* grads, zero_states_t* st,
+                       int64_t t, double lr, double beta1, double beta2, double eps,
+                       double weight_decay, int64_t bucket_bytes, const zero_event_t* ready,
+                       int64_t n_ready, zero_stream_t side, zero_event_t done,
+                       int64_t timeout_ms) {
+  if (!st) return fail(ZERO_EINVAL, "state handle is NULL");
+  int64_t B;
+  if (int e = bucket_elems(st->precision, bucket_bytes, &B)) return e;
+  const int64_t count = bucket_count_of(st->n, B);
+  if (ready ? n_ready != count : n_ready != 0)
+    return fail(ZERO_EINVAL, "need %lld ready events (got %lld%s)", (long long)count,
+                (long long)n_ready, ready ? "" : ", array NULL");
+  zk::StepArgs a;
+  bool vec = false;
+  int phase = 0;
+  if (int e = prepare_step(params, grads, st, &a, &vec, &phase)) return e;
+  if (int e = adam_consts(t, lr, beta1, beta2, eps, weight_decay, &a.c)) return e;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(side);
+  for (int64_t k = 0; k < count; ++k) {
+    if (ready && ready[k]) {
+      cudaError_t ce = cudaStreamWaitEvent(s, reinterpret_cast<cudaEvent_t>(ready[k]), 0);
+      if (ce != cudaSuccess) return cuda_fail(ce, "cudaStreamWaitEvent");
+    }
+    int64_t lo, hi;
+    bucket_range_of(st->n, B, k, &lo, &hi);
+    if (int e = launch_range(a, st, vec, phase, lo, hi, s)) return e;
+  }
+  if (done) {
+    cudaError_t ce = cudaEventRecord(reinterpret_cast<cudaEvent_t>(done), s);
+    if (ce != cudaSuccess) return cuda_fail(ce, "cudaEventRecord");
+  }
+  if (timeout_ms < 0) return ZERO_OK;
+  // Host-side deadline: poll, never block in the driver, never spin on the GPU.
+  const auto deadline = std::chrono::steady_clock::now() + std::chrono::milliseconds(timeout_ms);
+  for (;;) {
+    cudaError_t q = done ? cudaEventQuery(reinterpret_cast<cudaEvent_t>(done)) : cudaStreamQuery(s);
+    if (q == cudaSuccess) return ZERO_OK;
+    if (q != cudaErrorNotReady) return cuda_fail(q, "waiting for the bucketed step");
+    if (std::chrono::steady_clock::now() >= deadline)
+      return fail(ZERO_ETIMEDOUT, "bucketed step not finished after %lld ms", (long long)timeout_ms);
+    std::this_thread::sleep_for(std::chrono::microseconds(50));
+  }
+}
+
+int ddp_allreduce_mean(void* const* grads, int64_t n, int32_t N, int32_t precision,
+                       zero_stream_t stream) {
+  if (n < 0) return fail(ZERO_EINVAL, "n=%lld must be >= 0", (long long)n);
+  if (!valid_ranks(N)) return fail(ZERO_EINVAL, "N=%d outside [1, %d]", N, ZERO_MAX_RANKS);
+  if (precision != ZERO_FP32 && precision != ZERO_BF16_MIXED)
+    return fail(ZERO_EINVAL, "gradient precision must be FP32 or BF16_MIXED");
+  if (!grads) return fail(ZERO_EINVAL, "grads array is NULL");
+  const int es = precision == ZERO_BF16_MIXED ? 2 : 4;
+  zk::AllreduceArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.N = N;
+  a.fN = float(N);
+  int ph = -2;
+  bool same = true;
+  std::vector<Range> rs;
+  for (int32_t r = 0; r < N; ++r) {
+    if (!grads[r]) return fail(ZERO_EINVAL, "grads[%d] is NULL", r);
+    const int q = phase_of(grads[r], es);
+    if (q < 0) return fail(ZERO_EALIGN, "grads[%d] not aligned to %d bytes", r, es);
+    if (ph == -2) ph = q;
+    else if (ph != q) same = false;
+    a.grads[r] = grads[r];
+    if (n > 0) rs.push_back({uintptr_t(grads[r]), uintptr_t(grads[r]) + uintptr_t(n) * es, "a gradient"});
+  }
+  if (int e = check_disjoint(rs)) return e;
+  if (n == 0) return ZERO_OK;
+  a.sp = make_split(0, n, same, ph, es == 2 ? 8 : 4);
+  cudaError_t e = zk::launch_allreduce(a, es == 2, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "ddp_allreduce_mean kernel launch");
+  return ZERO_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,72 @@
+// Internal interface between the host library (zero_host.cpp) and the CUDA
+// kernels (zero_kernels.cu). Not part of the public C ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "zero_gb300.h"
+
+namespace zk {
+
+constexpr int kMaxRanks = ZERO_MAX_RANKS;
+
+// A contiguous index range [lo, lo + head + nvec*V + tail) split into a scalar
+// head (up to the first index where every buffer is 16-byte aligned), nvec
+// V-element vector units, and a scalar tail. When the buffers do not share a
+// 16-byte phase the whole range is the head (nvec = tail = 0).
+struct Split {
+  int64_t lo;
+  int64_t head;
+  int64_t nvec;
+  int64_t tail;
+};
+
+// Per-step float32 constants, formed in double on the host and rounded once.
+struct AdamConsts {
+  float decay;  // 1 - lr*wd
+  float b1;     // beta1
+  float omb1;   // 1 - beta1
+  float b2;     // beta2
+  float omb2;   // 1 - beta2
+  float step;   // lr / (1 - beta1^t)
+  float bc2s;   // sqrt(1 - beta2^t)
+  float eps;
+};
+
+// Kernel argument block of the fused step (passed by value as a
+// __grid_constant__ parameter; about 1.7 KB).
+struct StepArgs {
+  const void* grads[kMaxRanks];  // N gradient buffers (float or bf16)
+  void* reps[kMaxRanks];         // N parameter replicas (float or bf16)
+  int64_t bounds[kMaxRanks + 1]; // shard offsets a_0..a_N (owner lookup)
+  float* m;                      // flat fp32 state, global index order
+  float* v;
+  float* master;                 // mixed precision only
+  Split sp;
+  int32_t N;
+  float fN;                      // (float)N
+  AdamConsts c;
+};
+
+struct AllreduceArgs {
+  void* grads[kMaxRanks];
+  Split sp;
+  int32_t N;
+  float fN;
+};
+
+struct InitArgs {
+  float* m;
+  float* v;
+  float* master;       // NULL in fp32
+  const float* init;   // NULL in fp32
+  Split sp;
+};
+
+// Launchers (zero_kernels.cu). Each returns the launch status.
+cudaError_t launch_step(const StepArgs& a, bool mixed, cudaStream_t s);
+cudaError_t launch_allreduce(const AllreduceArgs& a, bool bf16, cudaStream_t s);
+cudaError_t launch_init(const InitArgs& a, cudaStream_t s);
+
+}  // namespace zk

@@ -1,0 +1,454 @@
+// CUDA kernels (sm_103a) of the ZeRO step over N simulated ranks in one HBM.
+//
+// The fused step does, per index j and in one pass over memory:
+//   reduce-scatter-mean  g = (sum_r g_r[j]) / N             (rank order 0..N-1)
+//   AdamW on the shard   p, m, v -> p', m', v'              (owner's state)
+//   all-gather           replica_r[j] = p' for every r      (bf16: RNE(p'))
+// ("ZeRO-Sharded Adam Step", section "The step"; "Data parallelism and ZeRO
+// stages 1 to 3", section 2, stages 1 and 2). The state is flat in global
+// index order, so the shard structure only decides whose replica holds the
+// authoritative fp32 parameter (the owner's) -- never the arithmetic.
+//
+// The step moves 8N+20 bytes per parameter in fp32 (4N+24 in mixed precision)
+// and does ~20 flops per parameter: it is bound by HBM bandwidth. Design:
+//  * 16-byte vector loads/stores, one V-element unit per thread per iteration
+//    (V = 4 fp32, V = 8 mixed: one uint4 of bf16 + two float4 of state);
+//  * every load of a unit is issued before any arithmetic, so a thread keeps
+//    (N+3) 16-byte requests in flight; streaming cache hints (ld/st .cs) since
+//    every byte is touched exactly once per step;
+//  * grid-stride loop over units with a grid of (SMs x resident blocks);
+//  * a scalar head/tail for ranges whose ends are not on a unit boundary, and
+//    a scalar path for buffers that do not share a 16-byte phase;
+//  * arithmetic with explicitly rounded IEEE fp32 intrinsics (__fadd_rn,
+//    __fmul_rn, __fdiv_rn, __fsqrt_rn): no contraction, so the result is
+//    independent of compiler scheduling and bit-reproducible.
+// No tensor cores: there is no contraction in this step.
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "zero_internal.h"
+
+namespace zk {
+namespace {
+
+constexpr int kThreads = 256;
+
+// ----------------------------------------------------------- memory helpers --
+
+__device__ __forceinline__ float4 ld4(const float* p) {
+  return __ldcs(reinterpret_cast<const float4*>(p));
+}
+__device__ __forceinline__ uint4 ld8h(const uint16_t* p) {
+  return __ldcs(reinterpret_cast<const uint4*>(p));
+}
+__device__ __forceinline__ void st4(float* p, float4 x) {
+  __stcs(reinterpret_cast<float4*>(p), x);
+}
+__device__ __forceinline__ void st8h(uint16_t* p, uint4 x) {
+  __stcs(reinterpret_cast<uint4*>(p), x);
+}
+
+// bf16 <-> fp32. Widening is exact (the bf16 bits are the top half of the
+// fp32 bits); narrowing uses CUDA's round-to-nearest-even conversion.
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+__device__ __forceinline__ float bf_one(uint16_t h) { return __uint_as_float(uint32_t(h) << 16); }
+__device__ __forceinline__ uint32_t pack_bf2(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+__device__ __forceinline__ uint16_t to_bf(float x) {
+  return __bfloat16_as_ushort(__float2bfloat16_rn(x));
+}
+
+__device__ __forceinline__ void unpack8(uint4 w, float (&f)[8]) {
+  f[0] = bf_lo(w.x); f[1] = bf_hi(w.x);
+  f[2] = bf_lo(w.y); f[3] = bf_hi(w.y);
+  f[4] = bf_lo(w.z); f[5] = bf_hi(w.z);
+  f[6] = bf_lo(w.w); f[7] = bf_hi(w.w);
+}
+__device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
+  return make_uint4(pack_bf2(f[0], f[1]), pack_bf2(f[2], f[3]), pack_bf2(f[4], f[5]),
+                    pack_bf2(f[6], f[7]));
+}
+
+// ----------------------------------------------------------------- the math --
+
+// Divide the rank-ordered sum by N. For a power-of-two N the product with 1/N
+// is the same correctly rounded value as the quotient, so it is used instead.
+template <int NR>
+__device__ __forceinline__ float mean_of(float s, float fN) {
+  if constexpr (NR > 0 && (NR & (NR - 1)) == 0) {
+    return __fmul_rn(s, 1.0f / float(NR));
+  } else {
+    return __fdiv_rn(s, fN);
+  }
+}
+
+// One AdamW element: decoupled decay, moments, bias-corrected update.
+__device__ __forceinline__ void adam1(const AdamConsts& c, float g, float& p, float& m,
+                                      float& v) {
+  p = __fmul_rn(p, c.decay);
+  m = __fadd_rn(__fmul_rn(c.b1, m), __fmul_rn(c.omb1, g));
+  v = __fadd_rn(__fmul_rn(c.b2, v), __fmul_rn(c.omb2, __fmul_rn(g, g)));
+  const float d = __fadd_rn(__fdiv_rn(__fsqrt_rn(v), c.bc2s), c.eps);
+  p = __fsub_rn(p, __fmul_rn(c.step, __fdiv_rn(m, d)));
+}
+
+template <int NR>
+__device__ __forceinline__ int ranks(const StepArgs& P) {
+  return NR > 0 ? NR : P.N;
+}
+
+// Owner of index j, advanced monotonically from `owner` (j never decreases
+// along one thread's iterations). bounds[N] = n > j stops the scan.
+__device__ __forceinline__ int advance_owner(const StepArgs& P, int owner, int64_t j) {
+  while (j >= P.bounds[owner + 1]) ++owner;
+  return owner;
+}
+
+// ------------------------------------------------------- scalar element path --
+
+template <int NR, bool MIXED>
+__device__ __forceinline__ void step_scalar(const StepArgs& P, int64_t j, int owner) {
+  const int N = ranks<NR>(P);
+  float s, p, m, v;
+  if constexpr (MIXED) {
+    s = bf_one(__ldcs(static_cast<const uint16_t*>(P.grads[0]) + j));
+    for (int r = 1; r < N; ++r)
+      s = __fadd_rn(s, bf_one(__ldcs(static_cast<const uint16_t*>(P.grads[r]) + j)));
+    p = __ldcs(P.master + j);
+  } else {
+    s = __ldcs(static_cast<const float*>(P.grads[0]) + j);
+    for (int r = 1; r < N; ++r) s = __fadd_rn(s, __ldcs(static_cast<const float*>(P.grads[r]) + j));
+    p = __ldcs(static_cast<const float*>(P.reps[owner]) + j);
+  }
+  m = __ldcs(P.m + j);
+  v = __ldcs(P.v + j);
+  const float g = mean_of<NR>(s, P.fN);
+  adam1(P.c, g, p, m, v);
+  __stcs(P.m + j, m);
+  __stcs(P.v + j, v);
+  if constexpr (MIXED) {
+    __stcs(P.master + j, p);
+    const uint16_t h = to_bf(p);
+    for (int r = 0; r < N; ++r) __stcs(static_cast<uint16_t*>(P.reps[r]) + j, h);
+  } else {
+    for (int r = 0; r < N; ++r) __stcs(static_cast<float*>(P.reps[r]) + j, p);
+  }
+}
+
+// ------------------------------------------------------- fp32 vector path (V=4)
+
+template <int NR>
+__device__ __forceinline__ void step_vec_fp32(const StepArgs& P, int64_t j, int owner) {
+  const int N = ranks<NR>(P);
+  // Loads first: parameter, state, then every rank's gradient.
+  float4 p;
+  if (j + 3 < P.bounds[owner + 1]) {
+    p = ld4(static_cast<const float*>(P.reps[owner]) + j);
+  } else {  // the unit straddles a shard boundary: per-element owners
+    float e[4];
+    int o = owner;
+    for (int k = 0; k < 4; ++k) {
+      o = advance_owner(P, o, j + k);
+      e[k] = __ldcs(static_cast<const float*>(P.reps[o]) + j + k);
+    }
+    p = make_float4(e[0], e[1], e[2], e[3]);
+  }
+  float4 m = ld4(P.m + j);
+  float4 v = ld4(P.v + j);
+  float4 s;
+  if constexpr (NR > 0) {
+    float4 g[NR];
+#pragma unroll
+    for (int r = 0; r < NR; ++r) g[r] = ld4(static_cast<const float*>(P.grads[r]) + j);
+    s = g[0];
+#pragma unroll
+    for (int r = 1; r < NR; ++r) {
+      s.x = __fadd_rn(s.x, g[r].x); s.y = __fadd_rn(s.y, g[r].y);
+      s.z = __fadd_rn(s.z, g[r].z); s.w = __fadd_rn(s.w, g[r].w);
+    }
+  } else {
+    s = ld4(static_cast<const float*>(P.grads[0]) + j);
+#pragma unroll 4
+    for (int r = 1; r < N; ++r) {
+      const float4 g = ld4(static_cast<const float*>(P.grads[r]) + j);
+      s.x = __fadd_rn(s.x, g.x); s.y = __fadd_rn(s.y, g.y);
+      s.z = __fadd_rn(s.z, g.z); s.w = __fadd_rn(s.w, g.w);
+    }
+  }
+  adam1(P.c, mean_of<NR>(s.x, P.fN), p.x, m.x, v.x);
+  adam1(P.c, mean_of<NR>(s.y, P.fN), p.y, m.y, v.y);
+  adam1(P.c, mean_of<NR>(s.z, P.fN), p.z, m.z, v.z);
+  adam1(P.c, mean_of<NR>(s.w, P.fN), p.w, m.w, v.w);
+  st4(P.m + j, m);
+  st4(P.v + j, v);
+  if constexpr (NR > 0) {
+#pragma unroll
+    for (int r = 0; r < NR; ++r) st4(static_cast<float*>(P.reps[r]) + j, p);
+  } else {
+    for (int r = 0; r < N; ++r) st4(static_cast<float*>(P.reps[r]) + j, p);
+  }
+}
+
+// ------------------------------------------------------ mixed vector path (V=8)
+
+template <int NR>
+__device__ __forceinline__ void step_vec_mixed(const StepArgs& P, int64_t j) {
+  const int N = ranks<NR>(P);
+  const float4 p0 = ld4(P.master + j), p1 = ld4(P.master + j + 4);
+  const float4 m0 = ld4(P.m + j), m1 = ld4(P.m + j + 4);
+  const float4 v0 = ld4(P.v + j), v1 = ld4(P.v + j + 4);
+  float s[8];
+  if constexpr (NR > 0) {
+    uint4 w[NR];
+#pragma unroll
+    for (int r = 0; r < NR; ++r) w[r] = ld8h(static_cast<const uint16_t*>(P.grads[r]) + j);
+    unpack8(w[0], s);
+#pragma unroll
+    for (int r = 1; r < NR; ++r) {
+      float f[8];
+      unpack8(w[r], f);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) s[k] = __fadd_rn(s[k], f[k]);
+    }
+  } else {
+    unpack8(ld8h(static_cast<const uint16_t*>(P.grads[0]) + j), s);
+#pragma unroll 4
+    for (int r = 1; r < N; ++r) {
+      float f[8];
+      unpack8(ld8h(static_cast<const uint16_t*>(P.grads[r]) + j), f);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) s[k] = __fadd_rn(s[k], f[k]);
+    }
+  }
+  float p[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+  float m[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
+  float v[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+  for (int k = 0; k < 8; ++k) adam1(P.c, mean_of<NR>(s[k], P.fN), p[k], m[k], v[k]);
+  st4(P.master + j, make_float4(p[0], p[1], p[2], p[3]));
+  st4(P.master + j + 4, make_float4(p[4], p[5], p[6], p[7]));
+  st4(P.m + j, make_float4(m[0], m[1], m[2], m[3]));
+  st4(P.m + j + 4, make_float4(m[4], m[5], m[6], m[7]));
+  st4(P.v + j, make_float4(v[0], v[1], v[2], v[3]));
+  st4(P.v + j + 4, make_float4(v[4], v[5], v[6], v[7]));
+  const uint4 h = pack8(p);
+  if constexpr (NR > 0) {
+#pragma unroll
+    for (int r = 0; r < NR; ++r) st8h(static_cast<uint16_t*>(P.reps[r]) + j, h);
+  } else {
+    for (int r = 0; r < N; ++r) st8h(static_cast<uint16_t*>(P.reps[r]) + j, h);
+  }
+}
+
+// ------------------------------------------------------------------ kernels --
+
+template <int NR, bool MIXED>
+__global__ void __launch_bounds__(kThreads) zero_step_kernel(const __grid_constant__ StepArgs P) {
+  constexpr int V = MIXED ? 8 : 4;
+  const int64_t tid = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+  const Split& sp = P.sp;
+
+  // Scalar head and tail (a handful of elements, or the whole range when the
+  // buffers do not share a 16-byte phase). j grows with s, so the owner scan
+  // only moves forward.
+  const int64_t nscalar = sp.head + sp.tail;
+  if (tid < nscalar) {
+    const int64_t body_end = sp.lo + sp.head + sp.nvec * V;
+    int owner = 0;
+    for (int64_t s = tid; s < nscalar; s += stride) {
+      const int64_t j = s < sp.head ? sp.lo + s : body_end + (s - sp.head);
+      owner = advance_owner(P, owner, j);
+      step_scalar<NR, MIXED>(P, j, owner);
+    }
+  }
+
+  // Vector body.
+  const int64_t base = sp.lo + sp.head;
+  int owner = 0;
+  for (int64_t u = tid; u < sp.nvec; u += stride) {
+    const int64_t j = base + u * V;
+    if constexpr (MIXED) {
+      step_vec_mixed<NR>(P, j);
+    } else {
+      owner = advance_owner(P, owner, j);
+      step_vec_fp32<NR>(P, j, owner);
+    }
+  }
+}
+
+template <int NR, bool BF16>
+__global__ void __launch_bounds__(kThreads)
+    allreduce_mean_kernel(const __grid_constant__ AllreduceArgs P) {
+  constexpr int V = BF16 ? 8 : 4;
+  const int N = NR > 0 ? NR : P.N;
+  const int64_t tid = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+  const Split& sp = P.sp;
+
+  const int64_t nscalar = sp.head + sp.tail;
+  const int64_t body_end = sp.lo + sp.head + sp.nvec * V;
+  for (int64_t s = tid; s < nscalar; s += stride) {
+    const int64_t j = s < sp.head ? sp.lo + s : body_end + (s - sp.head);
+    float acc;
+    if constexpr (BF16) {
+      acc = bf_one(__ldcs(static_cast<const uint16_t*>(P.grads[0]) + j));
+      for (int r = 1; r < N; ++r)
+        acc = __fadd_rn(acc, bf_one(__ldcs(static_cast<const uint16_t*>(P.grads[r]) + j)));
+      const uint16_t h = to_bf(mean_of<NR>(acc, P.fN));
+      for (int r = 0; r < N; ++r) __stcs(static_cast<uint16_t*>(P.grads[r]) + j, h);
+    } else {
+      acc = __ldcs(static_cast<const float*>(P.grads[0]) + j);
+      for (int r = 1; r < N; ++r)
+        acc = __fadd_rn(acc, __ldcs(static_cast<const float*>(P.grads[r]) + j));
+      const float g = mean_of<NR>(acc, P.fN);
+      for (int r = 0; r < N; ++r) __stcs(static_cast<float*>(P.grads[r]) + j, g);
+    }
+  }
+
+  const int64_t base = sp.lo + sp.head;
+  for (int64_t u = tid; u < sp.nvec; u += stride) {
+    const int64_t j = base + u * V;
+    if constexpr (BF16) {
+      float s[8];
+      unpack8(ld8h(static_cast<const uint16_t*>(P.grads[0]) + j), s);
+#pragma unroll 4
+      for (int r = 1; r < N; ++r) {
+        float f[8];
+        unpack8(ld8h(static_cast<const uint16_t*>(P.grads[r]) + j), f);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) s[k] = __fadd_rn(s[k], f[k]);
+      }
+#pragma unroll
+      for (int k = 0; k < 8; ++k) s[k] = mean_of<NR>(s[k], P.fN);
+      const uint4 h = pack8(s);
+      for (int r = 0; r < N; ++r) st8h(static_cast<uint16_t*>(P.grads[r]) + j, h);
+    } else {
+      float4 s = ld4(static_cast<const float*>(P.grads[0]) + j);
+#pragma unroll 4
+      for (int r = 1; r < N; ++r) {
+        const float4 g = ld4(static_cast<const float*>(P.grads[r]) + j);
+        s.x = __fadd_rn(s.x, g.x); s.y = __fadd_rn(s.y, g.y);
+        s.z = __fadd_rn(s.z, g.z); s.w = __fadd_rn(s.w, g.w);
+      }
+      s.x = mean_of<NR>(s.x, P.fN); s.y = mean_of<NR>(s.y, P.fN);
+      s.z = mean_of<NR>(s.z, P.fN); s.w = mean_of<NR>(s.w, P.fN);
+      for (int r = 0; r < N; ++r) st4(static_cast<float*>(P.grads[r]) + j, s);
+    }
+  }
+}
+
+// m = v = 0 and (mixed) master = init over the split range.
+__global__ void __launch_bounds__(kThreads) init_state_kernel(const __grid_constant__ InitArgs P) {
+  const int64_t tid = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+  const Split& sp = P.sp;
+  const int64_t nscalar = sp.head + sp.tail;
+  const int64_t body_end = sp.lo + sp.head + sp.nvec * 4;
+  for (int64_t s = tid; s < nscalar; s += stride) {
+    const int64_t j = s < sp.head ? sp.lo + s : body_end + (s - sp.head);
+    P.m[j] = 0.0f;
+    P.v[j] = 0.0f;
+    if (P.master) P.master[j] = P.init[j];
+  }
+  const int64_t base = sp.lo + sp.head;
+  const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int64_t u = tid; u < sp.nvec; u += stride) {
+    const int64_t j = base + u * 4;
+    st4(P.m + j, z);
+    st4(P.v + j, z);
+    if (P.master) st4(P.master + j, ld4(P.init + j));
+  }
+}
+
+// ------------------------------------------------------------ grid sizing --
+
+struct DevInfo {
+  int sms = 0;
+};
+
+int sm_count() {
+  static int cached[kMaxRanks * 2] = {0};  // indexed by device ordinal
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (dev < 0 || dev >= int(sizeof(cached) / sizeof(cached[0]))) return 0;
+  if (cached[dev] == 0) {
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    cached[dev] = sms;
+  }
+  return cached[dev];
+}
+
+// Blocks for `work` thread-iterations: enough to cover it, at most the number
+// of blocks resident at once on the whole GPU (a persistent-style grid).
+template <typename K>
+cudaError_t grid_for(K kernel, int64_t work, int* blocks) {
+  int sms = sm_count();
+  if (sms <= 0) return cudaErrorInvalidDevice;
+  int per_sm = 0;
+  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, 0);
+  if (e != cudaSuccess) return e;
+  if (per_sm < 1) per_sm = 1;
+  const int64_t cap = int64_t(sms) * per_sm;
+  int64_t need = (work + kThreads - 1) / kThreads;
+  if (need < 1) need = 1;
+  *blocks = int(need < cap ? need : cap);
+  return cudaSuccess;
+}
+
+template <typename K, typename A>
+cudaError_t launch(K kernel, const A& args, int64_t work, cudaStream_t s) {
+  int blocks = 0;
+  cudaError_t e = grid_for(kernel, work, &blocks);
+  if (e != cudaSuccess) return e;
+  kernel<<<blocks, kThreads, 0, s>>>(args);
+  return cudaGetLastError();
+}
+
+template <bool MIXED>
+cudaError_t launch_step_t(const StepArgs& a, cudaStream_t s) {
+  const int64_t work = a.sp.nvec > a.sp.head + a.sp.tail ? a.sp.nvec : a.sp.head + a.sp.tail;
+  switch (a.N) {
+    case 1: return launch(zero_step_kernel<1, MIXED>, a, work, s);
+    case 2: return launch(zero_step_kernel<2, MIXED>, a, work, s);
+    case 3: return launch(zero_step_kernel<3, MIXED>, a, work, s);
+    case 4: return launch(zero_step_kernel<4, MIXED>, a, work, s);
+    case 8: return launch(zero_step_kernel<8, MIXED>, a, work, s);
+    default: return launch(zero_step_kernel<0, MIXED>, a, work, s);
+  }
+}
+
+template <bool BF16>
+cudaError_t launch_allreduce_t(const AllreduceArgs& a, cudaStream_t s) {
+  const int64_t work = a.sp.nvec > a.sp.head + a.sp.tail ? a.sp.nvec : a.sp.head + a.sp.tail;
+  switch (a.N) {
+    case 1: return launch(allreduce_mean_kernel<1, BF16>, a, work, s);
+    case 2: return launch(allreduce_mean_kernel<2, BF16>, a, work, s);
+    case 4: return launch(allreduce_mean_kernel<4, BF16>, a, work, s);
+    case 8: return launch(allreduce_mean_kernel<8, BF16>, a, work, s);
+    default: return launch(allreduce_mean_kernel<0, BF16>, a, work, s);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_step(const StepArgs& a, bool mixed, cudaStream_t s) {
+  return mixed ? launch_step_t<true>(a, s) : launch_step_t<false>(a, s);
+}
+
+cudaError_t launch_allreduce(const AllreduceArgs& a, bool bf16, cudaStream_t s) {
+  return bf16 ? launch_allreduce_t<true>(a, s) : launch_allreduce_t<false>(a, s);
+}
+
+cudaError_t launch_init(const InitArgs& a, cudaStream_t s) {
+  const int64_t work = a.sp.nvec > a.sp.head + a.sp.tail ? a.sp.nvec : a.sp.head + a.sp.tail;
+  return launch(init_state_kernel, a, work, s);
+}
+
+}  // namespace zk

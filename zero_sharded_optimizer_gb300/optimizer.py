@@ -1,0 +1,107 @@
+"""User-facing ZeRO optimizer over N simulated data-parallel ranks on one GPU.
+
+Wraps the C ABI: allocates the flat state (m, v, and the fp32 master in mixed
+precision) with PyTorch, keeps the step counter, and runs one fused step per
+call. Gradients may be CUDA tensors, or host tensors (ideally pinned) that are
+copied into device staging buffers on the step's stream first.
+
+Checkpoint/resume: ``state_dict()`` / ``load_state_dict()`` copy the flat
+state and the step counter; continuing from a loaded state is bit-identical
+to an uninterrupted run because the step is a pure function of (state, grads).
+"""
+
+from __future__ import annotations
+
+import torch
+
+from . import abi
+
+BUCKET_BYTES_25MIB = 25 * 1024 * 1024
+
+
+class ZeroOptimizer:
+    def __init__(self, n: int, N: int, precision: int = abi.ZERO_FP32, lr: float = 1e-3,
+                 betas=(0.9, 0.999), eps: float = 1e-8, weight_decay: float = 0.0,
+                 master_init: torch.Tensor | None = None, device="cuda", stream=None):
+        self.n, self.N, self.precision = int(n), int(N), int(precision)
+        self.lr, self.beta1, self.beta2 = float(lr), float(betas[0]), float(betas[1])
+        self.eps, self.weight_decay = float(eps), float(weight_decay)
+        self.device = torch.device(device)
+        f32 = dict(dtype=torch.float32, device=self.device)
+        self.m = torch.empty(self.n, **f32)
+        self.v = torch.empty(self.n, **f32)
+        self.master = None
+        if self.precision == abi.ZERO_BF16_MIXED:
+            if master_init is None:
+                raise ValueError("mixed precision needs the fp32 initial weights (master_init)")
+            self.master = torch.empty(self.n, **f32)
+            master_init = master_init.to(self.device, torch.float32).contiguous()
+        self.states = abi.zero_init_states(self.n, self.N, self.precision, self.m, self.v,
+                                           self.master, master_init, stream)
+        self.t = 0
+        self._staging = None
+
+    # ------------------------------------------------------------------ step --
+
+    def _device_grads(self, grads, stream):
+        if all(g.is_cuda for g in grads):
+            return grads
+        dt = torch.bfloat16 if self.precision == abi.ZERO_BF16_MIXED else torch.float32
+        if self._staging is None:
+            self._staging = [torch.empty(self.n, dtype=dt, device=self.device)
+                             for _ in range(self.N)]
+        s = stream if stream is not None else torch.cuda.current_stream(self.device)
+        with torch.cuda.stream(s):
+            for dst, src in zip(self._staging, grads):
+                dst.copy_(src, non_blocking=True)
+        return self._staging
+
+    def step(self, params, grads, stream=None) -> int:
+        """One ZeRO step; returns the new step number t."""
+        g = self._device_grads(grads, stream)
+        abi.zero_step(params, g, self.states, self.t + 1, self.lr, self.beta1, self.beta2,
+                      self.eps, self.weight_decay, stream)
+        self.t += 1
+        return self.t
+
+    def step_bucketed(self, params, grads, ready=None, side=None,
+                      bucket_bytes: int = BUCKET_BYTES_25MIB, done=None,
+                      timeout_ms: int = -1) -> int:
+        """The step bucket by bucket on ``side``, each after its ``ready`` event."""
+        try:
+            abi.zero_step_bucketed(params, grads, self.states, self.t + 1, self.lr, self.beta1,
+                                   self.beta2, self.eps, self.weight_decay, bucket_bytes, ready,
+                                   side, done, timeout_ms)
+        except abi.ZeroError as e:
+            if e.code == abi.ZERO_ETIMEDOUT:
+                self.t += 1          # the work is queued and will complete
+            raise
+        self.t += 1
+        return self.t
+
+    def bucket_ranges(self, bucket_bytes: int = BUCKET_BYTES_25MIB) -> list:
+        count = abi.zero_bucket_count(self.n, self.precision, bucket_bytes)
+        return [abi.zero_bucket_range(self.n, self.precision, bucket_bytes, k)
+                for k in range(count)]
+
+    # --------------------------------------------------------------- memory --
+
+    def memory_bytes(self, stage: int, rank: int | None = None):
+        if rank is None:
+            return abi.zero_memory_bytes(self.n, self.N, stage, self.precision)
+        return abi.zero_memory_breakdown(self.n, self.N, stage, self.precision, rank)
+
+    # ------------------------------------------------------- checkpointing --
+
+    def state_dict(self) -> dict:
+        d = {"t": self.t, "m": self.m.clone(), "v": self.v.clone()}
+        if self.master is not None:
+            d["master"] = self.master.clone()
+        return d
+
+    def load_state_dict(self, d: dict) -> None:
+        self.t = int(d["t"])
+        self.m.copy_(d["m"])
+        self.v.copy_(d["v"])
+        if self.master is not None:
+            self.master.copy_(d["master"])
