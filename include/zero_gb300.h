@@ -21,6 +21,8 @@
  *    at least naturally aligned. Buffers sharing one 16-byte phase (the usual
  *    case: separate allocations) take the 16-byte vector path; any other
  *    layout is still correct, on a slower 4-/2-byte path.
+ *  - With n == 0 nothing is read or written and NULL buffer pointers are
+ *    accepted (the host arrays of pointers must still be non-NULL).
  *  - The caller owns every device buffer. The library never allocates device
  *    memory; zero_init_states allocates only a small host handle.
  *  - Device work is queued on the caller's stream (zero_stream_t is a

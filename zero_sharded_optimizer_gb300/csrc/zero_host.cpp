@@ -143,7 +143,8 @@ int prepare_step(void* const* params, const void* const* grads, const zero_state
     return true;
   };
   for (int32_t r = 0; r < N; ++r) {
-    if (!params[r] || !grads[r]) return fail(ZERO_EINVAL, "params[%d] or grads[%d] is NULL", r, r);
+    if (st->n > 0 && (!params[r] || !grads[r]))
+      return fail(ZERO_EINVAL, "params[%d] or grads[%d] is NULL", r, r);
     a->reps[r] = params[r];
     a->grads[r] = grads[r];
     int* ph = mixed ? &ph16 : &ph32;
@@ -295,9 +296,9 @@ int zero_init_states(int64_t n, int32_t N, int32_t precision, float* m, float* v
   if (!valid_ranks(N)) return fail(ZERO_EINVAL, "N=%d outside [1, %d]", N, ZERO_MAX_RANKS);
   if (precision != ZERO_FP32 && precision != ZERO_BF16_MIXED)
     return fail(ZERO_EINVAL, "state precision must be FP32 or BF16_MIXED");
-  if (!m || !v) return fail(ZERO_EINVAL, "m or v is NULL");
+  if (n > 0 && (!m || !v)) return fail(ZERO_EINVAL, "m or v is NULL");
   const bool mixed = precision == ZERO_BF16_MIXED;
-  if (mixed && (!master || !master_init))
+  if (mixed && n > 0 && (!master || !master_init))
     return fail(ZERO_EINVAL, "mixed precision needs master and master_init");
   if (!mixed && (master || master_init))
     return fail(ZERO_EINVAL, "fp32 state takes no master buffer");
@@ -483,7 +484,7 @@ int ddp_allreduce_mean(void* const* grads, int64_t n, int32_t N, int32_t precisi
   bool same = true;
   std::vector<Range> rs;
   for (int32_t r = 0; r < N; ++r) {
-    if (!grads[r]) return fail(ZERO_EINVAL, "grads[%d] is NULL", r);
+    if (n > 0 && !grads[r]) return fail(ZERO_EINVAL, "grads[%d] is NULL", r);
     const int q = phase_of(grads[r], es);
     if (q < 0) return fail(ZERO_EALIGN, "grads[%d] not aligned to %d bytes", r, es);
     if (ph == -2) ph = q;
