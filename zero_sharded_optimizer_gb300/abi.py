@@ -125,6 +125,14 @@ def _stream(stream) -> int | None:
     return int(stream)
 
 
+def _event_to_record(ev) -> int | None:
+    """Handle of an event the library will record. torch creates the CUDA event
+    on its first record, so a fresh event is recorded once here to exist."""
+    if isinstance(ev, torch.cuda.Event) and not ev.cuda_event:
+        ev.record()
+    return _event(ev)
+
+
 def _event(ev) -> int | None:
     if ev is None:
         return None
@@ -270,7 +278,7 @@ def zero_step_bucketed(params, grads, st: ZeroStates, t: int, lr: float, beta1: 
         arr = (_vp * len(ready))(*[_event(e) for e in ready])
         count = len(ready)
     _check(_lib.zero_step_bucketed(pp, gp, st.handle, t, lr, beta1, beta2, eps, weight_decay,
-                                   bucket_bytes, arr, count, _stream(side), _event(done),
+                                   bucket_bytes, arr, count, _stream(side), _event_to_record(done),
                                    timeout_ms), "zero_step_bucketed")
 
 
