@@ -205,6 +205,26 @@ int zero_memory_bytes(int64_t n, int32_t N, int32_t stage, int32_t precision, ui
 int zero_memory_breakdown(int64_t n, int32_t N, int32_t stage, int32_t precision,
                           int32_t rank, uint64_t out[3]);
 
+/* ---------------------------------------------------------------- health -- */
+
+/* Status bits a kernel may set on the device.
+ * ZERO_STATUS_WAIT_TIMEOUT: a bounded wait of a bulk-copy pipeline on its own
+ * copies ran out (after 2 s by default); that kernel stopped early, so the
+ * outputs of the call that launched it are incomplete. */
+enum { ZERO_STATUS_WAIT_TIMEOUT = 1 };
+
+/* Read the sticky device status word of the current device into *status (0:
+ * nothing happened) and clear it when `clear` is non-zero. Synchronizes the
+ * current device. Errors: EINVAL (NULL), ECUDA. */
+int zero_device_status(uint32_t *status, int32_t clear);
+
+/* Test hook: bound of every device-side wait of later launches, in
+ * nanoseconds (0 restores the default of 2 s). A tiny bound makes the
+ * pipeline give up on its first wait, which exercises the timeout path
+ * (status bit, bounded drain of its own copies, early return) without any
+ * fault. Process-wide; not for production use. Always returns ZERO_OK. */
+int zero_debug_set_wait_timeout_ns(uint64_t ns);
+
 /* ---------------------------------------------------------------- errors -- */
 
 /* Static description of a status code (never NULL). */

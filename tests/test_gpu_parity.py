@@ -121,7 +121,8 @@ class Case:
 
 
 GRID = [(1, 1), (5, 2), (7, 3), (33, 4), (4099, 5), (4099, 8), (100_003, 1), (100_003, 2),
-        (100_003, 3), (100_003, 4), (100_003, 8), (65_537, 13), (1_000_003, 4), (1_000_003, 8)]
+        (100_003, 3), (100_003, 4), (100_003, 8), (65_537, 13), (1_000_003, 4), (1_000_003, 8),
+        (300_007, 5), (300_007, 6), (300_007, 7), (2_000_000, 2)]
 
 
 @pytest.mark.parametrize("prec", [oracle.FP32, oracle.BF16_MIXED])
@@ -335,7 +336,7 @@ def test_bucketed_deadline_reports_timeout(abi, cuda):
 
 @pytest.mark.parametrize("prec", [oracle.FP32, oracle.BF16_MIXED])
 @pytest.mark.parametrize("n,N", [(1, 1), (9, 2), (4099, 3), (100_003, 4), (100_003, 8),
-                                 (65_537, 13)])
+                                 (65_537, 13), (1_000_003, 5), (1_000_003, 6), (1_000_003, 7)])
 def test_ddp_allreduce_mean(abi, cuda, n, N, prec):
     rng = np.random.default_rng(n + N)
     mixed = prec == oracle.BF16_MIXED
@@ -396,3 +397,65 @@ def test_optimizer_host_gradients_match_device(abi, cuda):
     b.step(pb, [h.to(cuda) for h in host])
     torch.cuda.synchronize()
     assert all(torch.equal(x, y) for x, y in zip(pa, pb))
+
+
+@pytest.mark.parametrize("prec", [oracle.FP32, oracle.BF16_MIXED])
+def test_pipeline_wait_timeout_is_reported_and_recoverable(abi, cuda, prec):
+    """A 1 ns bound on the bulk-copy waits makes every pipeline give up at its
+    first wait: the kernel records ZERO_STATUS_WAIT_TIMEOUT, drains its own
+    copies and returns. The context stays usable and later steps are exact."""
+    c = Case(abi, cuda, 2_000_003, 4, prec, seed=41)
+    c.new_grads()
+    torch.cuda.synchronize()
+    abi.zero_device_status(clear=True)
+    abi.zero_debug_set_wait_timeout_ns(1)
+    try:
+        c.t = 1
+        c.gpu_step()
+        dev = [g.clone() for g in c.grads]
+        abi.ddp_allreduce_mean(dev, prec)
+        status = abi.zero_device_status(clear=True)
+    finally:
+        abi.zero_debug_set_wait_timeout_ns(0)
+    assert status & abi.ZERO_STATUS_WAIT_TIMEOUT
+    assert abi.zero_device_status() == 0
+    d = Case(abi, cuda, 2_000_003, 4, prec, seed=42)
+    for _ in range(2):
+        d.step()
+        d.compare(exact=True)
+    assert abi.zero_device_status() == 0
+
+
+@pytest.mark.parametrize("prec", [oracle.FP32, oracle.BF16_MIXED])
+def test_zero_and_subnormal_state_bitwise(abi, cuda, prec):
+    """m and v at exact zero, in the subnormal range and just above it (what
+    zero gradients decay them into), stepped with zero and tiny gradients:
+    bit-exact against the oracle."""
+    n, N = 300_007, 4
+    c = Case(abi, cuda, n, N, prec, seed=51)
+    rng = np.random.default_rng(52)
+    kind = rng.integers(0, 4, n)
+    u = rng.uniform(-1, 1, n)
+    m = np.select([kind == 0, kind == 1, kind == 2], [0.0, u * 1e-40, u * 1e-37],
+                  rng.normal(0, 1e-3, n)).astype(np.float32)
+    v = np.select([kind == 0, kind == 1, kind == 2], [0.0, np.abs(u) * 1e-40, np.abs(u) * 1e-37],
+                  rng.uniform(0, 1e-6, n)).astype(np.float32)
+    assert np.any((m != 0) & (np.abs(m) < np.finfo(np.float32).tiny))
+    c.m.copy_(torch.from_numpy(m))
+    c.v.copy_(torch.from_numpy(v))
+    b = oracle.shard_bounds(n, N)
+    for i in range(N):
+        c.o_states[i]["m"] = m[b[i]:b[i + 1]].copy()
+        c.o_states[i]["v"] = v[b[i]:b[i + 1]].copy()
+    for t in range(2):
+        hs = []
+        for r in range(N):
+            g = np.where(kind < 2, 0.0, rng.normal(0, 1e-20, n)).astype(np.float32)
+            if c.mixed:
+                g = oracle.f32_to_bf16_rne(g)
+            hs.append(g)
+            c.grads[r].copy_(to_dev(g, c.dt, cuda))
+        c.oracle_step(hs)
+        c.gpu_step()
+        torch.cuda.synchronize()
+        c.compare(exact=True)

@@ -39,6 +39,7 @@ ZERO_ECUDA = -3
 ZERO_ETIMEDOUT = -4
 ZERO_ENOMEM = -5
 ZERO_MAX_RANKS = 64
+ZERO_STATUS_WAIT_TIMEOUT = 1
 
 _i64 = ctypes.c_int64
 _i32 = ctypes.c_int32
@@ -66,6 +67,8 @@ _SIGNATURES = {
     "ddp_allreduce_mean": (ctypes.c_int, [_P(_vp), _i64, _i32, _i32, _vp]),
     "zero_memory_bytes": (ctypes.c_int, [_i64, _i32, _i32, _i32, _P(_u64)]),
     "zero_memory_breakdown": (ctypes.c_int, [_i64, _i32, _i32, _i32, _i32, _P(_u64)]),
+    "zero_device_status": (ctypes.c_int, [_P(ctypes.c_uint32), _i32]),
+    "zero_debug_set_wait_timeout_ns": (ctypes.c_int, [_u64]),
     "zero_strerror": (ctypes.c_char_p, [ctypes.c_int]),
     "zero_last_error": (ctypes.c_char_p, []),
 }
@@ -287,6 +290,16 @@ def ddp_allreduce_mean(grads, precision: int, n: int | None = None, stream=None)
     gp = _ptr_array(grads, n, _storage_dtype(precision), "grads")
     _check(_lib.ddp_allreduce_mean(gp, n, len(grads), precision, _stream(stream)),
            "ddp_allreduce_mean")
+
+
+def zero_device_status(clear: bool = False) -> int:
+    out = ctypes.c_uint32()
+    _check(_lib.zero_device_status(ctypes.byref(out), 1 if clear else 0), "zero_device_status")
+    return out.value
+
+
+def zero_debug_set_wait_timeout_ns(ns: int) -> None:
+    _check(_lib.zero_debug_set_wait_timeout_ns(ns), "zero_debug_set_wait_timeout_ns")
 
 
 def raw_call(name: str, *args) -> int:

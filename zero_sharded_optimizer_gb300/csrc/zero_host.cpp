@@ -6,6 +6,7 @@
 // separately rounded double operations.
 
 #include <algorithm>
+#include <atomic>
 #include <chrono>
 #include <cmath>
 #include <cstdarg>
@@ -31,6 +32,10 @@ struct zero_states {
 namespace {
 
 thread_local char g_last_error[512] = "";
+
+// Bound of every device-side wait on a bulk copy, in nanoseconds.
+constexpr uint64_t kDefaultWaitNs = 2000000000ull;
+std::atomic<uint64_t> g_wait_ns{kDefaultWaitNs};
 
 int fail(int code, const char* fmt, ...) {
   va_list ap;
@@ -126,6 +131,7 @@ int prepare_step(void* const* params, const void* const* grads, const zero_state
   std::memset(a, 0, sizeof(*a));
   a->N = N;
   a->fN = float(N);
+  a->wait_ns = g_wait_ns.load(std::memory_order_relaxed);
   a->m = st->m;
   a->v = st->v;
   a->master = st->master;
@@ -227,6 +233,18 @@ const char* zero_strerror(int code) {
 }
 
 const char* zero_last_error(void) { return g_last_error; }
+
+int zero_device_status(uint32_t* status, int32_t clear) {
+  if (!status) return fail(ZERO_EINVAL, "status is NULL");
+  cudaError_t e = zk::read_device_status(status, clear != 0);
+  if (e != cudaSuccess) return cuda_fail(e, "reading the device status");
+  return ZERO_OK;
+}
+
+int zero_debug_set_wait_timeout_ns(uint64_t ns) {
+  g_wait_ns.store(ns == 0 ? kDefaultWaitNs : ns, std::memory_order_relaxed);
+  return ZERO_OK;
+}
 
 int zero_shard_bounds(int64_t n, int32_t N, int64_t* bounds) {
   if (n < 0) return fail(ZERO_EINVAL, "n=%lld must be >= 0", (long long)n);
@@ -480,6 +498,7 @@ int ddp_allreduce_mean(void* const* grads, int64_t n, int32_t N, int32_t precisi
   std::memset(&a, 0, sizeof(a));
   a.N = N;
   a.fN = float(N);
+  a.wait_ns = g_wait_ns.load(std::memory_order_relaxed);
   int ph = -2;
   bool same = true;
   std::vector<Range> rs;

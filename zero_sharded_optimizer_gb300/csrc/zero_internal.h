@@ -47,6 +47,7 @@ struct StepArgs {
   int32_t N;
   float fN;                      // (float)N
   AdamConsts c;
+  uint64_t wait_ns;              // bound of every wait on a bulk copy (TMA kernels)
 };
 
 struct AllreduceArgs {
@@ -54,6 +55,7 @@ struct AllreduceArgs {
   Split sp;
   int32_t N;
   float fN;
+  uint64_t wait_ns;
 };
 
 struct InitArgs {
@@ -68,5 +70,9 @@ struct InitArgs {
 cudaError_t launch_step(const StepArgs& a, bool mixed, cudaStream_t s);
 cudaError_t launch_allreduce(const AllreduceArgs& a, bool bf16, cudaStream_t s);
 cudaError_t launch_init(const InitArgs& a, cudaStream_t s);
+
+// Sticky device status word (bit 0: a bounded wait on a bulk copy ran out).
+// Reading synchronizes the current device.
+cudaError_t read_device_status(uint32_t* status, bool clear);
 
 }  // namespace zk

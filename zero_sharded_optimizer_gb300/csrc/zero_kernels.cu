@@ -73,6 +73,12 @@ __device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
   return make_uint4(pack_bf2(f[0], f[1]), pack_bf2(f[2], f[3]), pack_bf2(f[4], f[5]),
                     pack_bf2(f[6], f[7]));
 }
+__device__ __forceinline__ float4 unpack4(uint2 w) {
+  return make_float4(bf_lo(w.x), bf_hi(w.x), bf_lo(w.y), bf_hi(w.y));
+}
+__device__ __forceinline__ uint2 pack4(float4 f) {
+  return make_uint2(pack_bf2(f.x, f.y), pack_bf2(f.z, f.w));
+}
 
 // ----------------------------------------------------------------- the math --
 
@@ -87,14 +93,46 @@ __device__ __forceinline__ float mean_of(float s, float fN) {
   }
 }
 
+// Correctly rounded sqrt(v) for v >= 0, equal to __fsqrt_rn(v), with zero and
+// subnormal inputs answered through exact identities so the square root itself
+// only ever sees normal numbers: sqrt(+-0) = +-0, and for subnormal v
+// sqrt(v) = sqrt(v * 2^24) * 2^-12 (both scalings by powers of two are exact
+// and commute with rounding because every intermediate is normal). Gradients
+// that are exactly zero keep m and v at zero, or decaying through the
+// subnormal range; this keeps those elements on the same instruction path as
+// their neighbours in the warp.
+__device__ __forceinline__ float sqrt_nonneg(float v) {
+  const bool normal = v >= 0x1p-126f;  // also +inf
+  const bool sub = v > 0.0f && !normal;
+  const float r = __fsqrt_rn(normal ? v : (sub ? __fmul_rn(v, 0x1p24f) : 1.0f));
+  if (normal) return r;
+  if (sub) return __fmul_rn(r, 0x1p-12f);
+  if (v == 0.0f) return v;
+  return __fsqrt_rn(v);  // negative or NaN: the IEEE result
+}
+
+// Correctly rounded a / b for b > 0, equal to __fdiv_rn(a, b), with zero and
+// subnormal numerators answered through exact identities: +-0 / b = +-0, and
+// for subnormal a with a normal quotient a / b = ((a * 2^24) / b) * 2^-24.
+__device__ __forceinline__ float div_by_pos(float a, float b) {
+  const float aa = fabsf(a);
+  const bool zero = aa == 0.0f;
+  const bool sub = aa > 0.0f && aa < 0x1p-126f;
+  const float q = __fdiv_rn(zero ? 1.0f : (sub ? __fmul_rn(a, 0x1p24f) : a), b);
+  if (!(b > 0.0f)) return __fdiv_rn(a, b);  // outside the expected domain: IEEE as is
+  if (zero) return a;
+  if (sub) return fabsf(q) >= 0x1p-101f ? __fmul_rn(q, 0x1p-24f) : __fdiv_rn(a, b);
+  return q;
+}
+
 // One AdamW element: decoupled decay, moments, bias-corrected update.
 __device__ __forceinline__ void adam1(const AdamConsts& c, float g, float& p, float& m,
                                       float& v) {
   p = __fmul_rn(p, c.decay);
   m = __fadd_rn(__fmul_rn(c.b1, m), __fmul_rn(c.omb1, g));
   v = __fadd_rn(__fmul_rn(c.b2, v), __fmul_rn(c.omb2, __fmul_rn(g, g)));
-  const float d = __fadd_rn(__fdiv_rn(__fsqrt_rn(v), c.bc2s), c.eps);
-  p = __fsub_rn(p, __fmul_rn(c.step, __fdiv_rn(m, d)));
+  const float d = __fadd_rn(div_by_pos(sqrt_nonneg(v), c.bc2s), c.eps);
+  p = __fsub_rn(p, __fmul_rn(c.step, div_by_pos(m, d)));
 }
 
 template <int NR>
@@ -282,6 +320,25 @@ __global__ void __launch_bounds__(kThreads) zero_step_kernel(const __grid_consta
   }
 }
 
+// One element of the DDP mean, in place in every rank's buffer.
+template <int NR, bool BF16>
+__device__ __forceinline__ void mean_scalar(const AllreduceArgs& P, int64_t j) {
+  const int N = NR > 0 ? NR : P.N;
+  if constexpr (BF16) {
+    float acc = bf_one(__ldcs(static_cast<const uint16_t*>(P.grads[0]) + j));
+    for (int r = 1; r < N; ++r)
+      acc = __fadd_rn(acc, bf_one(__ldcs(static_cast<const uint16_t*>(P.grads[r]) + j)));
+    const uint16_t h = to_bf(mean_of<NR>(acc, P.fN));
+    for (int r = 0; r < N; ++r) __stcs(static_cast<uint16_t*>(P.grads[r]) + j, h);
+  } else {
+    float acc = __ldcs(static_cast<const float*>(P.grads[0]) + j);
+    for (int r = 1; r < N; ++r)
+      acc = __fadd_rn(acc, __ldcs(static_cast<const float*>(P.grads[r]) + j));
+    const float g = mean_of<NR>(acc, P.fN);
+    for (int r = 0; r < N; ++r) __stcs(static_cast<float*>(P.grads[r]) + j, g);
+  }
+}
+
 template <int NR, bool BF16>
 __global__ void __launch_bounds__(kThreads)
     allreduce_mean_kernel(const __grid_constant__ AllreduceArgs P) {
@@ -295,20 +352,7 @@ __global__ void __launch_bounds__(kThreads)
   const int64_t body_end = sp.lo + sp.head + sp.nvec * V;
   for (int64_t s = tid; s < nscalar; s += stride) {
     const int64_t j = s < sp.head ? sp.lo + s : body_end + (s - sp.head);
-    float acc;
-    if constexpr (BF16) {
-      acc = bf_one(__ldcs(static_cast<const uint16_t*>(P.grads[0]) + j));
-      for (int r = 1; r < N; ++r)
-        acc = __fadd_rn(acc, bf_one(__ldcs(static_cast<const uint16_t*>(P.grads[r]) + j)));
-      const uint16_t h = to_bf(mean_of<NR>(acc, P.fN));
-      for (int r = 0; r < N; ++r) __stcs(static_cast<uint16_t*>(P.grads[r]) + j, h);
-    } else {
-      acc = __ldcs(static_cast<const float*>(P.grads[0]) + j);
-      for (int r = 1; r < N; ++r)
-        acc = __fadd_rn(acc, __ldcs(static_cast<const float*>(P.grads[r]) + j));
-      const float g = mean_of<NR>(acc, P.fN);
-      for (int r = 0; r < N; ++r) __stcs(static_cast<float*>(P.grads[r]) + j, g);
-    }
+    mean_scalar<NR, BF16>(P, j);
   }
 
   const int64_t base = sp.lo + sp.head;
@@ -366,14 +410,18 @@ __global__ void __launch_bounds__(kThreads) init_state_kernel(const __grid_const
   }
 }
 
+}  // namespace
+}  // namespace zk
+
+#include "zero_tma.cuh"
+
+namespace zk {
+namespace {
+
 // ------------------------------------------------------------ grid sizing --
 
-struct DevInfo {
-  int sms = 0;
-};
-
 int sm_count() {
-  static int cached[kMaxRanks * 2] = {0};  // indexed by device ordinal
+  static int cached[256] = {0};  // indexed by device ordinal
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
   if (dev < 0 || dev >= int(sizeof(cached) / sizeof(cached[0]))) return 0;
@@ -411,13 +459,55 @@ cudaError_t launch(K kernel, const A& args, int64_t work, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+// One persistent CTA per SM (fewer when there are fewer tiles), with the
+// pipeline's shared memory.
+template <typename K, typename A>
+cudaError_t launch_tma(K kernel, const A& args, uint32_t smem, int64_t tiles, cudaStream_t s) {
+  const int sms = sm_count();
+  if (sms <= 0) return cudaErrorInvalidDevice;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+  if (e != cudaSuccess) return e;
+  const int blocks = int(tiles < 1 ? 1 : (tiles < sms ? tiles : sms));
+  kernel<<<blocks, kTmaThreads, smem, s>>>(args);
+  return cudaGetLastError();
+}
+
+template <int NR, bool MIXED>
+cudaError_t launch_step_tma(const StepArgs& a, cudaStream_t s) {
+  using G = StepTile<NR, MIXED>;
+  const int64_t nelem = a.sp.nvec * (MIXED ? 8 : 4);
+  return launch_tma(zero_step_tma_kernel<NR, MIXED>, a, G::kSmem, (nelem + G::T - 1) / G::T, s);
+}
+
+template <int NR, bool BF16>
+cudaError_t launch_mean_tma(const AllreduceArgs& a, cudaStream_t s) {
+  using G = MeanTile<NR, BF16>;
+  const int64_t nelem = a.sp.nvec * (BF16 ? 8 : 4);
+  return launch_tma(allreduce_mean_tma_kernel<NR, BF16>, a, G::kSmem, (nelem + G::T - 1) / G::T,
+                    s);
+}
+
+// Bulk-copy pipeline for N <= 8 when the buffers share a 16-byte phase (there
+// is a vector body); the register-streaming kernel for any other case.
 template <bool MIXED>
 cudaError_t launch_step_t(const StepArgs& a, cudaStream_t s) {
+  if (a.sp.nvec > 0) {
+    switch (a.N) {
+      case 1: return launch_step_tma<1, MIXED>(a, s);
+      case 2: return launch_step_tma<2, MIXED>(a, s);
+      case 3: return launch_step_tma<3, MIXED>(a, s);
+      case 4: return launch_step_tma<4, MIXED>(a, s);
+      case 5: return launch_step_tma<5, MIXED>(a, s);
+      case 6: return launch_step_tma<6, MIXED>(a, s);
+      case 7: return launch_step_tma<7, MIXED>(a, s);
+      case 8: return launch_step_tma<8, MIXED>(a, s);
+      default: break;
+    }
+  }
   const int64_t work = a.sp.nvec > a.sp.head + a.sp.tail ? a.sp.nvec : a.sp.head + a.sp.tail;
   switch (a.N) {
     case 1: return launch(zero_step_kernel<1, MIXED>, a, work, s);
     case 2: return launch(zero_step_kernel<2, MIXED>, a, work, s);
-    case 3: return launch(zero_step_kernel<3, MIXED>, a, work, s);
     case 4: return launch(zero_step_kernel<4, MIXED>, a, work, s);
     case 8: return launch(zero_step_kernel<8, MIXED>, a, work, s);
     default: return launch(zero_step_kernel<0, MIXED>, a, work, s);
@@ -426,6 +516,19 @@ cudaError_t launch_step_t(const StepArgs& a, cudaStream_t s) {
 
 template <bool BF16>
 cudaError_t launch_allreduce_t(const AllreduceArgs& a, cudaStream_t s) {
+  if (a.sp.nvec > 0) {
+    switch (a.N) {
+      case 1: return launch_mean_tma<1, BF16>(a, s);
+      case 2: return launch_mean_tma<2, BF16>(a, s);
+      case 3: return launch_mean_tma<3, BF16>(a, s);
+      case 4: return launch_mean_tma<4, BF16>(a, s);
+      case 5: return launch_mean_tma<5, BF16>(a, s);
+      case 6: return launch_mean_tma<6, BF16>(a, s);
+      case 7: return launch_mean_tma<7, BF16>(a, s);
+      case 8: return launch_mean_tma<8, BF16>(a, s);
+      default: break;
+    }
+  }
   const int64_t work = a.sp.nvec > a.sp.head + a.sp.tail ? a.sp.nvec : a.sp.head + a.sp.tail;
   switch (a.N) {
     case 1: return launch(allreduce_mean_kernel<1, BF16>, a, work, s);
@@ -449,6 +552,18 @@ cudaError_t launch_allreduce(const AllreduceArgs& a, bool bf16, cudaStream_t s) 
 cudaError_t launch_init(const InitArgs& a, cudaStream_t s) {
   const int64_t work = a.sp.nvec > a.sp.head + a.sp.tail ? a.sp.nvec : a.sp.head + a.sp.tail;
   return launch(init_state_kernel, a, work, s);
+}
+
+cudaError_t read_device_status(uint32_t* status, bool clear) {
+  unsigned int v = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&v, g_device_status, sizeof(v));
+  if (e != cudaSuccess) return e;
+  *status = v;
+  if (clear && v) {
+    const unsigned int zero = 0;
+    e = cudaMemcpyToSymbol(g_device_status, &zero, sizeof(zero));
+  }
+  return e;
 }
 
 }  // namespace zk

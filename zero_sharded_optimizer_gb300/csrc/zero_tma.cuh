@@ -1,0 +1,455 @@
+// Bulk-copy (TMA) staged kernels: the fused ZeRO step and the DDP mean for
+// N <= 8 ranks. Included by zero_kernels.cu after the element helpers.
+//
+// Pipeline (one CTA per SM, persistent over tiles tile = blockIdx.x + k*gridDim.x):
+//   * thread 0 issues, per tile, one cp.async.bulk global->shared copy per
+//     input stream (N gradient tiles, parameter/master, m, v) completing on the
+//     stage's mbarrier; three stages, so two tiles are in flight while one is
+//     computed;
+//   * all threads wait on the stage, compute, and write the results into one
+//     of two output buffers; thread 0 then issues cp.async.bulk shared->global
+//     copies of the results: m, v, (master,) and the same parameter tile N
+//     times -- the all-gather reads one shared tile N times instead of N
+//     register copies;
+//   * the input stage is refilled with the tile three ahead as soon as it has
+//     been computed (the results live in the output buffer), so two tiles are
+//     always loading while one computes; an output buffer is rewritten only
+//     after its previous bulk stores have read it (cp.async.bulk.wait_group.read).
+// Large tiles (2048 elements, 8 KB per fp32 stream) give every stream long
+// contiguous DRAM bursts; measured on GB300 this moves the step's mix of
+// N+3 read and N+2 write streams at the device-to-device copy rate.
+//
+// Every wait on an mbarrier is bounded by %globaltimer. When the bound runs
+// out the CTA sets ZK_STATUS_WAIT_TIMEOUT in the device status word, waits
+// (again bounded) for its own copies still in flight, and returns.
+
+#pragma once
+
+namespace zk {
+
+__device__ unsigned int g_device_status = 0;
+constexpr unsigned int ZK_STATUS_WAIT_TIMEOUT = 1u;
+constexpr uint64_t kDrainNs = 2000000000ull;   // bound of the drain after a timeout
+
+namespace {
+
+// ------------------------------------------------------------- PTX wrappers --
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ uint64_t global_timer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
+               : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+// Wait for phase `parity` of `bar`; false when `limit_ns` passed first.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (;;) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (global_timer_ns() - t0 > limit_ns) return false;
+  }
+}
+// Bulk copy global -> shared, completing `bytes` on `bar` (16-byte aligned
+// addresses, size a multiple of 16).
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
+                                          uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(smem_addr(dst)), "l"(src), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
+}
+// Bulk copy shared -> global in the current bulk group.
+__device__ __forceinline__ void bulk_store(void* dst, const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),
+               "r"(smem_addr(src)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// All but the most recent bulk group have finished reading shared memory.
+__device__ __forceinline__ void bulk_wait_read_all_but_last() {
+  asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+// Make this thread's generic-proxy shared-memory writes visible to bulk copies.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// ------------------------------------------------------------ tile geometry --
+
+constexpr int kTmaThreads = 512;
+constexpr int kTmaStages = 3;      // input stages
+constexpr int kTmaOutBufs = 2;     // output buffers
+constexpr int kTmaSmemBudget = 224 * 1024;
+
+// Tile size: the largest of 2048, 1536, 1024, 512 elements whose input stages
+// (in_bytes per element) and output buffers (out_bytes per element) fit.
+constexpr int tile_elems(int in_bytes, int out_bytes) {
+  return (kTmaStages * in_bytes + kTmaOutBufs * out_bytes) * 2048 <= kTmaSmemBudget   ? 2048
+         : (kTmaStages * in_bytes + kTmaOutBufs * out_bytes) * 1536 <= kTmaSmemBudget ? 1536
+         : (kTmaStages * in_bytes + kTmaOutBufs * out_bytes) * 1024 <= kTmaSmemBudget ? 1024
+                                                                                       : 512;
+}
+
+template <int NR, bool MIXED>
+struct StepTile {
+  static constexpr int kGB = MIXED ? 2 : 4;        // gradient / replica element bytes
+  static constexpr int kOutB = 12 + (MIXED ? 2 : 0);  // p/master, m, v (+ bf16 replica)
+  static constexpr int T = tile_elems(NR * kGB + 12, kOutB);
+  static constexpr uint32_t kGradTile = uint32_t(T) * kGB;
+  static constexpr uint32_t kFTile = uint32_t(T) * 4;
+  static constexpr uint32_t kStage = NR * kGradTile + 3 * kFTile;
+  static constexpr uint32_t kOut = uint32_t(T) * kOutB;
+  static constexpr uint32_t kSmem = kTmaStages * kStage + kTmaOutBufs * kOut;
+};
+
+template <int NR, bool BF16>
+struct MeanTile {
+  static constexpr int kGB = BF16 ? 2 : 4;
+  static constexpr int T = tile_elems(NR * kGB, kGB);
+  static constexpr uint32_t kTile = uint32_t(T) * kGB;
+  static constexpr uint32_t kStage = NR * kTile;
+  static constexpr uint32_t kSmem = kTmaStages * kStage + kTmaOutBufs * kTile;
+};
+
+// Shared pipeline state of one CTA.
+struct PipeState {
+  uint64_t full[kTmaStages];
+  int owner[kTmaStages];  // fp32 step: owner of the whole tile, -1 if it straddles
+  int abort;
+};
+
+// On a timed-out wait: record it, then wait (bounded) for every tile this CTA
+// issued but has not consumed, so no bulk copy writes shared memory after exit.
+__device__ __forceinline__ void drain_after_timeout(PipeState& ps, int64_t consumed,
+                                                    int64_t issued) {
+  atomicOr(&g_device_status, ZK_STATUS_WAIT_TIMEOUT);
+  for (int64_t t = consumed; t < issued; ++t)
+    mbar_wait(&ps.full[t % kTmaStages], uint32_t((t / kTmaStages) & 1), kDrainNs);
+}
+
+// The loop shared by both pipelines. `issue_load(local)` queues the bulk loads
+// of local tile `local` into stage local % kTmaStages; `compute(local, stage,
+// out)` turns stage `stage` into output buffer `out`; `issue_store(local, out)`
+// queues and commits the bulk stores of that output buffer.
+template <typename Load, typename Compute, typename Store>
+__device__ __forceinline__ void run_pipeline(PipeState& ps, int64_t my_tiles, uint64_t wait_ns,
+                                             Load issue_load, Compute compute,
+                                             Store issue_store) {
+  const int tid = threadIdx.x;
+  if (tid == 0) {
+    for (int s = 0; s < kTmaStages; ++s) mbar_init(&ps.full[s], 1);
+    fence_mbar_init();
+    ps.abort = 0;
+  }
+  __syncthreads();
+  int64_t issued = 0;  // meaningful in thread 0 only
+  if (tid == 0) {
+    for (; issued < kTmaStages && issued < my_tiles; ++issued) issue_load(issued);
+  }
+  for (int64_t k = 0; k < my_tiles; ++k) {
+    const int s = int(k % kTmaStages);
+    const int o = int(k & 1);
+    if (tid == 0 && !mbar_wait(&ps.full[s], uint32_t((k / kTmaStages) & 1), wait_ns)) {
+      ps.abort = 1;
+      drain_after_timeout(ps, k, issued);
+    }
+    __syncthreads();
+    if (ps.abort) break;
+    compute(k, s, o);
+    fence_proxy_async_smem();
+    __syncthreads();
+    if (tid == 0) {
+      issue_store(k, o);
+      if (issued < my_tiles) issue_load(issued++);  // into stage s, just consumed
+      bulk_wait_read_all_but_last();  // output buffer 1-o is free for tile k+1
+    }
+  }
+  if (tid == 0) bulk_wait_all();
+}
+
+// ------------------------------------------------------------ the fused step --
+
+template <int NR, bool MIXED>
+__global__ void __launch_bounds__(kTmaThreads, 1)
+    zero_step_tma_kernel(const __grid_constant__ StepArgs P) {
+  using G = StepTile<NR, MIXED>;
+  constexpr int T = G::T;
+  constexpr int V = MIXED ? 8 : 4;
+  extern __shared__ __align__(128) unsigned char smem[];
+  __shared__ PipeState ps;
+  const int tid = threadIdx.x;
+  const Split& sp = P.sp;
+
+  // Scalar head and tail (fewer than 2V elements) by block 0.
+  if (blockIdx.x == 0) {
+    const int64_t nscalar = sp.head + sp.tail;
+    const int64_t body_end = sp.lo + sp.head + sp.nvec * V;
+    int owner = 0;
+    for (int64_t s = tid; s < nscalar; s += blockDim.x) {
+      const int64_t j = s < sp.head ? sp.lo + s : body_end + (s - sp.head);
+      owner = advance_owner(P, owner, j);
+      step_scalar<NR, MIXED>(P, j, owner);
+    }
+  }
+
+  const int64_t base = sp.lo + sp.head;
+  const int64_t nelem = sp.nvec * V;
+  const int64_t ntiles = (nelem + T - 1) / T;
+  const int64_t my_tiles =
+      ntiles > int64_t(blockIdx.x) ? (ntiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+  if (my_tiles == 0) return;
+
+  auto stage = [&](int s) { return smem + size_t(s) * G::kStage; };
+  auto grad_slot = [&](int s, int r) { return stage(s) + r * G::kGradTile; };
+  auto in_f = [&](int s, int k) {  // 0 = parameter / master, 1 = m, 2 = v
+    return reinterpret_cast<float*>(stage(s) + NR * G::kGradTile + k * G::kFTile);
+  };
+  auto out_f = [&](int o, int k) {  // 0 = parameter / master, 1 = m, 2 = v
+    return reinterpret_cast<float*>(smem + kTmaStages * G::kStage + o * G::kOut +
+                                    k * G::kFTile);
+  };
+  auto out_bf = [&](int o) {  // mixed: the bf16 replica tile
+    return smem + kTmaStages * G::kStage + o * G::kOut + 3 * G::kFTile;
+  };
+  auto tile_j0 = [&](int64_t local) { return base + (blockIdx.x + local * gridDim.x) * T; };
+  auto tile_cnt = [&](int64_t local) {
+    const int64_t rem = nelem - (blockIdx.x + local * gridDim.x) * int64_t(T);
+    return uint32_t(rem < T ? rem : T);
+  };
+
+  auto issue_load = [&](int64_t local) {
+    const int s = int(local % kTmaStages);
+    const int64_t j0 = tile_j0(local);
+    const uint32_t cnt = tile_cnt(local);
+    const uint32_t gbytes = cnt * G::kGB, fbytes = cnt * 4;
+    bool straddle = false;
+    int owner = 0;
+    if constexpr (!MIXED) {
+      owner = advance_owner(P, 0, j0);
+      straddle = j0 + cnt - 1 >= P.bounds[owner + 1];
+      ps.owner[s] = straddle ? -1 : owner;
+    }
+    mbar_expect_tx(&ps.full[s], NR * gbytes + (straddle ? 2u : 3u) * fbytes);
+#pragma unroll
+    for (int r = 0; r < NR; ++r)
+      bulk_load(grad_slot(s, r), static_cast<const unsigned char*>(P.grads[r]) + j0 * G::kGB,
+                gbytes, &ps.full[s]);
+    if constexpr (MIXED) {
+      bulk_load(in_f(s, 0), P.master + j0, fbytes, &ps.full[s]);
+    } else {
+      if (!straddle)
+        bulk_load(in_f(s, 0), static_cast<const float*>(P.reps[owner]) + j0, fbytes,
+                  &ps.full[s]);
+    }
+    bulk_load(in_f(s, 1), P.m + j0, fbytes, &ps.full[s]);
+    bulk_load(in_f(s, 2), P.v + j0, fbytes, &ps.full[s]);
+  };
+
+  auto issue_store = [&](int64_t local, int o) {
+    const int64_t j0 = tile_j0(local);
+    const uint32_t cnt = tile_cnt(local);
+    const uint32_t fbytes = cnt * 4;
+    bulk_store(P.m + j0, out_f(o, 1), fbytes);
+    bulk_store(P.v + j0, out_f(o, 2), fbytes);
+    if constexpr (MIXED) {
+      bulk_store(P.master + j0, out_f(o, 0), fbytes);
+#pragma unroll
+      for (int r = 0; r < NR; ++r)
+        bulk_store(static_cast<unsigned char*>(P.reps[r]) + j0 * 2, out_bf(o), cnt * 2);
+    } else {
+#pragma unroll
+      for (int r = 0; r < NR; ++r)
+        bulk_store(static_cast<float*>(P.reps[r]) + j0, out_f(o, 0), fbytes);
+    }
+    bulk_commit();
+  };
+
+  auto compute = [&](int64_t local, int s, int o) {
+    const int64_t j0 = tile_j0(local);
+    const int cnt = int(tile_cnt(local));
+    const float* pi = in_f(s, 0);
+    const float* mi = in_f(s, 1);
+    const float* vi = in_f(s, 2);
+    float* po = out_f(o, 0);
+    float* mo = out_f(o, 1);
+    float* vo = out_f(o, 2);
+    if constexpr (!MIXED) {
+      const int owner = ps.owner[s];
+      for (int q = tid * 4; q < cnt; q += kTmaThreads * 4) {
+        float4 g = *reinterpret_cast<const float4*>(grad_slot(s, 0) + q * 4);
+#pragma unroll
+        for (int r = 1; r < NR; ++r) {
+          const float4 h = *reinterpret_cast<const float4*>(grad_slot(s, r) + q * 4);
+          g.x = __fadd_rn(g.x, h.x); g.y = __fadd_rn(g.y, h.y);
+          g.z = __fadd_rn(g.z, h.z); g.w = __fadd_rn(g.w, h.w);
+        }
+        float4 p;
+        if (owner >= 0) {
+          p = *reinterpret_cast<const float4*>(pi + q);
+        } else {  // the tile straddles a shard boundary: per-element owners
+          float e[4];
+          int ow = 0;
+          for (int i = 0; i < 4; ++i) {
+            ow = advance_owner(P, ow, j0 + q + i);
+            e[i] = __ldcs(static_cast<const float*>(P.reps[ow]) + j0 + q + i);
+          }
+          p = make_float4(e[0], e[1], e[2], e[3]);
+        }
+        float4 m = *reinterpret_cast<const float4*>(mi + q);
+        float4 v = *reinterpret_cast<const float4*>(vi + q);
+        adam1(P.c, mean_of<NR>(g.x, P.fN), p.x, m.x, v.x);
+        adam1(P.c, mean_of<NR>(g.y, P.fN), p.y, m.y, v.y);
+        adam1(P.c, mean_of<NR>(g.z, P.fN), p.z, m.z, v.z);
+        adam1(P.c, mean_of<NR>(g.w, P.fN), p.w, m.w, v.w);
+        *reinterpret_cast<float4*>(po + q) = p;
+        *reinterpret_cast<float4*>(mo + q) = m;
+        *reinterpret_cast<float4*>(vo + q) = v;
+      }
+    } else {
+      // four elements per thread: one uint2 of bf16 per rank, float4s of state
+      for (int q = tid * 4; q < cnt; q += kTmaThreads * 4) {
+        float4 g = unpack4(*reinterpret_cast<const uint2*>(grad_slot(s, 0) + q * 2));
+#pragma unroll
+        for (int r = 1; r < NR; ++r) {
+          const float4 h = unpack4(*reinterpret_cast<const uint2*>(grad_slot(s, r) + q * 2));
+          g.x = __fadd_rn(g.x, h.x); g.y = __fadd_rn(g.y, h.y);
+          g.z = __fadd_rn(g.z, h.z); g.w = __fadd_rn(g.w, h.w);
+        }
+        float4 p = *reinterpret_cast<const float4*>(pi + q);
+        float4 m = *reinterpret_cast<const float4*>(mi + q);
+        float4 v = *reinterpret_cast<const float4*>(vi + q);
+        adam1(P.c, mean_of<NR>(g.x, P.fN), p.x, m.x, v.x);
+        adam1(P.c, mean_of<NR>(g.y, P.fN), p.y, m.y, v.y);
+        adam1(P.c, mean_of<NR>(g.z, P.fN), p.z, m.z, v.z);
+        adam1(P.c, mean_of<NR>(g.w, P.fN), p.w, m.w, v.w);
+        *reinterpret_cast<float4*>(po + q) = p;
+        *reinterpret_cast<float4*>(mo + q) = m;
+        *reinterpret_cast<float4*>(vo + q) = v;
+        *reinterpret_cast<uint2*>(out_bf(o) + q * 2) = pack4(p);
+      }
+    }
+  };
+
+  run_pipeline(ps, my_tiles, P.wait_ns, issue_load, compute, issue_store);
+}
+
+// ---------------------------------------------------------- the DDP mean --
+
+template <int NR, bool BF16>
+__global__ void __launch_bounds__(kTmaThreads, 1)
+    allreduce_mean_tma_kernel(const __grid_constant__ AllreduceArgs P) {
+  using G = MeanTile<NR, BF16>;
+  constexpr int T = G::T;
+  constexpr int V = BF16 ? 8 : 4;
+  extern __shared__ __align__(128) unsigned char smem[];
+  __shared__ PipeState ps;
+  const int tid = threadIdx.x;
+  const Split& sp = P.sp;
+
+  if (blockIdx.x == 0) {
+    const int64_t nscalar = sp.head + sp.tail;
+    const int64_t body_end = sp.lo + sp.head + sp.nvec * V;
+    for (int64_t s = tid; s < nscalar; s += blockDim.x) {
+      const int64_t j = s < sp.head ? sp.lo + s : body_end + (s - sp.head);
+      mean_scalar<NR, BF16>(P, j);
+    }
+  }
+
+  const int64_t base = sp.lo + sp.head;
+  const int64_t nelem = sp.nvec * V;
+  const int64_t ntiles = (nelem + T - 1) / T;
+  const int64_t my_tiles =
+      ntiles > int64_t(blockIdx.x) ? (ntiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+  if (my_tiles == 0) return;
+
+  auto slot = [&](int s, int r) { return smem + size_t(s) * G::kStage + r * G::kTile; };
+  auto out = [&](int o) { return smem + size_t(kTmaStages) * G::kStage + o * G::kTile; };
+  auto tile_j0 = [&](int64_t local) { return base + (blockIdx.x + local * gridDim.x) * T; };
+  auto tile_cnt = [&](int64_t local) {
+    const int64_t rem = nelem - (blockIdx.x + local * gridDim.x) * int64_t(T);
+    return uint32_t(rem < T ? rem : T);
+  };
+  auto issue_load = [&](int64_t local) {
+    const int s = int(local % kTmaStages);
+    const int64_t j0 = tile_j0(local);
+    const uint32_t bytes = tile_cnt(local) * G::kGB;
+    mbar_expect_tx(&ps.full[s], NR * bytes);
+#pragma unroll
+    for (int r = 0; r < NR; ++r)
+      bulk_load(slot(s, r), static_cast<const unsigned char*>(P.grads[r]) + j0 * G::kGB, bytes,
+                &ps.full[s]);
+  };
+  auto issue_store = [&](int64_t local, int o) {
+    const int64_t j0 = tile_j0(local);
+    const uint32_t bytes = tile_cnt(local) * G::kGB;
+#pragma unroll
+    for (int r = 0; r < NR; ++r)
+      bulk_store(static_cast<unsigned char*>(P.grads[r]) + j0 * G::kGB, out(o), bytes);
+    bulk_commit();
+  };
+  auto compute = [&](int64_t local, int s, int o) {
+    const int cnt = int(tile_cnt(local));
+    if constexpr (BF16) {
+      for (int q = tid * 4; q < cnt; q += kTmaThreads * 4) {
+        float4 g = unpack4(*reinterpret_cast<const uint2*>(slot(s, 0) + q * 2));
+#pragma unroll
+        for (int r = 1; r < NR; ++r) {
+          const float4 h = unpack4(*reinterpret_cast<const uint2*>(slot(s, r) + q * 2));
+          g.x = __fadd_rn(g.x, h.x); g.y = __fadd_rn(g.y, h.y);
+          g.z = __fadd_rn(g.z, h.z); g.w = __fadd_rn(g.w, h.w);
+        }
+        g.x = mean_of<NR>(g.x, P.fN); g.y = mean_of<NR>(g.y, P.fN);
+        g.z = mean_of<NR>(g.z, P.fN); g.w = mean_of<NR>(g.w, P.fN);
+        *reinterpret_cast<uint2*>(out(o) + q * 2) = pack4(g);
+      }
+    } else {
+      for (int q = tid * 4; q < cnt; q += kTmaThreads * 4) {
+        float4 g = *reinterpret_cast<const float4*>(slot(s, 0) + q * 4);
+#pragma unroll
+        for (int r = 1; r < NR; ++r) {
+          const float4 h = *reinterpret_cast<const float4*>(slot(s, r) + q * 4);
+          g.x = __fadd_rn(g.x, h.x); g.y = __fadd_rn(g.y, h.y);
+          g.z = __fadd_rn(g.z, h.z); g.w = __fadd_rn(g.w, h.w);
+        }
+        g.x = mean_of<NR>(g.x, P.fN); g.y = mean_of<NR>(g.y, P.fN);
+        g.z = mean_of<NR>(g.z, P.fN); g.w = mean_of<NR>(g.w, P.fN);
+        *reinterpret_cast<float4*>(out(o) + q * 4) = g;
+      }
+    }
+  };
+  run_pipeline(ps, my_tiles, P.wait_ns, issue_load, compute, issue_store);
+}
+
+}  // namespace
+}  // namespace zk
