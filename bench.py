@@ -37,7 +37,8 @@ from zero_sharded_optimizer_gb300 import inputs  # noqa: E402
 METRIC = "ZeRO step params/s at N ranks on 1 GB300; achieved HBM GB/s vs peak"
 UNIT = "params/s"
 DEFAULT_WORKLOAD = "fp32_25m"
-KERNEL_SRC = os.path.join(ROOT, "zero_sharded_optimizer_gb300", "csrc", "zero_kernels.cu")
+KERNEL_SRCS = [os.path.join(ROOT, "zero_sharded_optimizer_gb300", "csrc", f)
+               for f in ("zero_kernels.cu", "zero_tma.cuh")]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 L2_BYTES = 129 * 10 ** 6
 
@@ -68,8 +69,13 @@ def load_peaks() -> tuple[float, str]:
 
 
 def kernel_source_hash() -> str:
-    with open(KERNEL_SRC, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    """sha256[:16] over the kernel sources, in order (ties a traffic record to
+    the code it was measured on)."""
+    h = hashlib.sha256()
+    for path in KERNEL_SRCS:
+        with open(path, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def traffic_per_launch(workload: str):
@@ -281,8 +287,12 @@ def run_gpu(args, wl, rank: int, world: int, local_rank: int) -> dict | None:
 
     # ---- end to end through the public API: host gradients in, parameters out
     K_e = max(3, min(K, 30))
-    host_grads = [g.cpu().pin_memory() for g in grads]
-    host_out = torch.empty(n, dtype=reps[0].dtype).pin_memory()
+    host_grads = []
+    for g in grads:
+        h = torch.empty(n, dtype=g.dtype, pin_memory=True)
+        h.copy_(g)
+        host_grads.append(h)
+    host_out = torch.empty(n, dtype=reps[0].dtype, pin_memory=True)
     for _ in range(2):
         opt.step(reps, host_grads)
         host_out.copy_(reps[0], non_blocking=True)
@@ -332,7 +342,7 @@ def run_gpu(args, wl, rank: int, world: int, local_rank: int) -> dict | None:
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs, copy "
                                     f"bandwidth)" if peak_kind == "measured" else "fallback",
                      "algorithmic_bytes_per_launch": step_bytes // launches_per_step,
-                     "kernel": "zero_step_kernel",
+                     "kernel": "zero_step_tma_kernel" if wl.N <= 8 else "zero_step_kernel",
                      "kernel_ms": kernel_ms / launches_per_step},
         "gpu_launches": K * launches_per_step,
         "clocks": clocks,
