@@ -172,6 +172,37 @@ int zero_step_bucketed(void *const *params, const void *const *grads, zero_state
                        int64_t n_ready, zero_stream_t side, zero_event_t done,
                        int64_t timeout_ms);
 
+/* ------------------------------------------------------------ host input -- */
+
+/* The step with the gradients in HOST memory, pipelined chunk by chunk. For
+ * every chunk [lo, hi) of B = chunk_bytes / element_size elements, in index
+ * order, this queues:
+ *   on `h2d`     the copies host_grads[r][lo:hi] -> staging[r][lo:hi], all r;
+ *   on `compute` the step on [lo, hi), once that chunk has arrived;
+ *   on `d2h`     (host_params_out not NULL) the copy of the updated
+ *                params[0][lo:hi] -> host_params_out[lo:hi].
+ * Copies in both directions overlap the step of other chunks. The copies start
+ * after everything already queued on `compute`, and `compute` completes only
+ * after the last chunk reached host_params_out, so synchronizing `compute`
+ * covers the whole call.
+ *   host_grads      : N HOST buffers of n elements, read-only (pinned memory
+ *                     for asynchronous copies).
+ *   staging         : N DEVICE buffers of n elements; they receive the
+ *                     gradients and are the step's gradient buffers.
+ *   host_params_out : NULL, or a HOST buffer of n elements.
+ *   h2d, d2h        : streams for the two copy directions (streams distinct
+ *                     from `compute` give the overlap; any streams are correct).
+ * The result equals zero_step on the same gradients bit for bit. The handle
+ * keeps 2*ceil(n/B)+2 CUDA events for these calls, created on first use;
+ * calls on one handle must not run concurrently from several host threads.
+ * Errors: as zero_step, plus EINVAL for a NULL host or staging buffer or a
+ * chunk smaller than one element, ECUDA for a failed copy. */
+int zero_step_from_host(void *const *params, const void *const *host_grads,
+                        void *const *staging, zero_states_t *st, int64_t t, double lr,
+                        double beta1, double beta2, double eps, double weight_decay,
+                        void *host_params_out, int64_t chunk_bytes, zero_stream_t compute,
+                        zero_stream_t h2d, zero_stream_t d2h);
+
 /* ------------------------------------------------------------------- DDP -- */
 
 /* DDP all_reduce(op="mean") in place ("Data parallelism and ZeRO stages 1 to 3",

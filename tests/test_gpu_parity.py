@@ -393,10 +393,34 @@ def test_optimizer_host_gradients_match_device(abi, cuda):
     b = ZeroOptimizer(n, N, lr=1e-3, weight_decay=0.01)
     pa = [p0.to(cuda) for _ in range(N)]
     pb = [p0.to(cuda) for _ in range(N)]
-    a.step(pa, host)
-    b.step(pb, [h.to(cuda) for h in host])
-    torch.cuda.synchronize()
-    assert all(torch.equal(x, y) for x, y in zip(pa, pb))
+    out = torch.empty(n, dtype=torch.float32).pin_memory()
+    for _ in range(3):
+        # chunks of 10,001 elements: chunk edges fall off the 16-byte vector grid
+        a.step(pa, host, host_params_out=out, chunk_bytes=40_004)
+        b.step(pb, [h.to(cuda) for h in host])
+        torch.cuda.synchronize()
+        assert all(torch.equal(x, y) for x, y in zip(pa, pb))
+        assert torch.equal(out, pb[0].cpu())
+
+
+def test_step_from_host_mixed_matches_device(abi, cuda):
+    from zero_sharded_optimizer_gb300.optimizer import ZeroOptimizer
+    n, N = 1_000_003, 8
+    rng = np.random.default_rng(23)
+    init = torch.from_numpy(rng.normal(0, 0.02, n).astype(np.float32))
+    kw = dict(precision=abi.ZERO_BF16_MIXED, lr=6e-4, weight_decay=0.1, master_init=init)
+    a, b = ZeroOptimizer(n, N, **kw), ZeroOptimizer(n, N, **kw)
+    pa = [init.to(cuda).to(torch.bfloat16) for _ in range(N)]
+    pb = [p.clone() for p in pa]
+    out = torch.empty(n, dtype=torch.bfloat16).pin_memory()
+    for _ in range(2):
+        host = [torch.from_numpy(rng.normal(0, 1e-3, n).astype(np.float32)).to(torch.bfloat16)
+                .pin_memory() for _ in range(N)]
+        a.step(pa, host, host_params_out=out, chunk_bytes=1 << 20)
+        b.step(pb, [h.to(cuda) for h in host])
+        torch.cuda.synchronize()
+        assert torch.equal(a.master, b.master) and all(torch.equal(x, y) for x, y in zip(pa, pb))
+        assert torch.equal(out, pb[0].cpu())
 
 
 @pytest.mark.parametrize("prec", [oracle.FP32, oracle.BF16_MIXED])

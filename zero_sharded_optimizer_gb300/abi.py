@@ -64,6 +64,8 @@ _SIGNATURES = {
                                         _i64, _i64, _vp, _vp]),
     "zero_step_bucketed": (ctypes.c_int, [_P(_vp), _P(_vp), _vp, _i64, _dbl, _dbl, _dbl, _dbl,
                                           _dbl, _i64, _P(_vp), _i64, _vp, _vp, _i64]),
+    "zero_step_from_host": (ctypes.c_int, [_P(_vp), _P(_vp), _P(_vp), _vp, _i64, _dbl, _dbl, _dbl,
+                                           _dbl, _dbl, _vp, _i64, _vp, _vp, _vp]),
     "ddp_allreduce_mean": (ctypes.c_int, [_P(_vp), _i64, _i32, _i32, _vp]),
     "zero_memory_bytes": (ctypes.c_int, [_i64, _i32, _i32, _i32, _P(_u64)]),
     "zero_memory_breakdown": (ctypes.c_int, [_i64, _i32, _i32, _i32, _i32, _P(_u64)]),
@@ -283,6 +285,37 @@ def zero_step_bucketed(params, grads, st: ZeroStates, t: int, lr: float, beta1: 
     _check(_lib.zero_step_bucketed(pp, gp, st.handle, t, lr, beta1, beta2, eps, weight_decay,
                                    bucket_bytes, arr, count, _stream(side), _event_to_record(done),
                                    timeout_ms), "zero_step_bucketed")
+
+
+def _host_ptr_array(tensors, n: int, dtype, what: str):
+    arr = (_vp * len(tensors))()
+    for i, t in enumerate(tensors):
+        if not isinstance(t, torch.Tensor) or t.is_cuda:
+            raise TypeError(f"{what}[{i}] must be a host tensor")
+        if t.dtype != dtype:
+            raise TypeError(f"{what}[{i}] has dtype {t.dtype}, expected {dtype}")
+        if not t.is_contiguous() or t.numel() < n:
+            raise ValueError(f"{what}[{i}] must be contiguous with at least {n} elements")
+        arr[i] = t.data_ptr()
+    return arr
+
+
+def zero_step_from_host(params, host_grads, staging, st: ZeroStates, t: int, lr: float,
+                        beta1: float, beta2: float, eps: float, weight_decay: float,
+                        host_params_out=None, chunk_bytes: int = 25 * 1024 * 1024,
+                        compute=None, h2d=None, d2h=None):
+    dt = _storage_dtype(st.precision)
+    if len(host_grads) != st.N or len(staging) != st.N or len(params) != st.N:
+        raise ValueError(f"need {st.N} params, host gradients and staging buffers")
+    pp = _ptr_array(params, st.n, dt, "params")
+    sp = _ptr_array(staging, st.n, dt, "staging")
+    hp = _host_ptr_array(host_grads, st.n, dt, "host_grads")
+    out = None
+    if host_params_out is not None:
+        out = _host_ptr_array([host_params_out], st.n, dt, "host_params_out")[0]
+    _check(_lib.zero_step_from_host(pp, hp, sp, st.handle, t, lr, beta1, beta2, eps, weight_decay,
+                                    out, chunk_bytes, _stream(compute), _stream(h2d), _stream(d2h)),
+           "zero_step_from_host")
 
 
 def ddp_allreduce_mean(grads, precision: int, n: int | None = None, stream=None):

@@ -27,6 +27,9 @@ struct zero_states {
   float* v;
   float* master;
   int64_t bounds[ZERO_MAX_RANKS + 1];
+  // Events of the host-input pipeline (created on first use, reused by later
+  // calls, destroyed with the handle).
+  std::vector<cudaEvent_t> events;
 };
 
 namespace {
@@ -354,6 +357,9 @@ int zero_init_states(int64_t n, int32_t N, int32_t precision, float* m, float* v
 }
 
 int zero_free_states(zero_states_t* st) {
+  if (st) {
+    for (cudaEvent_t e : st->events) cudaEventDestroy(e);
+  }
   delete st;
   return ZERO_OK;
 }
@@ -484,6 +490,76 @@ int zero_step_bucketed(void* const* params, const void* const* grads, zero_state
       return fail(ZERO_ETIMEDOUT, "bucketed step not finished after %lld ms", (long long)timeout_ms);
     std::this_thread::sleep_for(std::chrono::microseconds(50));
   }
+}
+
+int zero_step_from_host(void* const* params, const void* const* host_grads, void* const* staging,
+                        zero_states_t* st, int64_t t, double lr, double beta1, double beta2,
+                        double eps, double weight_decay, void* host_params_out,
+                        int64_t chunk_bytes, zero_stream_t compute, zero_stream_t h2d,
+                        zero_stream_t d2h) {
+  if (!st) return fail(ZERO_EINVAL, "state handle is NULL");
+  if (!host_grads) return fail(ZERO_EINVAL, "host_grads array is NULL");
+  const int32_t N = st->N;
+  const int64_t n = st->n;
+  for (int32_t r = 0; r < N; ++r)
+    if (n > 0 && !host_grads[r]) return fail(ZERO_EINVAL, "host_grads[%d] is NULL", r);
+  int64_t B;
+  if (int e = bucket_elems(st->precision, chunk_bytes, &B)) return e;
+  zk::StepArgs a;
+  bool vec = false;
+  int phase = 0;
+  // the staging buffers are the kernel's gradient buffers
+  if (int e = prepare_step(params, staging, st, &a, &vec, &phase)) return e;
+  if (int e = adam_consts(t, lr, beta1, beta2, eps, weight_decay, &a.c)) return e;
+  if (n == 0) return ZERO_OK;
+  const size_t es = st->precision == ZERO_BF16_MIXED ? 2 : 4;
+  const int64_t count = (n + B - 1) / B;
+  const size_t need = size_t(2 * count + 2);
+  while (st->events.size() < need) {
+    cudaEvent_t ev;
+    cudaError_t ce = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
+    if (ce != cudaSuccess) return cuda_fail(ce, "cudaEventCreateWithFlags");
+    st->events.push_back(ev);
+  }
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(compute);
+  cudaStream_t hs = reinterpret_cast<cudaStream_t>(h2d);
+  cudaStream_t ds = reinterpret_cast<cudaStream_t>(d2h);
+  cudaEvent_t* ev = st->events.data();
+  auto ck = [&](cudaError_t ce, const char* what) { return ce == cudaSuccess ? 0 : cuda_fail(ce, what); };
+  // Copies start after everything already queued on `compute` (the previous
+  // step may still read the staging buffers or write the replicas).
+  if (int e = ck(cudaEventRecord(ev[0], cs), "cudaEventRecord")) return e;
+  if (int e = ck(cudaStreamWaitEvent(hs, ev[0], 0), "cudaStreamWaitEvent")) return e;
+  if (host_params_out)
+    if (int e = ck(cudaStreamWaitEvent(ds, ev[0], 0), "cudaStreamWaitEvent")) return e;
+  for (int64_t k = 0; k < count; ++k) {
+    const int64_t lo = k * B, hi = std::min<int64_t>(n, lo + B);
+    const size_t off = size_t(lo) * es, bytes = size_t(hi - lo) * es;
+    for (int32_t r = 0; r < N; ++r) {
+      cudaError_t ce = cudaMemcpyAsync(static_cast<char*>(staging[r]) + off,
+                                       static_cast<const char*>(host_grads[r]) + off, bytes,
+                                       cudaMemcpyHostToDevice, hs);
+      if (ce != cudaSuccess) return cuda_fail(ce, "host-to-device copy of a gradient chunk");
+    }
+    cudaEvent_t in_ready = ev[2 + 2 * k], out_ready = ev[3 + 2 * k];
+    if (int e = ck(cudaEventRecord(in_ready, hs), "cudaEventRecord")) return e;
+    if (int e = ck(cudaStreamWaitEvent(cs, in_ready, 0), "cudaStreamWaitEvent")) return e;
+    if (int e = launch_range(a, st, vec, phase, lo, hi, cs)) return e;
+    if (host_params_out) {
+      if (int e = ck(cudaEventRecord(out_ready, cs), "cudaEventRecord")) return e;
+      if (int e = ck(cudaStreamWaitEvent(ds, out_ready, 0), "cudaStreamWaitEvent")) return e;
+      cudaError_t ce = cudaMemcpyAsync(static_cast<char*>(host_params_out) + off,
+                                       static_cast<const char*>(params[0]) + off, bytes,
+                                       cudaMemcpyDeviceToHost, ds);
+      if (ce != cudaSuccess) return cuda_fail(ce, "device-to-host copy of a parameter chunk");
+    }
+  }
+  if (host_params_out) {
+    // `compute` completes only after the last parameter chunk reached the host
+    if (int e = ck(cudaEventRecord(ev[1], ds), "cudaEventRecord")) return e;
+    if (int e = ck(cudaStreamWaitEvent(cs, ev[1], 0), "cudaStreamWaitEvent")) return e;
+  }
+  return ZERO_OK;
 }
 
 int ddp_allreduce_mean(void* const* grads, int64_t n, int32_t N, int32_t precision,

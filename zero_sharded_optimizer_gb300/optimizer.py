@@ -2,8 +2,10 @@
 
 Wraps the C ABI: allocates the flat state (m, v, and the fp32 master in mixed
 precision) with PyTorch, keeps the step counter, and runs one fused step per
-call. Gradients may be CUDA tensors, or host tensors (ideally pinned) that are
-copied into device staging buffers on the step's stream first.
+call. Gradients may be CUDA tensors, or host tensors (ideally pinned): those go
+through zero_step_from_host, which copies them into device staging buffers
+chunk by chunk on a copy stream while earlier chunks are being stepped, and can
+copy the updated parameters back to a host buffer on a second copy stream.
 
 Checkpoint/resume: ``state_dict()`` / ``load_state_dict()`` copy the flat
 state and the step counter; continuing from a loaded state is bit-identical
@@ -43,24 +45,36 @@ class ZeroOptimizer:
 
     # ------------------------------------------------------------------ step --
 
-    def _device_grads(self, grads, stream):
-        if all(g.is_cuda for g in grads):
-            return grads
-        dt = torch.bfloat16 if self.precision == abi.ZERO_BF16_MIXED else torch.float32
+    def _staging_buffers(self):
         if self._staging is None:
+            dt = torch.bfloat16 if self.precision == abi.ZERO_BF16_MIXED else torch.float32
             self._staging = [torch.empty(self.n, dtype=dt, device=self.device)
                              for _ in range(self.N)]
-        s = stream if stream is not None else torch.cuda.current_stream(self.device)
-        with torch.cuda.stream(s):
-            for dst, src in zip(self._staging, grads):
-                dst.copy_(src, non_blocking=True)
+            self._h2d = torch.cuda.Stream(self.device)
+            self._d2h = torch.cuda.Stream(self.device)
         return self._staging
 
-    def step(self, params, grads, stream=None) -> int:
-        """One ZeRO step; returns the new step number t."""
-        g = self._device_grads(grads, stream)
-        abi.zero_step(params, g, self.states, self.t + 1, self.lr, self.beta1, self.beta2,
-                      self.eps, self.weight_decay, stream)
+    def step(self, params, grads, stream=None, host_params_out=None,
+             chunk_bytes: int = BUCKET_BYTES_25MIB) -> int:
+        """One ZeRO step; returns the new step number t.
+
+        With host gradients the copies are pipelined with the step; when
+        ``host_params_out`` (a host tensor of n elements) is given, the updated
+        parameters are copied into it as well. Synchronize ``stream`` (the
+        current stream by default) before reading it.
+        """
+        if all(g.is_cuda for g in grads):
+            abi.zero_step(params, grads, self.states, self.t + 1, self.lr, self.beta1,
+                          self.beta2, self.eps, self.weight_decay, stream)
+            if host_params_out is not None:
+                s = stream if stream is not None else torch.cuda.current_stream(self.device)
+                with torch.cuda.stream(s):
+                    host_params_out.copy_(params[0], non_blocking=True)
+        else:
+            staging = self._staging_buffers()
+            abi.zero_step_from_host(params, grads, staging, self.states, self.t + 1, self.lr,
+                                    self.beta1, self.beta2, self.eps, self.weight_decay,
+                                    host_params_out, chunk_bytes, stream, self._h2d, self._d2h)
         self.t += 1
         return self.t
 
