@@ -460,31 +460,40 @@ cudaError_t launch(K kernel, const A& args, int64_t work, cudaStream_t s) {
 }
 
 // One persistent CTA per SM (fewer when there are fewer tiles), with the
-// pipeline's shared memory.
-template <typename K, typename A>
-cudaError_t launch_tma(K kernel, const A& args, uint32_t smem, int64_t tiles, cudaStream_t s) {
-  const int sms = sm_count();
-  if (sms <= 0) return cudaErrorInvalidDevice;
-  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+// pipeline's shared memory. The shared-memory opt-in is set once per kernel and
+// device.
+template <auto kernel, int THREADS, typename A>
+cudaError_t launch_tma(const A& args, uint32_t smem, int64_t tiles, cudaStream_t s) {
+  static bool configured[256] = {false};  // per device ordinal; one array per kernel
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
+  const int sms = sm_count();
+  if (sms <= 0 || dev < 0 || dev >= 256) return cudaErrorInvalidDevice;
+  if (!configured[dev]) {
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    if (e != cudaSuccess) return e;
+    configured[dev] = true;
+  }
   const int blocks = int(tiles < 1 ? 1 : (tiles < sms ? tiles : sms));
-  kernel<<<blocks, kTmaThreads, smem, s>>>(args);
+  kernel<<<blocks, THREADS, smem, s>>>(args);
   return cudaGetLastError();
 }
 
-template <int NR, bool MIXED>
+template <int NR, bool MIXED, class Cfg = DefaultPipe>
 cudaError_t launch_step_tma(const StepArgs& a, cudaStream_t s) {
-  using G = StepTile<NR, MIXED>;
+  using G = StepTile<NR, MIXED, Cfg>;
   const int64_t nelem = a.sp.nvec * (MIXED ? 8 : 4);
-  return launch_tma(zero_step_tma_kernel<NR, MIXED>, a, G::kSmem, (nelem + G::T - 1) / G::T, s);
+  return launch_tma<zero_step_tma_kernel<NR, MIXED, Cfg>, Cfg::kThreads>(
+      a, G::kSmem, (nelem + G::T - 1) / G::T, s);
 }
 
-template <int NR, bool BF16>
+template <int NR, bool BF16, class Cfg = DefaultPipe>
 cudaError_t launch_mean_tma(const AllreduceArgs& a, cudaStream_t s) {
-  using G = MeanTile<NR, BF16>;
+  using G = MeanTile<NR, BF16, Cfg>;
   const int64_t nelem = a.sp.nvec * (BF16 ? 8 : 4);
-  return launch_tma(allreduce_mean_tma_kernel<NR, BF16>, a, G::kSmem, (nelem + G::T - 1) / G::T,
-                    s);
+  return launch_tma<allreduce_mean_tma_kernel<NR, BF16, Cfg>, Cfg::kThreads>(
+      a, G::kSmem, (nelem + G::T - 1) / G::T, s);
 }
 
 // Bulk-copy pipeline for N <= 8 when the buffers share a 16-byte phase (there

@@ -4,20 +4,21 @@
 // Pipeline (one CTA per SM, persistent over tiles tile = blockIdx.x + k*gridDim.x):
 //   * thread 0 issues, per tile, one cp.async.bulk global->shared copy per
 //     input stream (N gradient tiles, parameter/master, m, v) completing on the
-//     stage's mbarrier; three stages, so two tiles are in flight while one is
-//     computed;
-//   * all threads wait on the stage, compute, and write the results into one
-//     of two output buffers; thread 0 then issues cp.async.bulk shared->global
-//     copies of the results: m, v, (master,) and the same parameter tile N
-//     times -- the all-gather reads one shared tile N times instead of N
-//     register copies;
-//   * the input stage is refilled with the tile three ahead as soon as it has
-//     been computed (the results live in the output buffer), so two tiles are
-//     always loading while one computes; an output buffer is rewritten only
-//     after its previous bulk stores have read it (cp.async.bulk.wait_group.read).
+//     stage's mbarrier;
+//   * all threads wait on the stage, compute, and write the results either into
+//     one of two output buffers or back into the stage; thread 0 then issues
+//     cp.async.bulk shared->global copies of the results: m, v, (master,) and
+//     the same parameter tile N times -- the all-gather reads one shared tile N
+//     times instead of N register copies;
+//   * with output buffers, the input stage is refilled with the tile kStages
+//     ahead as soon as it has been computed, and an output buffer is rewritten
+//     only after its previous bulk stores have read it; computed in place, a
+//     stage is refilled once the stores reading it are done
+//     (cp.async.bulk.wait_group.read).
 // Large tiles (2048 elements, 8 KB per fp32 stream) give every stream long
-// contiguous DRAM bursts; measured on GB300 this moves the step's mix of
-// N+3 read and N+2 write streams at the device-to-device copy rate.
+// contiguous DRAM bursts. The pipeline shape (threads, stages, output buffers,
+// shared-memory budget) is a template parameter; DefaultPipe is the measured
+// choice.
 //
 // Every wait on an mbarrier is bounded by %globaltimer. When the bound runs
 // out the CTA sets ZK_STATUS_WAIT_TIMEOUT in the device status word, waits
@@ -105,82 +106,92 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-// ------------------------------------------------------------ tile geometry --
+// ------------------------------------------------------------ pipeline shape --
 
-constexpr int kTmaThreads = 512;
-constexpr int kTmaStages = 3;      // input stages
-constexpr int kTmaOutBufs = 2;     // output buffers
-constexpr int kTmaSmemBudget = 224 * 1024;
+// THREADS per CTA, STAGES input stages, OUTBUFS output buffers (0: results are
+// written back into the input stage), BUDGET bytes of dynamic shared memory.
+template <int THREADS, int STAGES, int OUTBUFS, int BUDGET>
+struct PipeCfg {
+  static constexpr int kThreads = THREADS;
+  static constexpr int kStages = STAGES;
+  static constexpr int kOutBufs = OUTBUFS;
+  // Tile size: the largest of 2048, 1536, 1024, 512 elements whose input stages
+  // (in_bytes per element) and output buffers (out_bytes per element) fit.
+  static constexpr int tile(int in_bytes, int out_bytes) {
+    return (STAGES * in_bytes + OUTBUFS * out_bytes) * 2048 <= BUDGET   ? 2048
+           : (STAGES * in_bytes + OUTBUFS * out_bytes) * 1536 <= BUDGET ? 1536
+           : (STAGES * in_bytes + OUTBUFS * out_bytes) * 1024 <= BUDGET ? 1024
+                                                                        : 512;
+  }
+};
 
-// Tile size: the largest of 2048, 1536, 1024, 512 elements whose input stages
-// (in_bytes per element) and output buffers (out_bytes per element) fit.
-constexpr int tile_elems(int in_bytes, int out_bytes) {
-  return (kTmaStages * in_bytes + kTmaOutBufs * out_bytes) * 2048 <= kTmaSmemBudget   ? 2048
-         : (kTmaStages * in_bytes + kTmaOutBufs * out_bytes) * 1536 <= kTmaSmemBudget ? 1536
-         : (kTmaStages * in_bytes + kTmaOutBufs * out_bytes) * 1024 <= kTmaSmemBudget ? 1024
-                                                                                       : 512;
-}
+using DefaultPipe = PipeCfg<512, 3, 2, 224 * 1024>;
 
-template <int NR, bool MIXED>
+template <int NR, bool MIXED, class Cfg>
 struct StepTile {
-  static constexpr int kGB = MIXED ? 2 : 4;        // gradient / replica element bytes
+  static constexpr int kGB = MIXED ? 2 : 4;           // gradient / replica element bytes
   static constexpr int kOutB = 12 + (MIXED ? 2 : 0);  // p/master, m, v (+ bf16 replica)
-  static constexpr int T = tile_elems(NR * kGB + 12, kOutB);
+  static constexpr int T = Cfg::tile(NR * kGB + 12, kOutB);
   static constexpr uint32_t kGradTile = uint32_t(T) * kGB;
   static constexpr uint32_t kFTile = uint32_t(T) * 4;
   static constexpr uint32_t kStage = NR * kGradTile + 3 * kFTile;
   static constexpr uint32_t kOut = uint32_t(T) * kOutB;
-  static constexpr uint32_t kSmem = kTmaStages * kStage + kTmaOutBufs * kOut;
+  static constexpr uint32_t kSmem = Cfg::kStages * kStage + Cfg::kOutBufs * kOut;
 };
 
-template <int NR, bool BF16>
+template <int NR, bool BF16, class Cfg>
 struct MeanTile {
   static constexpr int kGB = BF16 ? 2 : 4;
-  static constexpr int T = tile_elems(NR * kGB, kGB);
+  static constexpr int T = Cfg::tile(NR * kGB, kGB);
   static constexpr uint32_t kTile = uint32_t(T) * kGB;
   static constexpr uint32_t kStage = NR * kTile;
-  static constexpr uint32_t kSmem = kTmaStages * kStage + kTmaOutBufs * kTile;
+  static constexpr uint32_t kSmem = Cfg::kStages * kStage + Cfg::kOutBufs * kTile;
 };
 
 // Shared pipeline state of one CTA.
+template <int S>
 struct PipeState {
-  uint64_t full[kTmaStages];
-  int owner[kTmaStages];  // fp32 step: owner of the whole tile, -1 if it straddles
+  uint64_t full[S];
+  int owner[S];  // fp32 step: owner of the whole tile, -1 if it straddles
   int abort;
 };
 
 // On a timed-out wait: record it, then wait (bounded) for every tile this CTA
 // issued but has not consumed, so no bulk copy writes shared memory after exit.
-__device__ __forceinline__ void drain_after_timeout(PipeState& ps, int64_t consumed,
+template <int S>
+__device__ __forceinline__ void drain_after_timeout(PipeState<S>& ps, int64_t consumed,
                                                     int64_t issued) {
   atomicOr(&g_device_status, ZK_STATUS_WAIT_TIMEOUT);
   for (int64_t t = consumed; t < issued; ++t)
-    mbar_wait(&ps.full[t % kTmaStages], uint32_t((t / kTmaStages) & 1), kDrainNs);
+    mbar_wait(&ps.full[t % S], uint32_t((t / S) & 1), kDrainNs);
 }
 
 // The loop shared by both pipelines. `issue_load(local)` queues the bulk loads
-// of local tile `local` into stage local % kTmaStages; `compute(local, stage,
-// out)` turns stage `stage` into output buffer `out`; `issue_store(local, out)`
-// queues and commits the bulk stores of that output buffer.
-template <typename Load, typename Compute, typename Store>
-__device__ __forceinline__ void run_pipeline(PipeState& ps, int64_t my_tiles, uint64_t wait_ns,
-                                             Load issue_load, Compute compute,
-                                             Store issue_store) {
+// of local tile `local` into stage local % kStages; `compute(local, stage, out)`
+// turns stage `stage` into output buffer `out` (or back into the stage when
+// there are no output buffers); `issue_store(local, stage, out)` queues and
+// commits the bulk stores of the results.
+template <class Cfg, typename Load, typename Compute, typename Store>
+__device__ __forceinline__ void run_pipeline(PipeState<Cfg::kStages>& ps, int64_t my_tiles,
+                                             uint64_t wait_ns, Load issue_load,
+                                             Compute compute, Store issue_store) {
+  constexpr int S = Cfg::kStages;
+  constexpr int OB = Cfg::kOutBufs > 0 ? Cfg::kOutBufs : 1;
   const int tid = threadIdx.x;
   if (tid == 0) {
-    for (int s = 0; s < kTmaStages; ++s) mbar_init(&ps.full[s], 1);
+    for (int s = 0; s < S; ++s) mbar_init(&ps.full[s], 1);
     fence_mbar_init();
     ps.abort = 0;
   }
   __syncthreads();
   int64_t issued = 0;  // meaningful in thread 0 only
   if (tid == 0) {
-    for (; issued < kTmaStages && issued < my_tiles; ++issued) issue_load(issued);
+    for (; issued < S && issued < my_tiles; ++issued) issue_load(issued);
   }
   for (int64_t k = 0; k < my_tiles; ++k) {
-    const int s = int(k % kTmaStages);
-    const int o = int(k & 1);
-    if (tid == 0 && !mbar_wait(&ps.full[s], uint32_t((k / kTmaStages) & 1), wait_ns)) {
+    const int s = int(k % S);
+    const int o = int(k % OB);
+    if (tid == 0 && !mbar_wait(&ps.full[s], uint32_t((k / S) & 1), wait_ns)) {
       ps.abort = 1;
       drain_after_timeout(ps, k, issued);
     }
@@ -190,9 +201,14 @@ __device__ __forceinline__ void run_pipeline(PipeState& ps, int64_t my_tiles, ui
     fence_proxy_async_smem();
     __syncthreads();
     if (tid == 0) {
-      issue_store(k, o);
-      if (issued < my_tiles) issue_load(issued++);  // into stage s, just consumed
-      bulk_wait_read_all_but_last();  // output buffer 1-o is free for tile k+1
+      issue_store(k, s, o);
+      if constexpr (Cfg::kOutBufs > 0) {
+        if (issued < my_tiles) issue_load(issued++);  // into stage s, just consumed
+        bulk_wait_read_all_but_last();  // the next output buffer has been read out
+      } else if (k >= 1) {
+        bulk_wait_read_all_but_last();  // stores of tile k-1 have read their stage
+        if (issued < my_tiles) issue_load(issued++);  // into the stage of tile k-1
+      }
     }
   }
   if (tid == 0) bulk_wait_all();
@@ -200,14 +216,16 @@ __device__ __forceinline__ void run_pipeline(PipeState& ps, int64_t my_tiles, ui
 
 // ------------------------------------------------------------ the fused step --
 
-template <int NR, bool MIXED>
-__global__ void __launch_bounds__(kTmaThreads, 1)
+template <int NR, bool MIXED, class Cfg = DefaultPipe>
+__global__ void __launch_bounds__(Cfg::kThreads, 1)
     zero_step_tma_kernel(const __grid_constant__ StepArgs P) {
-  using G = StepTile<NR, MIXED>;
+  using G = StepTile<NR, MIXED, Cfg>;
   constexpr int T = G::T;
   constexpr int V = MIXED ? 8 : 4;
+  constexpr int S = Cfg::kStages;
+  constexpr int TH = Cfg::kThreads;
   extern __shared__ __align__(128) unsigned char smem[];
-  __shared__ PipeState ps;
+  __shared__ PipeState<S> ps;
   const int tid = threadIdx.x;
   const Split& sp = P.sp;
 
@@ -235,12 +253,13 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
   auto in_f = [&](int s, int k) {  // 0 = parameter / master, 1 = m, 2 = v
     return reinterpret_cast<float*>(stage(s) + NR * G::kGradTile + k * G::kFTile);
   };
-  auto out_f = [&](int o, int k) {  // 0 = parameter / master, 1 = m, 2 = v
-    return reinterpret_cast<float*>(smem + kTmaStages * G::kStage + o * G::kOut +
-                                    k * G::kFTile);
+  auto out_f = [&](int s, int o, int k) {
+    if constexpr (Cfg::kOutBufs == 0) return in_f(s, k);
+    return reinterpret_cast<float*>(smem + S * G::kStage + o * G::kOut + k * G::kFTile);
   };
-  auto out_bf = [&](int o) {  // mixed: the bf16 replica tile
-    return smem + kTmaStages * G::kStage + o * G::kOut + 3 * G::kFTile;
+  auto out_bf = [&](int s, int o) {  // mixed: the bf16 replica tile
+    if constexpr (Cfg::kOutBufs == 0) return grad_slot(s, 0);  // consumed gradient slot
+    return smem + S * G::kStage + o * G::kOut + 3 * G::kFTile;
   };
   auto tile_j0 = [&](int64_t local) { return base + (blockIdx.x + local * gridDim.x) * T; };
   auto tile_cnt = [&](int64_t local) {
@@ -249,7 +268,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
   };
 
   auto issue_load = [&](int64_t local) {
-    const int s = int(local % kTmaStages);
+    const int s = int(local % S);
     const int64_t j0 = tile_j0(local);
     const uint32_t cnt = tile_cnt(local);
     const uint32_t gbytes = cnt * G::kGB, fbytes = cnt * 4;
@@ -276,21 +295,21 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
     bulk_load(in_f(s, 2), P.v + j0, fbytes, &ps.full[s]);
   };
 
-  auto issue_store = [&](int64_t local, int o) {
+  auto issue_store = [&](int64_t local, int s, int o) {
     const int64_t j0 = tile_j0(local);
     const uint32_t cnt = tile_cnt(local);
     const uint32_t fbytes = cnt * 4;
-    bulk_store(P.m + j0, out_f(o, 1), fbytes);
-    bulk_store(P.v + j0, out_f(o, 2), fbytes);
+    bulk_store(P.m + j0, out_f(s, o, 1), fbytes);
+    bulk_store(P.v + j0, out_f(s, o, 2), fbytes);
     if constexpr (MIXED) {
-      bulk_store(P.master + j0, out_f(o, 0), fbytes);
+      bulk_store(P.master + j0, out_f(s, o, 0), fbytes);
 #pragma unroll
       for (int r = 0; r < NR; ++r)
-        bulk_store(static_cast<unsigned char*>(P.reps[r]) + j0 * 2, out_bf(o), cnt * 2);
+        bulk_store(static_cast<unsigned char*>(P.reps[r]) + j0 * 2, out_bf(s, o), cnt * 2);
     } else {
 #pragma unroll
       for (int r = 0; r < NR; ++r)
-        bulk_store(static_cast<float*>(P.reps[r]) + j0, out_f(o, 0), fbytes);
+        bulk_store(static_cast<float*>(P.reps[r]) + j0, out_f(s, o, 0), fbytes);
     }
     bulk_commit();
   };
@@ -301,79 +320,70 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
     const float* pi = in_f(s, 0);
     const float* mi = in_f(s, 1);
     const float* vi = in_f(s, 2);
-    float* po = out_f(o, 0);
-    float* mo = out_f(o, 1);
-    float* vo = out_f(o, 2);
-    if constexpr (!MIXED) {
-      const int owner = ps.owner[s];
-      for (int q = tid * 4; q < cnt; q += kTmaThreads * 4) {
-        float4 g = *reinterpret_cast<const float4*>(grad_slot(s, 0) + q * 4);
-#pragma unroll
-        for (int r = 1; r < NR; ++r) {
-          const float4 h = *reinterpret_cast<const float4*>(grad_slot(s, r) + q * 4);
-          g.x = __fadd_rn(g.x, h.x); g.y = __fadd_rn(g.y, h.y);
-          g.z = __fadd_rn(g.z, h.z); g.w = __fadd_rn(g.w, h.w);
-        }
-        float4 p;
-        if (owner >= 0) {
-          p = *reinterpret_cast<const float4*>(pi + q);
-        } else {  // the tile straddles a shard boundary: per-element owners
-          float e[4];
-          int ow = 0;
-          for (int i = 0; i < 4; ++i) {
-            ow = advance_owner(P, ow, j0 + q + i);
-            e[i] = __ldcs(static_cast<const float*>(P.reps[ow]) + j0 + q + i);
-          }
-          p = make_float4(e[0], e[1], e[2], e[3]);
-        }
-        float4 m = *reinterpret_cast<const float4*>(mi + q);
-        float4 v = *reinterpret_cast<const float4*>(vi + q);
-        adam1(P.c, mean_of<NR>(g.x, P.fN), p.x, m.x, v.x);
-        adam1(P.c, mean_of<NR>(g.y, P.fN), p.y, m.y, v.y);
-        adam1(P.c, mean_of<NR>(g.z, P.fN), p.z, m.z, v.z);
-        adam1(P.c, mean_of<NR>(g.w, P.fN), p.w, m.w, v.w);
-        *reinterpret_cast<float4*>(po + q) = p;
-        *reinterpret_cast<float4*>(mo + q) = m;
-        *reinterpret_cast<float4*>(vo + q) = v;
-      }
-    } else {
-      // four elements per thread: one uint2 of bf16 per rank, float4s of state
-      for (int q = tid * 4; q < cnt; q += kTmaThreads * 4) {
-        float4 g = unpack4(*reinterpret_cast<const uint2*>(grad_slot(s, 0) + q * 2));
+    float* po = out_f(s, o, 0);
+    float* mo = out_f(s, o, 1);
+    float* vo = out_f(s, o, 2);
+    // four elements per thread: float4s of fp32, or one uint2 of bf16 per rank
+    for (int q = tid * 4; q < cnt; q += TH * 4) {
+      float4 g;
+      if constexpr (MIXED) {
+        g = unpack4(*reinterpret_cast<const uint2*>(grad_slot(s, 0) + q * 2));
 #pragma unroll
         for (int r = 1; r < NR; ++r) {
           const float4 h = unpack4(*reinterpret_cast<const uint2*>(grad_slot(s, r) + q * 2));
           g.x = __fadd_rn(g.x, h.x); g.y = __fadd_rn(g.y, h.y);
           g.z = __fadd_rn(g.z, h.z); g.w = __fadd_rn(g.w, h.w);
         }
-        float4 p = *reinterpret_cast<const float4*>(pi + q);
-        float4 m = *reinterpret_cast<const float4*>(mi + q);
-        float4 v = *reinterpret_cast<const float4*>(vi + q);
-        adam1(P.c, mean_of<NR>(g.x, P.fN), p.x, m.x, v.x);
-        adam1(P.c, mean_of<NR>(g.y, P.fN), p.y, m.y, v.y);
-        adam1(P.c, mean_of<NR>(g.z, P.fN), p.z, m.z, v.z);
-        adam1(P.c, mean_of<NR>(g.w, P.fN), p.w, m.w, v.w);
-        *reinterpret_cast<float4*>(po + q) = p;
-        *reinterpret_cast<float4*>(mo + q) = m;
-        *reinterpret_cast<float4*>(vo + q) = v;
-        *reinterpret_cast<uint2*>(out_bf(o) + q * 2) = pack4(p);
+      } else {
+        g = *reinterpret_cast<const float4*>(grad_slot(s, 0) + q * 4);
+#pragma unroll
+        for (int r = 1; r < NR; ++r) {
+          const float4 h = *reinterpret_cast<const float4*>(grad_slot(s, r) + q * 4);
+          g.x = __fadd_rn(g.x, h.x); g.y = __fadd_rn(g.y, h.y);
+          g.z = __fadd_rn(g.z, h.z); g.w = __fadd_rn(g.w, h.w);
+        }
       }
+      float4 p;
+      if (MIXED || ps.owner[s] >= 0) {
+        p = *reinterpret_cast<const float4*>(pi + q);
+      } else {  // the fp32 tile straddles a shard boundary: per-element owners
+        float e[4];
+        int ow = 0;
+        for (int i = 0; i < 4; ++i) {
+          ow = advance_owner(P, ow, j0 + q + i);
+          e[i] = __ldcs(static_cast<const float*>(P.reps[ow]) + j0 + q + i);
+        }
+        p = make_float4(e[0], e[1], e[2], e[3]);
+      }
+      float4 m = *reinterpret_cast<const float4*>(mi + q);
+      float4 v = *reinterpret_cast<const float4*>(vi + q);
+      adam1(P.c, mean_of<NR>(g.x, P.fN), p.x, m.x, v.x);
+      adam1(P.c, mean_of<NR>(g.y, P.fN), p.y, m.y, v.y);
+      adam1(P.c, mean_of<NR>(g.z, P.fN), p.z, m.z, v.z);
+      adam1(P.c, mean_of<NR>(g.w, P.fN), p.w, m.w, v.w);
+      *reinterpret_cast<float4*>(po + q) = p;
+      *reinterpret_cast<float4*>(mo + q) = m;
+      *reinterpret_cast<float4*>(vo + q) = v;
+      // in place, this thread's own 8 bytes of the consumed gradient slot
+      if constexpr (MIXED) *reinterpret_cast<uint2*>(out_bf(s, o) + q * 2) = pack4(p);
     }
   };
 
-  run_pipeline(ps, my_tiles, P.wait_ns, issue_load, compute, issue_store);
+  run_pipeline<Cfg>(ps, my_tiles, P.wait_ns, issue_load, compute, issue_store);
 }
 
 // ---------------------------------------------------------- the DDP mean --
 
-template <int NR, bool BF16>
-__global__ void __launch_bounds__(kTmaThreads, 1)
+template <int NR, bool BF16, class Cfg = DefaultPipe>
+__global__ void __launch_bounds__(Cfg::kThreads, 1)
     allreduce_mean_tma_kernel(const __grid_constant__ AllreduceArgs P) {
-  using G = MeanTile<NR, BF16>;
+  using G = MeanTile<NR, BF16, Cfg>;
   constexpr int T = G::T;
   constexpr int V = BF16 ? 8 : 4;
+  constexpr int S = Cfg::kStages;
+  constexpr int TH = Cfg::kThreads;
   extern __shared__ __align__(128) unsigned char smem[];
-  __shared__ PipeState ps;
+  __shared__ PipeState<S> ps;
   const int tid = threadIdx.x;
   const Split& sp = P.sp;
 
@@ -394,14 +404,17 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
   if (my_tiles == 0) return;
 
   auto slot = [&](int s, int r) { return smem + size_t(s) * G::kStage + r * G::kTile; };
-  auto out = [&](int o) { return smem + size_t(kTmaStages) * G::kStage + o * G::kTile; };
+  auto out = [&](int s, int o) {
+    if constexpr (Cfg::kOutBufs == 0) return slot(s, 0);
+    return smem + size_t(S) * G::kStage + o * G::kTile;
+  };
   auto tile_j0 = [&](int64_t local) { return base + (blockIdx.x + local * gridDim.x) * T; };
   auto tile_cnt = [&](int64_t local) {
     const int64_t rem = nelem - (blockIdx.x + local * gridDim.x) * int64_t(T);
     return uint32_t(rem < T ? rem : T);
   };
   auto issue_load = [&](int64_t local) {
-    const int s = int(local % kTmaStages);
+    const int s = int(local % S);
     const int64_t j0 = tile_j0(local);
     const uint32_t bytes = tile_cnt(local) * G::kGB;
     mbar_expect_tx(&ps.full[s], NR * bytes);
@@ -410,45 +423,45 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
       bulk_load(slot(s, r), static_cast<const unsigned char*>(P.grads[r]) + j0 * G::kGB, bytes,
                 &ps.full[s]);
   };
-  auto issue_store = [&](int64_t local, int o) {
+  auto issue_store = [&](int64_t local, int s, int o) {
     const int64_t j0 = tile_j0(local);
     const uint32_t bytes = tile_cnt(local) * G::kGB;
 #pragma unroll
     for (int r = 0; r < NR; ++r)
-      bulk_store(static_cast<unsigned char*>(P.grads[r]) + j0 * G::kGB, out(o), bytes);
+      bulk_store(static_cast<unsigned char*>(P.grads[r]) + j0 * G::kGB, out(s, o), bytes);
     bulk_commit();
   };
   auto compute = [&](int64_t local, int s, int o) {
     const int cnt = int(tile_cnt(local));
-    if constexpr (BF16) {
-      for (int q = tid * 4; q < cnt; q += kTmaThreads * 4) {
-        float4 g = unpack4(*reinterpret_cast<const uint2*>(slot(s, 0) + q * 2));
+    for (int q = tid * 4; q < cnt; q += TH * 4) {
+      float4 g;
+      if constexpr (BF16) {
+        g = unpack4(*reinterpret_cast<const uint2*>(slot(s, 0) + q * 2));
 #pragma unroll
         for (int r = 1; r < NR; ++r) {
           const float4 h = unpack4(*reinterpret_cast<const uint2*>(slot(s, r) + q * 2));
           g.x = __fadd_rn(g.x, h.x); g.y = __fadd_rn(g.y, h.y);
           g.z = __fadd_rn(g.z, h.z); g.w = __fadd_rn(g.w, h.w);
         }
-        g.x = mean_of<NR>(g.x, P.fN); g.y = mean_of<NR>(g.y, P.fN);
-        g.z = mean_of<NR>(g.z, P.fN); g.w = mean_of<NR>(g.w, P.fN);
-        *reinterpret_cast<uint2*>(out(o) + q * 2) = pack4(g);
-      }
-    } else {
-      for (int q = tid * 4; q < cnt; q += kTmaThreads * 4) {
-        float4 g = *reinterpret_cast<const float4*>(slot(s, 0) + q * 4);
+      } else {
+        g = *reinterpret_cast<const float4*>(slot(s, 0) + q * 4);
 #pragma unroll
         for (int r = 1; r < NR; ++r) {
           const float4 h = *reinterpret_cast<const float4*>(slot(s, r) + q * 4);
           g.x = __fadd_rn(g.x, h.x); g.y = __fadd_rn(g.y, h.y);
           g.z = __fadd_rn(g.z, h.z); g.w = __fadd_rn(g.w, h.w);
         }
-        g.x = mean_of<NR>(g.x, P.fN); g.y = mean_of<NR>(g.y, P.fN);
-        g.z = mean_of<NR>(g.z, P.fN); g.w = mean_of<NR>(g.w, P.fN);
-        *reinterpret_cast<float4*>(out(o) + q * 4) = g;
+      }
+      g.x = mean_of<NR>(g.x, P.fN); g.y = mean_of<NR>(g.y, P.fN);
+      g.z = mean_of<NR>(g.z, P.fN); g.w = mean_of<NR>(g.w, P.fN);
+      if constexpr (BF16) {
+        *reinterpret_cast<uint2*>(out(s, o) + q * 2) = pack4(g);
+      } else {
+        *reinterpret_cast<float4*>(out(s, o) + q * 4) = g;
       }
     }
   };
-  run_pipeline(ps, my_tiles, P.wait_ns, issue_load, compute, issue_store);
+  run_pipeline<Cfg>(ps, my_tiles, P.wait_ns, issue_load, compute, issue_store);
 }
 
 }  // namespace
