@@ -27,6 +27,10 @@ ranks and workers only):
   "Data parallelism and ZeRO stages 1 to 3", section 3).
 * ``bucket_bounds``  -- 25 MiB gradient buckets built from the end of the flat
   gradient ("ZeRO One: Sharding the Optimizer", section "Bucketing").
+* ``grad_norm`` / ``grad_multiplier`` -- the global gradient norm from squared
+  chunk norms, and the clip / accumulation factor applied to the mean gradient
+  ("Data parallelism and ZeRO stages 1 to 3", "Going further"; "Data
+  Parallelism & ZeRO", "Two more things you'll actually hit").
 
 Arithmetic modes:
 
@@ -53,6 +57,8 @@ Readings taken where the pages are silent (each is listed in the design notes):
    are upcast exactly, the mean is kept in fp32, replicas are the
    round-to-nearest-even bf16 of the new master.
 5. NaN/Inf propagate as IEEE arithmetic gives them.
+6. Clipping: coefficient max_norm / (norm + 1e-6) capped at 1, applied with the
+   accumulation factor as one float64 multiplier rounded to float32.
 
 Parity status: every function here is pinned by a CPU test against values the
 pages print, closed forms, invariants or library routines (np.array_split,
@@ -68,6 +74,7 @@ import numpy as np
 __all__ = [
     "FP32", "BF16_MIXED", "FP64_EMU",
     "shard_bounds", "init_states", "zero_step", "adam_full", "allreduce_mean",
+    "grad_norm", "grad_multiplier",
     "memory_bytes", "memory_breakdown", "bucket_bounds",
     "bf16_to_f32", "f32_to_bf16_rne", "mirror_scalars",
 ]
@@ -253,8 +260,45 @@ def _all_gather(new_shards, N, precision, mode):
     return [replica.copy() for _ in range(N)]
 
 
+def grad_norm(grads, precision=FP32, mode="fp32") -> float:
+    """Global L2 norm of the mean gradient, assembled from the shards.
+
+    "Data parallelism and ZeRO stages 1 to 3", "Going further" (clipping):
+    sharded global-norm clipping all-reduces the squared norms of the chunks
+    before the step. Each worker squares and sums its shard of the mean
+    gradient (float64 sums of the mode's mean values); the N squared chunk
+    norms are added in rank order and the square root taken.
+    """
+    N = len(grads)
+    n = len(grads[0])
+    bounds = shard_bounds(n, N)
+    total = 0.0
+    for i in range(N):
+        a, b = bounds[i], bounds[i + 1]
+        g_bar = _reduce_scatter_mean(grads, a, b, precision, mode).astype(np.float64)
+        total += float(np.sum(g_bar * g_bar))           # squared chunk norm
+    return math.sqrt(total)
+
+
+def grad_multiplier(norm: float, grad_scale: float = 1.0, max_grad_norm=None) -> float:
+    """The factor that multiplies the mean gradient before the update.
+
+    ``grad_scale`` turns a sum of k accumulated micro-batch gradients into their
+    mean (1/k; "Data Parallelism & ZeRO", "Two more things you'll actually
+    hit": scale by 1/k so the accumulated gradient is a mean). With
+    ``max_grad_norm`` the scaled gradient is clipped to that global norm; the
+    pages give no formula, the reading is the usual one: coefficient
+    max_norm / (norm + 1e-6), never above 1. Formed in float64.
+    """
+    coef = 1.0
+    if max_grad_norm is not None and max_grad_norm > 0:
+        coef = min(1.0, max_grad_norm / (grad_scale * norm + 1e-6))
+    return grad_scale * coef
+
+
 def zero_step(params, grads, states, t, lr=1e-2, beta1=0.9, beta2=0.999, eps=1e-8,
-              weight_decay=0.0, precision=FP32, mode="fp32"):
+              weight_decay=0.0, precision=FP32, mode="fp32", grad_scale=1.0,
+              max_grad_norm=None):
     """One ZeRO step; returns (new_params, new_states).
 
     ``params``: N full-length replicas (float32, or bf16 bits as uint16).
@@ -268,16 +312,26 @@ def zero_step(params, grads, states, t, lr=1e-2, beta1=0.9, beta2=0.999, eps=1e-
          source is its own replica's shard in fp32, its master in mixed mode);
       3. all-gather: the updated shards are concatenated and every worker's
          replica becomes the full updated vector.
+    With ``grad_scale`` != 1 or ``max_grad_norm`` set, the mean gradient is
+    first multiplied by ``grad_multiplier`` (rounded to float32 in the fp32
+    mode); the global norm it needs comes from ``grad_norm`` of the same
+    gradients.
     """
     N = len(grads)
     if len(params) != N or len(states) != N:
         raise ValueError("params, grads and states need one entry per worker")
     n = len(params[0])
     bounds = shard_bounds(n, N)
+    mult = None
+    if grad_scale != 1.0 or (max_grad_norm is not None and max_grad_norm > 0):
+        norm = grad_norm(grads, precision, mode) if max_grad_norm else 0.0
+        mult = _dtype(mode)(grad_multiplier(norm, grad_scale, max_grad_norm))
     new_shards, new_states = [], []
     for i in range(N):                                   # loop over workers only
         a, b = bounds[i], bounds[i + 1]
         g_bar = _reduce_scatter_mean(grads, a, b, precision, mode)          # 1.
+        if mult is not None:
+            g_bar = g_bar * mult
         st = states[i]
         if precision == BF16_MIXED:
             p_src = st["master"]

@@ -479,3 +479,66 @@ def test_mutant_dropped_hyperparameters(monkeypatch):
         return real(params, grads, states, t, **kw)
     monkeypatch.setattr(oracle, "zero_step", default_lr)
     assert _fails(lambda: test_p2_worked_example("fp64"))
+
+
+# ---------------------------------------------------------------------------
+# Global-norm clipping and the accumulation factor
+# ---------------------------------------------------------------------------
+
+def test_grad_norm_closed_form():
+    # a constant mean gradient c on n entries has norm |c| sqrt(n), whatever the shards
+    for n, N in [(10, 4), (1001, 3), (64, 8)]:
+        grads = [np.full(n, 3.0 * (r + 1), np.float32) for r in range(N)]
+        c = 3.0 * (N + 1) / 2
+        assert oracle.grad_norm(grads, mode="fp64") == pytest.approx(abs(c) * math.sqrt(n),
+                                                                      rel=1e-15)
+
+
+@pytest.mark.parametrize("max_norm,scale", [(0.5, 1.0), (100.0, 1.0), (0.05, 0.25), (None, 0.5)])
+def test_clipped_step_matches_torch(max_norm, scale):
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(31)
+    n, N, lr, b1, b2, eps, wd = 777, 4, 1e-3, 0.9, 0.95, 1e-8, 0.1
+    p0 = rng.normal(0, 0.02, size=n)
+    p = torch.tensor(p0, dtype=torch.float64, requires_grad=True)
+    opt = torch.optim.AdamW([p], lr=lr, betas=(b1, b2), eps=eps, weight_decay=wd, foreach=False)
+    params = [p0.copy() for _ in range(N)]
+    states = oracle.init_states(n, N, mode="fp64")
+    for t in range(1, 5):
+        grads = [rng.normal(0, 0.05, size=n) for _ in range(N)]
+        gbar = np.mean(np.stack(grads), 0) * scale
+        p.grad = torch.tensor(gbar, dtype=torch.float64)
+        if max_norm is not None:
+            total = torch.nn.utils.clip_grad_norm_([p], max_norm)
+            assert oracle.grad_norm(grads, mode="fp64") * scale == pytest.approx(float(total),
+                                                                                  rel=1e-12)
+        opt.step()
+        params, states = oracle.zero_step(params, grads, states, t, lr=lr, beta1=b1, beta2=b2,
+                                          eps=eps, weight_decay=wd, mode="fp64",
+                                          grad_scale=scale, max_grad_norm=max_norm)
+        np.testing.assert_allclose(params[0], p.detach().numpy(), rtol=1e-11, atol=1e-16)
+
+
+def test_accumulation_factor_equals_mean_of_micro_batches():
+    # k micro-batches summed with factor 1/k is the step on their mean (exact in
+    # float64 for k a power of two)
+    rng = np.random.default_rng(32)
+    n, N, k = 513, 2, 4
+    micro = [[rng.normal(size=n) for _ in range(N)] for _ in range(k)]
+    summed = [sum(micro[i][r] for i in range(k)) for r in range(N)]
+    mean = [summed[r] / k for r in range(N)]
+    p0 = rng.normal(size=n)
+    a, _ = oracle.zero_step([p0] * N, summed, oracle.init_states(n, N, mode="fp64"), 1,
+                            mode="fp64", grad_scale=1.0 / k)
+    b, _ = oracle.zero_step([p0] * N, mean, oracle.init_states(n, N, mode="fp64"), 1,
+                            mode="fp64")
+    assert np.array_equal(a[0], b[0])
+
+
+def test_mutant_clip_on_sum_of_gradients(monkeypatch):
+    real = zo.grad_norm
+
+    def norm_of_sum(grads, precision=oracle.FP32, mode="fp32"):
+        return real(grads, precision, mode) * len(grads)
+    monkeypatch.setattr(zo, "grad_norm", norm_of_sum)
+    assert _fails(lambda: test_clipped_step_matches_torch(0.5, 1.0))
