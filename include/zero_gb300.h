@@ -133,6 +133,52 @@ int zero_step_range(void *const *params, const void *const *grads, zero_states_t
                     int64_t t, double lr, double beta1, double beta2, double eps,
                     double weight_decay, int64_t lo, int64_t hi, zero_stream_t stream);
 
+/* ----------------------------------------------- clipping, accumulation -- */
+
+/* Squared global L2 norm of the mean gradient, ||(1/N) sum_r g_r||^2, written
+ * to the DEVICE scalar *norm_sq (queued on `stream`). This is the first half
+ * of sharded global-norm clipping ("Data parallelism and ZeRO stages 1 to 3",
+ * "Going further": an all-reduce of the squared chunk norms before the step):
+ * the float mean of every element (rank order, as in the step) is squared
+ * exactly in double; fixed chunks of 32,768 elements give partial sums in
+ * `scratch` (a DEVICE buffer of at least zero_grad_norm_scratch_count doubles,
+ * caller-owned, contents overwritten), which one block adds in a fixed order.
+ * The result does not depend on the GPU's size and is bit-reproducible.
+ * Errors: EINVAL (n < 0, N outside [1, ZERO_MAX_RANKS], bad precision, NULL,
+ * scratch too small, overlapping buffers), EALIGN, ECUDA. */
+int zero_grad_norm_scratch_count(int64_t n, int32_t precision, int64_t *count);
+int zero_grad_norm_sq(const void *const *grads, int64_t n, int32_t N, int32_t precision,
+                      double *scratch, int64_t scratch_count, double *norm_sq,
+                      zero_stream_t stream);
+
+/* Options of zero_step_ex. */
+typedef struct zero_step_opts {
+  int64_t t;             /* step number, >= 1 */
+  double lr, beta1, beta2, eps, weight_decay;
+  /* Multiplies the mean gradient: 1.0 leaves it as is; 1/k turns the sum of k
+   * accumulated micro-batch gradients into their mean ("Data Parallelism &
+   * ZeRO", "Two more things you'll actually hit"). Finite, > 0. */
+  double grad_scale;
+  /* > 0: clip the scaled mean gradient to this global L2 norm with the
+   * coefficient min(1, max_grad_norm / (grad_scale * sqrt(*norm_sq) + 1e-6));
+   * <= 0: no clipping. */
+  double max_grad_norm;
+  /* DEVICE scalar from zero_grad_norm_sq on the same gradients, read on the
+   * device when the step runs (no host synchronisation); required when
+   * clipping, ignored otherwise. */
+  const double *norm_sq;
+  int64_t lo, hi;        /* index range of the step; hi < 0 means n */
+} zero_step_opts_t;
+
+/* zero_step with the options above. The multiplier grad_scale * coefficient
+ * is formed on the device in double and rounded to float once; the mean
+ * gradient is multiplied by it (one IEEE fp32 multiply) before the update.
+ * With grad_scale = 1 and no clipping the result equals zero_step bit for bit.
+ * Errors: as zero_step_range, plus EINVAL for a bad grad_scale or
+ * max_grad_norm, or clipping without norm_sq. */
+int zero_step_ex(void *const *params, const void *const *grads, zero_states_t *st,
+                 const zero_step_opts_t *opts, zero_stream_t stream);
+
 /* --------------------------------------------------------------- buckets -- */
 
 /* Gradient buckets ("ZeRO One: Sharding the Optimizer", section "Bucketing":

@@ -69,6 +69,9 @@ _SIGNATURES = {
     "ddp_allreduce_mean": (ctypes.c_int, [_P(_vp), _i64, _i32, _i32, _vp]),
     "zero_memory_bytes": (ctypes.c_int, [_i64, _i32, _i32, _i32, _P(_u64)]),
     "zero_memory_breakdown": (ctypes.c_int, [_i64, _i32, _i32, _i32, _i32, _P(_u64)]),
+    "zero_grad_norm_scratch_count": (ctypes.c_int, [_i64, _i32, _P(_i64)]),
+    "zero_grad_norm_sq": (ctypes.c_int, [_P(_vp), _i64, _i32, _i32, _vp, _i64, _vp, _vp]),
+    "zero_step_ex": (ctypes.c_int, [_P(_vp), _P(_vp), _vp, _vp, _vp]),
     "zero_device_status": (ctypes.c_int, [_P(ctypes.c_uint32), _i32]),
     "zero_debug_set_wait_timeout_ns": (ctypes.c_int, [_u64]),
     "zero_strerror": (ctypes.c_char_p, [ctypes.c_int]),
@@ -285,6 +288,49 @@ def zero_step_bucketed(params, grads, st: ZeroStates, t: int, lr: float, beta1: 
     _check(_lib.zero_step_bucketed(pp, gp, st.handle, t, lr, beta1, beta2, eps, weight_decay,
                                    bucket_bytes, arr, count, _stream(side), _event_to_record(done),
                                    timeout_ms), "zero_step_bucketed")
+
+
+class StepOpts(ctypes.Structure):
+    """zero_step_opts_t."""
+    _fields_ = [("t", _i64), ("lr", _dbl), ("beta1", _dbl), ("beta2", _dbl), ("eps", _dbl),
+                ("weight_decay", _dbl), ("grad_scale", _dbl), ("max_grad_norm", _dbl),
+                ("norm_sq", _vp), ("lo", _i64), ("hi", _i64)]
+
+
+def _f64_device_ptr(t, count: int, what: str):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dtype != torch.float64:
+        raise TypeError(f"{what} must be a float64 CUDA tensor")
+    if not t.is_contiguous() or t.numel() < count:
+        raise ValueError(f"{what} must be contiguous with at least {count} elements")
+    return t.data_ptr()
+
+
+def zero_grad_norm_scratch_count(n: int, precision: int) -> int:
+    out = _i64()
+    _check(_lib.zero_grad_norm_scratch_count(n, precision, ctypes.byref(out)),
+           "zero_grad_norm_scratch_count")
+    return out.value
+
+
+def zero_grad_norm_sq(grads, precision: int, scratch, norm_sq, n: int | None = None,
+                      stream=None):
+    """Queue ||mean of grads||^2 into the float64 CUDA scalar ``norm_sq``."""
+    n = grads[0].numel() if n is None else n
+    gp = _ptr_array(grads, n, _storage_dtype(precision), "grads")
+    sp = _f64_device_ptr(scratch, 1, "scratch")
+    op = _f64_device_ptr(norm_sq, 1, "norm_sq")
+    _check(_lib.zero_grad_norm_sq(gp, n, len(grads), precision, sp, scratch.numel(), op,
+                                  _stream(stream)), "zero_grad_norm_sq")
+
+
+def zero_step_ex(params, grads, st: ZeroStates, t: int, lr: float, beta1: float = 0.9,
+                 beta2: float = 0.999, eps: float = 1e-8, weight_decay: float = 0.0,
+                 grad_scale: float = 1.0, max_grad_norm: float = 0.0, norm_sq=None,
+                 lo: int = 0, hi: int = -1, stream=None):
+    pp, gp = _step_ptrs(params, grads, st)
+    nq = None if norm_sq is None else _f64_device_ptr(norm_sq, 1, "norm_sq")
+    o = StepOpts(t, lr, beta1, beta2, eps, weight_decay, grad_scale, max_grad_norm, nq, lo, hi)
+    _check(_lib.zero_step_ex(pp, gp, st.handle, ctypes.byref(o), _stream(stream)), "zero_step_ex")
 
 
 def _host_ptr_array(tensors, n: int, dtype, what: str):

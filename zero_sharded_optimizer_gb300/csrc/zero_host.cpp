@@ -135,6 +135,9 @@ int prepare_step(void* const* params, const void* const* grads, const zero_state
   a->N = N;
   a->fN = float(N);
   a->wait_ns = g_wait_ns.load(std::memory_order_relaxed);
+  a->norm_sq = nullptr;  // no clipping
+  a->gscale = 1.0;       // mean gradient used as is
+  a->max_norm = 0.0;
   a->m = st->m;
   a->v = st->v;
   a->master = st->master;
@@ -217,6 +220,34 @@ bool mul_add(uint64_t a, uint64_t b, uint64_t* acc) {
   if (*acc > UINT64_MAX - p) return false;
   *acc += p;
   return true;
+}
+
+// Checks the gradients of a norm pass and fills NormArgs except the buffers.
+int prepare_norm(const void* const* grads, int64_t n, int32_t N, int32_t precision,
+                 zk::NormArgs* a) {
+  if (n < 0) return fail(ZERO_EINVAL, "n=%lld must be >= 0", (long long)n);
+  if (!valid_ranks(N)) return fail(ZERO_EINVAL, "N=%d outside [1, %d]", N, ZERO_MAX_RANKS);
+  if (precision != ZERO_FP32 && precision != ZERO_BF16_MIXED)
+    return fail(ZERO_EINVAL, "gradient precision must be FP32 or BF16_MIXED");
+  if (!grads) return fail(ZERO_EINVAL, "grads array is NULL");
+  const int es = precision == ZERO_BF16_MIXED ? 2 : 4;
+  const int V = es == 2 ? 8 : 4;
+  std::memset(a, 0, sizeof(*a));
+  a->N = N;
+  a->fN = float(N);
+  int ph = -2;
+  bool same = true;
+  for (int32_t r = 0; r < N; ++r) {
+    if (n > 0 && !grads[r]) return fail(ZERO_EINVAL, "grads[%d] is NULL", r);
+    const int q = phase_of(grads[r], es);
+    if (q < 0) return fail(ZERO_EALIGN, "grads[%d] not aligned to %d bytes", r, es);
+    if (ph == -2) ph = q;
+    else if (ph != q) same = false;
+    a->grads[r] = grads[r];
+  }
+  a->sp = make_split(0, n, same, ph, V);
+  a->nchunks = (a->sp.nvec * V + zk::kNormChunk - 1) / zk::kNormChunk;
+  return ZERO_OK;
 }
 
 }  // namespace
@@ -405,6 +436,66 @@ int zero_step(void* const* params, const void* const* grads, zero_states_t* st, 
   if (!st) return fail(ZERO_EINVAL, "state handle is NULL");
   return zero_step_range(params, grads, st, t, lr, beta1, beta2, eps, weight_decay, 0, st->n,
                          stream);
+}
+
+int zero_step_ex(void* const* params, const void* const* grads, zero_states_t* st,
+                 const zero_step_opts_t* o, zero_stream_t stream) {
+  if (!st) return fail(ZERO_EINVAL, "state handle is NULL");
+  if (!o) return fail(ZERO_EINVAL, "options are NULL");
+  zk::StepArgs a;
+  bool vec = false;
+  int phase = 0;
+  if (int e = prepare_step(params, grads, st, &a, &vec, &phase)) return e;
+  const int64_t lo = o->lo, hi = o->hi < 0 ? st->n : o->hi;
+  if (lo < 0 || hi < lo || hi > st->n)
+    return fail(ZERO_EINVAL, "range [%lld, %lld) outside [0, %lld)", (long long)lo, (long long)hi,
+                (long long)st->n);
+  if (int e = adam_consts(o->t, o->lr, o->beta1, o->beta2, o->eps, o->weight_decay, &a.c)) return e;
+  if (!std::isfinite(o->grad_scale) || !(o->grad_scale > 0.0))
+    return fail(ZERO_EINVAL, "grad_scale must be finite and > 0");
+  a.gscale = o->grad_scale;
+  if (o->max_grad_norm > 0.0) {
+    if (!std::isfinite(o->max_grad_norm)) return fail(ZERO_EINVAL, "max_grad_norm must be finite");
+    if (!o->norm_sq) return fail(ZERO_EINVAL, "clipping needs the squared norm (norm_sq)");
+    a.norm_sq = o->norm_sq;
+    a.max_norm = o->max_grad_norm;
+  }
+  return launch_range(a, st, vec, phase, lo, hi, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int zero_grad_norm_scratch_count(int64_t n, int32_t precision, int64_t* count) {
+  if (!count) return fail(ZERO_EINVAL, "count is NULL");
+  if (n < 0) return fail(ZERO_EINVAL, "n=%lld must be >= 0", (long long)n);
+  if (precision != ZERO_FP32 && precision != ZERO_BF16_MIXED)
+    return fail(ZERO_EINVAL, "gradient precision must be FP32 or BF16_MIXED");
+  *count = (n + zk::kNormChunk - 1) / zk::kNormChunk + 1;
+  return ZERO_OK;
+}
+
+int zero_grad_norm_sq(const void* const* grads, int64_t n, int32_t N, int32_t precision,
+                      double* scratch, int64_t scratch_count, double* norm_sq,
+                      zero_stream_t stream) {
+  zk::NormArgs a;
+  if (int e = prepare_norm(grads, n, N, precision, &a)) return e;
+  if (!scratch || !norm_sq) return fail(ZERO_EINVAL, "scratch or norm_sq is NULL");
+  if (reinterpret_cast<uintptr_t>(scratch) % 8 || reinterpret_cast<uintptr_t>(norm_sq) % 8)
+    return fail(ZERO_EALIGN, "scratch and norm_sq must be 8-byte aligned");
+  if (scratch_count < a.nchunks + 1)
+    return fail(ZERO_EINVAL, "scratch holds %lld doubles, %lld needed", (long long)scratch_count,
+                (long long)(a.nchunks + 1));
+  const int es = precision == ZERO_BF16_MIXED ? 2 : 4;
+  std::vector<Range> rs;
+  if (n > 0)
+    for (int32_t r = 0; r < N; ++r)
+      rs.push_back({uintptr_t(grads[r]), uintptr_t(grads[r]) + uintptr_t(n) * es, "a gradient"});
+  rs.push_back({uintptr_t(scratch), uintptr_t(scratch) + uintptr_t(a.nchunks + 1) * 8, "the scratch"});
+  rs.push_back({uintptr_t(norm_sq), uintptr_t(norm_sq) + 8, "norm_sq"});
+  if (int e = check_disjoint(rs)) return e;
+  a.partials = scratch;
+  a.out = norm_sq;
+  cudaError_t e = zk::launch_norm(a, es == 2, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "gradient norm kernel launch");
+  return ZERO_OK;
 }
 
 int zero_bucket_count(int64_t n, int32_t precision, int64_t bucket_bytes, int64_t* count) {

@@ -48,6 +48,25 @@ struct StepArgs {
   float fN;                      // (float)N
   AdamConsts c;
   uint64_t wait_ns;              // bound of every wait on a bulk copy (TMA kernels)
+  // Multiplier of the mean gradient: gscale, times the clip coefficient
+  // min(1, max_norm / (gscale * sqrt(*norm_sq) + 1e-6)) when norm_sq is set
+  // (formed on the device, in double, rounded to float once).
+  const double* norm_sq;         // device scalar, or NULL (no clipping)
+  double gscale;
+  double max_norm;
+};
+
+// Squared global norm of the mean gradient, as fixed-size partial sums.
+constexpr int64_t kNormChunk = 32768;  // elements per partial sum
+
+struct NormArgs {
+  const void* grads[kMaxRanks];
+  Split sp;          // the whole range [0, n)
+  int32_t N;
+  float fN;
+  int64_t nchunks;   // vector chunks (kNormChunk / V units each); partial nchunks = scalars
+  double* partials;  // nchunks + 1 doubles
+  double* out;       // device scalar receiving the sum of the partials
 };
 
 struct AllreduceArgs {
@@ -70,6 +89,8 @@ struct InitArgs {
 cudaError_t launch_step(const StepArgs& a, bool mixed, cudaStream_t s);
 cudaError_t launch_allreduce(const AllreduceArgs& a, bool bf16, cudaStream_t s);
 cudaError_t launch_init(const InitArgs& a, cudaStream_t s);
+// Partial sums then their fixed-order total (two launches, deterministic).
+cudaError_t launch_norm(const NormArgs& a, bool bf16, cudaStream_t s);
 
 // Sticky device status word (bit 0: a bounded wait on a bulk copy ran out).
 // Reading synchronizes the current device.

@@ -140,6 +140,25 @@ __device__ __forceinline__ int ranks(const StepArgs& P) {
   return NR > 0 ? NR : P.N;
 }
 
+// Multiplier of the mean gradient: the accumulation factor gscale, times the
+// clip coefficient min(1, max_norm / (gscale * sqrt(norm_sq) + 1e-6)) when a
+// squared global norm is given. Formed in double with separately rounded
+// operations (no contraction), rounded to float once; 1.0f when neither is set.
+__device__ __forceinline__ float grad_multiplier(const StepArgs& P) {
+  double c = 1.0;
+  if (P.norm_sq) {
+    const double denom = __dadd_rn(__dmul_rn(P.gscale, __dsqrt_rn(*P.norm_sq)), 1e-6);
+    c = fmin(1.0, __ddiv_rn(P.max_norm, denom));
+  }
+  return __double2float_rn(__dmul_rn(P.gscale, c));
+}
+
+// The mean of the rank-ordered sum, times the gradient multiplier.
+template <int NR>
+__device__ __forceinline__ float scaled_mean(float s, const StepArgs& P, float gm) {
+  return __fmul_rn(mean_of<NR>(s, P.fN), gm);
+}
+
 // Owner of index j, advanced monotonically from `owner` (j never decreases
 // along one thread's iterations). bounds[N] = n > j stops the scan.
 __device__ __forceinline__ int advance_owner(const StepArgs& P, int owner, int64_t j) {
@@ -150,7 +169,7 @@ __device__ __forceinline__ int advance_owner(const StepArgs& P, int owner, int64
 // ------------------------------------------------------- scalar element path --
 
 template <int NR, bool MIXED>
-__device__ __forceinline__ void step_scalar(const StepArgs& P, int64_t j, int owner) {
+__device__ __forceinline__ void step_scalar(const StepArgs& P, int64_t j, int owner, float gm) {
   const int N = ranks<NR>(P);
   float s, p, m, v;
   if constexpr (MIXED) {
@@ -165,8 +184,7 @@ __device__ __forceinline__ void step_scalar(const StepArgs& P, int64_t j, int ow
   }
   m = __ldcs(P.m + j);
   v = __ldcs(P.v + j);
-  const float g = mean_of<NR>(s, P.fN);
-  adam1(P.c, g, p, m, v);
+  adam1(P.c, scaled_mean<NR>(s, P, gm), p, m, v);
   __stcs(P.m + j, m);
   __stcs(P.v + j, v);
   if constexpr (MIXED) {
@@ -181,7 +199,7 @@ __device__ __forceinline__ void step_scalar(const StepArgs& P, int64_t j, int ow
 // ------------------------------------------------------- fp32 vector path (V=4)
 
 template <int NR>
-__device__ __forceinline__ void step_vec_fp32(const StepArgs& P, int64_t j, int owner) {
+__device__ __forceinline__ void step_vec_fp32(const StepArgs& P, int64_t j, int owner, float gm) {
   const int N = ranks<NR>(P);
   // Loads first: parameter, state, then every rank's gradient.
   float4 p;
@@ -218,10 +236,10 @@ __device__ __forceinline__ void step_vec_fp32(const StepArgs& P, int64_t j, int 
       s.z = __fadd_rn(s.z, g.z); s.w = __fadd_rn(s.w, g.w);
     }
   }
-  adam1(P.c, mean_of<NR>(s.x, P.fN), p.x, m.x, v.x);
-  adam1(P.c, mean_of<NR>(s.y, P.fN), p.y, m.y, v.y);
-  adam1(P.c, mean_of<NR>(s.z, P.fN), p.z, m.z, v.z);
-  adam1(P.c, mean_of<NR>(s.w, P.fN), p.w, m.w, v.w);
+  adam1(P.c, scaled_mean<NR>(s.x, P, gm), p.x, m.x, v.x);
+  adam1(P.c, scaled_mean<NR>(s.y, P, gm), p.y, m.y, v.y);
+  adam1(P.c, scaled_mean<NR>(s.z, P, gm), p.z, m.z, v.z);
+  adam1(P.c, scaled_mean<NR>(s.w, P, gm), p.w, m.w, v.w);
   st4(P.m + j, m);
   st4(P.v + j, v);
   if constexpr (NR > 0) {
@@ -235,7 +253,7 @@ __device__ __forceinline__ void step_vec_fp32(const StepArgs& P, int64_t j, int 
 // ------------------------------------------------------ mixed vector path (V=8)
 
 template <int NR>
-__device__ __forceinline__ void step_vec_mixed(const StepArgs& P, int64_t j) {
+__device__ __forceinline__ void step_vec_mixed(const StepArgs& P, int64_t j, float gm) {
   const int N = ranks<NR>(P);
   const float4 p0 = ld4(P.master + j), p1 = ld4(P.master + j + 4);
   const float4 m0 = ld4(P.m + j), m1 = ld4(P.m + j + 4);
@@ -267,7 +285,7 @@ __device__ __forceinline__ void step_vec_mixed(const StepArgs& P, int64_t j) {
   float m[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
   float v[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
 #pragma unroll
-  for (int k = 0; k < 8; ++k) adam1(P.c, mean_of<NR>(s[k], P.fN), p[k], m[k], v[k]);
+  for (int k = 0; k < 8; ++k) adam1(P.c, scaled_mean<NR>(s[k], P, gm), p[k], m[k], v[k]);
   st4(P.master + j, make_float4(p[0], p[1], p[2], p[3]));
   st4(P.master + j + 4, make_float4(p[4], p[5], p[6], p[7]));
   st4(P.m + j, make_float4(m[0], m[1], m[2], m[3]));
@@ -291,6 +309,7 @@ __global__ void __launch_bounds__(kThreads) zero_step_kernel(const __grid_consta
   const int64_t tid = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
   const int64_t stride = int64_t(gridDim.x) * blockDim.x;
   const Split& sp = P.sp;
+  const float gm = grad_multiplier(P);
 
   // Scalar head and tail (a handful of elements, or the whole range when the
   // buffers do not share a 16-byte phase). j grows with s, so the owner scan
@@ -302,7 +321,7 @@ __global__ void __launch_bounds__(kThreads) zero_step_kernel(const __grid_consta
     for (int64_t s = tid; s < nscalar; s += stride) {
       const int64_t j = s < sp.head ? sp.lo + s : body_end + (s - sp.head);
       owner = advance_owner(P, owner, j);
-      step_scalar<NR, MIXED>(P, j, owner);
+      step_scalar<NR, MIXED>(P, j, owner, gm);
     }
   }
 
@@ -312,12 +331,110 @@ __global__ void __launch_bounds__(kThreads) zero_step_kernel(const __grid_consta
   for (int64_t u = tid; u < sp.nvec; u += stride) {
     const int64_t j = base + u * V;
     if constexpr (MIXED) {
-      step_vec_mixed<NR>(P, j);
+      step_vec_mixed<NR>(P, j, gm);
     } else {
       owner = advance_owner(P, owner, j);
-      step_vec_fp32<NR>(P, j, owner);
+      step_vec_fp32<NR>(P, j, owner, gm);
     }
   }
+}
+
+// ------------------------------------------------- squared global gradient norm
+
+// Deterministic block sum of one double per thread (fixed shuffle tree, then
+// warps in order); the result is valid in thread 0.
+__device__ __forceinline__ double block_sum(double x) {
+  __shared__ double warp_sums[32];
+  for (int off = 16; off > 0; off >>= 1) x += __shfl_down_sync(0xffffffffu, x, off);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (lane == 0) warp_sums[warp] = x;
+  __syncthreads();
+  double t = 0.0;
+  if (threadIdx.x == 0) {
+    for (int w = 0; w < int(blockDim.x >> 5); ++w) t += warp_sums[w];
+  }
+  __syncthreads();
+  return t;
+}
+
+// Partial sums of ||mean gradient||^2. Partial c < nchunks covers the vector
+// units [c*U, (c+1)*U) with U = kNormChunk / V; partial nchunks covers the
+// scalar head and tail. The float mean of every element is squared exactly in
+// double and accumulated in double per thread; blocks reduce in a fixed
+// order, so every partial -- and the total -- is independent of the grid size.
+template <int NR, bool BF16>
+__device__ __forceinline__ double norm_chunk_sum(const NormArgs& P, int64_t c) {
+  constexpr int V = BF16 ? 8 : 4;
+  constexpr int64_t U = kNormChunk / V;
+  const int N = NR > 0 ? NR : P.N;
+  const Split& sp = P.sp;
+  const int64_t base = sp.lo + sp.head;
+  double acc = 0.0;
+  if (c < P.nchunks) {
+    const int64_t u_end = (c + 1) * U < sp.nvec ? (c + 1) * U : sp.nvec;
+    for (int64_t u = c * U + threadIdx.x; u < u_end; u += blockDim.x) {
+      const int64_t j = base + u * V;
+      float s[V];
+      if constexpr (BF16) {
+        unpack8(ld8h(static_cast<const uint16_t*>(P.grads[0]) + j), s);
+        for (int r = 1; r < N; ++r) {
+          float f[8];
+          unpack8(ld8h(static_cast<const uint16_t*>(P.grads[r]) + j), f);
+#pragma unroll
+          for (int k = 0; k < 8; ++k) s[k] = __fadd_rn(s[k], f[k]);
+        }
+      } else {
+        float4 a = ld4(static_cast<const float*>(P.grads[0]) + j);
+        for (int r = 1; r < N; ++r) {
+          const float4 b = ld4(static_cast<const float*>(P.grads[r]) + j);
+          a.x = __fadd_rn(a.x, b.x); a.y = __fadd_rn(a.y, b.y);
+          a.z = __fadd_rn(a.z, b.z); a.w = __fadd_rn(a.w, b.w);
+        }
+        s[0] = a.x; s[1] = a.y; s[2] = a.z; s[3] = a.w;
+      }
+#pragma unroll
+      for (int k = 0; k < V; ++k) {
+        const double g = double(mean_of<NR>(s[k], P.fN));
+        acc += g * g;  // the product of two floats is exact in double
+      }
+    }
+  } else {
+    const int64_t nscalar = sp.head + sp.tail;
+    const int64_t body_end = base + sp.nvec * V;
+    for (int64_t t = threadIdx.x; t < nscalar; t += blockDim.x) {
+      const int64_t j = t < sp.head ? sp.lo + t : body_end + (t - sp.head);
+      float s;
+      if constexpr (BF16) {
+        s = bf_one(__ldcs(static_cast<const uint16_t*>(P.grads[0]) + j));
+        for (int r = 1; r < N; ++r)
+          s = __fadd_rn(s, bf_one(__ldcs(static_cast<const uint16_t*>(P.grads[r]) + j)));
+      } else {
+        s = __ldcs(static_cast<const float*>(P.grads[0]) + j);
+        for (int r = 1; r < N; ++r)
+          s = __fadd_rn(s, __ldcs(static_cast<const float*>(P.grads[r]) + j));
+      }
+      const double g = double(mean_of<NR>(s, P.fN));
+      acc += g * g;
+    }
+  }
+  return block_sum(acc);
+}
+
+template <int NR, bool BF16>
+__global__ void __launch_bounds__(kThreads)
+    grad_norm_partials_kernel(const __grid_constant__ NormArgs P) {
+  for (int64_t c = blockIdx.x; c <= P.nchunks; c += gridDim.x) {
+    const double total = norm_chunk_sum<NR, BF16>(P, c);
+    if (threadIdx.x == 0) P.partials[c] = total;
+  }
+}
+
+// The partials added in a fixed order by one block.
+__global__ void __launch_bounds__(kThreads) grad_norm_total_kernel(const __grid_constant__ NormArgs P) {
+  double acc = 0.0;
+  for (int64_t c = threadIdx.x; c <= P.nchunks; c += blockDim.x) acc += P.partials[c];
+  const double total = block_sum(acc);
+  if (threadIdx.x == 0) *P.out = total;
 }
 
 // One element of the DDP mean, in place in every rank's buffer.
@@ -561,6 +678,28 @@ cudaError_t launch_allreduce(const AllreduceArgs& a, bool bf16, cudaStream_t s) 
 cudaError_t launch_init(const InitArgs& a, cudaStream_t s) {
   const int64_t work = a.sp.nvec > a.sp.head + a.sp.tail ? a.sp.nvec : a.sp.head + a.sp.tail;
   return launch(init_state_kernel, a, work, s);
+}
+
+namespace {
+template <bool BF16>
+cudaError_t launch_norm_t(const NormArgs& a, cudaStream_t s) {
+  const int64_t work = (a.nchunks + 1) * kThreads;  // one block per partial at most
+  cudaError_t e;
+  switch (a.N) {
+    case 1: e = launch(grad_norm_partials_kernel<1, BF16>, a, work, s); break;
+    case 2: e = launch(grad_norm_partials_kernel<2, BF16>, a, work, s); break;
+    case 4: e = launch(grad_norm_partials_kernel<4, BF16>, a, work, s); break;
+    case 8: e = launch(grad_norm_partials_kernel<8, BF16>, a, work, s); break;
+    default: e = launch(grad_norm_partials_kernel<0, BF16>, a, work, s); break;
+  }
+  if (e != cudaSuccess) return e;
+  grad_norm_total_kernel<<<1, kThreads, 0, s>>>(a);
+  return cudaGetLastError();
+}
+}  // namespace
+
+cudaError_t launch_norm(const NormArgs& a, bool bf16, cudaStream_t s) {
+  return bf16 ? launch_norm_t<true>(a, s) : launch_norm_t<false>(a, s);
 }
 
 cudaError_t read_device_status(uint32_t* status, bool clear) {

@@ -228,6 +228,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
   __shared__ PipeState<S> ps;
   const int tid = threadIdx.x;
   const Split& sp = P.sp;
+  const float gm = grad_multiplier(P);
 
   // Scalar head and tail (fewer than 2V elements) by block 0.
   if (blockIdx.x == 0) {
@@ -237,7 +238,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
     for (int64_t s = tid; s < nscalar; s += blockDim.x) {
       const int64_t j = s < sp.head ? sp.lo + s : body_end + (s - sp.head);
       owner = advance_owner(P, owner, j);
-      step_scalar<NR, MIXED>(P, j, owner);
+      step_scalar<NR, MIXED>(P, j, owner, gm);
     }
   }
 
@@ -357,10 +358,10 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
       }
       float4 m = *reinterpret_cast<const float4*>(mi + q);
       float4 v = *reinterpret_cast<const float4*>(vi + q);
-      adam1(P.c, mean_of<NR>(g.x, P.fN), p.x, m.x, v.x);
-      adam1(P.c, mean_of<NR>(g.y, P.fN), p.y, m.y, v.y);
-      adam1(P.c, mean_of<NR>(g.z, P.fN), p.z, m.z, v.z);
-      adam1(P.c, mean_of<NR>(g.w, P.fN), p.w, m.w, v.w);
+      adam1(P.c, scaled_mean<NR>(g.x, P, gm), p.x, m.x, v.x);
+      adam1(P.c, scaled_mean<NR>(g.y, P, gm), p.y, m.y, v.y);
+      adam1(P.c, scaled_mean<NR>(g.z, P, gm), p.z, m.z, v.z);
+      adam1(P.c, scaled_mean<NR>(g.w, P, gm), p.w, m.w, v.w);
       *reinterpret_cast<float4*>(po + q) = p;
       *reinterpret_cast<float4*>(mo + q) = m;
       *reinterpret_cast<float4*>(vo + q) = v;

@@ -24,8 +24,15 @@ BUCKET_BYTES_25MIB = 25 * 1024 * 1024
 class ZeroOptimizer:
     def __init__(self, n: int, N: int, precision: int = abi.ZERO_FP32, lr: float = 1e-3,
                  betas=(0.9, 0.999), eps: float = 1e-8, weight_decay: float = 0.0,
-                 master_init: torch.Tensor | None = None, device="cuda", stream=None):
+                 master_init: torch.Tensor | None = None, device="cuda", stream=None,
+                 max_grad_norm: float = 0.0, grad_scale: float = 1.0):
+        """``max_grad_norm`` > 0 clips the (scaled) mean gradient to that global
+        norm before every step; ``grad_scale`` multiplies the mean gradient
+        (1/k when the gradient buffers hold the sum of k micro-batches)."""
         self.n, self.N, self.precision = int(n), int(N), int(precision)
+        self.max_grad_norm, self.grad_scale = float(max_grad_norm), float(grad_scale)
+        self._norm = None
+        self._norm_scratch = None
         self.lr, self.beta1, self.beta2 = float(lr), float(betas[0]), float(betas[1])
         self.eps, self.weight_decay = float(eps), float(weight_decay)
         self.device = torch.device(device)
@@ -63,9 +70,33 @@ class ZeroOptimizer:
         parameters are copied into it as well. Synchronize ``stream`` (the
         current stream by default) before reading it.
         """
+        clipping = self.max_grad_norm > 0
+        if clipping and not all(g.is_cuda for g in grads):
+            # the global norm needs every gradient before any update: copy first
+            staging = self._staging_buffers()
+            s = stream if stream is not None else torch.cuda.current_stream(self.device)
+            with torch.cuda.stream(s):
+                for dst, src in zip(staging, grads):
+                    dst.copy_(src, non_blocking=True)
+            grads = staging
         if all(g.is_cuda for g in grads):
-            abi.zero_step(params, grads, self.states, self.t + 1, self.lr, self.beta1,
-                          self.beta2, self.eps, self.weight_decay, stream)
+            if clipping or self.grad_scale != 1.0:
+                norm = None
+                if clipping:
+                    if self._norm is None:
+                        count = abi.zero_grad_norm_scratch_count(self.n, self.precision)
+                        f64 = dict(dtype=torch.float64, device=self.device)
+                        self._norm_scratch = torch.empty(count, **f64)
+                        self._norm = torch.empty(1, **f64)
+                    abi.zero_grad_norm_sq(grads, self.precision, self._norm_scratch, self._norm,
+                                          self.n, stream)
+                    norm = self._norm
+                abi.zero_step_ex(params, grads, self.states, self.t + 1, self.lr, self.beta1,
+                                 self.beta2, self.eps, self.weight_decay, self.grad_scale,
+                                 self.max_grad_norm, norm, 0, -1, stream)
+            else:
+                abi.zero_step(params, grads, self.states, self.t + 1, self.lr, self.beta1,
+                              self.beta2, self.eps, self.weight_decay, stream)
             if host_params_out is not None:
                 s = stream if stream is not None else torch.cuda.current_stream(self.device)
                 with torch.cuda.stream(s):
