@@ -151,6 +151,30 @@ int zero_grad_norm_sq(const void *const *grads, int64_t n, int32_t N, int32_t pr
                       double *scratch, int64_t scratch_count, double *norm_sq,
                       zero_stream_t stream);
 
+/* zero_grad_norm_sq without caller-provided scratch. Some callers cannot
+ * allocate device memory at all: a process that runs inside a fixed memory
+ * pool frozen after start-up, code that must not call cudaMalloc because it
+ * synchronizes the device and would stall the work in flight on other
+ * streams, or a hook (a logger, a health check) that only borrows the
+ * gradient buffers and has no allocator of its own. This entry point allocates
+ * nothing: its partial sums live in an array of 65,536 doubles (512 KB) that
+ * the library keeps on every GPU that loads it, until the process exits.
+ * There is no counterpart on the pages; it computes exactly what
+ * zero_grad_norm_sq computes, bit for bit.
+ *   grads, n, N, precision, stream : as zero_grad_norm_sq.
+ *   norm_sq : DEVICE scalar receiving ||(1/N) sum_r g_r||^2 (caller-owned).
+ * The first call on a device, with that device current, looks up the device
+ * address of the array (a host-side runtime call); make that first call
+ * before any stream capture. Every call shares the one array: calls whose
+ * work can overlap on the GPU (other streams, other host threads) race and
+ * must be ordered by the caller. Each call writes every partial it reads, so
+ * nothing needs clearing between calls.
+ * Errors: as zero_grad_norm_sq, plus EINVAL when n > ZERO_NOALLOC_MAX_N
+ * (use zero_grad_norm_sq with your own scratch above that). */
+#define ZERO_NOALLOC_MAX_N 2147450880LL /* 65,535 partials x 32,768 elements */
+int zero_grad_norm_sq_noalloc(const void *const *grads, int64_t n, int32_t N, int32_t precision,
+                              double *norm_sq, zero_stream_t stream);
+
 /* Options of zero_step_ex. */
 typedef struct zero_step_opts {
   int64_t t;             /* step number, >= 1 */

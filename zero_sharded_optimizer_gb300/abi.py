@@ -72,6 +72,7 @@ _SIGNATURES = {
     "zero_grad_norm_scratch_count": (ctypes.c_int, [_i64, _i32, _P(_i64)]),
     "zero_grad_norm_sq": (ctypes.c_int, [_P(_vp), _i64, _i32, _i32, _vp, _i64, _vp, _vp]),
     "zero_step_ex": (ctypes.c_int, [_P(_vp), _P(_vp), _vp, _vp, _vp]),
+    "zero_grad_norm_sq_noalloc": (ctypes.c_int, [_P(_vp), _i64, _i32, _i32, _vp, _vp]),
     "zero_device_status": (ctypes.c_int, [_P(ctypes.c_uint32), _i32]),
     "zero_debug_set_wait_timeout_ns": (ctypes.c_int, [_u64]),
     "zero_strerror": (ctypes.c_char_p, [ctypes.c_int]),
@@ -321,6 +322,20 @@ def zero_grad_norm_sq(grads, precision: int, scratch, norm_sq, n: int | None = N
     op = _f64_device_ptr(norm_sq, 1, "norm_sq")
     _check(_lib.zero_grad_norm_sq(gp, n, len(grads), precision, sp, scratch.numel(), op,
                                   _stream(stream)), "zero_grad_norm_sq")
+
+
+ZERO_NOALLOC_MAX_N = 2147450880
+
+
+def zero_grad_norm_sq_noalloc(grads, precision: int, norm_sq, n: int | None = None,
+                              stream=None):
+    """zero_grad_norm_sq using the library's own scratch array (no allocation);
+    for callers that cannot allocate device memory. n <= ZERO_NOALLOC_MAX_N."""
+    n = grads[0].numel() if n is None else n
+    gp = _ptr_array(grads, n, _storage_dtype(precision), "grads")
+    op = _f64_device_ptr(norm_sq, 1, "norm_sq")
+    _check(_lib.zero_grad_norm_sq_noalloc(gp, n, len(grads), precision, op, _stream(stream)),
+           "zero_grad_norm_sq_noalloc")
 
 
 def zero_step_ex(params, grads, st: ZeroStates, t: int, lr: float, beta1: float = 0.9,

@@ -498,6 +498,34 @@ int zero_grad_norm_sq(const void* const* grads, int64_t n, int32_t N, int32_t pr
   return ZERO_OK;
 }
 
+int zero_grad_norm_sq_noalloc(const void* const* grads, int64_t n, int32_t N, int32_t precision,
+                              double* norm_sq, zero_stream_t stream) {
+  zk::NormArgs a;
+  if (int e = prepare_norm(grads, n, N, precision, &a)) return e;
+  if (!norm_sq) return fail(ZERO_EINVAL, "norm_sq is NULL");
+  if (reinterpret_cast<uintptr_t>(norm_sq) % 8) return fail(ZERO_EALIGN, "norm_sq not 8-byte aligned");
+  if (n > ZERO_NOALLOC_MAX_N || a.nchunks + 1 > zk::kNoAllocPartials)
+    return fail(ZERO_EINVAL,
+                "n=%lld exceeds the %lld elements the library's own scratch covers; use "
+                "zero_grad_norm_sq with caller-provided scratch",
+                (long long)n, (long long)ZERO_NOALLOC_MAX_N);
+  const int es = precision == ZERO_BF16_MIXED ? 2 : 4;
+  std::vector<Range> rs;
+  if (n > 0)
+    for (int32_t r = 0; r < N; ++r)
+      rs.push_back({uintptr_t(grads[r]), uintptr_t(grads[r]) + uintptr_t(n) * es, "a gradient"});
+  rs.push_back({uintptr_t(norm_sq), uintptr_t(norm_sq) + 8, "norm_sq"});
+  if (int e = check_disjoint(rs)) return e;
+  double* partials = nullptr;
+  cudaError_t ce = zk::noalloc_partials(&partials);
+  if (ce != cudaSuccess) return cuda_fail(ce, "looking up the library's scratch array");
+  a.partials = partials;
+  a.out = norm_sq;
+  ce = zk::launch_norm(a, es == 2, reinterpret_cast<cudaStream_t>(stream));
+  if (ce != cudaSuccess) return cuda_fail(ce, "gradient norm kernel launch");
+  return ZERO_OK;
+}
+
 int zero_bucket_count(int64_t n, int32_t precision, int64_t bucket_bytes, int64_t* count) {
   if (!count) return fail(ZERO_EINVAL, "count is NULL");
   if (n < 0) return fail(ZERO_EINVAL, "n=%lld must be >= 0", (long long)n);

@@ -92,6 +92,12 @@ cudaError_t launch_init(const InitArgs& a, cudaStream_t s);
 // Partial sums then their fixed-order total (two launches, deterministic).
 cudaError_t launch_norm(const NormArgs& a, bool bf16, cudaStream_t s);
 
+// Capacity of the library's own partial-sum array (zero_grad_norm_sq_noalloc),
+// and the device address of that array on the current device (looked up on
+// first use per device).
+constexpr int64_t kNoAllocPartials = 65536;
+cudaError_t noalloc_partials(double** ptr);
+
 // Sticky device status word (bit 0: a bounded wait on a bulk copy ran out).
 // Reading synchronizes the current device.
 cudaError_t read_device_status(uint32_t* status, bool clear);

@@ -28,6 +28,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "zero_internal.h"
 
 namespace zk {
@@ -700,6 +702,35 @@ cudaError_t launch_norm_t(const NormArgs& a, cudaStream_t s) {
 
 cudaError_t launch_norm(const NormArgs& a, bool bf16, cudaStream_t s) {
   return bf16 ? launch_norm_t<true>(a, s) : launch_norm_t<false>(a, s);
+}
+
+// ---------------------------------------------- partial sums without allocation
+//
+// Scratch for zero_grad_norm_sq_noalloc: the partial sums live in this fixed
+// array, which every GPU that loads the library keeps (512 KB) until the
+// process exits. Every call shares it and leaves its partials behind; each
+// partial a call reads was written earlier in that same call, so nothing has
+// to start at zero. Calls whose work overlaps on the GPU race on it.
+static __device__ __align__(256) double g_noalloc_partials[kNoAllocPartials];
+
+cudaError_t noalloc_partials(double** ptr) {
+  // In host code g_noalloc_partials is only a stand-in for the device array;
+  // its device address is looked up once per device, with that device current.
+  static std::mutex mu;
+  static double* addr[256] = {nullptr};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 256) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_partials);
+    if (e != cudaSuccess) return e;
+    addr[dev] = static_cast<double*>(p);
+  }
+  *ptr = addr[dev];
+  return cudaSuccess;
 }
 
 cudaError_t read_device_status(uint32_t* status, bool clear) {
