@@ -243,11 +243,15 @@ def run_gpu(args, wl, rank: int, world: int, local_rank: int) -> dict | None:
     reps = inputs.make_replicas(init, N, wl.precision)
     grads = inputs.make_grads(n, N, wl.precision, device=dev)
     inputs.fill_grads(grads, wl, step=1, seed=rank)
+    clip = args.max_grad_norm > 0
     opt = ZeroOptimizer(n, N, wl.precision, lr=wl.lr, betas=(wl.beta1, wl.beta2), eps=wl.eps,
-                        weight_decay=wl.weight_decay, master_init=init if mixed else None)
+                        weight_decay=wl.weight_decay, master_init=init if mixed else None,
+                        max_grad_norm=args.max_grad_norm)
     del init
     bucketed = wl.bucket_bytes > 0
     launches_per_step = len(opt.bucket_ranges(wl.bucket_bytes)) if bucketed else 1
+    if clip:
+        launches_per_step = 3       # norm partials, norm total, clipped step
     stream = torch.cuda.current_stream()
 
     def one_step():
@@ -316,10 +320,13 @@ def run_gpu(args, wl, rank: int, world: int, local_rank: int) -> dict | None:
         return None
     peak, peak_kind = load_peaks()
     step_bytes = n * bytes_per_param(wl)
+    if clip:  # the norm pass reads every rank's gradient once more
+        step_bytes += n * N * (2 if mixed else 4)
     achieved = step_bytes / (kernel_ms / 1e3) / 1e9
     traffic = traffic_per_launch(wl.name)
-    if traffic is not None and bucketed:
+    if traffic is not None and (bucketed or clip):
         traffic = None
+    per = 1 if clip else launches_per_step  # clip: the roofline covers the whole step
     line = {
         "metric": METRIC,
         "value": whole_job_rate(n, world, ms_step),
@@ -334,15 +341,18 @@ def run_gpu(args, wl, rank: int, world: int, local_rank: int) -> dict | None:
         "dtype": "f32",
         "data": "synthetic (seeded device draws; inputs resident in HBM)",
         "config": config_of(wl, {"parallelism": f"{N} simulated ranks per GPU; "
-                                                f"{world} independent GPU replica(s)"}),
+                                                f"{world} independent GPU replica(s)",
+                                 **({"max_grad_norm": args.max_grad_norm} if clip else {})}),
         "hbm_gbs": step_bytes / (ms_step / 1e3) / 1e9,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs, copy "
                                     f"bandwidth)" if peak_kind == "measured" else "fallback",
-                     "algorithmic_bytes_per_launch": step_bytes // launches_per_step,
-                     "kernel": "zero_step_tma_kernel" if wl.N <= 8 else "zero_step_kernel",
-                     "kernel_ms": kernel_ms / launches_per_step},
+                     "algorithmic_bytes_per_launch": step_bytes // per,
+                     "kernel": ("grad_norm_partials_kernel + grad_norm_total_kernel + "
+                                "zero_step_tma_kernel (whole clipped step)") if clip else
+                               ("zero_step_tma_kernel" if wl.N <= 8 else "zero_step_kernel"),
+                     "kernel_ms": kernel_ms / per},
         "gpu_launches": K * launches_per_step,
         "clocks": clocks,
         "e2e": e2e,
@@ -397,12 +407,16 @@ def main(argv=None):
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(inputs.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    ap.add_argument("--max-grad-norm", type=float, default=0.0,
+                    help="> 0: sharded global-norm clipping before every step (norm pass + step)")
     args = ap.parse_args(argv)
     wl = inputs.WORKLOADS[args.workload]
     if args.steps is None:
         args.steps = default_steps(wl)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.max_grad_norm > 0 and wl.bucket_bytes:
+        ap.error("clipping needs the whole gradient before the step: not with bucket streaming")
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))

@@ -359,10 +359,42 @@ __device__ __forceinline__ double block_sum(double x) {
   return t;
 }
 
+// Running sum of squares of floats, accurate to about double precision while
+// spending float operations only (the GPU's double rate is low): every square
+// is split exactly into p + e with p = fl(x*x), e = fma(x, x, -p); the p are
+// added with Neumaier's compensated summation (s, c) and the small e directly.
+// Squares outside the normal float range (|x| > 2^60, or 0 < |x| < 2^-60) go
+// to a double accumulator instead. value() adds the parts in double.
+// The rare out-of-range square, kept out of line so the common path carries no
+// double-precision instruction (a branch, not a predicated sequence).
+__device__ __noinline__ double add_wide_square(double wide, float x) {
+  return wide + double(x) * double(x);
+}
+
+struct SquareSum {
+  float s = 0.0f, c = 0.0f, e = 0.0f;
+  double wide = 0.0;
+  __device__ __forceinline__ void add(float x) {
+    const float ax = fabsf(x);
+    if (ax > 0x1p60f || (ax < 0x1p-60f && ax != 0.0f)) {
+      wide = add_wide_square(wide, x);
+      return;
+    }
+    const float p = __fmul_rn(x, x);
+    e = __fadd_rn(e, fmaf(x, x, -p));
+    const float t = __fadd_rn(s, p);
+    c = __fadd_rn(c, s >= p ? __fadd_rn(__fsub_rn(s, t), p) : __fadd_rn(__fsub_rn(p, t), s));
+    s = t;
+  }
+  __device__ __forceinline__ double value() const {
+    return (double(s) + double(c)) + (double(e) + wide);
+  }
+};
+
 // Partial sums of ||mean gradient||^2. Partial c < nchunks covers the vector
 // units [c*U, (c+1)*U) with U = kNormChunk / V; partial nchunks covers the
-// scalar head and tail. The float mean of every element is squared exactly in
-// double and accumulated in double per thread; blocks reduce in a fixed
+// scalar head and tail. Every thread accumulates the squares of the float
+// means of its elements (SquareSum), then blocks reduce in double in a fixed
 // order, so every partial -- and the total -- is independent of the grid size.
 template <int NR, bool BF16>
 __device__ __forceinline__ double norm_chunk_sum(const NormArgs& P, int64_t c) {
@@ -371,33 +403,49 @@ __device__ __forceinline__ double norm_chunk_sum(const NormArgs& P, int64_t c) {
   const int N = NR > 0 ? NR : P.N;
   const Split& sp = P.sp;
   const int64_t base = sp.lo + sp.head;
-  double acc = 0.0;
+  SquareSum acc;
   if (c < P.nchunks) {
     const int64_t u_end = (c + 1) * U < sp.nvec ? (c + 1) * U : sp.nvec;
-    for (int64_t u = c * U + threadIdx.x; u < u_end; u += blockDim.x) {
-      const int64_t j = base + u * V;
-      float s[V];
+    // Two units per thread per iteration: every load of both is issued before
+    // any arithmetic. The element order within the thread is fixed, so the
+    // partial stays independent of the grid.
+    for (int64_t u0 = c * U + threadIdx.x; u0 < u_end; u0 += 2 * blockDim.x) {
+      const int64_t u1 = u0 + blockDim.x;
+      const bool has1 = u1 < u_end;
+      const int64_t j0 = base + u0 * V, j1 = base + (has1 ? u1 : u0) * V;
+      float s0[V], s1[V];
       if constexpr (BF16) {
-        unpack8(ld8h(static_cast<const uint16_t*>(P.grads[0]) + j), s);
+        unpack8(ld8h(static_cast<const uint16_t*>(P.grads[0]) + j0), s0);
+        unpack8(ld8h(static_cast<const uint16_t*>(P.grads[0]) + j1), s1);
         for (int r = 1; r < N; ++r) {
-          float f[8];
-          unpack8(ld8h(static_cast<const uint16_t*>(P.grads[r]) + j), f);
+          float f0[8], f1[8];
+          unpack8(ld8h(static_cast<const uint16_t*>(P.grads[r]) + j0), f0);
+          unpack8(ld8h(static_cast<const uint16_t*>(P.grads[r]) + j1), f1);
 #pragma unroll
-          for (int k = 0; k < 8; ++k) s[k] = __fadd_rn(s[k], f[k]);
+          for (int k = 0; k < 8; ++k) {
+            s0[k] = __fadd_rn(s0[k], f0[k]);
+            s1[k] = __fadd_rn(s1[k], f1[k]);
+          }
         }
       } else {
-        float4 a = ld4(static_cast<const float*>(P.grads[0]) + j);
+        float4 a = ld4(static_cast<const float*>(P.grads[0]) + j0);
+        float4 b = ld4(static_cast<const float*>(P.grads[0]) + j1);
         for (int r = 1; r < N; ++r) {
-          const float4 b = ld4(static_cast<const float*>(P.grads[r]) + j);
-          a.x = __fadd_rn(a.x, b.x); a.y = __fadd_rn(a.y, b.y);
-          a.z = __fadd_rn(a.z, b.z); a.w = __fadd_rn(a.w, b.w);
+          const float4 x = ld4(static_cast<const float*>(P.grads[r]) + j0);
+          const float4 y = ld4(static_cast<const float*>(P.grads[r]) + j1);
+          a.x = __fadd_rn(a.x, x.x); a.y = __fadd_rn(a.y, x.y);
+          a.z = __fadd_rn(a.z, x.z); a.w = __fadd_rn(a.w, x.w);
+          b.x = __fadd_rn(b.x, y.x); b.y = __fadd_rn(b.y, y.y);
+          b.z = __fadd_rn(b.z, y.z); b.w = __fadd_rn(b.w, y.w);
         }
-        s[0] = a.x; s[1] = a.y; s[2] = a.z; s[3] = a.w;
+        s0[0] = a.x; s0[1] = a.y; s0[2] = a.z; s0[3] = a.w;
+        s1[0] = b.x; s1[1] = b.y; s1[2] = b.z; s1[3] = b.w;
       }
 #pragma unroll
-      for (int k = 0; k < V; ++k) {
-        const double g = double(mean_of<NR>(s[k], P.fN));
-        acc += g * g;  // the product of two floats is exact in double
+      for (int k = 0; k < V; ++k) acc.add(mean_of<NR>(s0[k], P.fN));
+      if (has1) {
+#pragma unroll
+        for (int k = 0; k < V; ++k) acc.add(mean_of<NR>(s1[k], P.fN));
       }
     }
   } else {
@@ -415,11 +463,10 @@ __device__ __forceinline__ double norm_chunk_sum(const NormArgs& P, int64_t c) {
         for (int r = 1; r < N; ++r)
           s = __fadd_rn(s, __ldcs(static_cast<const float*>(P.grads[r]) + j));
       }
-      const double g = double(mean_of<NR>(s, P.fN));
-      acc += g * g;
+      acc.add(mean_of<NR>(s, P.fN));
     }
   }
-  return block_sum(acc);
+  return block_sum(acc.value());
 }
 
 template <int NR, bool BF16>
