@@ -25,6 +25,8 @@ ranks and workers only):
   Analysis" and "ZeRO-1/2/3"; "ZeRO One: Sharding the Optimizer", section
   "Training Memory Requirements"; the float64 bookkeeping table of
   "Data parallelism and ZeRO stages 1 to 3", section 3).
+* ``tensor_shard_bounds`` -- shards of whole tensors ("ZeRO One: Sharding the
+  Optimizer", "Sharding Parameters").
 * ``bucket_bounds``  -- 25 MiB gradient buckets built from the end of the flat
   gradient ("ZeRO One: Sharding the Optimizer", section "Bucketing").
 * ``grad_norm`` / ``grad_multiplier`` -- the global gradient norm from squared
@@ -74,7 +76,7 @@ import numpy as np
 __all__ = [
     "FP32", "BF16_MIXED", "FP64_EMU",
     "shard_bounds", "init_states", "zero_step", "adam_full", "allreduce_mean",
-    "grad_norm", "grad_multiplier",
+    "grad_norm", "grad_multiplier", "tensor_shard_bounds",
     "memory_bytes", "memory_breakdown", "bucket_bounds",
     "bf16_to_f32", "f32_to_bf16_rne", "mirror_scalars",
 ]
@@ -103,6 +105,32 @@ def shard_bounds(n: int, N: int) -> list[int]:
         raise ValueError("number of parameters must be >= 0")
     q, r = divmod(n, N)
     return [i * q + min(i, r) for i in range(N + 1)]
+
+
+def tensor_shard_bounds(numels, N: int) -> list[int]:
+    """Element offsets of N shards made of whole tensors.
+
+    "ZeRO One: Sharding the Optimizer", "Sharding Parameters": the list of
+    parameter tensors (in parameters() order) is divided like the indices are
+    in "The shards" -- rank i gets tensors [i*q + min(i, r), (i+1)*q + min(i+1, r))
+    with q, r = divmod(len(tensors), N) -- so a shard never splits a tensor.
+    Returns the flat-vector offsets of those tensor boundaries.
+    """
+    T = len(numels)
+    if any(int(x) < 0 for x in numels):
+        raise ValueError("tensor sizes must be >= 0")
+    first = shard_bounds(T, N)                      # tensor indices
+    offsets = [0]
+    for x in numels:
+        offsets.append(offsets[-1] + int(x))
+    return [offsets[k] for k in first]
+
+
+def _check_bounds(bounds, n, N):
+    if len(bounds) != N + 1 or bounds[0] != 0 or bounds[-1] != n or any(
+            b > c for b, c in zip(bounds, bounds[1:])):
+        raise ValueError("shard bounds must rise from 0 to n in N steps")
+    return list(bounds)
 
 
 # --------------------------------------------------------------------------
@@ -225,7 +253,8 @@ def _replica_from(p, precision, mode="fp32"):
 # The ZeRO step
 # --------------------------------------------------------------------------
 
-def init_states(n: int, N: int, precision: int = FP32, master_init=None, mode: str = "fp32"):
+def init_states(n: int, N: int, precision: int = FP32, master_init=None, mode: str = "fp32",
+                bounds=None):
     """One state dict per worker, each the size of that worker's shard.
 
     "ZeRO-Sharded Adam Step", "What to implement": init_states gives N pairs
@@ -234,7 +263,7 @@ def init_states(n: int, N: int, precision: int = FP32, master_init=None, mode: s
     "Memory Consumption Analysis": master weights are part of the 12 bytes of
     optimizer state); it starts as the fp32 initial weights.
     """
-    bounds = shard_bounds(n, N)
+    bounds = shard_bounds(n, N) if bounds is None else _check_bounds(bounds, n, N)
     dt = _dtype(mode)
     states = []
     for i in range(N):
@@ -298,7 +327,7 @@ def grad_multiplier(norm: float, grad_scale: float = 1.0, max_grad_norm=None) ->
 
 def zero_step(params, grads, states, t, lr=1e-2, beta1=0.9, beta2=0.999, eps=1e-8,
               weight_decay=0.0, precision=FP32, mode="fp32", grad_scale=1.0,
-              max_grad_norm=None):
+              max_grad_norm=None, bounds=None):
     """One ZeRO step; returns (new_params, new_states).
 
     ``params``: N full-length replicas (float32, or bf16 bits as uint16).
@@ -312,6 +341,9 @@ def zero_step(params, grads, states, t, lr=1e-2, beta1=0.9, beta2=0.999, eps=1e-
          source is its own replica's shard in fp32, its master in mixed mode);
       3. all-gather: the updated shards are concatenated and every worker's
          replica becomes the full updated vector.
+    ``bounds`` (N+1 offsets, default the array_split shards) sets who owns
+    what, e.g. whole tensors from ``tensor_shard_bounds``; it must match the
+    bounds ``states`` were built with.
     With ``grad_scale`` != 1 or ``max_grad_norm`` set, the mean gradient is
     first multiplied by ``grad_multiplier`` (rounded to float32 in the fp32
     mode); the global norm it needs comes from ``grad_norm`` of the same
@@ -321,7 +353,7 @@ def zero_step(params, grads, states, t, lr=1e-2, beta1=0.9, beta2=0.999, eps=1e-
     if len(params) != N or len(states) != N:
         raise ValueError("params, grads and states need one entry per worker")
     n = len(params[0])
-    bounds = shard_bounds(n, N)
+    bounds = shard_bounds(n, N) if bounds is None else _check_bounds(bounds, n, N)
     mult = None
     if grad_scale != 1.0 or (max_grad_norm is not None and max_grad_norm > 0):
         norm = grad_norm(grads, precision, mode) if max_grad_norm else 0.0
@@ -382,7 +414,8 @@ def allreduce_mean(grads, precision=FP32, mode="fp32"):
 _PER_PARAM = {FP32: (4, 4, 8), BF16_MIXED: (2, 2, 12)}
 
 
-def memory_breakdown(n: int, N: int, stage: int, precision: int, rank: int = 0) -> tuple:
+def memory_breakdown(n: int, N: int, stage: int, precision: int, rank: int = 0,
+                     bounds=None) -> tuple:
     """(params, grads, optimizer) bytes held by ``rank`` after a step.
 
     Stage 0 is plain data parallelism (everything replicated). Stages 1, 2, 3
@@ -398,10 +431,11 @@ def memory_breakdown(n: int, N: int, stage: int, precision: int, rank: int = 0) 
     the full averaged .grad plus the chunk's gradient; stages 1 and 2 hold m, v
     and a master copy of the chunk; in stage 3 the chunk is the parameter
     storage (m and v only); one process holds m and v for all n.
+    ``bounds`` replaces the array_split shards (e.g. whole-tensor shards).
     """
     if N < 1 or n < 0 or stage not in (0, 1, 2, 3) or not 0 <= rank < N:
         raise ValueError("bad memory-accounting arguments")
-    bounds = shard_bounds(n, N)
+    bounds = shard_bounds(n, N) if bounds is None else _check_bounds(bounds, n, N)
     s = bounds[rank + 1] - bounds[rank]
     if precision == FP64_EMU:
         b = 8

@@ -542,3 +542,57 @@ def test_mutant_clip_on_sum_of_gradients(monkeypatch):
         return real(grads, precision, mode) * len(grads)
     monkeypatch.setattr(zo, "grad_norm", norm_of_sum)
     assert _fails(lambda: test_clipped_step_matches_torch(0.5, 1.0))
+
+
+# ---------------------------------------------------------------------------
+# Whole-tensor shards
+# ---------------------------------------------------------------------------
+
+def test_tensor_shards_page_example():
+    # "ZeRO One", "Sharding Parameters": 291 tensors over 4 ranks -> tensors
+    # (0,73), (73,146), (146,219), (219,291); with unit sizes the element offsets
+    # equal the tensor indices, with other sizes they are the tensors' offsets
+    assert oracle.tensor_shard_bounds([1] * 291, 4) == [0, 73, 146, 219, 291]
+    rng = np.random.default_rng(81)
+    numels = rng.integers(0, 5000, 291).tolist()
+    offsets = np.concatenate([[0], np.cumsum(numels)])
+    b = oracle.tensor_shard_bounds(numels, 4)
+    assert b == [int(offsets[k]) for k in (0, 73, 146, 219, 291)]
+    # counts per rank follow array_split over the tensor list
+    for T, N in [(148, 8), (5, 8), (13, 3)]:
+        sizes = [len(p) for p in np.array_split(np.arange(T), N)]
+        b = oracle.tensor_shard_bounds([1] * T, N)
+        assert np.diff(b).tolist() == sizes
+
+
+@pytest.mark.parametrize("mode", ["fp32", "fp64"])
+def test_tensor_shards_change_nothing_but_ownership(mode):
+    rng = np.random.default_rng(82)
+    numels = rng.integers(1, 300, 37).tolist()
+    n, N = int(sum(numels)), 4
+    dt = np.float64 if mode == "fp64" else np.float32
+    p = rng.normal(size=n).astype(dt)
+    tb = oracle.tensor_shard_bounds(numels, N)
+    assert tb != oracle.shard_bounds(n, N)
+    a_p, b_p = [p.copy() for _ in range(N)], [p.copy() for _ in range(N)]
+    a_s = oracle.init_states(n, N, mode=mode, bounds=tb)
+    b_s = oracle.init_states(n, N, mode=mode)
+    assert [len(s["m"]) for s in a_s] == np.diff(tb).tolist()
+    for t in range(1, 4):
+        grads = [rng.normal(size=n).astype(np.float32) for _ in range(N)]
+        a_p, a_s = oracle.zero_step(a_p, grads, a_s, t, weight_decay=0.1, mode=mode, bounds=tb)
+        b_p, b_s = oracle.zero_step(b_p, grads, b_s, t, weight_decay=0.1, mode=mode)
+        assert all(np.array_equal(x, b_p[0]) for x in a_p)
+        assert np.array_equal(flat_state(a_s, "v"), flat_state(b_s, "v"))
+
+
+def test_tensor_shard_memory():
+    numels = [100, 7, 7, 900, 3]
+    tb = oracle.tensor_shard_bounds(numels, 2)           # tensors (0..3), (3..5)
+    assert tb == [0, 114, 1017]
+    assert oracle.memory_breakdown(1017, 2, 1, oracle.BF16_MIXED, 0, bounds=tb) == \
+        (2 * 1017, 2 * 1017, 12 * 114)
+    assert oracle.memory_breakdown(1017, 2, 3, oracle.FP32, 1, bounds=tb) == \
+        (4 * 903, 4 * 903, 8 * 903)
+    with pytest.raises(ValueError):
+        oracle.memory_breakdown(1017, 2, 1, oracle.FP32, 0, bounds=[0, 2000, 1017])
