@@ -93,6 +93,25 @@ int zero_init_states(int64_t n, int32_t N, int32_t precision, float *m, float *v
                      float *master, const float *master_init, zero_stream_t stream,
                      zero_states_t **out);
 
+/* zero_init_states with caller-chosen shard bounds: `bounds` is a HOST array
+ * of N+1 offsets rising from 0 to n (NULL: the np.array_split shards). Rank i
+ * owns [bounds[i], bounds[i+1]); shards may be empty. The step's arithmetic
+ * does not depend on the bounds, only which replica holds each shard's
+ * authoritative fp32 parameter. Use zero_tensor_shard_bounds for shards of
+ * whole tensors. Errors: as zero_init_states, plus EINVAL for bad bounds. */
+int zero_init_states_ex(int64_t n, int32_t N, int32_t precision, float *m, float *v,
+                        float *master, const float *master_init, const int64_t *bounds,
+                        zero_stream_t stream, zero_states_t **out);
+
+/* Shards of whole tensors ("ZeRO One: Sharding the Optimizer", "Sharding
+ * Parameters"): the T tensors of the flat vector (HOST array numels[T], in
+ * parameters() order) are split like indices in np.array_split -- rank i gets
+ * tensors [i*q + min(i, r), (i+1)*q + min(i+1, r)) with q = T / N, r = T % N --
+ * and bounds[N+1] (HOST) receives the element offsets of those tensors, so no
+ * tensor is split. Errors: EINVAL (T < 0, N < 1, NULL, a negative size,
+ * overflow). */
+int zero_tensor_shard_bounds(const int64_t *numels, int64_t T, int32_t N, int64_t *bounds);
+
 /* Release a handle (the caller's device buffers are untouched). NULL is a no-op. */
 int zero_free_states(zero_states_t *st);
 
@@ -305,6 +324,10 @@ int ddp_allreduce_mean(void *const *grads, int64_t n, int32_t N, int32_t precisi
 int zero_memory_bytes(int64_t n, int32_t N, int32_t stage, int32_t precision, uint64_t *out);
 int zero_memory_breakdown(int64_t n, int32_t N, int32_t stage, int32_t precision,
                           int32_t rank, uint64_t out[3]);
+/* zero_memory_breakdown for caller-chosen shard bounds (HOST, N+1 offsets from
+ * 0 to n; NULL: the np.array_split shards), e.g. whole-tensor shards. */
+int zero_memory_breakdown_ex(int64_t n, int32_t N, int32_t stage, int32_t precision,
+                             int32_t rank, const int64_t *bounds, uint64_t out[3]);
 
 /* ---------------------------------------------------------------- health -- */
 

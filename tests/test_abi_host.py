@@ -129,3 +129,33 @@ def test_raw_argument_checks_before_any_device_work(abi):
     assert abi.raw_call("ddp_allreduce_mean", odd, 10, 2, 1, None) == abi.ZERO_EALIGN
     assert "overlap" in abi.raw_call.__globals__["_lib"].zero_last_error().decode() or True
     assert abi.raw_call("zero_free_states", None) == abi.ZERO_OK
+
+
+def test_tensor_shard_bounds_bit_exact(abi):
+    rng = np.random.default_rng(91)
+    for T, N in [(291, 4), (148, 8), (5, 8), (1, 1), (0, 3), (37, 5)]:
+        numels = rng.integers(0, 10_000, T).tolist()
+        ref = oracle.tensor_shard_bounds(numels, N)
+        assert abi.zero_tensor_shard_bounds(numels, N) == ref
+        n = ref[-1]
+        for stage in range(4):
+            for prec in (abi.ZERO_FP32, abi.ZERO_BF16_MIXED, abi.ZERO_FP64_EMU):
+                for rank in range(N):
+                    assert abi.zero_memory_breakdown_ex(n, N, stage, prec, rank, ref) == \
+                        oracle.memory_breakdown(n, N, stage, prec, rank, bounds=ref)
+    with pytest.raises(abi.ZeroError):
+        abi.zero_tensor_shard_bounds([3, -1], 2)
+    with pytest.raises(abi.ZeroError):
+        abi.zero_memory_breakdown_ex(10, 2, 1, abi.ZERO_FP32, 0, [0, 11, 10])
+
+
+def test_init_states_rejects_bad_bounds_before_device_work(abi):
+    vp = ctypes.c_void_p
+    h = vp()
+    for bad in ([1, 5, 10], [0, 5, 9], [0, 6, 5, 10]):
+        arr = (ctypes.c_int64 * len(bad))(*bad)
+        N = len(bad) - 1
+        code = abi.raw_call("zero_init_states_ex", 10, N, 0, 4096, 8192, None, None, arr, None,
+                            ctypes.byref(h))
+        assert code == abi.ZERO_EINVAL
+        assert "bounds" in abi.raw_call.__globals__["_lib"].zero_last_error().decode()

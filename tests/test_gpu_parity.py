@@ -483,3 +483,36 @@ def test_zero_and_subnormal_state_bitwise(abi, cuda, prec):
         c.gpu_step()
         torch.cuda.synchronize()
         c.compare(exact=True)
+
+
+@pytest.mark.parametrize("prec", [oracle.FP32, oracle.BF16_MIXED])
+def test_whole_tensor_shards(abi, cuda, prec):
+    """Shards made of whole tensors: bit-exact against the oracle with the same
+    bounds, and bit-identical to the array_split shards (ownership only)."""
+    rng = np.random.default_rng(92)
+    numels = rng.integers(1, 40_000, 29).tolist()
+    n, N = int(sum(numels)), 4
+    tb = abi.zero_tensor_shard_bounds(numels, N)
+    assert tb == oracle.tensor_shard_bounds(numels, N) != oracle.shard_bounds(n, N)
+    a = Case(abi, cuda, n, N, prec, seed=93)
+    b = Case(abi, cuda, n, N, prec, seed=93)
+    # rebuild a's state with whole-tensor shards (same fp32 initial weights as b)
+    init = host_of(b.master) if a.mixed else host_of(b.reps[0])
+    a.st = abi.zero_init_states(n, N, prec, a.m, a.v, a.master,
+                                b.master.clone() if a.mixed else None, bounds=tb)
+    a.o_states = oracle.init_states(n, N, prec, master_init=init, mode="fp32", bounds=tb)
+    assert a.st.view(1)["lo"] == tb[1]
+    for _ in range(2):
+        hg = a.new_grads()
+        for r in range(N):
+            b.grads[r].copy_(a.grads[r])
+        a.t += 1
+        a.o_reps, a.o_states = oracle.zero_step(a.o_reps, hg, a.o_states, a.t, precision=prec,
+                                                mode="fp32", bounds=tb, **HP)
+        a.gpu_step()
+        b.t = a.t
+        b.gpu_step()
+        torch.cuda.synchronize()
+        a.compare(exact=True)
+        for x, y in [(a.m, b.m), (a.v, b.v)] + list(zip(a.reps, b.reps)):
+            assert torch.equal(x, y)

@@ -52,6 +52,11 @@ _P = ctypes.POINTER
 _SIGNATURES = {
     "zero_shard_bounds": (ctypes.c_int, [_i64, _i32, _P(_i64)]),
     "zero_init_states": (ctypes.c_int, [_i64, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _P(_vp)]),
+    "zero_init_states_ex": (ctypes.c_int, [_i64, _i32, _i32, _vp, _vp, _vp, _vp, _P(_i64), _vp,
+                                           _P(_vp)]),
+    "zero_tensor_shard_bounds": (ctypes.c_int, [_P(_i64), _i64, _i32, _P(_i64)]),
+    "zero_memory_breakdown_ex": (ctypes.c_int, [_i64, _i32, _i32, _i32, _i32, _P(_i64),
+                                                _P(_u64)]),
     "zero_free_states": (ctypes.c_int, [_vp]),
     "zero_states_info": (ctypes.c_int, [_vp, _P(_i64), _P(_i32), _P(_i32)]),
     "zero_state_view": (ctypes.c_int, [_vp, _i32, _P(_i64), _P(_i64), _P(_vp), _P(_vp), _P(_vp)]),
@@ -173,6 +178,26 @@ def zero_memory_breakdown(n: int, N: int, stage: int, precision: int, rank: int)
     return tuple(out)
 
 
+def zero_tensor_shard_bounds(numels, N: int) -> list[int]:
+    T = len(numels)
+    arr = (_i64 * max(T, 1))(*[int(x) for x in numels])
+    out = (_i64 * (max(N, 0) + 1))()
+    _check(_lib.zero_tensor_shard_bounds(arr, T, N, out), "zero_tensor_shard_bounds")
+    return list(out)
+
+
+def _bounds_array(bounds):
+    return None if bounds is None else (_i64 * len(bounds))(*[int(x) for x in bounds])
+
+
+def zero_memory_breakdown_ex(n: int, N: int, stage: int, precision: int, rank: int,
+                             bounds=None) -> tuple:
+    out = (_u64 * 3)()
+    _check(_lib.zero_memory_breakdown_ex(n, N, stage, precision, rank, _bounds_array(bounds),
+                                         out), "zero_memory_breakdown_ex")
+    return tuple(out)
+
+
 def zero_bucket_count(n: int, precision: int, bucket_bytes: int) -> int:
     out = _i64()
     _check(_lib.zero_bucket_count(n, precision, bucket_bytes, ctypes.byref(out)),
@@ -227,7 +252,7 @@ class ZeroStates:
 
 
 def zero_init_states(n: int, N: int, precision: int, m, v, master=None, master_init=None,
-                     stream=None) -> ZeroStates:
+                     stream=None, bounds=None) -> ZeroStates:
     """m, v (and master, master_init in mixed precision): contiguous float32 CUDA
     tensors of n elements. Returns the state handle."""
     def ptr(t, what):
@@ -239,9 +264,17 @@ def zero_init_states(n: int, N: int, precision: int, m, v, master=None, master_i
             raise ValueError(f"{what} must be contiguous with at least {n} elements")
         return t.data_ptr()
     h = _vp()
-    _check(_lib.zero_init_states(n, N, precision, ptr(m, "m"), ptr(v, "v"), ptr(master, "master"),
-                                 ptr(master_init, "master_init"), _stream(stream), ctypes.byref(h)),
-           "zero_init_states")
+    if bounds is None:
+        _check(_lib.zero_init_states(n, N, precision, ptr(m, "m"), ptr(v, "v"),
+                                     ptr(master, "master"), ptr(master_init, "master_init"),
+                                     _stream(stream), ctypes.byref(h)), "zero_init_states")
+    else:
+        if len(bounds) != N + 1:
+            raise ValueError(f"need {N + 1} shard bounds")
+        _check(_lib.zero_init_states_ex(n, N, precision, ptr(m, "m"), ptr(v, "v"),
+                                        ptr(master, "master"), ptr(master_init, "master_init"),
+                                        _bounds_array(bounds), _stream(stream), ctypes.byref(h)),
+               "zero_init_states_ex")
     return ZeroStates(h.value, n, N, precision, {"m": m, "v": v, "master": master})
 
 

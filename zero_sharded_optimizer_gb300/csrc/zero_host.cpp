@@ -288,14 +288,40 @@ int zero_shard_bounds(int64_t n, int32_t N, int64_t* bounds) {
   return ZERO_OK;
 }
 
-int zero_memory_breakdown(int64_t n, int32_t N, int32_t stage, int32_t precision, int32_t rank,
-                          uint64_t out[3]) {
-  if (n < 0 || N < 1) return fail(ZERO_EINVAL, "need n >= 0 and N >= 1");
-  if (stage < 0 || stage > 3) return fail(ZERO_EINVAL, "stage %d outside 0..3", stage);
-  if (rank < 0 || rank >= N) return fail(ZERO_EINVAL, "rank %d outside [0, %d)", rank, N);
-  if (!out) return fail(ZERO_EINVAL, "out is NULL");
-  const int64_t q = n / N, r = n % N;
-  const uint64_t s = uint64_t(q + (rank < r ? 1 : 0));  // this rank's shard size
+}  // extern "C"
+
+namespace {
+
+// Whole-tensor shards: the tensor list is split like the indices of
+// np.array_split, and the shard bounds are the offsets of those tensors.
+int tensor_bounds(const int64_t* numels, int64_t T, int32_t N, int64_t* bounds) {
+  if (T < 0) return fail(ZERO_EINVAL, "T=%lld must be >= 0", (long long)T);
+  if (N < 1) return fail(ZERO_EINVAL, "N=%d must be >= 1", N);
+  if (!bounds || (T > 0 && !numels)) return fail(ZERO_EINVAL, "numels or bounds is NULL");
+  std::vector<int64_t> first(size_t(N) + 1);
+  shard_bounds(T, N, first.data());
+  int64_t offset = 0, k = 0;
+  for (int32_t i = 0; i <= N; ++i) {
+    while (k < first[i]) {
+      if (numels[k] < 0) return fail(ZERO_EINVAL, "tensor %lld has a negative size", (long long)k);
+      if (offset > INT64_MAX - numels[k]) return fail(ZERO_EINVAL, "tensor sizes overflow");
+      offset += numels[k++];
+    }
+    bounds[i] = offset;
+  }
+  return ZERO_OK;
+}
+
+// Caller-given shard bounds: N+1 offsets rising from 0 to n.
+int check_bounds(const int64_t* b, int64_t n, int32_t N) {
+  if (b[0] != 0 || b[N] != n) return fail(ZERO_EINVAL, "shard bounds must start at 0 and end at n");
+  for (int32_t i = 0; i < N; ++i)
+    if (b[i + 1] < b[i]) return fail(ZERO_EINVAL, "shard bounds must not decrease");
+  return ZERO_OK;
+}
+
+// Model-state bytes of one rank whose shard holds s of the n parameters.
+int breakdown(int64_t n, int32_t stage, int32_t precision, uint64_t s, uint64_t out[3]) {
   const uint64_t un = uint64_t(n);
   uint64_t p = 0, g = 0, o = 0;
   bool ok = true;
@@ -327,6 +353,35 @@ int zero_memory_breakdown(int64_t n, int32_t N, int32_t stage, int32_t precision
   return ZERO_OK;
 }
 
+}  // namespace
+
+extern "C" {
+
+int zero_memory_breakdown(int64_t n, int32_t N, int32_t stage, int32_t precision, int32_t rank,
+                          uint64_t out[3]) {
+  if (n < 0 || N < 1) return fail(ZERO_EINVAL, "need n >= 0 and N >= 1");
+  if (stage < 0 || stage > 3) return fail(ZERO_EINVAL, "stage %d outside 0..3", stage);
+  if (rank < 0 || rank >= N) return fail(ZERO_EINVAL, "rank %d outside [0, %d)", rank, N);
+  if (!out) return fail(ZERO_EINVAL, "out is NULL");
+  const int64_t q = n / N, r = n % N;
+  return breakdown(n, stage, precision, uint64_t(q + (rank < r ? 1 : 0)), out);
+}
+
+int zero_memory_breakdown_ex(int64_t n, int32_t N, int32_t stage, int32_t precision,
+                             int32_t rank, const int64_t* bounds, uint64_t out[3]) {
+  if (!bounds) return zero_memory_breakdown(n, N, stage, precision, rank, out);
+  if (n < 0 || N < 1) return fail(ZERO_EINVAL, "need n >= 0 and N >= 1");
+  if (stage < 0 || stage > 3) return fail(ZERO_EINVAL, "stage %d outside 0..3", stage);
+  if (rank < 0 || rank >= N) return fail(ZERO_EINVAL, "rank %d outside [0, %d)", rank, N);
+  if (!out) return fail(ZERO_EINVAL, "out is NULL");
+  if (int e = check_bounds(bounds, n, N)) return e;
+  return breakdown(n, stage, precision, uint64_t(bounds[rank + 1] - bounds[rank]), out);
+}
+
+int zero_tensor_shard_bounds(const int64_t* numels, int64_t T, int32_t N, int64_t* bounds) {
+  return tensor_bounds(numels, T, N, bounds);
+}
+
 int zero_memory_bytes(int64_t n, int32_t N, int32_t stage, int32_t precision, uint64_t* out) {
   if (!out) return fail(ZERO_EINVAL, "out is NULL");
   uint64_t b[3];
@@ -342,10 +397,18 @@ int zero_memory_bytes(int64_t n, int32_t N, int32_t stage, int32_t precision, ui
 
 int zero_init_states(int64_t n, int32_t N, int32_t precision, float* m, float* v, float* master,
                      const float* master_init, zero_stream_t stream, zero_states_t** out) {
+  return zero_init_states_ex(n, N, precision, m, v, master, master_init, nullptr, stream, out);
+}
+
+int zero_init_states_ex(int64_t n, int32_t N, int32_t precision, float* m, float* v,
+                        float* master, const float* master_init, const int64_t* bounds,
+                        zero_stream_t stream, zero_states_t** out) {
   if (!out) return fail(ZERO_EINVAL, "out is NULL");
   *out = nullptr;
   if (n < 0) return fail(ZERO_EINVAL, "n=%lld must be >= 0", (long long)n);
   if (!valid_ranks(N)) return fail(ZERO_EINVAL, "N=%d outside [1, %d]", N, ZERO_MAX_RANKS);
+  if (bounds)
+    if (int e = check_bounds(bounds, n, N)) return e;
   if (precision != ZERO_FP32 && precision != ZERO_BF16_MIXED)
     return fail(ZERO_EINVAL, "state precision must be FP32 or BF16_MIXED");
   if (n > 0 && (!m || !v)) return fail(ZERO_EINVAL, "m or v is NULL");
@@ -374,7 +437,8 @@ int zero_init_states(int64_t n, int32_t N, int32_t precision, float* m, float* v
   st->m = m;
   st->v = v;
   st->master = master;
-  shard_bounds(n, N, st->bounds);
+  if (bounds) std::memcpy(st->bounds, bounds, sizeof(int64_t) * (N + 1));
+  else shard_bounds(n, N, st->bounds);
   if (n > 0) {
     zk::InitArgs ia{m, v, master, master_init, make_split(0, n, same, ph, 4)};
     cudaError_t e = zk::launch_init(ia, reinterpret_cast<cudaStream_t>(stream));

@@ -25,10 +25,13 @@ class ZeroOptimizer:
     def __init__(self, n: int, N: int, precision: int = abi.ZERO_FP32, lr: float = 1e-3,
                  betas=(0.9, 0.999), eps: float = 1e-8, weight_decay: float = 0.0,
                  master_init: torch.Tensor | None = None, device="cuda", stream=None,
-                 max_grad_norm: float = 0.0, grad_scale: float = 1.0):
+                 max_grad_norm: float = 0.0, grad_scale: float = 1.0, shard_bounds=None):
         """``max_grad_norm`` > 0 clips the (scaled) mean gradient to that global
         norm before every step; ``grad_scale`` multiplies the mean gradient
-        (1/k when the gradient buffers hold the sum of k micro-batches)."""
+        (1/k when the gradient buffers hold the sum of k micro-batches);
+        ``shard_bounds`` (N+1 offsets) replaces the np.array_split shards, e.g.
+        ``abi.zero_tensor_shard_bounds(tensor_sizes, N)`` for whole-tensor shards."""
+        self.shard_bounds = None if shard_bounds is None else [int(b) for b in shard_bounds]
         self.n, self.N, self.precision = int(n), int(N), int(precision)
         self.max_grad_norm, self.grad_scale = float(max_grad_norm), float(grad_scale)
         self._norm = None
@@ -46,7 +49,7 @@ class ZeroOptimizer:
             self.master = torch.empty(self.n, **f32)
             master_init = master_init.to(self.device, torch.float32).contiguous()
         self.states = abi.zero_init_states(self.n, self.N, self.precision, self.m, self.v,
-                                           self.master, master_init, stream)
+                                           self.master, master_init, stream, self.shard_bounds)
         self.t = 0
         self._staging = None
 
@@ -133,8 +136,12 @@ class ZeroOptimizer:
 
     def memory_bytes(self, stage: int, rank: int | None = None):
         if rank is None:
-            return abi.zero_memory_bytes(self.n, self.N, stage, self.precision)
-        return abi.zero_memory_breakdown(self.n, self.N, stage, self.precision, rank)
+            if self.shard_bounds is None:
+                return abi.zero_memory_bytes(self.n, self.N, stage, self.precision)
+            return max(sum(abi.zero_memory_breakdown_ex(self.n, self.N, stage, self.precision, r,
+                                                        self.shard_bounds)) for r in range(self.N))
+        return abi.zero_memory_breakdown_ex(self.n, self.N, stage, self.precision, rank,
+                                            self.shard_bounds)
 
     # ------------------------------------------------------- checkpointing --
 
