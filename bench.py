@@ -244,9 +244,14 @@ def run_gpu(args, wl, rank: int, world: int, local_rank: int) -> dict | None:
     grads = inputs.make_grads(n, N, wl.precision, device=dev)
     inputs.fill_grads(grads, wl, step=1, seed=rank)
     clip = args.max_grad_norm > 0
+    bounds = None
+    if args.partition == "tensor":
+        # whole-tensor shards over the workload's parameter list
+        bounds = abi.zero_tensor_shard_bounds([int(np.prod(s)) for _, s in
+                                               inputs.gpt2_small_shapes()], N)
     opt = ZeroOptimizer(n, N, wl.precision, lr=wl.lr, betas=(wl.beta1, wl.beta2), eps=wl.eps,
                         weight_decay=wl.weight_decay, master_init=init if mixed else None,
-                        max_grad_norm=args.max_grad_norm)
+                        max_grad_norm=args.max_grad_norm, shard_bounds=bounds)
     del init
     bucketed = wl.bucket_bytes > 0
     launches_per_step = len(opt.bucket_ranges(wl.bucket_bytes)) if bucketed else 1
@@ -342,7 +347,10 @@ def run_gpu(args, wl, rank: int, world: int, local_rank: int) -> dict | None:
         "data": "synthetic (seeded device draws; inputs resident in HBM)",
         "config": config_of(wl, {"parallelism": f"{N} simulated ranks per GPU; "
                                                 f"{world} independent GPU replica(s)",
-                                 **({"max_grad_norm": args.max_grad_norm} if clip else {})}),
+                                 **({"max_grad_norm": args.max_grad_norm} if clip else {}),
+                                 "partition": ("whole tensors (" + ", ".join(
+                                     str(int(b2 - b1)) for b1, b2 in zip(bounds, bounds[1:])) +
+                                     " params per rank)") if bounds else "np.array_split"}),
         "hbm_gbs": step_bytes / (ms_step / 1e3) / 1e9,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
@@ -407,6 +415,8 @@ def main(argv=None):
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(inputs.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    ap.add_argument("--partition", default="array_split", choices=["array_split", "tensor"],
+                    help="tensor: shards of whole tensors (workloads with a tensor list)")
     ap.add_argument("--max-grad-norm", type=float, default=0.0,
                     help="> 0: sharded global-norm clipping before every step (norm pass + step)")
     args = ap.parse_args(argv)
@@ -415,6 +425,8 @@ def main(argv=None):
         args.steps = default_steps(wl)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.partition == "tensor" and wl.name != "gpt2_small":
+        ap.error("--partition tensor needs a workload with a tensor list (gpt2_small)")
     if args.max_grad_norm > 0 and wl.bucket_bytes:
         ap.error("clipping needs the whole gradient before the step: not with bucket streaming")
     world = int(os.environ.get("WORLD_SIZE", "1"))

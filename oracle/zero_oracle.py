@@ -76,7 +76,7 @@ import numpy as np
 __all__ = [
     "FP32", "BF16_MIXED", "FP64_EMU",
     "shard_bounds", "init_states", "zero_step", "adam_full", "allreduce_mean",
-    "grad_norm", "grad_multiplier", "tensor_shard_bounds",
+    "grad_norm", "grad_multiplier", "tensor_shard_bounds", "gather",
     "memory_bytes", "memory_breakdown", "bucket_bounds",
     "bf16_to_f32", "f32_to_bf16_rne", "mirror_scalars",
 ]
@@ -327,7 +327,7 @@ def grad_multiplier(norm: float, grad_scale: float = 1.0, max_grad_norm=None) ->
 
 def zero_step(params, grads, states, t, lr=1e-2, beta1=0.9, beta2=0.999, eps=1e-8,
               weight_decay=0.0, precision=FP32, mode="fp32", grad_scale=1.0,
-              max_grad_norm=None, bounds=None):
+              max_grad_norm=None, bounds=None, all_gather=True):
     """One ZeRO step; returns (new_params, new_states).
 
     ``params``: N full-length replicas (float32, or bf16 bits as uint16).
@@ -344,6 +344,8 @@ def zero_step(params, grads, states, t, lr=1e-2, beta1=0.9, beta2=0.999, eps=1e-
     ``bounds`` (N+1 offsets, default the array_split shards) sets who owns
     what, e.g. whole tensors from ``tensor_shard_bounds``; it must match the
     bounds ``states`` were built with.
+    With ``all_gather=False`` (ZeRO-3) step 3 is left out: each rank's entry
+    of the result is only its own updated chunk (``gather`` assembles them).
     With ``grad_scale`` != 1 or ``max_grad_norm`` set, the mean gradient is
     first multiplied by ``grad_multiplier`` (rounded to float32 in the fp32
     mode); the global norm it needs comes from ``grad_norm`` of the same
@@ -376,7 +378,20 @@ def zero_step(params, grads, states, t, lr=1e-2, beta1=0.9, beta2=0.999, eps=1e-
             ns["master"] = p_new
         new_states.append(ns)
         new_shards.append(p_new)
+    if not all_gather:
+        # ZeRO-3 ("Data parallelism and ZeRO stages 1 to 3", section 2, stage 3):
+        # between steps each rank keeps only its own chunk of the parameters
+        return [_replica_from(sh, precision, mode) for sh in new_shards], new_states
     return _all_gather(new_shards, N, precision, mode), new_states                # 3.
+
+
+def gather(shards, precision=FP32, mode="fp32"):
+    """ZeRO-3 gather(): all-gather the ranks' parameter chunks into the full
+    parameters on every rank ("Data parallelism and ZeRO stages 1 to 3", section
+    2, stage 3, and section 4, ``gather()`` before the forward pass). ``shards``
+    are the chunks in storage form (float32, or bf16 bits)."""
+    full = np.concatenate(shards) if shards else np.zeros(0, np.float32)
+    return [full.copy() for _ in range(len(shards))]
 
 
 def adam_full(param, mean_grad, m, v, t, lr=1e-2, beta1=0.9, beta2=0.999, eps=1e-8,

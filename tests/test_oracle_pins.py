@@ -596,3 +596,43 @@ def test_tensor_shard_memory():
         (4 * 903, 4 * 903, 8 * 903)
     with pytest.raises(ValueError):
         oracle.memory_breakdown(1017, 2, 1, oracle.FP32, 0, bounds=[0, 2000, 1017])
+
+
+# ---------------------------------------------------------------------------
+# ZeRO-3: release after the step, gather before the forward pass
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("mode", ["fp64", "fp32"])
+def test_p1_worked_example_stage3(mode):
+    # course page section 3: "every stage gives this on every rank: rank 0 computes
+    # entries 0 to 2, rank 3 entries 8 and 9, and ... stage 3's gather() assembles
+    # the rest"
+    ex = golden("p1_worked_example.json")
+    w = np.array(ex["w"], np.float32)
+    p = ex["p"]
+    grads = [w - np.float32(r) for r in range(p)]
+    states = oracle.init_states(len(w), p, mode=mode)
+    shards, _ = oracle.zero_step([w.copy() for _ in range(p)], grads, states, 1, lr=ex["lr"],
+                                 weight_decay=ex["weight_decay"], mode=mode, all_gather=False)
+    assert [len(s) for s in shards] == ex["chunk_sizes"]
+    np.testing.assert_allclose(shards[0], ex["expected_w"][:3], atol=1e-6)
+    np.testing.assert_allclose(shards[3], ex["expected_w"][8:], atol=1e-6)
+    for rep in oracle.gather(shards):
+        np.testing.assert_allclose(rep, ex["expected_w"], atol=1e-6)
+
+
+def test_stage3_gather_equals_all_gather():
+    rng = np.random.default_rng(101)
+    n, N = 1009, 5
+    init = rng.normal(0, 0.02, n).astype(np.float32)
+    for prec in (oracle.FP32, oracle.BF16_MIXED):
+        reps = [oracle.f32_to_bf16_rne(init) if prec else init.copy() for _ in range(N)]
+        a_s = oracle.init_states(n, N, prec, master_init=init)
+        b_s = oracle.init_states(n, N, prec, master_init=init)
+        g = [rng.normal(size=n).astype(np.float32) for _ in range(N)]
+        if prec:
+            g = [oracle.f32_to_bf16_rne(x) for x in g]
+        full, _ = oracle.zero_step(reps, g, a_s, 1, precision=prec)
+        shards, _ = oracle.zero_step(reps, g, b_s, 1, precision=prec, all_gather=False)
+        for x, y in zip(oracle.gather(shards), full):
+            assert np.array_equal(x, y)
