@@ -251,12 +251,16 @@ def run_gpu(args, wl, rank: int, world: int, local_rank: int) -> dict | None:
                                                inputs.gpt2_small_shapes()], N)
     opt = ZeroOptimizer(n, N, wl.precision, lr=wl.lr, betas=(wl.beta1, wl.beta2), eps=wl.eps,
                         weight_decay=wl.weight_decay, master_init=init if mixed else None,
-                        max_grad_norm=args.max_grad_norm, shard_bounds=bounds)
+                        max_grad_norm=args.max_grad_norm, shard_bounds=bounds,
+                        stage=args.stage)
     del init
+    stage3 = args.stage == 3
     bucketed = wl.bucket_bytes > 0
     launches_per_step = len(opt.bucket_ranges(wl.bucket_bytes)) if bucketed else 1
     if clip:
         launches_per_step = 3       # norm partials, norm total, clipped step
+    if stage3:
+        launches_per_step += 1      # the gather after the owner-only step
     stream = torch.cuda.current_stream()
 
     def one_step():
@@ -264,6 +268,8 @@ def run_gpu(args, wl, rank: int, world: int, local_rank: int) -> dict | None:
             opt.step_bucketed(reps, grads, None, stream, wl.bucket_bytes)
         else:
             opt.step(reps, grads)
+            if stage3:
+                opt.gather(reps)
 
     def barrier():
         if world > 1:
@@ -327,11 +333,14 @@ def run_gpu(args, wl, rank: int, world: int, local_rank: int) -> dict | None:
     step_bytes = n * bytes_per_param(wl)
     if clip:  # the norm pass reads every rank's gradient once more
         step_bytes += n * N * (2 if mixed else 4)
+    if stage3:  # the step writes 1 replica, not N; the gather reads 1 and writes N-1
+        step_bytes += n * (2 if mixed else 4)
     achieved = step_bytes / (kernel_ms / 1e3) / 1e9
     traffic = traffic_per_launch(wl.name)
-    if traffic is not None and (bucketed or clip):
+    if traffic is not None and (bucketed or clip or stage3):
         traffic = None
-    per = 1 if clip else launches_per_step  # clip: the roofline covers the whole step
+    whole = clip or stage3  # the roofline covers the whole step (several kernels)
+    per = 1 if whole else launches_per_step
     line = {
         "metric": METRIC,
         "value": whole_job_rate(n, world, ms_step),
@@ -348,6 +357,7 @@ def run_gpu(args, wl, rank: int, world: int, local_rank: int) -> dict | None:
         "config": config_of(wl, {"parallelism": f"{N} simulated ranks per GPU; "
                                                 f"{world} independent GPU replica(s)",
                                  **({"max_grad_norm": args.max_grad_norm} if clip else {}),
+                                 **({"zero_stage": 3} if stage3 else {}),
                                  "partition": ("whole tensors (" + ", ".join(
                                      str(int(b2 - b1)) for b1, b2 in zip(bounds, bounds[1:])) +
                                      " params per rank)") if bounds else "np.array_split"}),
@@ -359,6 +369,8 @@ def run_gpu(args, wl, rank: int, world: int, local_rank: int) -> dict | None:
                      "algorithmic_bytes_per_launch": step_bytes // per,
                      "kernel": ("grad_norm_partials_kernel + grad_norm_total_kernel + "
                                 "zero_step_tma_kernel (whole clipped step)") if clip else
+                               ("zero_step_tma_kernel (owner-only) + gather_kernel "
+                                "(whole stage-3 step)") if stage3 else
                                ("zero_step_tma_kernel" if wl.N <= 8 else "zero_step_kernel"),
                      "kernel_ms": kernel_ms / per},
         "gpu_launches": K * launches_per_step,
@@ -419,6 +431,8 @@ def main(argv=None):
                     help="tensor: shards of whole tensors (workloads with a tensor list)")
     ap.add_argument("--max-grad-norm", type=float, default=0.0,
                     help="> 0: sharded global-norm clipping before every step (norm pass + step)")
+    ap.add_argument("--stage", type=int, default=2, choices=[2, 3],
+                    help="3: owner-only step, then the gather of the full parameters (2 launches)")
     args = ap.parse_args(argv)
     wl = inputs.WORKLOADS[args.workload]
     if args.steps is None:
@@ -429,6 +443,8 @@ def main(argv=None):
         ap.error("--partition tensor needs a workload with a tensor list (gpt2_small)")
     if args.max_grad_norm > 0 and wl.bucket_bytes:
         ap.error("clipping needs the whole gradient before the step: not with bucket streaming")
+    if args.stage == 3 and wl.bucket_bytes:
+        ap.error("bucket streaming runs the step with its all-gather: not with --stage 3")
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))

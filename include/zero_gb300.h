@@ -211,6 +211,12 @@ typedef struct zero_step_opts {
    * clipping, ignored otherwise. */
   const double *norm_sq;
   int64_t lo, hi;        /* index range of the step; hi < 0 means n */
+  /* Nonzero: ZeRO stage 3 ("Data parallelism and ZeRO stages 1 to 3",
+   * section 2, stage 3). The all-gather is left out: the new parameters are
+   * written only into the owner's replica, over the owner's shard, and every
+   * other replica element is left as it was (released). zero_gather brings the
+   * replicas back to the full parameters. 0: the stage-1/2 step. */
+  int32_t owner_only;
 } zero_step_opts_t;
 
 /* zero_step with the options above. The multiplier grad_scale * coefficient
@@ -221,6 +227,20 @@ typedef struct zero_step_opts {
  * max_grad_norm, or clipping without norm_sq. */
 int zero_step_ex(void *const *params, const void *const *grads, zero_states_t *st,
                  const zero_step_opts_t *opts, zero_stream_t stream);
+
+/* ZeRO-3 gather(): all-gather the parameter shards into every replica
+ * ("Data parallelism and ZeRO stages 1 to 3", section 2, stage 3, and
+ * section 4, gather() before the forward pass). For every index j in
+ * [lo, hi) with owner r (bounds[r] <= j < bounds[r+1], the state's shard
+ * bounds), params[r][j] is copied into params[q][j] for every q != r; the
+ * owner's element is only read. params: st->N device replicas of n elements
+ * (float in ZERO_FP32, bf16 bits in ZERO_BF16_MIXED), disjoint; hi < 0 means
+ * n. One kernel on `stream`, asynchronous; the copy is exact. Reads one and
+ * writes N-1 elements per index.
+ * Errors: EINVAL (NULL handle or replica, bad range, overlapping replicas),
+ * EALIGN (a replica not aligned to its element size), ECUDA (launch). */
+int zero_gather(void *const *params, zero_states_t *st, int64_t lo, int64_t hi,
+                zero_stream_t stream);
 
 /* --------------------------------------------------------------- buckets -- */
 

@@ -77,6 +77,7 @@ _SIGNATURES = {
     "zero_grad_norm_scratch_count": (ctypes.c_int, [_i64, _i32, _P(_i64)]),
     "zero_grad_norm_sq": (ctypes.c_int, [_P(_vp), _i64, _i32, _i32, _vp, _i64, _vp, _vp]),
     "zero_step_ex": (ctypes.c_int, [_P(_vp), _P(_vp), _vp, _vp, _vp]),
+    "zero_gather": (ctypes.c_int, [_P(_vp), _vp, _i64, _i64, _vp]),
     "zero_grad_norm_sq_noalloc": (ctypes.c_int, [_P(_vp), _i64, _i32, _i32, _vp, _vp]),
     "zero_device_status": (ctypes.c_int, [_P(ctypes.c_uint32), _i32]),
     "zero_debug_set_wait_timeout_ns": (ctypes.c_int, [_u64]),
@@ -328,7 +329,7 @@ class StepOpts(ctypes.Structure):
     """zero_step_opts_t."""
     _fields_ = [("t", _i64), ("lr", _dbl), ("beta1", _dbl), ("beta2", _dbl), ("eps", _dbl),
                 ("weight_decay", _dbl), ("grad_scale", _dbl), ("max_grad_norm", _dbl),
-                ("norm_sq", _vp), ("lo", _i64), ("hi", _i64)]
+                ("norm_sq", _vp), ("lo", _i64), ("hi", _i64), ("owner_only", _i32)]
 
 
 def _f64_device_ptr(t, count: int, what: str):
@@ -374,11 +375,22 @@ def zero_grad_norm_sq_noalloc(grads, precision: int, norm_sq, n: int | None = No
 def zero_step_ex(params, grads, st: ZeroStates, t: int, lr: float, beta1: float = 0.9,
                  beta2: float = 0.999, eps: float = 1e-8, weight_decay: float = 0.0,
                  grad_scale: float = 1.0, max_grad_norm: float = 0.0, norm_sq=None,
-                 lo: int = 0, hi: int = -1, stream=None):
+                 lo: int = 0, hi: int = -1, stream=None, owner_only: bool = False):
+    """``owner_only`` (ZeRO-3): write the new parameters into the owner's
+    replica over its own shard only; ``zero_gather`` restores the replicas."""
     pp, gp = _step_ptrs(params, grads, st)
     nq = None if norm_sq is None else _f64_device_ptr(norm_sq, 1, "norm_sq")
-    o = StepOpts(t, lr, beta1, beta2, eps, weight_decay, grad_scale, max_grad_norm, nq, lo, hi)
+    o = StepOpts(t, lr, beta1, beta2, eps, weight_decay, grad_scale, max_grad_norm, nq, lo, hi,
+                 1 if owner_only else 0)
     _check(_lib.zero_step_ex(pp, gp, st.handle, ctypes.byref(o), _stream(stream)), "zero_step_ex")
+
+
+def zero_gather(params, st: ZeroStates, lo: int = 0, hi: int = -1, stream=None):
+    """ZeRO-3 gather: copy every shard from its owner's replica into the others."""
+    if len(params) != st.N:
+        raise ValueError(f"need {st.N} params")
+    pp = _ptr_array(params, st.n, _storage_dtype(st.precision), "params")
+    _check(_lib.zero_gather(pp, st.handle, lo, hi, _stream(stream)), "zero_gather")
 
 
 def _host_ptr_array(tensors, n: int, dtype, what: str):

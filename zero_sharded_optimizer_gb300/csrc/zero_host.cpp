@@ -524,7 +524,45 @@ int zero_step_ex(void* const* params, const void* const* grads, zero_states_t* s
     a.norm_sq = o->norm_sq;
     a.max_norm = o->max_grad_norm;
   }
+  a.owner_only = o->owner_only != 0;
   return launch_range(a, st, vec, phase, lo, hi, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int zero_gather(void* const* params, zero_states_t* st, int64_t lo, int64_t hi,
+                zero_stream_t stream) {
+  if (!st) return fail(ZERO_EINVAL, "state handle is NULL");
+  if (!params) return fail(ZERO_EINVAL, "params array is NULL");
+  if (hi < 0) hi = st->n;
+  if (lo < 0 || hi < lo || hi > st->n)
+    return fail(ZERO_EINVAL, "range [%lld, %lld) outside [0, %lld)", (long long)lo, (long long)hi,
+                (long long)st->n);
+  const int32_t N = st->N;
+  const bool bf16 = st->precision == ZERO_BF16_MIXED;
+  const int es = bf16 ? 2 : 4;
+  zk::GatherArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.N = N;
+  std::memcpy(a.bounds, st->bounds, sizeof(int64_t) * (N + 1));
+  std::vector<Range> rs;
+  int ph = -2;
+  bool same = true;
+  for (int32_t r = 0; r < N; ++r) {
+    if (st->n > 0 && !params[r]) return fail(ZERO_EINVAL, "params[%d] is NULL", r);
+    const int q = phase_of(params[r], es);
+    if (q < 0) return fail(ZERO_EALIGN, "params[%d] not aligned to %d bytes", r, es);
+    if (ph == -2) ph = q;
+    else if (ph != q) same = false;
+    a.reps[r] = params[r];
+    if (st->n > 0)
+      rs.push_back({uintptr_t(params[r]), uintptr_t(params[r]) + uintptr_t(st->n) * es,
+                    "a parameter replica"});
+  }
+  if (int e = check_disjoint(rs)) return e;
+  if (hi <= lo || N == 1) return ZERO_OK;
+  a.sp = make_split(lo, hi, same, ph, bf16 ? 8 : 4);
+  cudaError_t e = zk::launch_gather(a, bf16, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "zero_gather kernel launch");
+  return ZERO_OK;
 }
 
 int zero_grad_norm_scratch_count(int64_t n, int32_t precision, int64_t* count) {

@@ -54,6 +54,9 @@ struct StepArgs {
   const double* norm_sq;         // device scalar, or NULL (no clipping)
   double gscale;
   double max_norm;
+  // Stage 3: write the new parameters only into the owner's replica, over the
+  // owner's shard; the other replicas' elements are left untouched.
+  int32_t owner_only;
 };
 
 // Squared global norm of the mean gradient, as fixed-size partial sums.
@@ -77,6 +80,15 @@ struct AllreduceArgs {
   uint64_t wait_ns;
 };
 
+// Stage-3 all-gather: copy each shard [bounds[r], bounds[r+1]) of replica r
+// into every other replica, over the range of sp.
+struct GatherArgs {
+  void* reps[kMaxRanks];
+  int64_t bounds[kMaxRanks + 1];
+  Split sp;
+  int32_t N;
+};
+
 struct InitArgs {
   float* m;
   float* v;
@@ -89,6 +101,7 @@ struct InitArgs {
 cudaError_t launch_step(const StepArgs& a, bool mixed, cudaStream_t s);
 cudaError_t launch_allreduce(const AllreduceArgs& a, bool bf16, cudaStream_t s);
 cudaError_t launch_init(const InitArgs& a, cudaStream_t s);
+cudaError_t launch_gather(const GatherArgs& a, bool bf16, cudaStream_t s);
 // Partial sums then their fixed-order total (two launches, deterministic).
 cudaError_t launch_norm(const NormArgs& a, bool bf16, cudaStream_t s);
 

@@ -29,6 +29,7 @@
 #include <stdint.h>
 
 #include <mutex>
+#include <type_traits>
 
 #include "zero_internal.h"
 
@@ -189,12 +190,14 @@ __device__ __forceinline__ void step_scalar(const StepArgs& P, int64_t j, int ow
   adam1(P.c, scaled_mean<NR>(s, P, gm), p, m, v);
   __stcs(P.m + j, m);
   __stcs(P.v + j, v);
+  // Stage 3 (owner_only) keeps only the owner's replica current.
+  const int r_lo = P.owner_only ? owner : 0, r_hi = P.owner_only ? owner : N - 1;
   if constexpr (MIXED) {
     __stcs(P.master + j, p);
     const uint16_t h = to_bf(p);
-    for (int r = 0; r < N; ++r) __stcs(static_cast<uint16_t*>(P.reps[r]) + j, h);
+    for (int r = r_lo; r <= r_hi; ++r) __stcs(static_cast<uint16_t*>(P.reps[r]) + j, h);
   } else {
-    for (int r = 0; r < N; ++r) __stcs(static_cast<float*>(P.reps[r]) + j, p);
+    for (int r = r_lo; r <= r_hi; ++r) __stcs(static_cast<float*>(P.reps[r]) + j, p);
   }
 }
 
@@ -244,7 +247,19 @@ __device__ __forceinline__ void step_vec_fp32(const StepArgs& P, int64_t j, int 
   adam1(P.c, scaled_mean<NR>(s.w, P, gm), p.w, m.w, v.w);
   st4(P.m + j, m);
   st4(P.v + j, v);
-  if constexpr (NR > 0) {
+  if (P.owner_only) {  // stage 3: the owners of the unit's elements only
+    const int last = advance_owner(P, owner, j + 3);
+    if (last == owner) {
+      st4(static_cast<float*>(P.reps[owner]) + j, p);
+    } else {
+      const float e[4] = {p.x, p.y, p.z, p.w};
+      int o = owner;
+      for (int k = 0; k < 4; ++k) {
+        o = advance_owner(P, o, j + k);
+        __stcs(static_cast<float*>(P.reps[o]) + j + k, e[k]);
+      }
+    }
+  } else if constexpr (NR > 0) {
 #pragma unroll
     for (int r = 0; r < NR; ++r) st4(static_cast<float*>(P.reps[r]) + j, p);
   } else {
@@ -255,7 +270,7 @@ __device__ __forceinline__ void step_vec_fp32(const StepArgs& P, int64_t j, int 
 // ------------------------------------------------------ mixed vector path (V=8)
 
 template <int NR>
-__device__ __forceinline__ void step_vec_mixed(const StepArgs& P, int64_t j, float gm) {
+__device__ __forceinline__ void step_vec_mixed(const StepArgs& P, int64_t j, int owner, float gm) {
   const int N = ranks<NR>(P);
   const float4 p0 = ld4(P.master + j), p1 = ld4(P.master + j + 4);
   const float4 m0 = ld4(P.m + j), m1 = ld4(P.m + j + 4);
@@ -295,7 +310,18 @@ __device__ __forceinline__ void step_vec_mixed(const StepArgs& P, int64_t j, flo
   st4(P.v + j, make_float4(v[0], v[1], v[2], v[3]));
   st4(P.v + j + 4, make_float4(v[4], v[5], v[6], v[7]));
   const uint4 h = pack8(p);
-  if constexpr (NR > 0) {
+  if (P.owner_only) {  // stage 3: the owners of the unit's elements only
+    const int last = advance_owner(P, owner, j + 7);
+    if (last == owner) {
+      st8h(static_cast<uint16_t*>(P.reps[owner]) + j, h);
+    } else {
+      int o = owner;
+      for (int k = 0; k < 8; ++k) {
+        o = advance_owner(P, o, j + k);
+        __stcs(static_cast<uint16_t*>(P.reps[o]) + j + k, to_bf(p[k]));
+      }
+    }
+  } else if constexpr (NR > 0) {
 #pragma unroll
     for (int r = 0; r < NR; ++r) st8h(static_cast<uint16_t*>(P.reps[r]) + j, h);
   } else {
@@ -333,7 +359,8 @@ __global__ void __launch_bounds__(kThreads) zero_step_kernel(const __grid_consta
   for (int64_t u = tid; u < sp.nvec; u += stride) {
     const int64_t j = base + u * V;
     if constexpr (MIXED) {
-      step_vec_mixed<NR>(P, j, gm);
+      if (P.owner_only) owner = advance_owner(P, owner, j);
+      step_vec_mixed<NR>(P, j, owner, gm);
     } else {
       owner = advance_owner(P, owner, j);
       step_vec_fp32<NR>(P, j, owner, gm);
@@ -553,6 +580,60 @@ __global__ void __launch_bounds__(kThreads)
   }
 }
 
+// ------------------------------------------------------- stage-3 all-gather --
+
+// Every replica receives each shard from its owner's replica: one 16-byte load
+// and N-1 16-byte stores per unit (V = 4 fp32 or 8 bf16 elements); a unit that
+// straddles a shard boundary, and the scalar head and tail, go element by
+// element. A pure copy: the bits are moved, never converted.
+__device__ __forceinline__ int gather_owner(const GatherArgs& P, int owner, int64_t j) {
+  while (j >= P.bounds[owner + 1]) ++owner;
+  return owner;
+}
+
+template <typename E>
+__device__ __forceinline__ void gather_one(const GatherArgs& P, int owner, int64_t j) {
+  const E x = __ldcs(static_cast<const E*>(P.reps[owner]) + j);
+  for (int r = 0; r < P.N; ++r)
+    if (r != owner) __stcs(static_cast<E*>(P.reps[r]) + j, x);
+}
+
+template <bool BF16>
+__global__ void __launch_bounds__(kThreads) gather_kernel(const __grid_constant__ GatherArgs P) {
+  using E = typename std::conditional<BF16, uint16_t, float>::type;
+  constexpr int V = 16 / int(sizeof(E));
+  const int64_t tid = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+  const Split& sp = P.sp;
+
+  const int64_t nscalar = sp.head + sp.tail;
+  const int64_t body_end = sp.lo + sp.head + sp.nvec * V;
+  int owner = 0;
+  for (int64_t s = tid; s < nscalar; s += stride) {
+    const int64_t j = s < sp.head ? sp.lo + s : body_end + (s - sp.head);
+    owner = gather_owner(P, owner, j);
+    gather_one<E>(P, owner, j);
+  }
+
+  const int64_t base = sp.lo + sp.head;
+  owner = 0;
+  for (int64_t u = tid; u < sp.nvec; u += stride) {
+    const int64_t j = base + u * V;
+    owner = gather_owner(P, owner, j);
+    if (j + V - 1 < P.bounds[owner + 1]) {
+      const uint4 x = __ldcs(reinterpret_cast<const uint4*>(static_cast<const E*>(P.reps[owner]) + j));
+      for (int r = 0; r < P.N; ++r)
+        if (r != owner) __stcs(reinterpret_cast<uint4*>(static_cast<E*>(P.reps[r]) + j), x);
+    } else {
+      int o = owner;
+      for (int k = 0; k < V; ++k) {
+        o = gather_owner(P, o, j + k);
+        gather_one<E>(P, o, j + k);
+      }
+    }
+  }
+}
+
 // m = v = 0 and (mixed) master = init over the split range.
 __global__ void __launch_bounds__(kThreads) init_state_kernel(const __grid_constant__ InitArgs P) {
   const int64_t tid = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -727,6 +808,11 @@ cudaError_t launch_allreduce(const AllreduceArgs& a, bool bf16, cudaStream_t s) 
 cudaError_t launch_init(const InitArgs& a, cudaStream_t s) {
   const int64_t work = a.sp.nvec > a.sp.head + a.sp.tail ? a.sp.nvec : a.sp.head + a.sp.tail;
   return launch(init_state_kernel, a, work, s);
+}
+
+cudaError_t launch_gather(const GatherArgs& a, bool bf16, cudaStream_t s) {
+  const int64_t work = a.sp.nvec > a.sp.head + a.sp.tail ? a.sp.nvec : a.sp.head + a.sp.tail;
+  return bf16 ? launch(gather_kernel<true>, a, work, s) : launch(gather_kernel<false>, a, work, s);
 }
 
 namespace {

@@ -148,6 +148,21 @@ struct MeanTile {
   static constexpr uint32_t kSmem = Cfg::kStages * kStage + Cfg::kOutBufs * kTile;
 };
 
+// Elements [a, b) of a shared-memory tile whose first element j0 sits on a
+// 16-byte boundary of dst: the 16-byte-aligned middle as one bulk copy, the
+// ragged ends (fewer than 16 bytes each) as plain stores by this thread.
+template <typename E>
+__device__ __forceinline__ void store_slice(E* dst, const E* tile, int64_t j0, int64_t a,
+                                            int64_t b) {
+  constexpr int64_t U = 16 / int64_t(sizeof(E));
+  int64_t a16 = j0 + (a - j0 + U - 1) / U * U;
+  int64_t b16 = j0 + (b - j0) / U * U;
+  if (a16 >= b16) a16 = b16 = b;  // no aligned middle: all plain stores
+  for (int64_t k = a; k < a16; ++k) __stcs(dst + k, tile[k - j0]);
+  if (b16 > a16) bulk_store(dst + a16, tile + (a16 - j0), uint32_t((b16 - a16) * sizeof(E)));
+  for (int64_t k = b16; k < b; ++k) __stcs(dst + k, tile[k - j0]);
+}
+
 // Shared pipeline state of one CTA.
 template <int S>
 struct PipeState {
@@ -302,8 +317,20 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
     const uint32_t fbytes = cnt * 4;
     bulk_store(P.m + j0, out_f(s, o, 1), fbytes);
     bulk_store(P.v + j0, out_f(s, o, 2), fbytes);
-    if constexpr (MIXED) {
-      bulk_store(P.master + j0, out_f(s, o, 0), fbytes);
+    if constexpr (MIXED) bulk_store(P.master + j0, out_f(s, o, 0), fbytes);
+    if (P.owner_only) {  // stage 3: each owner's slice of its own replica only
+      const int r_lo = advance_owner(P, 0, j0);
+      const int r_hi = advance_owner(P, r_lo, j0 + cnt - 1);
+      for (int r = r_lo; r <= r_hi; ++r) {
+        const int64_t a = j0 > P.bounds[r] ? j0 : P.bounds[r];
+        const int64_t b = j0 + cnt < P.bounds[r + 1] ? j0 + cnt : P.bounds[r + 1];
+        if constexpr (MIXED)
+          store_slice(static_cast<uint16_t*>(P.reps[r]),
+                      reinterpret_cast<const uint16_t*>(out_bf(s, o)), j0, a, b);
+        else
+          store_slice(static_cast<float*>(P.reps[r]), out_f(s, o, 0), j0, a, b);
+      }
+    } else if constexpr (MIXED) {
 #pragma unroll
       for (int r = 0; r < NR; ++r)
         bulk_store(static_cast<unsigned char*>(P.reps[r]) + j0 * 2, out_bf(s, o), cnt * 2);

@@ -25,12 +25,19 @@ class ZeroOptimizer:
     def __init__(self, n: int, N: int, precision: int = abi.ZERO_FP32, lr: float = 1e-3,
                  betas=(0.9, 0.999), eps: float = 1e-8, weight_decay: float = 0.0,
                  master_init: torch.Tensor | None = None, device="cuda", stream=None,
-                 max_grad_norm: float = 0.0, grad_scale: float = 1.0, shard_bounds=None):
+                 max_grad_norm: float = 0.0, grad_scale: float = 1.0, shard_bounds=None,
+                 stage: int = 2):
         """``max_grad_norm`` > 0 clips the (scaled) mean gradient to that global
         norm before every step; ``grad_scale`` multiplies the mean gradient
         (1/k when the gradient buffers hold the sum of k micro-batches);
         ``shard_bounds`` (N+1 offsets) replaces the np.array_split shards, e.g.
-        ``abi.zero_tensor_shard_bounds(tensor_sizes, N)`` for whole-tensor shards."""
+        ``abi.zero_tensor_shard_bounds(tensor_sizes, N)`` for whole-tensor shards.
+        ``stage`` 3 leaves the all-gather out of the step: each replica keeps
+        only its own shard current until ``gather`` (stages 1 and 2 run the
+        same fused step; they differ only in what a rank would keep)."""
+        if stage not in (1, 2, 3):
+            raise ValueError("stage must be 1, 2 or 3")
+        self.stage = int(stage)
         self.shard_bounds = None if shard_bounds is None else [int(b) for b in shard_bounds]
         self.n, self.N, self.precision = int(n), int(N), int(precision)
         self.max_grad_norm, self.grad_scale = float(max_grad_norm), float(grad_scale)
@@ -74,8 +81,10 @@ class ZeroOptimizer:
         current stream by default) before reading it.
         """
         clipping = self.max_grad_norm > 0
-        if clipping and not all(g.is_cuda for g in grads):
-            # the global norm needs every gradient before any update: copy first
+        owner_only = self.stage == 3
+        if (clipping or owner_only) and not all(g.is_cuda for g in grads):
+            # the global norm needs every gradient before any update, and the
+            # chunked host pipeline runs the full all-gather: copy first
             staging = self._staging_buffers()
             s = stream if stream is not None else torch.cuda.current_stream(self.device)
             with torch.cuda.stream(s):
@@ -83,7 +92,7 @@ class ZeroOptimizer:
                     dst.copy_(src, non_blocking=True)
             grads = staging
         if all(g.is_cuda for g in grads):
-            if clipping or self.grad_scale != 1.0:
+            if clipping or owner_only or self.grad_scale != 1.0:
                 norm = None
                 if clipping:
                     if self._norm is None:
@@ -96,11 +105,13 @@ class ZeroOptimizer:
                     norm = self._norm
                 abi.zero_step_ex(params, grads, self.states, self.t + 1, self.lr, self.beta1,
                                  self.beta2, self.eps, self.weight_decay, self.grad_scale,
-                                 self.max_grad_norm, norm, 0, -1, stream)
+                                 self.max_grad_norm, norm, 0, -1, stream, owner_only)
             else:
                 abi.zero_step(params, grads, self.states, self.t + 1, self.lr, self.beta1,
                               self.beta2, self.eps, self.weight_decay, stream)
             if host_params_out is not None:
+                if owner_only:
+                    self.gather(params, stream=stream)
                 s = stream if stream is not None else torch.cuda.current_stream(self.device)
                 with torch.cuda.stream(s):
                     host_params_out.copy_(params[0], non_blocking=True)
@@ -112,10 +123,17 @@ class ZeroOptimizer:
         self.t += 1
         return self.t
 
+    def gather(self, params, lo: int = 0, hi: int = -1, stream=None) -> None:
+        """ZeRO-3 gather: every replica receives each shard from its owner's
+        replica over [lo, hi) (hi < 0: n), e.g. one layer before its forward."""
+        abi.zero_gather(params, self.states, lo, hi, stream)
+
     def step_bucketed(self, params, grads, ready=None, side=None,
                       bucket_bytes: int = BUCKET_BYTES_25MIB, done=None,
                       timeout_ms: int = -1) -> int:
         """The step bucket by bucket on ``side``, each after its ``ready`` event."""
+        if self.stage == 3:
+            raise ValueError("bucket streaming runs the stage-1/2 step (with all-gather)")
         try:
             abi.zero_step_bucketed(params, grads, self.states, self.t + 1, self.lr, self.beta1,
                                    self.beta2, self.eps, self.weight_decay, bucket_bytes, ready,
