@@ -369,7 +369,7 @@ def run_gpu(args, wl, rank: int, world: int, local_rank: int) -> dict | None:
                      "algorithmic_bytes_per_launch": step_bytes // per,
                      "kernel": ("grad_norm_partials_kernel + grad_norm_total_kernel + "
                                 "zero_step_tma_kernel (whole clipped step)") if clip else
-                               ("zero_step_tma_kernel (owner-only) + gather_kernel "
+                               ("zero_step_tma_kernel (owner-only) + gather_tma_kernel "
                                 "(whole stage-3 step)") if stage3 else
                                ("zero_step_tma_kernel" if wl.N <= 8 else "zero_step_kernel"),
                      "kernel_ms": kernel_ms / per},

@@ -810,9 +810,21 @@ cudaError_t launch_init(const InitArgs& a, cudaStream_t s) {
   return launch(init_state_kernel, a, work, s);
 }
 
+namespace {
+template <bool BF16>
+cudaError_t launch_gather_t(const GatherArgs& a, cudaStream_t s) {
+  if (a.sp.nvec > 0) {  // the replicas share a 16-byte phase: bulk-copy pipeline
+    using G = GatherTile<BF16>;
+    const int64_t tiles = (a.sp.nvec * (16 / G::kEB) + G::T - 1) / G::T;
+    return launch_tma<gather_tma_kernel<BF16>, GatherPipe::kThreads>(a, G::kSmem, tiles, s);
+  }
+  const int64_t work = a.sp.head + a.sp.tail;
+  return launch(gather_kernel<BF16>, a, work, s);
+}
+}  // namespace
+
 cudaError_t launch_gather(const GatherArgs& a, bool bf16, cudaStream_t s) {
-  const int64_t work = a.sp.nvec > a.sp.head + a.sp.tail ? a.sp.nvec : a.sp.head + a.sp.tail;
-  return bf16 ? launch(gather_kernel<true>, a, work, s) : launch(gather_kernel<false>, a, work, s);
+  return bf16 ? launch_gather_t<true>(a, s) : launch_gather_t<false>(a, s);
 }
 
 namespace {
