@@ -29,6 +29,11 @@ ranks and workers only):
   Optimizer", "Sharding Parameters").
 * ``bucket_bounds``  -- 25 MiB gradient buckets built from the end of the flat
   gradient ("ZeRO One: Sharding the Optimizer", section "Bucketing").
+* ``zero_step_sgd`` -- the same ZeRO step with momentum SGD as the wrapped
+  optimizer ("Data parallelism and ZeRO stages 1 to 3", section 2, stage 1:
+  SGD is elementwise like AdamW, so the chunked update equals the unsharded
+  one; section 4 tests DDP with momentum-SGD steps); ``sgd_full`` is its
+  unsharded reference.
 * ``grad_norm`` / ``grad_multiplier`` -- the global gradient norm from squared
   chunk norms, and the clip / accumulation factor applied to the mean gradient
   ("Data parallelism and ZeRO stages 1 to 3", "Going further"; "Data
@@ -61,6 +66,12 @@ Readings taken where the pages are silent (each is listed in the design notes):
 5. NaN/Inf propagate as IEEE arithmetic gives them.
 6. Clipping: coefficient max_norm / (norm + 1e-6) capped at 1, applied with the
    accumulation factor as one float64 multiplier rounded to float32.
+7. Momentum SGD is named, not printed. Reading: torch.optim.SGD -- coupled
+   weight decay g <- g + wd*p (skipped at wd = 0); with momentum mu the buffer
+   is g at t = 1 and mu*buf + (1-dampening)*g after; the direction is the
+   buffer, or g + mu*buf with Nesterov; p <- p - lr*direction. Without
+   momentum there is no buffer and the direction is g. fp32 constants lr, wd,
+   mu and (1 - dampening) are formed in float64 and rounded once.
 
 Parity status: every function here is pinned by a CPU test against values the
 pages print, closed forms, invariants or library routines (np.array_split,
@@ -76,6 +87,7 @@ import numpy as np
 __all__ = [
     "FP32", "BF16_MIXED", "FP64_EMU",
     "shard_bounds", "init_states", "zero_step", "adam_full", "allreduce_mean",
+    "zero_step_sgd", "sgd_full", "init_states_sgd",
     "grad_norm", "grad_multiplier", "tensor_shard_bounds", "gather",
     "memory_bytes", "memory_breakdown", "bucket_bounds",
     "bf16_to_f32", "f32_to_bf16_rne", "mirror_scalars",
@@ -219,6 +231,37 @@ def _adam(p, g, m, v, t, lr, beta1, beta2, eps, weight_decay, mode):
     raise ValueError(f"unknown arithmetic mode {mode!r}")
 
 
+def _sgd(p, g, buf, t, lr, momentum, dampening, weight_decay, nesterov, mode):
+    """One momentum-SGD step on arrays of equal length; returns new (p, buf).
+
+    g <- g + wd*p (wd != 0); buf <- g at t = 1, else mu*buf + (1-dampening)*g
+    (mu != 0); direction d = g + mu*buf (Nesterov) or buf, or d = g without
+    momentum (buf stays None); p <- p - lr*d.
+    """
+    if t < 1:
+        raise ValueError("step number t starts at 1")
+    if nesterov and (momentum <= 0 or dampening != 0):
+        raise ValueError("Nesterov momentum needs momentum > 0 and zero dampening")
+    dt = _dtype(mode)
+    lr_, wd_, mu_, omd_ = (dt(x) for x in (float(lr), float(weight_decay), float(momentum),
+                                           1.0 - float(dampening)))
+    p = np.asarray(p, dtype=dt)
+    g = np.asarray(g, dtype=dt)
+    if weight_decay != 0:
+        g = g + wd_ * p
+    if momentum != 0:
+        if t == 1:
+            buf = g.copy()
+        else:
+            buf = mu_ * np.asarray(buf, dtype=dt) + omd_ * g
+        d = g + mu_ * buf if nesterov else buf
+    else:
+        buf = None
+        d = g
+    p = p - lr_ * d
+    return p, buf
+
+
 def _dtype(mode):
     return np.float64 if mode == "fp64" else np.float32
 
@@ -269,6 +312,24 @@ def init_states(n: int, N: int, precision: int = FP32, master_init=None, mode: s
     for i in range(N):
         a, b = bounds[i], bounds[i + 1]
         st = {"m": np.zeros(b - a, dtype=dt), "v": np.zeros(b - a, dtype=dt)}
+        if precision == BF16_MIXED:
+            if master_init is None:
+                raise ValueError("mixed precision needs the fp32 initial weights")
+            st["master"] = np.asarray(master_init[a:b], dtype=np.float32).astype(dt)
+        states.append(st)
+    return states
+
+
+def init_states_sgd(n: int, N: int, precision: int = FP32, master_init=None,
+                    mode: str = "fp32", bounds=None, momentum: bool = True):
+    """Momentum-SGD state per worker: the momentum buffer of its shard (zeros;
+    none without momentum) and, in mixed precision, the fp32 master copy."""
+    bounds = shard_bounds(n, N) if bounds is None else _check_bounds(bounds, n, N)
+    dt = _dtype(mode)
+    states = []
+    for i in range(N):
+        a, b = bounds[i], bounds[i + 1]
+        st = {"buf": np.zeros(b - a, dtype=dt) if momentum else None}
         if precision == BF16_MIXED:
             if master_init is None:
                 raise ValueError("mixed precision needs the fp32 initial weights")
@@ -383,6 +444,54 @@ def zero_step(params, grads, states, t, lr=1e-2, beta1=0.9, beta2=0.999, eps=1e-
         # between steps each rank keeps only its own chunk of the parameters
         return [_replica_from(sh, precision, mode) for sh in new_shards], new_states
     return _all_gather(new_shards, N, precision, mode), new_states                # 3.
+
+
+def zero_step_sgd(params, grads, states, t, lr=1e-2, momentum=0.0, dampening=0.0,
+                  weight_decay=0.0, nesterov=False, precision=FP32, mode="fp32",
+                  grad_scale=1.0, max_grad_norm=None, bounds=None, all_gather=True):
+    """One ZeRO step with momentum SGD on each shard; returns (new_params, new_states).
+
+    The same three steps as ``zero_step`` ("Data parallelism and ZeRO stages 1
+    to 3", section 2, stage 1: the wrapped optimizer steps the rank's chunk
+    with the chunk of the mean gradient, then the chunks are all-gathered),
+    with ``_sgd`` in place of Adam. ``states`` come from ``init_states_sgd``.
+    """
+    N = len(grads)
+    if len(params) != N or len(states) != N:
+        raise ValueError("params, grads and states need one entry per worker")
+    n = len(params[0])
+    bounds = shard_bounds(n, N) if bounds is None else _check_bounds(bounds, n, N)
+    mult = None
+    if grad_scale != 1.0 or (max_grad_norm is not None and max_grad_norm > 0):
+        norm = grad_norm(grads, precision, mode) if max_grad_norm else 0.0
+        mult = _dtype(mode)(grad_multiplier(norm, grad_scale, max_grad_norm))
+    new_shards, new_states = [], []
+    for i in range(N):
+        a, b = bounds[i], bounds[i + 1]
+        g_bar = _reduce_scatter_mean(grads, a, b, precision, mode)
+        if mult is not None:
+            g_bar = g_bar * mult
+        st = states[i]
+        if precision == BF16_MIXED:
+            p_src = st["master"]
+        else:
+            p_src = _as_compute(params[i][a:b], precision, mode)
+        p_new, buf = _sgd(p_src, g_bar, st["buf"], t, lr, momentum, dampening, weight_decay,
+                          nesterov, mode)
+        ns = {"buf": buf}
+        if precision == BF16_MIXED:
+            ns["master"] = p_new
+        new_states.append(ns)
+        new_shards.append(p_new)
+    if not all_gather:
+        return [_replica_from(sh, precision, mode) for sh in new_shards], new_states
+    return _all_gather(new_shards, N, precision, mode), new_states
+
+
+def sgd_full(param, mean_grad, buf, t, lr=1e-2, momentum=0.0, dampening=0.0,
+             weight_decay=0.0, nesterov=False, mode="fp32"):
+    """Unsharded momentum SGD on the whole vector with the mean gradient."""
+    return _sgd(param, mean_grad, buf, t, lr, momentum, dampening, weight_decay, nesterov, mode)
 
 
 def gather(shards, precision=FP32, mode="fp32"):

@@ -636,3 +636,203 @@ def test_stage3_gather_equals_all_gather():
         shards, _ = oracle.zero_step(reps, g, b_s, 1, precision=prec, all_gather=False)
         for x, y in zip(oracle.gather(shards), full):
             assert np.array_equal(x, y)
+
+
+# ---------------------------------------------------------------------------
+# Momentum SGD as the wrapped optimizer
+# ---------------------------------------------------------------------------
+
+def _torch_sgd(p0, seq, lr, momentum, dampening, wd, nesterov, dtype):
+    """torch.optim.SGD stepped on np.mean of each step's gradients."""
+    torch = pytest.importorskip("torch")
+    w = torch.nn.Parameter(torch.tensor(np.asarray(p0), dtype=dtype))
+    opt = torch.optim.SGD([w], lr=lr, momentum=momentum, dampening=dampening, weight_decay=wd,
+                          nesterov=nesterov)
+    out = []
+    for grads in seq:
+        w.grad = torch.tensor(np.mean(np.stack([np.asarray(g, np.float64) for g in grads]),
+                                      axis=0), dtype=dtype)
+        opt.step()
+        buf = opt.state[w].get("momentum_buffer")
+        out.append((w.detach().numpy().copy(), None if buf is None else buf.numpy().copy()))
+    return out
+
+
+SGD_CASES = [  # (N, momentum, dampening, wd, nesterov)
+    (1, 0.0, 0.0, 0.0, False), (2, 0.9, 0.0, 0.0, False), (4, 0.9, 0.1, 0.01, False),
+    (3, 0.5, 0.0, 0.1, True), (8, 0.99, 0.0, 0.0, True), (4, 0.0, 0.0, 0.05, False)]
+
+
+@pytest.mark.parametrize("N,mu,damp,wd,nest", SGD_CASES)
+def test_sgd_fp64_matches_torch_sgd(N, mu, damp, wd, nest):
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(40 + N)
+    n, lr = 1003, 0.05
+    p0 = rng.normal(0, 0.5, size=n)
+    seq = [[rng.normal(0, 1.0, size=n) for _ in range(N)] for _ in range(5)]
+    ref = _torch_sgd(p0, seq, lr, mu, damp, wd, nest, torch.float64)
+    params = [p0.copy() for _ in range(N)]
+    states = oracle.init_states_sgd(n, N, mode="fp64", momentum=mu != 0)
+    for t, grads in enumerate(seq, start=1):
+        params, states = oracle.zero_step_sgd(params, grads, states, t, lr=lr, momentum=mu,
+                                              dampening=damp, weight_decay=wd, nesterov=nest,
+                                              mode="fp64")
+        rp, rb = ref[t - 1]
+        for rep in params:
+            np.testing.assert_allclose(rep, rp, rtol=1e-12, atol=1e-14)
+        if mu:
+            assert all(s["buf"] is not None for s in states)
+            np.testing.assert_allclose(flat_state(states, "buf"), rb, rtol=1e-12, atol=1e-14)
+        else:
+            assert rb is None and all(s["buf"] is None for s in states)
+
+
+@pytest.mark.parametrize("N,mu,damp,wd,nest", SGD_CASES[1:4])
+def test_sgd_fp32_mirror_close_to_torch_fp32(N, mu, damp, wd, nest):
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(50 + N)
+    n, lr = 4099, 1e-2
+    p0 = rng.normal(0, 0.02, size=n).astype(np.float32)
+    seq = [[rng.normal(0, 1e-3, size=n).astype(np.float32) for _ in range(N)] for _ in range(5)]
+    ref = _torch_sgd(p0, seq, lr, mu, damp, wd, nest, torch.float32)
+    params = [p0.copy() for _ in range(N)]
+    states = oracle.init_states_sgd(n, N, mode="fp32")
+    for t, grads in enumerate(seq, start=1):
+        params, states = oracle.zero_step_sgd(params, grads, states, t, lr=lr, momentum=mu,
+                                              dampening=damp, weight_decay=wd, nesterov=nest)
+        rp, rb = ref[t - 1]
+        assert params[0].dtype == np.float32
+        assert np.all(np.abs(params[0] - rp) <= 1e-6 + 1e-5 * np.abs(rp))
+        b = flat_state(states, "buf")
+        assert np.all(np.abs(b - rb) <= 1e-6 * np.abs(rb).max() + 1e-5 * np.abs(rb))
+
+
+@pytest.mark.parametrize("nest", [False, True])
+def test_sgd_constant_gradient_closed_form(nest):
+    # constant g, no decay or dampening: buf_t = g (1 - mu^t) / (1 - mu); the step
+    # moves by lr * buf_t, or lr * (g + mu buf_t) with Nesterov
+    n, N, lr, mu, t_max = 7, 3, 0.1, 0.9, 6
+    g = np.linspace(-2.0, 3.0, n)
+    p0 = np.linspace(1.0, -1.0, n)
+    params = [p0.copy() for _ in range(N)]
+    states = oracle.init_states_sgd(n, N, mode="fp64")
+    moved = np.zeros(n)
+    for t in range(1, t_max + 1):
+        params, states = oracle.zero_step_sgd(params, [g] * N, states, t, lr=lr, momentum=mu,
+                                              nesterov=nest, mode="fp64")
+        buf = g * (1.0 - mu ** t) / (1.0 - mu)
+        moved += lr * (g + mu * buf if nest else buf)
+        np.testing.assert_allclose(flat_state(states, "buf"), buf, rtol=1e-13)
+        np.testing.assert_allclose(params[1], p0 - moved, rtol=1e-12, atol=1e-13)
+
+
+@pytest.mark.parametrize("N", [1, 2, 3, 4, 7, 8])
+@pytest.mark.parametrize("mode", ["fp32", "fp64"])
+def test_sgd_sharded_equals_unsharded(N, mode):
+    rng = np.random.default_rng(200 + N)
+    n = 1009
+    dt = np.float64 if mode == "fp64" else np.float32
+    p = rng.normal(size=n).astype(dt)
+    params = [p.copy() for _ in range(N)]
+    states = oracle.init_states_sgd(n, N, mode=mode)
+    buf = None
+    for t in range(1, 5):
+        grads = [rng.normal(size=n).astype(np.float32) for _ in range(N)]
+        gbar = zo._mean_over_ranks([g.astype(dt) for g in grads], mode)
+        params, states = oracle.zero_step_sgd(params, grads, states, t, lr=1e-2, momentum=0.9,
+                                              dampening=0.1, weight_decay=0.05, mode=mode)
+        p, buf = oracle.sgd_full(p, gbar, buf, t, lr=1e-2, momentum=0.9, dampening=0.1,
+                                 weight_decay=0.05, mode=mode)
+        for rep in params:
+            assert rep.dtype == dt and np.array_equal(rep, p)
+        assert np.array_equal(flat_state(states, "buf"), buf)
+
+
+@pytest.mark.parametrize("N", [2, 4])
+def test_sgd_ddp_matches_single_process(N):
+    # course page section 4, test_ddp_matches_single_process: 2 and 4 ranks,
+    # 5 momentum-SGD steps agree with one process on the whole batch to 1e-10.
+    # Least squares: rank r's gradient is that of its slice's mean loss; the
+    # single process differentiates the whole batch's mean loss directly.
+    rng = np.random.default_rng(300 + N)
+    n, B = 12, 6
+    X = rng.normal(size=(N * B, n))
+    y = rng.normal(size=N * B)
+    w0 = rng.normal(size=n)
+    params = [w0.copy() for _ in range(N)]
+    states = oracle.init_states_sgd(n, N, mode="fp64")
+    w = w0.copy()
+    buf = np.zeros(n)
+    for t in range(1, 6):
+        grads = [X[r * B:(r + 1) * B].T @ (X[r * B:(r + 1) * B] @ params[r] - y[r * B:(r + 1) * B])
+                 / B for r in range(N)]
+        params, states = oracle.zero_step_sgd(params, grads, states, t, lr=0.05, momentum=0.9,
+                                              mode="fp64")
+        g_full = X.T @ (X @ w - y) / (N * B)
+        buf = g_full if t == 1 else 0.9 * buf + g_full
+        w = w - 0.05 * buf
+        for rep in params:
+            np.testing.assert_allclose(rep, w, rtol=0, atol=1e-10)
+
+
+def test_sgd_stage3_gather_equals_all_gather():
+    rng = np.random.default_rng(77)
+    n, N = 1009, 4
+    init = rng.normal(0, 0.02, n).astype(np.float32)
+    for prec in (oracle.FP32, oracle.BF16_MIXED):
+        reps = [oracle.f32_to_bf16_rne(init) if prec else init.copy() for _ in range(N)]
+        g = [rng.normal(size=n).astype(np.float32) for _ in range(N)]
+        if prec:
+            g = [oracle.f32_to_bf16_rne(x) for x in g]
+        full, a = oracle.zero_step_sgd(reps, g, oracle.init_states_sgd(n, N, prec, init), 1,
+                                       momentum=0.9, precision=prec)
+        shards, b = oracle.zero_step_sgd(reps, g, oracle.init_states_sgd(n, N, prec, init), 1,
+                                         momentum=0.9, precision=prec, all_gather=False)
+        for x, y in zip(oracle.gather(shards), full):
+            assert np.array_equal(x, y)
+        if prec:
+            np.testing.assert_array_equal(full[0], oracle.f32_to_bf16_rne(flat_state(a, "master")))
+
+
+def test_sgd_rejects():
+    with pytest.raises(ValueError):
+        zo._sgd(np.zeros(3), np.zeros(3), None, 0, 0.1, 0.9, 0.0, 0.0, False, "fp64")
+    with pytest.raises(ValueError):
+        zo._sgd(np.zeros(3), np.zeros(3), None, 1, 0.1, 0.0, 0.0, 0.0, True, "fp64")
+    with pytest.raises(ValueError):
+        zo._sgd(np.zeros(3), np.zeros(3), None, 1, 0.1, 0.9, 0.1, 0.0, True, "fp64")
+
+
+def _sgd_mutant(**override):
+    real = zo._sgd
+
+    def mutant(p, g, buf, t, lr, momentum, dampening, weight_decay, nesterov, mode):
+        kw = dict(lr=lr, momentum=momentum, dampening=dampening, weight_decay=weight_decay,
+                  nesterov=nesterov)
+        kw.update(override)
+        return real(p, g, buf, t, kw["lr"], kw["momentum"], kw["dampening"],
+                    kw["weight_decay"], kw["nesterov"], mode)
+    return mutant
+
+
+@pytest.mark.parametrize("override,case", [
+    (dict(dampening=0.0), (4, 0.9, 0.1, 0.01, False)),
+    (dict(nesterov=False), (3, 0.5, 0.0, 0.1, True)),
+    (dict(momentum=0.0, nesterov=False), (2, 0.9, 0.0, 0.0, False)),
+    (dict(weight_decay=0.0), (4, 0.0, 0.0, 0.05, False))])
+def test_mutant_sgd_dropped_terms(monkeypatch, override, case):
+    monkeypatch.setattr(zo, "_sgd", _sgd_mutant(**override))
+    assert _fails(lambda: test_sgd_fp64_matches_torch_sgd(*case))
+
+
+def test_mutant_sgd_first_step_damped(monkeypatch):
+    # the buffer starts as (1 - dampening) g instead of g
+    real = zo._sgd
+
+    def mutant(p, g, buf, t, lr, momentum, dampening, weight_decay, nesterov, mode):
+        if t == 1 and momentum:
+            buf = np.zeros_like(np.asarray(g, dtype=zo._dtype(mode)))
+            t = 2
+        return real(p, g, buf, t, lr, momentum, dampening, weight_decay, nesterov, mode)
+    monkeypatch.setattr(zo, "_sgd", mutant)
+    assert _fails(lambda: test_sgd_fp64_matches_torch_sgd(4, 0.9, 0.1, 0.01, False))
