@@ -252,7 +252,8 @@ def run_gpu(args, wl, rank: int, world: int, local_rank: int) -> dict | None:
     opt = ZeroOptimizer(n, N, wl.precision, lr=wl.lr, betas=(wl.beta1, wl.beta2), eps=wl.eps,
                         weight_decay=wl.weight_decay, master_init=init if mixed else None,
                         max_grad_norm=args.max_grad_norm, shard_bounds=bounds,
-                        stage=args.stage)
+                        stage=args.stage, optimizer=args.optimizer,
+                        momentum=0.9 if args.optimizer == "sgd" else 0.0)
     del init
     stage3 = args.stage == 3
     bucketed = wl.bucket_bytes > 0
@@ -331,13 +332,16 @@ def run_gpu(args, wl, rank: int, world: int, local_rank: int) -> dict | None:
         return None
     peak, peak_kind = load_peaks()
     step_bytes = n * bytes_per_param(wl)
+    sgd = args.optimizer == "sgd"
+    if sgd:  # one fp32 buffer (read + write) instead of m and v
+        step_bytes -= n * 8
     if clip:  # the norm pass reads every rank's gradient once more
         step_bytes += n * N * (2 if mixed else 4)
     if stage3:  # the step writes 1 replica, not N; the gather reads 1 and writes N-1
         step_bytes += n * (2 if mixed else 4)
     achieved = step_bytes / (kernel_ms / 1e3) / 1e9
     traffic = traffic_per_launch(wl.name)
-    if traffic is not None and (bucketed or clip or stage3):
+    if traffic is not None and (bucketed or clip or stage3 or sgd):
         traffic = None
     whole = clip or stage3  # the roofline covers the whole step (several kernels)
     per = 1 if whole else launches_per_step
@@ -358,6 +362,7 @@ def run_gpu(args, wl, rank: int, world: int, local_rank: int) -> dict | None:
                                                 f"{world} independent GPU replica(s)",
                                  **({"max_grad_norm": args.max_grad_norm} if clip else {}),
                                  **({"zero_stage": 3} if stage3 else {}),
+                                 **({"optimizer": "momentum SGD (0.9)"} if sgd else {}),
                                  "partition": ("whole tensors (" + ", ".join(
                                      str(int(b2 - b1)) for b1, b2 in zip(bounds, bounds[1:])) +
                                      " params per rank)") if bounds else "np.array_split"}),
@@ -431,6 +436,8 @@ def main(argv=None):
                     help="tensor: shards of whole tensors (workloads with a tensor list)")
     ap.add_argument("--max-grad-norm", type=float, default=0.0,
                     help="> 0: sharded global-norm clipping before every step (norm pass + step)")
+    ap.add_argument("--optimizer", default="adamw", choices=["adamw", "sgd"],
+                    help="sgd: momentum SGD (momentum 0.9, the workload's lr and decay)")
     ap.add_argument("--stage", type=int, default=2, choices=[2, 3],
                     help="3: owner-only step, then the gather of the full parameters (2 launches)")
     args = ap.parse_args(argv)
@@ -443,6 +450,8 @@ def main(argv=None):
         ap.error("--partition tensor needs a workload with a tensor list (gpt2_small)")
     if args.max_grad_norm > 0 and wl.bucket_bytes:
         ap.error("clipping needs the whole gradient before the step: not with bucket streaming")
+    if args.optimizer == "sgd" and wl.bucket_bytes:
+        ap.error("bucket streaming runs the AdamW step: not with --optimizer sgd")
     if args.stage == 3 and wl.bucket_bytes:
         ap.error("bucket streaming runs the step with its all-gather: not with --stage 3")
     world = int(os.environ.get("WORLD_SIZE", "1"))

@@ -79,7 +79,10 @@ int zero_shard_bounds(int64_t n, int32_t N, int64_t *bounds);
  * size). State is stored flat in global index order: rank i's m, v (and
  * master) are elements [a_i, a_{i+1}) of the caller's n-element device
  * buffers m, v, master, so a shard is a pure index range.
- *   m, v        : device float[n], zeroed here (queued on `stream`).
+ *   m, v        : device float[n], zeroed here (queued on `stream`). For
+ *                 momentum SGD (zero_step_sgd) pass v = NULL: m is the
+ *                 momentum buffer; for SGD without momentum m = v = NULL.
+ *                 The AdamW steps reject a state without v.
  *   master      : ZERO_BF16_MIXED only: device float[n], set to master_init;
  *                 must be NULL for ZERO_FP32.
  *   master_init : ZERO_BF16_MIXED only: device float[n], the fp32 initial
@@ -88,7 +91,7 @@ int zero_shard_bounds(int64_t n, int32_t N, int64_t *bounds);
  *   out         : receives a host handle; release it with zero_free_states.
  * The handle records the buffers; they must outlive it.
  * Errors: EINVAL (n < 0, N outside [1, ZERO_MAX_RANKS], precision not FP32 or
- * BF16_MIXED, NULL or extra pointer), EALIGN, ECUDA, ENOMEM. */
+ * BF16_MIXED, NULL or extra pointer, v without m), EALIGN, ECUDA, ENOMEM. */
 int zero_init_states(int64_t n, int32_t N, int32_t precision, float *m, float *v,
                      float *master, const float *master_init, zero_stream_t stream,
                      zero_states_t **out);
@@ -118,8 +121,8 @@ int zero_free_states(zero_states_t *st);
 /* n, N and precision of a handle (any output pointer may be NULL). */
 int zero_states_info(const zero_states_t *st, int64_t *n, int32_t *N, int32_t *precision);
 
-/* Rank `rank`'s shard [lo, hi) and its views into m, v, master (master is NULL
- * in fp32). Errors: EINVAL for a NULL handle or a rank outside [0, N). */
+/* Rank `rank`'s shard [lo, hi) and its views into m, v, master (NULL for a
+ * buffer the state does not have: master in fp32, v or m for SGD). Errors: EINVAL for a NULL handle or a rank outside [0, N). */
 int zero_state_view(const zero_states_t *st, int32_t rank, int64_t *lo, int64_t *hi,
                     float **m, float **v, float **master);
 
@@ -227,6 +230,44 @@ typedef struct zero_step_opts {
  * max_grad_norm, or clipping without norm_sq. */
 int zero_step_ex(void *const *params, const void *const *grads, zero_states_t *st,
                  const zero_step_opts_t *opts, zero_stream_t stream);
+
+/* Options of zero_step_sgd: momentum SGD as the optimizer of the step. The
+ * pages name SGD beside AdamW as an elementwise optimizer that ZeRO wraps
+ * unchanged ("Data parallelism and ZeRO stages 1 to 3", section 2, stage 1;
+ * its tests step DDP with momentum SGD, section 4) without printing its
+ * update; this follows torch.optim.SGD. */
+typedef struct zero_sgd_opts {
+  int64_t t;             /* step number, >= 1; at t = 1 the buffer starts as g */
+  double lr;             /* finite, >= 0 */
+  double momentum;       /* mu >= 0; 0 = plain SGD (no buffer) */
+  double dampening;      /* the buffer update is mu*buf + (1 - dampening)*g */
+  double weight_decay;   /* coupled: g <- g + weight_decay * p (0: none) */
+  int32_t nesterov;      /* nonzero: direction g + mu*buf (needs mu > 0, dampening 0) */
+  double grad_scale;     /* as zero_step_opts_t */
+  double max_grad_norm;  /* as zero_step_opts_t */
+  const double *norm_sq; /* as zero_step_opts_t */
+  int64_t lo, hi;        /* index range of the step; hi < 0 means n */
+  int32_t owner_only;    /* as zero_step_opts_t: ZeRO stage 3 */
+} zero_sgd_opts_t;
+
+/* The fused ZeRO step with momentum SGD on each shard: reduce-scatter-mean
+ * (times the multiplier of zero_step_ex), then per element, in IEEE fp32 with
+ * every operation rounded separately:
+ *   g <- g + wd*p                     (wd != 0)
+ *   buf <- g (t = 1), else mu*buf + (1 - dampening)*g      (mu != 0)
+ *   d = g + mu*buf (Nesterov), buf (mu != 0), or g (mu = 0)
+ *   p <- p - lr*d
+ * with lr, wd, mu and 1 - dampening rounded from double to float once; then
+ * the all-gather (or the owner's slice only, owner_only). The state's m is the
+ * momentum buffer (a state without m serves only mu = 0); v is not used. The
+ * parameter source is the owner's replica (fp32) or the master (mixed).
+ * Algorithmic bytes per parameter: fp32 8N + 12 (8N + 4 without momentum),
+ * mixed 4N + 16 (4N + 8 without momentum).
+ * Errors: as zero_step_ex, plus EINVAL for a negative or non-finite momentum,
+ * Nesterov without momentum or with dampening, or a state without m when
+ * mu > 0. */
+int zero_step_sgd(void *const *params, const void *const *grads, zero_states_t *st,
+                  const zero_sgd_opts_t *opts, zero_stream_t stream);
 
 /* ZeRO-3 gather(): all-gather the parameter shards into every replica
  * ("Data parallelism and ZeRO stages 1 to 3", section 2, stage 3, and

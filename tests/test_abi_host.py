@@ -159,3 +159,60 @@ def test_init_states_rejects_bad_bounds_before_device_work(abi):
                             ctypes.byref(h))
         assert code == abi.ZERO_EINVAL
         assert "bounds" in abi.raw_call.__globals__["_lib"].zero_last_error().decode()
+
+
+def test_option_structs_match_the_header(abi, tmp_path):
+    """The ctypes mirrors of zero_step_opts_t and zero_sgd_opts_t have the C
+    layout (size and every field offset), checked by compiling the header."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    structs = {"zero_step_opts_t": abi.StepOpts, "zero_sgd_opts_t": abi.SgdOpts}
+    lines = ["#include <stdio.h>", "#include <stddef.h>", '#include "zero_gb300.h"',
+             "int main(void) {"]
+    for cname, py in structs.items():
+        lines.append(f'  printf("{cname} size %zu\\n", sizeof({cname}));')
+        for field, _ in py._fields_:
+            lines.append(f'  printf("{cname} {field} %zu\\n", offsetof({cname}, {field}));')
+    lines += ["  return 0;", "}"]
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines) + "\n")
+    exe = tmp_path / "layout"
+    subprocess.run([cc, "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)],
+                   check=True)
+    out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout
+    seen = {}
+    for line in out.splitlines():
+        cname, field, value = line.split()
+        seen[(cname, field)] = int(value)
+    for cname, py in structs.items():
+        assert seen[(cname, "size")] == ctypes.sizeof(py), cname
+        for field, _ in py._fields_:
+            assert seen[(cname, field)] == getattr(py, field).offset, (cname, field)
+
+
+def test_sgd_and_gather_argument_checks(abi):
+    vp = ctypes.c_void_p
+    arr = (vp * 2)(16, 32)
+    o = abi.SgdOpts(1, 0.1, 0.9, 0.0, 0.0, 0, 1.0, 0.0, None, 0, -1, 0)
+    assert abi.raw_call("zero_step_sgd", arr, arr, None, ctypes.byref(o), None) == abi.ZERO_EINVAL
+    assert abi.raw_call("zero_gather", arr, None, 0, -1, None) == abi.ZERO_EINVAL
+    # a host-only state (n = 0 needs no device work) to reach the option checks
+    h = vp()
+    assert abi.raw_call("zero_init_states", 0, 2, 0, None, None, None, None, None,
+                        ctypes.byref(h)) == abi.ZERO_OK
+    bad = [abi.SgdOpts(0, 0.1, 0.9, 0.0, 0.0, 0, 1.0, 0.0, None, 0, -1, 0),     # t = 0
+           abi.SgdOpts(1, -0.1, 0.9, 0.0, 0.0, 0, 1.0, 0.0, None, 0, -1, 0),    # lr < 0
+           abi.SgdOpts(1, 0.1, -0.9, 0.0, 0.0, 0, 1.0, 0.0, None, 0, -1, 0),    # mu < 0
+           abi.SgdOpts(1, 0.1, 0.9, 0.1, 0.0, 1, 1.0, 0.0, None, 0, -1, 0),     # nesterov+damp
+           abi.SgdOpts(1, 0.1, 0.0, 0.0, 0.0, 1, 1.0, 0.0, None, 0, -1, 0),     # nesterov, mu 0
+           abi.SgdOpts(1, 0.1, 0.9, 0.0, 0.0, 0, 0.0, 0.0, None, 0, -1, 0),     # grad_scale 0
+           abi.SgdOpts(1, 0.1, 0.9, 0.0, 0.0, 0, 1.0, 1.0, None, 0, -1, 0)]     # clip, no norm
+    empty = (vp * 2)(None, None)
+    for o in bad:
+        assert abi.raw_call("zero_step_sgd", empty, empty, h, ctypes.byref(o), None) \
+            == abi.ZERO_EINVAL
+    assert abi.raw_call("zero_gather", empty, h, 0, 1, None) == abi.ZERO_EINVAL  # hi > n
+    assert abi.raw_call("zero_free_states", h) == abi.ZERO_OK

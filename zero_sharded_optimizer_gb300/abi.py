@@ -78,6 +78,7 @@ _SIGNATURES = {
     "zero_grad_norm_sq": (ctypes.c_int, [_P(_vp), _i64, _i32, _i32, _vp, _i64, _vp, _vp]),
     "zero_step_ex": (ctypes.c_int, [_P(_vp), _P(_vp), _vp, _vp, _vp]),
     "zero_gather": (ctypes.c_int, [_P(_vp), _vp, _i64, _i64, _vp]),
+    "zero_step_sgd": (ctypes.c_int, [_P(_vp), _P(_vp), _vp, _vp, _vp]),
     "zero_grad_norm_sq_noalloc": (ctypes.c_int, [_P(_vp), _i64, _i32, _i32, _vp, _vp]),
     "zero_device_status": (ctypes.c_int, [_P(ctypes.c_uint32), _i32]),
     "zero_debug_set_wait_timeout_ns": (ctypes.c_int, [_u64]),
@@ -383,6 +384,28 @@ def zero_step_ex(params, grads, st: ZeroStates, t: int, lr: float, beta1: float 
     o = StepOpts(t, lr, beta1, beta2, eps, weight_decay, grad_scale, max_grad_norm, nq, lo, hi,
                  1 if owner_only else 0)
     _check(_lib.zero_step_ex(pp, gp, st.handle, ctypes.byref(o), _stream(stream)), "zero_step_ex")
+
+
+class SgdOpts(ctypes.Structure):
+    """zero_sgd_opts_t."""
+    _fields_ = [("t", _i64), ("lr", _dbl), ("momentum", _dbl), ("dampening", _dbl),
+                ("weight_decay", _dbl), ("nesterov", _i32), ("grad_scale", _dbl),
+                ("max_grad_norm", _dbl), ("norm_sq", _vp), ("lo", _i64), ("hi", _i64),
+                ("owner_only", _i32)]
+
+
+def zero_step_sgd(params, grads, st: ZeroStates, t: int, lr: float, momentum: float = 0.0,
+                  dampening: float = 0.0, weight_decay: float = 0.0, nesterov: bool = False,
+                  grad_scale: float = 1.0, max_grad_norm: float = 0.0, norm_sq=None,
+                  lo: int = 0, hi: int = -1, stream=None, owner_only: bool = False):
+    """The fused ZeRO step with momentum SGD (torch.optim.SGD semantics); the
+    state's m is the momentum buffer."""
+    pp, gp = _step_ptrs(params, grads, st)
+    nq = None if norm_sq is None else _f64_device_ptr(norm_sq, 1, "norm_sq")
+    o = SgdOpts(t, lr, momentum, dampening, weight_decay, 1 if nesterov else 0, grad_scale,
+                max_grad_norm, nq, lo, hi, 1 if owner_only else 0)
+    _check(_lib.zero_step_sgd(pp, gp, st.handle, ctypes.byref(o), _stream(stream)),
+           "zero_step_sgd")
 
 
 def zero_gather(params, st: ZeroStates, lo: int = 0, hi: int = -1, stream=None):

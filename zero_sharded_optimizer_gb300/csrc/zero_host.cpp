@@ -122,12 +122,17 @@ int adam_consts(int64_t t, double lr, double beta1, double beta2, double eps, do
   return ZERO_OK;
 }
 
-// Checks the buffers of a step and fills everything in StepArgs except the
-// split and the constants.
+// Checks the buffers of a step with optimizer `opt` and fills everything in
+// StepArgs except the split and the constants.
 int prepare_step(void* const* params, const void* const* grads, const zero_states* st,
-                 zk::StepArgs* a, bool* vector_ok, int* phase) {
+                 zk::Opt opt, zk::StepArgs* a, bool* vector_ok, int* phase) {
   if (!st) return fail(ZERO_EINVAL, "state handle is NULL");
   if (!params || !grads) return fail(ZERO_EINVAL, "params/grads array is NULL");
+  const int nstates = opt == zk::Opt::AdamW ? 2 : (opt == zk::Opt::SgdMomentum ? 1 : 0);
+  if (st->n > 0 && nstates >= 1 && !st->m)
+    return fail(ZERO_EINVAL, "the state has no first buffer (m), which this optimizer needs");
+  if (st->n > 0 && nstates >= 2 && !st->v)
+    return fail(ZERO_EINVAL, "the state has no second moment (v): initialised for SGD");
   const int32_t N = st->N;
   const bool mixed = st->precision == ZERO_BF16_MIXED;
   const int es = mixed ? 2 : 4;
@@ -168,7 +173,9 @@ int prepare_step(void* const* params, const void* const* grads, const zero_state
     }
   }
   const float* sbufs[3] = {st->m, st->v, st->master};
-  for (int k = 0; k < (mixed ? 3 : 2); ++k) {
+  for (int k = 0; k < 3; ++k) {
+    const bool used = k < nstates || (k == 2 && mixed);
+    if (!used) continue;
     if (!note(sbufs[k], 4, &ph32)) return fail(ZERO_EALIGN, "state buffer not 4-byte aligned");
     if (st->n > 0) rs.push_back({uintptr_t(sbufs[k]), uintptr_t(sbufs[k]) + sbytes, "a state buffer"});
   }
@@ -186,11 +193,11 @@ int prepare_step(void* const* params, const void* const* grads, const zero_state
 }
 
 int launch_range(zk::StepArgs& a, const zero_states* st, bool vector_ok, int phase, int64_t lo,
-                 int64_t hi, cudaStream_t s) {
+                 int64_t hi, cudaStream_t s, zk::Opt opt = zk::Opt::AdamW) {
   if (hi <= lo) return ZERO_OK;
   const bool mixed = st->precision == ZERO_BF16_MIXED;
   a.sp = make_split(lo, hi, vector_ok, phase, mixed ? 8 : 4);
-  cudaError_t e = zk::launch_step(a, mixed, s);
+  cudaError_t e = zk::launch_step(a, mixed, opt, s);
   if (e != cudaSuccess) return cuda_fail(e, "zero_step kernel launch");
   return ZERO_OK;
 }
@@ -411,7 +418,8 @@ int zero_init_states_ex(int64_t n, int32_t N, int32_t precision, float* m, float
     if (int e = check_bounds(bounds, n, N)) return e;
   if (precision != ZERO_FP32 && precision != ZERO_BF16_MIXED)
     return fail(ZERO_EINVAL, "state precision must be FP32 or BF16_MIXED");
-  if (n > 0 && (!m || !v)) return fail(ZERO_EINVAL, "m or v is NULL");
+  // v = NULL: state for momentum SGD (m is its buffer); m = v = NULL: plain SGD.
+  if (n > 0 && !m && v) return fail(ZERO_EINVAL, "v without m");
   const bool mixed = precision == ZERO_BF16_MIXED;
   if (mixed && n > 0 && (!master || !master_init))
     return fail(ZERO_EINVAL, "mixed precision needs master and master_init");
@@ -422,6 +430,7 @@ int zero_init_states_ex(int64_t n, int32_t N, int32_t precision, float* m, float
   const float* bufs[4] = {m, v, master, master_init};
   std::vector<Range> rs;
   for (int k = 0; k < (mixed ? 4 : 2); ++k) {
+    if (!bufs[k]) continue;  // an absent m or v (SGD state)
     const int q = phase_of(bufs[k], 4);
     if (q < 0) return fail(ZERO_EALIGN, "state buffer not 4-byte aligned");
     if (ph == -2) ph = q;
@@ -474,8 +483,8 @@ int zero_state_view(const zero_states_t* st, int32_t rank, int64_t* lo, int64_t*
   const int64_t a = st->bounds[rank], b = st->bounds[rank + 1];
   if (lo) *lo = a;
   if (hi) *hi = b;
-  if (m) *m = st->m + a;
-  if (v) *v = st->v + a;
+  if (m) *m = st->m ? st->m + a : nullptr;
+  if (v) *v = st->v ? st->v + a : nullptr;
   if (master) *master = st->master ? st->master + a : nullptr;
   return ZERO_OK;
 }
@@ -486,7 +495,7 @@ int zero_step_range(void* const* params, const void* const* grads, zero_states_t
   zk::StepArgs a;
   bool vec = false;
   int phase = 0;
-  if (int e = prepare_step(params, grads, st, &a, &vec, &phase)) return e;
+  if (int e = prepare_step(params, grads, st, zk::Opt::AdamW, &a, &vec, &phase)) return e;
   if (lo < 0 || hi < lo || hi > st->n)
     return fail(ZERO_EINVAL, "range [%lld, %lld) outside [0, %lld)", (long long)lo, (long long)hi,
                 (long long)st->n);
@@ -509,7 +518,7 @@ int zero_step_ex(void* const* params, const void* const* grads, zero_states_t* s
   zk::StepArgs a;
   bool vec = false;
   int phase = 0;
-  if (int e = prepare_step(params, grads, st, &a, &vec, &phase)) return e;
+  if (int e = prepare_step(params, grads, st, zk::Opt::AdamW, &a, &vec, &phase)) return e;
   const int64_t lo = o->lo, hi = o->hi < 0 ? st->n : o->hi;
   if (lo < 0 || hi < lo || hi > st->n)
     return fail(ZERO_EINVAL, "range [%lld, %lld) outside [0, %lld)", (long long)lo, (long long)hi,
@@ -564,6 +573,47 @@ int zero_gather(void* const* params, zero_states_t* st, int64_t lo, int64_t hi,
   cudaError_t e = zk::launch_gather(a, bf16, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "zero_gather kernel launch");
   return ZERO_OK;
+}
+
+int zero_step_sgd(void* const* params, const void* const* grads, zero_states_t* st,
+                  const zero_sgd_opts_t* o, zero_stream_t stream) {
+  if (!st) return fail(ZERO_EINVAL, "state handle is NULL");
+  if (!o) return fail(ZERO_EINVAL, "options are NULL");
+  if (o->t < 1) return fail(ZERO_EINVAL, "step number t=%lld must be >= 1", (long long)o->t);
+  if (!std::isfinite(o->lr) || o->lr < 0.0) return fail(ZERO_EINVAL, "lr must be finite and >= 0");
+  if (!std::isfinite(o->momentum) || o->momentum < 0.0)
+    return fail(ZERO_EINVAL, "momentum must be finite and >= 0");
+  if (!std::isfinite(o->dampening)) return fail(ZERO_EINVAL, "dampening must be finite");
+  if (!std::isfinite(o->weight_decay)) return fail(ZERO_EINVAL, "weight_decay must be finite");
+  if (o->nesterov && (o->momentum <= 0.0 || o->dampening != 0.0))
+    return fail(ZERO_EINVAL, "Nesterov momentum needs momentum > 0 and zero dampening");
+  const zk::Opt opt = o->momentum != 0.0 ? zk::Opt::SgdMomentum : zk::Opt::Sgd;
+  zk::StepArgs a;
+  bool vec = false;
+  int phase = 0;
+  if (int e = prepare_step(params, grads, st, opt, &a, &vec, &phase)) return e;
+  const int64_t lo = o->lo, hi = o->hi < 0 ? st->n : o->hi;
+  if (lo < 0 || hi < lo || hi > st->n)
+    return fail(ZERO_EINVAL, "range [%lld, %lld) outside [0, %lld)", (long long)lo, (long long)hi,
+                (long long)st->n);
+  a.sgd.lr = float(o->lr);
+  a.sgd.wd = float(o->weight_decay);
+  a.sgd.mu = float(o->momentum);
+  a.sgd.omd = float(1.0 - o->dampening);
+  a.sgd.wd_on = o->weight_decay != 0.0;
+  a.sgd.first = o->t == 1;
+  a.sgd.nesterov = o->nesterov != 0;
+  if (!std::isfinite(o->grad_scale) || !(o->grad_scale > 0.0))
+    return fail(ZERO_EINVAL, "grad_scale must be finite and > 0");
+  a.gscale = o->grad_scale;
+  if (o->max_grad_norm > 0.0) {
+    if (!std::isfinite(o->max_grad_norm)) return fail(ZERO_EINVAL, "max_grad_norm must be finite");
+    if (!o->norm_sq) return fail(ZERO_EINVAL, "clipping needs the squared norm (norm_sq)");
+    a.norm_sq = o->norm_sq;
+    a.max_norm = o->max_grad_norm;
+  }
+  a.owner_only = o->owner_only != 0;
+  return launch_range(a, st, vec, phase, lo, hi, reinterpret_cast<cudaStream_t>(stream), opt);
 }
 
 int zero_grad_norm_scratch_count(int64_t n, int32_t precision, int64_t* count) {
@@ -660,7 +710,7 @@ int zero_step_bucket(void* const* params, const void* const* grads, zero_states_
   zk::StepArgs a;
   bool vec = false;
   int phase = 0;
-  if (int e = prepare_step(params, grads, st, &a, &vec, &phase)) return e;
+  if (int e = prepare_step(params, grads, st, zk::Opt::AdamW, &a, &vec, &phase)) return e;
   if (int e = adam_consts(t, lr, beta1, beta2, eps, weight_decay, &a.c)) return e;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(side);
   if (ready) {
@@ -685,7 +735,7 @@ int zero_step_bucketed(void* const* params, const void* const* grads, zero_state
   zk::StepArgs a;
   bool vec = false;
   int phase = 0;
-  if (int e = prepare_step(params, grads, st, &a, &vec, &phase)) return e;
+  if (int e = prepare_step(params, grads, st, zk::Opt::AdamW, &a, &vec, &phase)) return e;
   if (int e = adam_consts(t, lr, beta1, beta2, eps, weight_decay, &a.c)) return e;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(side);
   for (int64_t k = 0; k < count; ++k) {
@@ -731,7 +781,7 @@ int zero_step_from_host(void* const* params, const void* const* host_grads, void
   bool vec = false;
   int phase = 0;
   // the staging buffers are the kernel's gradient buffers
-  if (int e = prepare_step(params, staging, st, &a, &vec, &phase)) return e;
+  if (int e = prepare_step(params, staging, st, zk::Opt::AdamW, &a, &vec, &phase)) return e;
   if (int e = adam_consts(t, lr, beta1, beta2, eps, weight_decay, &a.c)) return e;
   if (n == 0) return ZERO_OK;
   const size_t es = st->precision == ZERO_BF16_MIXED ? 2 : 4;

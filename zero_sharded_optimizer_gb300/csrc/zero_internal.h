@@ -34,6 +34,18 @@ struct AdamConsts {
   float eps;
 };
 
+// Per-step float32 constants of momentum SGD, formed in double on the host and
+// rounded once, with its switches.
+struct SgdConsts {
+  float lr;
+  float wd;          // coupled decay g += wd*p, applied when wd_on
+  float mu;          // momentum
+  float omd;         // 1 - dampening
+  int32_t wd_on;
+  int32_t first;     // t == 1: the buffer starts as the gradient
+  int32_t nesterov;
+};
+
 // Kernel argument block of the fused step (passed by value as a
 // __grid_constant__ parameter; about 1.7 KB).
 struct StepArgs {
@@ -46,7 +58,8 @@ struct StepArgs {
   Split sp;
   int32_t N;
   float fN;                      // (float)N
-  AdamConsts c;
+  AdamConsts c;                  // AdamW steps
+  SgdConsts sgd;                 // momentum-SGD steps (the buffer is m)
   uint64_t wait_ns;              // bound of every wait on a bulk copy (TMA kernels)
   // Multiplier of the mean gradient: gscale, times the clip coefficient
   // min(1, max_norm / (gscale * sqrt(*norm_sq) + 1e-6)) when norm_sq is set
@@ -98,8 +111,13 @@ struct InitArgs {
   Split sp;
 };
 
+// The optimizer a fused step runs. Each keeps some fp32 state streams per
+// parameter besides the parameter (or master): AdamW m and v, momentum SGD
+// its buffer (in m), plain SGD none.
+enum class Opt : int { AdamW = 0, SgdMomentum = 1, Sgd = 2 };
+
 // Launchers (zero_kernels.cu). Each returns the launch status.
-cudaError_t launch_step(const StepArgs& a, bool mixed, cudaStream_t s);
+cudaError_t launch_step(const StepArgs& a, bool mixed, Opt opt, cudaStream_t s);
 cudaError_t launch_allreduce(const AllreduceArgs& a, bool bf16, cudaStream_t s);
 cudaError_t launch_init(const InitArgs& a, cudaStream_t s);
 cudaError_t launch_gather(const GatherArgs& a, bool bf16, cudaStream_t s);

@@ -169,12 +169,69 @@ __device__ __forceinline__ int advance_owner(const StepArgs& P, int owner, int64
   return owner;
 }
 
+// ------------------------------------------------------ the optimizer update --
+
+// fp32 state streams per parameter besides the parameter itself; arrays are
+// sized at least 1.
+template <Opt O>
+constexpr int kStates = O == Opt::AdamW ? 2 : (O == Opt::SgdMomentum ? 1 : 0);
+template <Opt O>
+constexpr int kSA = kStates<O> > 0 ? kStates<O> : 1;
+
+// State stream k: m (AdamW's first moment, or the SGD momentum buffer), v.
+__device__ __forceinline__ float* state_ptr(const StepArgs& P, int k) {
+  return k == 0 ? P.m : P.v;
+}
+
+// One momentum-SGD element (torch.optim.SGD semantics): coupled decay
+// g += wd*p; the buffer is g at the first step, else mu*buf + (1-dampening)*g;
+// the direction is the buffer, or g + mu*buf with Nesterov (plain SGD: g);
+// p -= lr*direction.
+template <Opt O>
+__device__ __forceinline__ void sgd1(const SgdConsts& c, float g, float& p, float& buf) {
+  if (c.wd_on) g = __fadd_rn(g, __fmul_rn(c.wd, p));
+  float d = g;
+  if constexpr (O == Opt::SgdMomentum) {
+    buf = c.first ? g : __fadd_rn(__fmul_rn(c.mu, buf), __fmul_rn(c.omd, g));
+    d = c.nesterov ? __fadd_rn(g, __fmul_rn(c.mu, buf)) : buf;
+  }
+  p = __fsub_rn(p, __fmul_rn(c.lr, d));
+}
+
+// The element update of optimizer O with the (scaled) mean gradient g.
+template <Opt O>
+__device__ __forceinline__ void update1(const StepArgs& P, float g, float& p, float (&s)[kSA<O>]) {
+  if constexpr (O == Opt::AdamW) {
+    adam1(P.c, g, p, s[0], s[1]);
+  } else {
+    sgd1<O>(P.sgd, g, p, s[0]);
+  }
+}
+
+// Four consecutive elements: rank sums g, parameters p, state streams st.
+// Written out per component (no indexed access into the vectors).
+template <int NR, Opt O>
+__device__ __forceinline__ void update4(const StepArgs& P, float gm, float4 g, float4& p,
+                                        float4 (&st)[kSA<O>]) {
+  if constexpr (O == Opt::AdamW) {
+    adam1(P.c, scaled_mean<NR>(g.x, P, gm), p.x, st[0].x, st[1].x);
+    adam1(P.c, scaled_mean<NR>(g.y, P, gm), p.y, st[0].y, st[1].y);
+    adam1(P.c, scaled_mean<NR>(g.z, P, gm), p.z, st[0].z, st[1].z);
+    adam1(P.c, scaled_mean<NR>(g.w, P, gm), p.w, st[0].w, st[1].w);
+  } else {
+    sgd1<O>(P.sgd, scaled_mean<NR>(g.x, P, gm), p.x, st[0].x);
+    sgd1<O>(P.sgd, scaled_mean<NR>(g.y, P, gm), p.y, st[0].y);
+    sgd1<O>(P.sgd, scaled_mean<NR>(g.z, P, gm), p.z, st[0].z);
+    sgd1<O>(P.sgd, scaled_mean<NR>(g.w, P, gm), p.w, st[0].w);
+  }
+}
+
 // ------------------------------------------------------- scalar element path --
 
-template <int NR, bool MIXED>
+template <int NR, bool MIXED, Opt O>
 __device__ __forceinline__ void step_scalar(const StepArgs& P, int64_t j, int owner, float gm) {
   const int N = ranks<NR>(P);
-  float s, p, m, v;
+  float s, p;
   if constexpr (MIXED) {
     s = bf_one(__ldcs(static_cast<const uint16_t*>(P.grads[0]) + j));
     for (int r = 1; r < N; ++r)
@@ -185,11 +242,12 @@ __device__ __forceinline__ void step_scalar(const StepArgs& P, int64_t j, int ow
     for (int r = 1; r < N; ++r) s = __fadd_rn(s, __ldcs(static_cast<const float*>(P.grads[r]) + j));
     p = __ldcs(static_cast<const float*>(P.reps[owner]) + j);
   }
-  m = __ldcs(P.m + j);
-  v = __ldcs(P.v + j);
-  adam1(P.c, scaled_mean<NR>(s, P, gm), p, m, v);
-  __stcs(P.m + j, m);
-  __stcs(P.v + j, v);
+  float st[kSA<O>];
+#pragma unroll
+  for (int k = 0; k < kStates<O>; ++k) st[k] = __ldcs(state_ptr(P, k) + j);
+  update1<O>(P, scaled_mean<NR>(s, P, gm), p, st);
+#pragma unroll
+  for (int k = 0; k < kStates<O>; ++k) __stcs(state_ptr(P, k) + j, st[k]);
   // Stage 3 (owner_only) keeps only the owner's replica current.
   const int r_lo = P.owner_only ? owner : 0, r_hi = P.owner_only ? owner : N - 1;
   if constexpr (MIXED) {
@@ -203,7 +261,7 @@ __device__ __forceinline__ void step_scalar(const StepArgs& P, int64_t j, int ow
 
 // ------------------------------------------------------- fp32 vector path (V=4)
 
-template <int NR>
+template <int NR, Opt O>
 __device__ __forceinline__ void step_vec_fp32(const StepArgs& P, int64_t j, int owner, float gm) {
   const int N = ranks<NR>(P);
   // Loads first: parameter, state, then every rank's gradient.
@@ -219,8 +277,9 @@ __device__ __forceinline__ void step_vec_fp32(const StepArgs& P, int64_t j, int 
     }
     p = make_float4(e[0], e[1], e[2], e[3]);
   }
-  float4 m = ld4(P.m + j);
-  float4 v = ld4(P.v + j);
+  float4 st[kSA<O>];
+#pragma unroll
+  for (int k = 0; k < kStates<O>; ++k) st[k] = ld4(state_ptr(P, k) + j);
   float4 s;
   if constexpr (NR > 0) {
     float4 g[NR];
@@ -241,12 +300,9 @@ __device__ __forceinline__ void step_vec_fp32(const StepArgs& P, int64_t j, int 
       s.z = __fadd_rn(s.z, g.z); s.w = __fadd_rn(s.w, g.w);
     }
   }
-  adam1(P.c, scaled_mean<NR>(s.x, P, gm), p.x, m.x, v.x);
-  adam1(P.c, scaled_mean<NR>(s.y, P, gm), p.y, m.y, v.y);
-  adam1(P.c, scaled_mean<NR>(s.z, P, gm), p.z, m.z, v.z);
-  adam1(P.c, scaled_mean<NR>(s.w, P, gm), p.w, m.w, v.w);
-  st4(P.m + j, m);
-  st4(P.v + j, v);
+  update4<NR, O>(P, gm, s, p, st);
+#pragma unroll
+  for (int k = 0; k < kStates<O>; ++k) st4(state_ptr(P, k) + j, st[k]);
   if (P.owner_only) {  // stage 3: the owners of the unit's elements only
     const int last = advance_owner(P, owner, j + 3);
     if (last == owner) {
@@ -269,12 +325,16 @@ __device__ __forceinline__ void step_vec_fp32(const StepArgs& P, int64_t j, int 
 
 // ------------------------------------------------------ mixed vector path (V=8)
 
-template <int NR>
+template <int NR, Opt O>
 __device__ __forceinline__ void step_vec_mixed(const StepArgs& P, int64_t j, int owner, float gm) {
   const int N = ranks<NR>(P);
-  const float4 p0 = ld4(P.master + j), p1 = ld4(P.master + j + 4);
-  const float4 m0 = ld4(P.m + j), m1 = ld4(P.m + j + 4);
-  const float4 v0 = ld4(P.v + j), v1 = ld4(P.v + j + 4);
+  float4 p4[2] = {ld4(P.master + j), ld4(P.master + j + 4)};
+  float4 st[2][kSA<O>];
+#pragma unroll
+  for (int k = 0; k < kStates<O>; ++k) {
+    st[0][k] = ld4(state_ptr(P, k) + j);
+    st[1][k] = ld4(state_ptr(P, k) + j + 4);
+  }
   float s[8];
   if constexpr (NR > 0) {
     uint4 w[NR];
@@ -298,17 +358,16 @@ __device__ __forceinline__ void step_vec_mixed(const StepArgs& P, int64_t j, int
       for (int k = 0; k < 8; ++k) s[k] = __fadd_rn(s[k], f[k]);
     }
   }
-  float p[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
-  float m[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
-  float v[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+  update4<NR, O>(P, gm, make_float4(s[0], s[1], s[2], s[3]), p4[0], st[0]);
+  update4<NR, O>(P, gm, make_float4(s[4], s[5], s[6], s[7]), p4[1], st[1]);
+  st4(P.master + j, p4[0]);
+  st4(P.master + j + 4, p4[1]);
 #pragma unroll
-  for (int k = 0; k < 8; ++k) adam1(P.c, scaled_mean<NR>(s[k], P, gm), p[k], m[k], v[k]);
-  st4(P.master + j, make_float4(p[0], p[1], p[2], p[3]));
-  st4(P.master + j + 4, make_float4(p[4], p[5], p[6], p[7]));
-  st4(P.m + j, make_float4(m[0], m[1], m[2], m[3]));
-  st4(P.m + j + 4, make_float4(m[4], m[5], m[6], m[7]));
-  st4(P.v + j, make_float4(v[0], v[1], v[2], v[3]));
-  st4(P.v + j + 4, make_float4(v[4], v[5], v[6], v[7]));
+  for (int k = 0; k < kStates<O>; ++k) {
+    st4(state_ptr(P, k) + j, st[0][k]);
+    st4(state_ptr(P, k) + j + 4, st[1][k]);
+  }
+  const float p[8] = {p4[0].x, p4[0].y, p4[0].z, p4[0].w, p4[1].x, p4[1].y, p4[1].z, p4[1].w};
   const uint4 h = pack8(p);
   if (P.owner_only) {  // stage 3: the owners of the unit's elements only
     const int last = advance_owner(P, owner, j + 7);
@@ -331,7 +390,7 @@ __device__ __forceinline__ void step_vec_mixed(const StepArgs& P, int64_t j, int
 
 // ------------------------------------------------------------------ kernels --
 
-template <int NR, bool MIXED>
+template <int NR, bool MIXED, Opt O>
 __global__ void __launch_bounds__(kThreads) zero_step_kernel(const __grid_constant__ StepArgs P) {
   constexpr int V = MIXED ? 8 : 4;
   const int64_t tid = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -349,7 +408,7 @@ __global__ void __launch_bounds__(kThreads) zero_step_kernel(const __grid_consta
     for (int64_t s = tid; s < nscalar; s += stride) {
       const int64_t j = s < sp.head ? sp.lo + s : body_end + (s - sp.head);
       owner = advance_owner(P, owner, j);
-      step_scalar<NR, MIXED>(P, j, owner, gm);
+      step_scalar<NR, MIXED, O>(P, j, owner, gm);
     }
   }
 
@@ -360,10 +419,10 @@ __global__ void __launch_bounds__(kThreads) zero_step_kernel(const __grid_consta
     const int64_t j = base + u * V;
     if constexpr (MIXED) {
       if (P.owner_only) owner = advance_owner(P, owner, j);
-      step_vec_mixed<NR>(P, j, owner, gm);
+      step_vec_mixed<NR, O>(P, j, owner, gm);
     } else {
       owner = advance_owner(P, owner, j);
-      step_vec_fp32<NR>(P, j, owner, gm);
+      step_vec_fp32<NR, O>(P, j, owner, gm);
     }
   }
 }
@@ -634,7 +693,7 @@ __global__ void __launch_bounds__(kThreads) gather_kernel(const __grid_constant_
   }
 }
 
-// m = v = 0 and (mixed) master = init over the split range.
+// m = v = 0 (each when present) and (mixed) master = init over the split range.
 __global__ void __launch_bounds__(kThreads) init_state_kernel(const __grid_constant__ InitArgs P) {
   const int64_t tid = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
   const int64_t stride = int64_t(gridDim.x) * blockDim.x;
@@ -643,16 +702,16 @@ __global__ void __launch_bounds__(kThreads) init_state_kernel(const __grid_const
   const int64_t body_end = sp.lo + sp.head + sp.nvec * 4;
   for (int64_t s = tid; s < nscalar; s += stride) {
     const int64_t j = s < sp.head ? sp.lo + s : body_end + (s - sp.head);
-    P.m[j] = 0.0f;
-    P.v[j] = 0.0f;
+    if (P.m) P.m[j] = 0.0f;
+    if (P.v) P.v[j] = 0.0f;
     if (P.master) P.master[j] = P.init[j];
   }
   const int64_t base = sp.lo + sp.head;
   const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
   for (int64_t u = tid; u < sp.nvec; u += stride) {
     const int64_t j = base + u * 4;
-    st4(P.m + j, z);
-    st4(P.v + j, z);
+    if (P.m) st4(P.m + j, z);
+    if (P.v) st4(P.v + j, z);
     if (P.master) st4(P.master + j, ld4(P.init + j));
   }
 }
@@ -727,11 +786,11 @@ cudaError_t launch_tma(const A& args, uint32_t smem, int64_t tiles, cudaStream_t
   return cudaGetLastError();
 }
 
-template <int NR, bool MIXED, class Cfg = DefaultPipe>
+template <int NR, bool MIXED, Opt O, class Cfg = DefaultPipe>
 cudaError_t launch_step_tma(const StepArgs& a, cudaStream_t s) {
-  using G = StepTile<NR, MIXED, Cfg>;
+  using G = StepTile<NR, MIXED, kStates<O>, Cfg>;
   const int64_t nelem = a.sp.nvec * (MIXED ? 8 : 4);
-  return launch_tma<zero_step_tma_kernel<NR, MIXED, Cfg>, Cfg::kThreads>(
+  return launch_tma<zero_step_tma_kernel<NR, MIXED, O, Cfg>, Cfg::kThreads>(
       a, G::kSmem, (nelem + G::T - 1) / G::T, s);
 }
 
@@ -745,29 +804,34 @@ cudaError_t launch_mean_tma(const AllreduceArgs& a, cudaStream_t s) {
 
 // Bulk-copy pipeline for N <= 8 when the buffers share a 16-byte phase (there
 // is a vector body); the register-streaming kernel for any other case.
-template <bool MIXED>
+template <bool MIXED, Opt O>
 cudaError_t launch_step_t(const StepArgs& a, cudaStream_t s) {
   if (a.sp.nvec > 0) {
     switch (a.N) {
-      case 1: return launch_step_tma<1, MIXED>(a, s);
-      case 2: return launch_step_tma<2, MIXED>(a, s);
-      case 3: return launch_step_tma<3, MIXED>(a, s);
-      case 4: return launch_step_tma<4, MIXED>(a, s);
-      case 5: return launch_step_tma<5, MIXED>(a, s);
-      case 6: return launch_step_tma<6, MIXED>(a, s);
-      case 7: return launch_step_tma<7, MIXED>(a, s);
-      case 8: return launch_step_tma<8, MIXED>(a, s);
+      case 1: return launch_step_tma<1, MIXED, O>(a, s);
+      case 2: return launch_step_tma<2, MIXED, O>(a, s);
+      case 3: return launch_step_tma<3, MIXED, O>(a, s);
+      case 4: return launch_step_tma<4, MIXED, O>(a, s);
+      case 5: return launch_step_tma<5, MIXED, O>(a, s);
+      case 6: return launch_step_tma<6, MIXED, O>(a, s);
+      case 7: return launch_step_tma<7, MIXED, O>(a, s);
+      case 8: return launch_step_tma<8, MIXED, O>(a, s);
       default: break;
     }
   }
   const int64_t work = a.sp.nvec > a.sp.head + a.sp.tail ? a.sp.nvec : a.sp.head + a.sp.tail;
   switch (a.N) {
-    case 1: return launch(zero_step_kernel<1, MIXED>, a, work, s);
-    case 2: return launch(zero_step_kernel<2, MIXED>, a, work, s);
-    case 4: return launch(zero_step_kernel<4, MIXED>, a, work, s);
-    case 8: return launch(zero_step_kernel<8, MIXED>, a, work, s);
-    default: return launch(zero_step_kernel<0, MIXED>, a, work, s);
+    case 1: return launch(zero_step_kernel<1, MIXED, O>, a, work, s);
+    case 2: return launch(zero_step_kernel<2, MIXED, O>, a, work, s);
+    case 4: return launch(zero_step_kernel<4, MIXED, O>, a, work, s);
+    case 8: return launch(zero_step_kernel<8, MIXED, O>, a, work, s);
+    default: return launch(zero_step_kernel<0, MIXED, O>, a, work, s);
   }
+}
+
+template <Opt O>
+cudaError_t launch_step_o(const StepArgs& a, bool mixed, cudaStream_t s) {
+  return mixed ? launch_step_t<true, O>(a, s) : launch_step_t<false, O>(a, s);
 }
 
 template <bool BF16>
@@ -797,8 +861,13 @@ cudaError_t launch_allreduce_t(const AllreduceArgs& a, cudaStream_t s) {
 
 }  // namespace
 
-cudaError_t launch_step(const StepArgs& a, bool mixed, cudaStream_t s) {
-  return mixed ? launch_step_t<true>(a, s) : launch_step_t<false>(a, s);
+cudaError_t launch_step(const StepArgs& a, bool mixed, Opt opt, cudaStream_t s) {
+  switch (opt) {
+    case Opt::AdamW: return launch_step_o<Opt::AdamW>(a, mixed, s);
+    case Opt::SgdMomentum: return launch_step_o<Opt::SgdMomentum>(a, mixed, s);
+    case Opt::Sgd: return launch_step_o<Opt::Sgd>(a, mixed, s);
+  }
+  return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_allreduce(const AllreduceArgs& a, bool bf16, cudaStream_t s) {

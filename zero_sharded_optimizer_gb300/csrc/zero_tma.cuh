@@ -127,14 +127,17 @@ struct PipeCfg {
 
 using DefaultPipe = PipeCfg<512, 3, 2, 224 * 1024>;
 
-template <int NR, bool MIXED, class Cfg>
+// KS fp32 state streams besides the parameter / master (AdamW 2, momentum
+// SGD 1, plain SGD 0).
+template <int NR, bool MIXED, int KS, class Cfg>
 struct StepTile {
-  static constexpr int kGB = MIXED ? 2 : 4;           // gradient / replica element bytes
-  static constexpr int kOutB = 12 + (MIXED ? 2 : 0);  // p/master, m, v (+ bf16 replica)
-  static constexpr int T = Cfg::tile(NR * kGB + 12, kOutB);
+  static constexpr int kGB = MIXED ? 2 : 4;                   // gradient / replica bytes
+  static constexpr int kF = 1 + KS;                           // fp32 streams per element
+  static constexpr int kOutB = 4 * kF + (MIXED ? 2 : 0);      // (+ bf16 replica)
+  static constexpr int T = Cfg::tile(NR * kGB + 4 * kF, kOutB);
   static constexpr uint32_t kGradTile = uint32_t(T) * kGB;
   static constexpr uint32_t kFTile = uint32_t(T) * 4;
-  static constexpr uint32_t kStage = NR * kGradTile + 3 * kFTile;
+  static constexpr uint32_t kStage = NR * kGradTile + kF * kFTile;
   static constexpr uint32_t kOut = uint32_t(T) * kOutB;
   static constexpr uint32_t kSmem = Cfg::kStages * kStage + Cfg::kOutBufs * kOut;
 };
@@ -231,10 +234,11 @@ __device__ __forceinline__ void run_pipeline(PipeState<Cfg::kStages>& ps, int64_
 
 // ------------------------------------------------------------ the fused step --
 
-template <int NR, bool MIXED, class Cfg = DefaultPipe>
+template <int NR, bool MIXED, Opt O, class Cfg = DefaultPipe>
 __global__ void __launch_bounds__(Cfg::kThreads, 1)
     zero_step_tma_kernel(const __grid_constant__ StepArgs P) {
-  using G = StepTile<NR, MIXED, Cfg>;
+  constexpr int KS = kStates<O>;
+  using G = StepTile<NR, MIXED, KS, Cfg>;
   constexpr int T = G::T;
   constexpr int V = MIXED ? 8 : 4;
   constexpr int S = Cfg::kStages;
@@ -253,7 +257,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
     for (int64_t s = tid; s < nscalar; s += blockDim.x) {
       const int64_t j = s < sp.head ? sp.lo + s : body_end + (s - sp.head);
       owner = advance_owner(P, owner, j);
-      step_scalar<NR, MIXED>(P, j, owner, gm);
+      step_scalar<NR, MIXED, O>(P, j, owner, gm);
     }
   }
 
@@ -266,7 +270,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
 
   auto stage = [&](int s) { return smem + size_t(s) * G::kStage; };
   auto grad_slot = [&](int s, int r) { return stage(s) + r * G::kGradTile; };
-  auto in_f = [&](int s, int k) {  // 0 = parameter / master, 1 = m, 2 = v
+  auto in_f = [&](int s, int k) {  // 0 = parameter / master, 1.. = state streams (m, v)
     return reinterpret_cast<float*>(stage(s) + NR * G::kGradTile + k * G::kFTile);
   };
   auto out_f = [&](int s, int o, int k) {
@@ -275,7 +279,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
   };
   auto out_bf = [&](int s, int o) {  // mixed: the bf16 replica tile
     if constexpr (Cfg::kOutBufs == 0) return grad_slot(s, 0);  // consumed gradient slot
-    return smem + S * G::kStage + o * G::kOut + 3 * G::kFTile;
+    return smem + S * G::kStage + o * G::kOut + G::kF * G::kFTile;
   };
   auto tile_j0 = [&](int64_t local) { return base + (blockIdx.x + local * gridDim.x) * T; };
   auto tile_cnt = [&](int64_t local) {
@@ -295,7 +299,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
       straddle = j0 + cnt - 1 >= P.bounds[owner + 1];
       ps.owner[s] = straddle ? -1 : owner;
     }
-    mbar_expect_tx(&ps.full[s], NR * gbytes + (straddle ? 2u : 3u) * fbytes);
+    mbar_expect_tx(&ps.full[s], NR * gbytes + uint32_t(straddle ? KS : KS + 1) * fbytes);
 #pragma unroll
     for (int r = 0; r < NR; ++r)
       bulk_load(grad_slot(s, r), static_cast<const unsigned char*>(P.grads[r]) + j0 * G::kGB,
@@ -307,16 +311,16 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
         bulk_load(in_f(s, 0), static_cast<const float*>(P.reps[owner]) + j0, fbytes,
                   &ps.full[s]);
     }
-    bulk_load(in_f(s, 1), P.m + j0, fbytes, &ps.full[s]);
-    bulk_load(in_f(s, 2), P.v + j0, fbytes, &ps.full[s]);
+#pragma unroll
+    for (int k = 0; k < KS; ++k) bulk_load(in_f(s, k + 1), state_ptr(P, k) + j0, fbytes, &ps.full[s]);
   };
 
   auto issue_store = [&](int64_t local, int s, int o) {
     const int64_t j0 = tile_j0(local);
     const uint32_t cnt = tile_cnt(local);
     const uint32_t fbytes = cnt * 4;
-    bulk_store(P.m + j0, out_f(s, o, 1), fbytes);
-    bulk_store(P.v + j0, out_f(s, o, 2), fbytes);
+#pragma unroll
+    for (int k = 0; k < KS; ++k) bulk_store(state_ptr(P, k) + j0, out_f(s, o, k + 1), fbytes);
     if constexpr (MIXED) bulk_store(P.master + j0, out_f(s, o, 0), fbytes);
     if (P.owner_only) {  // stage 3: each owner's slice of its own replica only
       const int r_lo = advance_owner(P, 0, j0);
@@ -346,11 +350,14 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
     const int64_t j0 = tile_j0(local);
     const int cnt = int(tile_cnt(local));
     const float* pi = in_f(s, 0);
-    const float* mi = in_f(s, 1);
-    const float* vi = in_f(s, 2);
     float* po = out_f(s, o, 0);
-    float* mo = out_f(s, o, 1);
-    float* vo = out_f(s, o, 2);
+    const float* si[kSA<O>];
+    float* so[kSA<O>];
+#pragma unroll
+    for (int k = 0; k < KS; ++k) {
+      si[k] = in_f(s, k + 1);
+      so[k] = out_f(s, o, k + 1);
+    }
     // four elements per thread: float4s of fp32, or one uint2 of bf16 per rank
     for (int q = tid * 4; q < cnt; q += TH * 4) {
       float4 g;
@@ -383,15 +390,13 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
         }
         p = make_float4(e[0], e[1], e[2], e[3]);
       }
-      float4 m = *reinterpret_cast<const float4*>(mi + q);
-      float4 v = *reinterpret_cast<const float4*>(vi + q);
-      adam1(P.c, scaled_mean<NR>(g.x, P, gm), p.x, m.x, v.x);
-      adam1(P.c, scaled_mean<NR>(g.y, P, gm), p.y, m.y, v.y);
-      adam1(P.c, scaled_mean<NR>(g.z, P, gm), p.z, m.z, v.z);
-      adam1(P.c, scaled_mean<NR>(g.w, P, gm), p.w, m.w, v.w);
+      float4 st[kSA<O>];
+#pragma unroll
+      for (int k = 0; k < KS; ++k) st[k] = *reinterpret_cast<const float4*>(si[k] + q);
+      update4<NR, O>(P, gm, g, p, st);
       *reinterpret_cast<float4*>(po + q) = p;
-      *reinterpret_cast<float4*>(mo + q) = m;
-      *reinterpret_cast<float4*>(vo + q) = v;
+#pragma unroll
+      for (int k = 0; k < KS; ++k) *reinterpret_cast<float4*>(so[k] + q) = st[k];
       // in place, this thread's own 8 bytes of the consumed gradient slot
       if constexpr (MIXED) *reinterpret_cast<uint2*>(out_bf(s, o) + q * 2) = pack4(p);
     }

@@ -26,7 +26,8 @@ class ZeroOptimizer:
                  betas=(0.9, 0.999), eps: float = 1e-8, weight_decay: float = 0.0,
                  master_init: torch.Tensor | None = None, device="cuda", stream=None,
                  max_grad_norm: float = 0.0, grad_scale: float = 1.0, shard_bounds=None,
-                 stage: int = 2):
+                 stage: int = 2, optimizer: str = "adamw", momentum: float = 0.0,
+                 dampening: float = 0.0, nesterov: bool = False):
         """``max_grad_norm`` > 0 clips the (scaled) mean gradient to that global
         norm before every step; ``grad_scale`` multiplies the mean gradient
         (1/k when the gradient buffers hold the sum of k micro-batches);
@@ -34,9 +35,18 @@ class ZeroOptimizer:
         ``abi.zero_tensor_shard_bounds(tensor_sizes, N)`` for whole-tensor shards.
         ``stage`` 3 leaves the all-gather out of the step: each replica keeps
         only its own shard current until ``gather`` (stages 1 and 2 run the
-        same fused step; they differ only in what a rank would keep)."""
+        same fused step; they differ only in what a rank would keep).
+        ``optimizer`` "sgd" runs momentum SGD (torch.optim.SGD semantics:
+        ``momentum``, ``dampening``, ``nesterov``, coupled ``weight_decay``;
+        ``betas`` and ``eps`` unused) with one fp32 buffer per parameter (none
+        without momentum) instead of AdamW's m and v."""
         if stage not in (1, 2, 3):
             raise ValueError("stage must be 1, 2 or 3")
+        if optimizer not in ("adamw", "sgd"):
+            raise ValueError("optimizer must be 'adamw' or 'sgd'")
+        self.optimizer = optimizer
+        self.momentum, self.dampening = float(momentum), float(dampening)
+        self.nesterov = bool(nesterov)
         self.stage = int(stage)
         self.shard_bounds = None if shard_bounds is None else [int(b) for b in shard_bounds]
         self.n, self.N, self.precision = int(n), int(N), int(precision)
@@ -47,8 +57,9 @@ class ZeroOptimizer:
         self.eps, self.weight_decay = float(eps), float(weight_decay)
         self.device = torch.device(device)
         f32 = dict(dtype=torch.float32, device=self.device)
-        self.m = torch.empty(self.n, **f32)
-        self.v = torch.empty(self.n, **f32)
+        sgd = optimizer == "sgd"
+        self.m = None if sgd and self.momentum == 0 else torch.empty(self.n, **f32)
+        self.v = None if sgd else torch.empty(self.n, **f32)
         self.master = None
         if self.precision == abi.ZERO_BF16_MIXED:
             if master_init is None:
@@ -82,9 +93,10 @@ class ZeroOptimizer:
         """
         clipping = self.max_grad_norm > 0
         owner_only = self.stage == 3
-        if (clipping or owner_only) and not all(g.is_cuda for g in grads):
+        sgd = self.optimizer == "sgd"
+        if (clipping or owner_only or sgd) and not all(g.is_cuda for g in grads):
             # the global norm needs every gradient before any update, and the
-            # chunked host pipeline runs the full all-gather: copy first
+            # chunked host pipeline runs the stage-1/2 AdamW step: copy first
             staging = self._staging_buffers()
             s = stream if stream is not None else torch.cuda.current_stream(self.device)
             with torch.cuda.stream(s):
@@ -92,7 +104,7 @@ class ZeroOptimizer:
                     dst.copy_(src, non_blocking=True)
             grads = staging
         if all(g.is_cuda for g in grads):
-            if clipping or owner_only or self.grad_scale != 1.0:
+            if clipping or owner_only or sgd or self.grad_scale != 1.0:
                 norm = None
                 if clipping:
                     if self._norm is None:
@@ -103,9 +115,16 @@ class ZeroOptimizer:
                     abi.zero_grad_norm_sq(grads, self.precision, self._norm_scratch, self._norm,
                                           self.n, stream)
                     norm = self._norm
-                abi.zero_step_ex(params, grads, self.states, self.t + 1, self.lr, self.beta1,
-                                 self.beta2, self.eps, self.weight_decay, self.grad_scale,
-                                 self.max_grad_norm, norm, 0, -1, stream, owner_only)
+                if sgd:
+                    abi.zero_step_sgd(params, grads, self.states, self.t + 1, self.lr,
+                                      self.momentum, self.dampening, self.weight_decay,
+                                      self.nesterov, self.grad_scale, self.max_grad_norm, norm,
+                                      0, -1, stream, owner_only)
+                else:
+                    abi.zero_step_ex(params, grads, self.states, self.t + 1, self.lr,
+                                     self.beta1, self.beta2, self.eps, self.weight_decay,
+                                     self.grad_scale, self.max_grad_norm, norm, 0, -1, stream,
+                                     owner_only)
             else:
                 abi.zero_step(params, grads, self.states, self.t + 1, self.lr, self.beta1,
                               self.beta2, self.eps, self.weight_decay, stream)
@@ -132,8 +151,8 @@ class ZeroOptimizer:
                       bucket_bytes: int = BUCKET_BYTES_25MIB, done=None,
                       timeout_ms: int = -1) -> int:
         """The step bucket by bucket on ``side``, each after its ``ready`` event."""
-        if self.stage == 3:
-            raise ValueError("bucket streaming runs the stage-1/2 step (with all-gather)")
+        if self.stage == 3 or self.optimizer != "adamw":
+            raise ValueError("bucket streaming runs the stage-1/2 AdamW step (with all-gather)")
         try:
             abi.zero_step_bucketed(params, grads, self.states, self.t + 1, self.lr, self.beta1,
                                    self.beta2, self.eps, self.weight_decay, bucket_bytes, ready,
@@ -164,14 +183,14 @@ class ZeroOptimizer:
     # ------------------------------------------------------- checkpointing --
 
     def state_dict(self) -> dict:
-        d = {"t": self.t, "m": self.m.clone(), "v": self.v.clone()}
-        if self.master is not None:
-            d["master"] = self.master.clone()
+        d = {"t": self.t}
+        for key in ("m", "v", "master"):
+            if getattr(self, key) is not None:
+                d[key] = getattr(self, key).clone()
         return d
 
     def load_state_dict(self, d: dict) -> None:
         self.t = int(d["t"])
-        self.m.copy_(d["m"])
-        self.v.copy_(d["v"])
-        if self.master is not None:
-            self.master.copy_(d["master"])
+        for key in ("m", "v", "master"):
+            if getattr(self, key) is not None:
+                getattr(self, key).copy_(d[key])
