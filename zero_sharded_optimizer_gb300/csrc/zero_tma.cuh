@@ -98,6 +98,11 @@ __device__ __forceinline__ void bulk_commit() {
 __device__ __forceinline__ void bulk_wait_read_all_but_last() {
   asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
 }
+// All but the KEEP most recent bulk groups have finished reading shared memory.
+template <int KEEP>
+__device__ __forceinline__ void bulk_wait_read_keep() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(KEEP) : "memory");
+}
 __device__ __forceinline__ void bulk_wait_all() {
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
@@ -184,11 +189,13 @@ __device__ __forceinline__ void drain_after_timeout(PipeState<S>& ps, int64_t co
     mbar_wait(&ps.full[t % S], uint32_t((t / S) & 1), kDrainNs);
 }
 
-// The loop shared by both pipelines. `issue_load(local)` queues the bulk loads
-// of local tile `local` into stage local % kStages; `compute(local, stage, out)`
-// turns stage `stage` into output buffer `out` (or back into the stage when
-// there are no output buffers); `issue_store(local, stage, out)` queues and
-// commits the bulk stores of the results.
+// The lock-step loop: every thread computes, thread 0 also issues the copies,
+// and block barriers separate the phases. `issue_load(local)` queues the bulk
+// loads of local tile `local` into stage local % kStages;
+// `compute(local, stage, out)` turns stage `stage` into output
+// buffer `out` (or back into the stage when there are no output buffers);
+// `issue_store(local, stage, out)` queues and commits the bulk stores of the
+// results.
 template <class Cfg, typename Load, typename Compute, typename Store>
 __device__ __forceinline__ void run_pipeline(PipeState<Cfg::kStages>& ps, int64_t my_tiles,
                                              uint64_t wait_ns, Load issue_load,
@@ -222,7 +229,8 @@ __device__ __forceinline__ void run_pipeline(PipeState<Cfg::kStages>& ps, int64_
       issue_store(k, s, o);
       if constexpr (Cfg::kOutBufs > 0) {
         if (issued < my_tiles) issue_load(issued++);  // into stage s, just consumed
-        bulk_wait_read_all_but_last();  // the next output buffer has been read out
+        // the next output buffer (last used OB tiles ago) has been read out
+        bulk_wait_read_keep<Cfg::kOutBufs - 1>();
       } else if (k >= 1) {
         bulk_wait_read_all_but_last();  // stores of tile k-1 have read their stage
         if (issued < my_tiles) issue_load(issued++);  // into the stage of tile k-1
@@ -232,20 +240,157 @@ __device__ __forceinline__ void run_pipeline(PipeState<Cfg::kStages>& ps, int64_
   if (tid == 0) bulk_wait_all();
 }
 
+// ------------------------------------------------- warp-specialised pipeline --
+//
+// Used by the kernels with output buffers. Thread 0 issues the bulk loads,
+// thread 32 issues the bulk stores, and warps 2.. (Cfg::kThreads threads)
+// compute. The roles hand tiles over through mbarriers instead of block-wide
+// barriers, so neither the issue of copies nor the wait for stores to drain
+// holds up the arithmetic of the next tile:
+//   full[s]   the loads of stage s landed           (producer's arrive + bytes)
+//   empty[s]  the compute threads are done with s   (one arrival per warp)
+//   ready[o]  output buffer o is written            (one arrival per warp)
+//   free_[o]  the stores of buffer o have read it   (storer)
+// Tile k uses stage k % S and output buffer k % OB; each barrier completes one
+// phase per use, so the parity of use u is u & 1.
+constexpr int kWsExtraThreads = 64;
+
+template <int S, int OB>
+struct PipeStateWS {
+  uint64_t full[S];
+  uint64_t empty[S];
+  uint64_t ready[OB];
+  uint64_t free_[OB];
+  int owner[S];  // fp32 step: owner of the whole tile, -1 if it straddles
+  volatile int abort;
+};
+
+// Bounded wait of one role: false when the bound ran out (recorded in the
+// device status, and every other role told to stop) or another role stopped.
+template <class PS>
+__device__ __forceinline__ bool role_wait(PS& ps, uint64_t* bar, uint32_t parity,
+                                          uint64_t limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (;;) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (ps.abort) return false;
+    if (global_timer_ns() - t0 > limit_ns) {
+      ps.abort = 1;
+      atomicOr(&g_device_status, ZK_STATUS_WAIT_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+// `issue_load(local)` queues the loads of local tile `local` (arrive.expect_tx
+// on full[local % S]); `compute(local, s, o)`, run by the Cfg::kThreads
+// compute threads (thread index minus kWsExtraThreads), turns stage s into
+// output buffer o; `issue_store(local, s, o)`
+// queues and commits the stores of buffer o.
+template <class Cfg, typename Load, typename Compute, typename Store>
+__device__ __forceinline__ void run_pipeline_ws(PipeStateWS<Cfg::kStages, Cfg::kOutBufs>& ps,
+                                                int64_t my_tiles, uint64_t wait_ns,
+                                                Load issue_load, Compute compute,
+                                                Store issue_store) {
+  constexpr int S = Cfg::kStages;
+  constexpr int OB = Cfg::kOutBufs;
+  constexpr int C = Cfg::kThreads;  // compute threads
+  static_assert(OB >= 2, "the warp-specialised pipeline needs two output buffers");
+  static_assert(C % 32 == 0, "whole compute warps");
+  const int tid = threadIdx.x;
+  if (tid == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&ps.full[s], 1);
+      mbar_init(&ps.empty[s], C / 32);
+    }
+    for (int o = 0; o < OB; ++o) {
+      mbar_init(&ps.ready[o], C / 32);
+      mbar_init(&ps.free_[o], 1);
+    }
+    fence_mbar_init();
+    ps.abort = 0;
+  }
+  __syncthreads();
+  // Every loop below exits warp-uniformly (one lane decides and broadcasts,
+  // or the lanes vote), so all threads meet the final block barrier converged.
+  const int lane = tid & 31, warp = tid >> 5;
+  int64_t issued = 0;  // producer lane only
+  if (warp == 0) {
+    for (int64_t k = 0; k < my_tiles; ++k) {
+      const int s = int(k % S);
+      int ok = 1;
+      if (lane == 0) {
+        if (k >= S) ok = role_wait(ps, &ps.empty[s], uint32_t((k / S - 1) & 1), wait_ns);
+        if (ok) {
+          issue_load(k);
+          issued = k + 1;
+        }
+      }
+      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+    }
+  } else if (warp == 1) {
+    for (int64_t k = 0; k < my_tiles; ++k) {
+      const int s = int(k % S), o = int(k % OB);
+      int ok = 1;
+      if (lane == 0) {
+        ok = role_wait(ps, &ps.ready[o], uint32_t((k / OB) & 1), wait_ns);
+        if (ok) {
+          issue_store(k, s, o);
+          bulk_wait_read_keep<OB - 1>();  // tile k - OB + 1 has been read out
+          if (k - OB + 1 >= 0) mbar_arrive(&ps.free_[(k - OB + 1) % OB]);
+        }
+      }
+      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+    }
+  } else {
+    for (int64_t k = 0; k < my_tiles; ++k) {
+      const int s = int(k % S), o = int(k % OB);
+      int ok = role_wait(ps, &ps.full[s], uint32_t((k / S) & 1), wait_ns);
+      if (ok && k >= OB) ok = role_wait(ps, &ps.free_[o], uint32_t((k / OB - 1) & 1), wait_ns);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      compute(k, s, o);
+      fence_proxy_async_smem();  // this thread's writes to buffer o, seen by the bulk stores
+      __syncwarp();              // the warp's reads of stage s and writes are done
+      if (lane == 0) {
+        mbar_arrive(&ps.empty[s]);
+        mbar_arrive(&ps.ready[o]);
+      }
+    }
+  }
+  __syncthreads();
+  if (tid == 32) bulk_wait_all();  // every store has finished
+  if (tid == 0 && ps.abort) {
+    // wait (bounded) for the loads still in flight: the last S issued tiles
+    for (int64_t t = issued > S ? issued - S : 0; t < issued; ++t)
+      mbar_wait(&ps.full[t % S], uint32_t((t / S) & 1), kDrainNs);
+  }
+}
+
 // ------------------------------------------------------------ the fused step --
 
-template <int NR, bool MIXED, Opt O, class Cfg = DefaultPipe>
-__global__ void __launch_bounds__(Cfg::kThreads, 1)
+// WS: the warp-specialised pipeline (Cfg::kThreads + kWsExtraThreads threads)
+// instead of the lock-step one (Cfg::kThreads threads).
+template <int NR, bool MIXED, Opt O, bool WS, class Cfg = DefaultPipe>
+__global__ void __launch_bounds__(Cfg::kThreads + (WS ? kWsExtraThreads : 0), 1)
     zero_step_tma_kernel(const __grid_constant__ StepArgs P) {
   constexpr int KS = kStates<O>;
   using G = StepTile<NR, MIXED, KS, Cfg>;
   constexpr int T = G::T;
   constexpr int V = MIXED ? 8 : 4;
   constexpr int S = Cfg::kStages;
-  constexpr int TH = Cfg::kThreads;
+  constexpr int TH = Cfg::kThreads;  // compute threads
   extern __shared__ __align__(128) unsigned char smem[];
-  __shared__ PipeState<S> ps;
+  __shared__ typename std::conditional<WS, PipeStateWS<S, Cfg::kOutBufs>, PipeState<S>>::type ps;
   const int tid = threadIdx.x;
+  // compute-thread index, derived here from threadIdx.x: with its range known
+  // and a compile-time stride the compute loop is resolved at compile time
+  // (a runtime index or stride measured 1-2 % slower on the whole step)
+  const int ct = WS ? tid - kWsExtraThreads : tid;
   const Split& sp = P.sp;
   const float gm = grad_multiplier(P);
 
@@ -359,7 +504,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
       so[k] = out_f(s, o, k + 1);
     }
     // four elements per thread: float4s of fp32, or one uint2 of bf16 per rank
-    for (int q = tid * 4; q < cnt; q += TH * 4) {
+    for (int q = ct * 4; q < cnt; q += TH * 4) {
       float4 g;
       if constexpr (MIXED) {
         g = unpack4(*reinterpret_cast<const uint2*>(grad_slot(s, 0) + q * 2));
@@ -402,7 +547,11 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
     }
   };
 
-  run_pipeline<Cfg>(ps, my_tiles, P.wait_ns, issue_load, compute, issue_store);
+  if constexpr (WS) {
+    run_pipeline_ws<Cfg>(ps, my_tiles, P.wait_ns, issue_load, compute, issue_store);
+  } else {
+    run_pipeline<Cfg>(ps, my_tiles, P.wait_ns, issue_load, compute, issue_store);
+  }
 }
 
 // ---------------------------------------------------------- the DDP mean --
