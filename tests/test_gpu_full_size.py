@@ -101,3 +101,78 @@ def test_full_size_sampled(abi, cuda, name):
             # the shared zero mask leaves ~1% of indices with an exact zero mean
             zeros = np.all(np.stack([inputs.to_numpy_storage(g[idx_d]) for g in grads]) == 0, 0)
             assert 0.003 < zeros.mean() < 0.03
+
+
+def oracle_sgd_on_sample(wl, t, g_s, p_s, buf_s, master_s, momentum):
+    N, k = wl.N, len(p_s)
+    b = oracle.shard_bounds(k, N)
+    states = []
+    for i in range(N):
+        st = {"buf": buf_s[b[i]:b[i + 1]].copy()}
+        if master_s is not None:
+            st["master"] = master_s[b[i]:b[i + 1]].copy()
+        states.append(st)
+    reps, new = oracle.zero_step_sgd([p_s] * N, g_s, states, t, lr=wl.lr, momentum=momentum,
+                                     weight_decay=wl.weight_decay, precision=wl.precision,
+                                     mode="fp32")
+    cat = lambda key: np.concatenate([s[key] for s in new])  # noqa: E731
+    return reps[0], cat("buf"), (cat("master") if master_s is not None else None)
+
+
+@pytest.mark.parametrize("name", ["gpt2_small", "fp32_320m"])
+@pytest.mark.parametrize("variant", ["sgd", "stage3"])
+def test_full_size_sampled_sgd_and_stage3(abi, cuda, name, variant):
+    """Momentum SGD, and the stage-3 owner-only step followed by the gather, at
+    full size: sampled outputs against the oracle; after the gather every
+    replica equal to the owner's on the device over all n."""
+    from zero_sharded_optimizer_gb300.optimizer import ZeroOptimizer
+    wl = inputs.WORKLOADS[name]
+    n, N = wl.n, wl.N
+    mixed = wl.precision == inputs.BF16_MIXED
+    sgd = variant == "sgd"
+    init = inputs.init_params_fp32(n, wl, seed=1, device=cuda)
+    reps = inputs.make_replicas(init, N, wl.precision)
+    grads = inputs.make_grads(n, N, wl.precision, device=cuda)
+    opt = ZeroOptimizer(n, N, wl.precision, lr=wl.lr, betas=(wl.beta1, wl.beta2), eps=wl.eps,
+                        weight_decay=wl.weight_decay, master_init=init if mixed else None,
+                        optimizer="sgd" if sgd else "adamw", momentum=0.9 if sgd else 0.0,
+                        stage=2 if sgd else 3)
+    del init
+    idx = sample_indices(n, N, seed=7 + len(name))
+    idx_d = torch.from_numpy(idx).to(cuda)
+    take = lambda x: inputs.to_numpy_storage(x[idx_d])  # noqa: E731
+    bounds = np.array(oracle.shard_bounds(n, N))
+    owner = np.searchsorted(bounds, idx, side="right") - 1
+    for t in range(1, 4):
+        p_before = take(opt.master) if mixed else take(reps[0])
+        s_before = [take(opt.m)] if sgd else [take(opt.m), take(opt.v)]
+        inputs.fill_grads(grads, wl, step=t, seed=1)
+        opt.step(reps, grads)
+        torch.cuda.synchronize()
+        g_s = [take(g) for g in grads]
+        if sgd:
+            ref_p, ref_buf, ref_master = oracle_sgd_on_sample(
+                wl, t, g_s, p_before, s_before[0], p_before if mixed else None, 0.9)
+            assert_fp32_close(take(opt.m), ref_buf, f"{name} t={t} buf")
+        else:
+            ref_p, ref_m, ref_v, ref_master = oracle_on_sample(
+                wl, t, g_s, p_before, s_before[0], s_before[1], p_before if mixed else None)
+            assert_fp32_close(take(opt.m), ref_m, f"{name} t={t} m")
+            assert_fp32_close(take(opt.v), ref_v, f"{name} t={t} v")
+            # released: each replica is current only over its own shard
+            own = np.stack([take(reps[r]) for r in range(N)])[owner, np.arange(len(idx))]
+            if mixed:
+                assert_bf16_within_one_ulp(own, ref_master, f"{name} t={t} own shards")
+            else:
+                assert_fp32_close(own, ref_p, f"{name} t={t} own shards")
+            opt.gather(reps)
+            torch.cuda.synchronize()
+        if mixed:
+            assert_fp32_close(take(opt.master), ref_master, f"{name} t={t} master")
+            for r in range(N):
+                assert_bf16_within_one_ulp(take(reps[r]), ref_master, f"{name} t={t} rep {r}")
+        else:
+            for r in range(N):
+                assert_fp32_close(take(reps[r]), ref_p, f"{name} t={t} rep {r}")
+        for r in range(1, N):
+            assert torch.equal(reps[r], reps[0])
