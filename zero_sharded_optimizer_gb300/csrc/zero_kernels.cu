@@ -790,16 +790,22 @@ cudaError_t launch_tma(const A& args, uint32_t smem, int64_t tiles, cudaStream_t
 // fastest there); the warp-specialised one for the owner-only (stage 3) and
 // SGD steps, which move fewer bytes per tile and gain from overlapping the
 // issue of copies with the arithmetic.
-template <int NR, bool MIXED, Opt O, class Cfg = DefaultPipe>
-cudaError_t launch_step_tma(const StepArgs& a, cudaStream_t s) {
+template <int NR, bool MIXED, Opt O, bool WS, class Cfg>
+cudaError_t launch_step_cfg(const StepArgs& a, cudaStream_t s) {
   using G = StepTile<NR, MIXED, kStates<O>, Cfg>;
   const int64_t nelem = a.sp.nvec * (MIXED ? 8 : 4);
-  const int64_t tiles = (nelem + G::T - 1) / G::T;
-  if (O == Opt::AdamW && !a.owner_only)
-    return launch_tma<zero_step_tma_kernel<NR, MIXED, O, false, Cfg>, Cfg::kThreads>(
-        a, G::kSmem, tiles, s);
-  return launch_tma<zero_step_tma_kernel<NR, MIXED, O, true, Cfg>,
-                    Cfg::kThreads + kWsExtraThreads>(a, G::kSmem, tiles, s);
+  return launch_tma<zero_step_tma_kernel<NR, MIXED, O, WS, Cfg>,
+                    Cfg::kThreads + (WS ? kWsExtraThreads : 0)>(a, G::kSmem,
+                                                                (nelem + G::T - 1) / G::T, s);
+}
+
+template <int NR, bool MIXED, Opt O>
+cudaError_t launch_step_tma(const StepArgs& a, cudaStream_t s) {
+  if constexpr (O == Opt::AdamW) {
+    if (!a.owner_only) return launch_step_cfg<NR, MIXED, O, false, DefaultPipe>(a, s);
+  }
+  using Ws = typename std::conditional<O == Opt::AdamW, WsPipeAdamW, WsPipeSgd>::type;
+  return launch_step_cfg<NR, MIXED, O, true, Ws>(a, s);
 }
 
 template <int NR, bool BF16, class Cfg = DefaultPipe>
