@@ -745,6 +745,9 @@ int zero_step_bucketed(void* const* params, const void* const* grads, zero_state
     }
     int64_t lo, hi;
     bucket_range_of(st->n, B, k, &lo, &hi);
+    // buckets after the first may start while the previous one finishes:
+    // their index ranges are disjoint
+    a.dependent = k > 0;
     if (int e = launch_range(a, st, vec, phase, lo, hi, s)) return e;
   }
   if (done) {

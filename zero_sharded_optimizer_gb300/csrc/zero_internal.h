@@ -70,6 +70,10 @@ struct StepArgs {
   // Stage 3: write the new parameters only into the owner's replica, over the
   // owner's shard; the other replicas' elements are left untouched.
   int32_t owner_only;
+  // Launch as a programmatic dependent of the previous kernel on the stream,
+  // which must touch indices disjoint from this range (a later bucket of the
+  // same step). Honoured by the bulk-copy kernels.
+  int32_t dependent;
 };
 
 // Squared global norm of the mean gradient, as fixed-size partial sums.

@@ -768,8 +768,12 @@ cudaError_t launch(K kernel, const A& args, int64_t work, cudaStream_t s) {
 // One persistent CTA per SM (fewer when there are fewer tiles), with the
 // pipeline's shared memory. The shared-memory opt-in is set once per kernel and
 // device.
+// With `dependent` the launch may begin while the previous kernel on the
+// stream is still finishing (programmatic dependent launch): only for a kernel
+// whose data is disjoint from that kernel's (the next bucket of one step).
 template <auto kernel, int THREADS, typename A>
-cudaError_t launch_tma(const A& args, uint32_t smem, int64_t tiles, cudaStream_t s) {
+cudaError_t launch_tma(const A& args, uint32_t smem, int64_t tiles, cudaStream_t s,
+                       bool dependent = false) {
   static bool configured[256] = {false};  // per device ordinal; one array per kernel
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -782,8 +786,21 @@ cudaError_t launch_tma(const A& args, uint32_t smem, int64_t tiles, cudaStream_t
     configured[dev] = true;
   }
   const int blocks = int(tiles < 1 ? 1 : (tiles < sms ? tiles : sms));
-  kernel<<<blocks, THREADS, smem, s>>>(args);
-  return cudaGetLastError();
+  if (!dependent) {
+    kernel<<<blocks, THREADS, smem, s>>>(args);
+    return cudaGetLastError();
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(blocks));
+  cfg.blockDim = dim3(unsigned(THREADS));
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args);
 }
 
 // The lock-step pipeline for the AdamW step with its all-gather (measured
@@ -795,8 +812,8 @@ cudaError_t launch_step_cfg(const StepArgs& a, cudaStream_t s) {
   using G = StepTile<NR, MIXED, kStates<O>, Cfg>;
   const int64_t nelem = a.sp.nvec * (MIXED ? 8 : 4);
   return launch_tma<zero_step_tma_kernel<NR, MIXED, O, WS, Cfg>,
-                    Cfg::kThreads + (WS ? kWsExtraThreads : 0)>(a, G::kSmem,
-                                                                (nelem + G::T - 1) / G::T, s);
+                    Cfg::kThreads + (WS ? kWsExtraThreads : 0)>(
+      a, G::kSmem, (nelem + G::T - 1) / G::T, s, a.dependent != 0);
 }
 
 template <int NR, bool MIXED, Opt O>

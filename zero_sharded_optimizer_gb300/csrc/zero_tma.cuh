@@ -110,6 +110,15 @@ __device__ __forceinline__ void bulk_wait_all() {
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
+// Programmatic dependent launch: let the next kernel on the stream start
+// (once every CTA here has said so), and wait for the kernel before this one
+// to complete (a no-op when this kernel was launched without the attribute).
+__device__ __forceinline__ void pdl_allow_next() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait_previous() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
 
 // ------------------------------------------------------------ pipeline shape --
 
@@ -399,6 +408,10 @@ __global__ void __launch_bounds__(Cfg::kThreads + (WS ? kWsExtraThreads : 0), 1)
   const int ct = WS ? tid - kWsExtraThreads : tid;
   const Split& sp = P.sp;
   const float gm = grad_multiplier(P);
+  // Buckets of one step touch disjoint indices: the next one may start now.
+  // This kernel still completes only after the one before it (the wait at the
+  // end), so completion on the stream keeps its order.
+  pdl_allow_next();
 
   // Scalar head and tail (fewer than 2V elements) by block 0.
   if (blockIdx.x == 0) {
@@ -417,7 +430,10 @@ __global__ void __launch_bounds__(Cfg::kThreads + (WS ? kWsExtraThreads : 0), 1)
   const int64_t ntiles = (nelem + T - 1) / T;
   const int64_t my_tiles =
       ntiles > int64_t(blockIdx.x) ? (ntiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
-  if (my_tiles == 0) return;
+  if (my_tiles == 0) {
+    pdl_wait_previous();
+    return;
+  }
 
   auto stage = [&](int s) { return smem + size_t(s) * G::kStage; };
   auto grad_slot = [&](int s, int r) { return stage(s) + r * G::kGradTile; };
@@ -558,6 +574,7 @@ __global__ void __launch_bounds__(Cfg::kThreads + (WS ? kWsExtraThreads : 0), 1)
   } else {
     run_pipeline<Cfg>(ps, my_tiles, P.wait_ns, issue_load, compute, issue_store);
   }
+  pdl_wait_previous();
 }
 
 // ---------------------------------------------------------- the DDP mean --
