@@ -1,24 +1,26 @@
-// Bulk-copy (TMA) staged kernels: the fused ZeRO step and the DDP mean for
-// N <= 8 ranks. Included by zero_kernels.cu after the element helpers.
+// Bulk-copy (TMA) staged kernels: the fused ZeRO step (AdamW or SGD, with the
+// all-gather or owner-only), the DDP mean for N <= 8 ranks, and the stage-3
+// gather. Included by zero_kernels.cu after the element helpers.
 //
 // Pipeline (one CTA per SM, persistent over tiles tile = blockIdx.x + k*gridDim.x):
-//   * thread 0 issues, per tile, one cp.async.bulk global->shared copy per
-//     input stream (N gradient tiles, parameter/master, m, v) completing on the
+//   * per tile, one cp.async.bulk global->shared copy per input stream (N
+//     gradient tiles, parameter/master, optimizer state) completing on the
 //     stage's mbarrier;
-//   * all threads wait on the stage, compute, and write the results either into
-//     one of two output buffers or back into the stage; thread 0 then issues
-//     cp.async.bulk shared->global copies of the results: m, v, (master,) and
-//     the same parameter tile N times -- the all-gather reads one shared tile N
-//     times instead of N register copies;
-//   * with output buffers, the input stage is refilled with the tile kStages
-//     ahead as soon as it has been computed, and an output buffer is rewritten
-//     only after its previous bulk stores have read it; computed in place, a
-//     stage is refilled once the stores reading it are done
-//     (cp.async.bulk.wait_group.read).
-// Large tiles (2048 elements, 8 KB per fp32 stream) give every stream long
-// contiguous DRAM bursts. The pipeline shape (threads, stages, output buffers,
-// shared-memory budget) is a template parameter; DefaultPipe is the measured
-// choice.
+//   * the compute threads wait on the stage, compute, and write the results
+//     into an output buffer (or back into the stage); then cp.async.bulk
+//     shared->global copies store them: state, (master,) and the same
+//     parameter tile N times -- the all-gather reads one shared tile N times
+//     instead of N register copies;
+//   * an input stage is refilled with the tile kStages ahead once it has been
+//     computed, and an output buffer is rewritten only after its previous bulk
+//     stores have read it (cp.async.bulk.wait_group.read).
+// Two drivers run that loop: the lock-step one (every thread computes, thread
+// 0 also issues the copies, block barriers between phases) and the
+// warp-specialised one (a load warp, a store warp and compute warps handing
+// tiles over by mbarriers). Large tiles (2048 elements, 8 KB per fp32 stream)
+// give every stream long contiguous DRAM bursts. The pipeline shape (threads,
+// stages, output buffers, shared-memory budget) is a template parameter; the
+// named shapes below are the measured choices.
 //
 // Every wait on an mbarrier is bounded by %globaltimer. When the bound runs
 // out the CTA sets ZK_STATUS_WAIT_TIMEOUT in the device status word, waits
