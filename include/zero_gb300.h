@@ -162,8 +162,10 @@ int zero_step_range(void *const *params, const void *const *grads, zero_states_t
  * of sharded global-norm clipping ("Data parallelism and ZeRO stages 1 to 3",
  * "Going further": an all-reduce of the squared chunk norms before the step):
  * the float mean of every element (rank order, as in the step) is squared
- * exactly in double; fixed chunks of 32,768 elements give partial sums in
- * `scratch` (a DEVICE buffer of at least zero_grad_norm_scratch_count doubles,
+ * without rounding error (split into a float product and its exact error) and
+ * summed with compensation, so each partial is accurate to about double
+ * precision; fixed chunks of 32,768 elements give partial sums in `scratch` (a
+ * DEVICE buffer of at least zero_grad_norm_scratch_count doubles,
  * caller-owned, contents overwritten), which one block adds in a fixed order.
  * The result does not depend on the GPU's size and is bit-reproducible.
  * Errors: EINVAL (n < 0, N outside [1, ZERO_MAX_RANKS], bad precision, NULL,

@@ -253,7 +253,8 @@ int prepare_norm(const void* const* grads, int64_t n, int32_t N, int32_t precisi
     a->grads[r] = grads[r];
   }
   a->sp = make_split(0, n, same, ph, V);
-  a->nchunks = (a->sp.nvec * V + zk::kNormChunk - 1) / zk::kNormChunk;
+  a->chunk = zk::kNormChunk;
+  a->nchunks = (a->sp.nvec * V + a->chunk - 1) / a->chunk;
   return ZERO_OK;
 }
 

@@ -478,14 +478,14 @@ struct SquareSum {
 };
 
 // Partial sums of ||mean gradient||^2. Partial c < nchunks covers the vector
-// units [c*U, (c+1)*U) with U = kNormChunk / V; partial nchunks covers the
+// units [c*U, (c+1)*U) with U = P.chunk / V; partial nchunks covers the
 // scalar head and tail. Every thread accumulates the squares of the float
 // means of its elements (SquareSum), then blocks reduce in double in a fixed
 // order, so every partial -- and the total -- is independent of the grid size.
 template <int NR, bool BF16>
 __device__ __forceinline__ double norm_chunk_sum(const NormArgs& P, int64_t c) {
   constexpr int V = BF16 ? 8 : 4;
-  constexpr int64_t U = kNormChunk / V;
+  const int64_t U = P.chunk / V;
   const int N = NR > 0 ? NR : P.N;
   const Split& sp = P.sp;
   const int64_t base = sp.lo + sp.head;
