@@ -237,3 +237,18 @@ def test_sgd_state_and_option_errors(abi, cuda):
     assert e.value.code == abi.ZERO_EINVAL
     abi.zero_step_sgd(plain.reps, plain.grads, plain.st, 1, lr=0.1)  # plain SGD is fine
     torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("prec", [oracle.FP32, oracle.BF16_MIXED])
+def test_sgd_empty_shards_and_empty_vector(abi, cuda, prec):
+    numels = [30_011, 9, 70_001]
+    n, N = int(sum(numels)), 6
+    tb = abi.zero_tensor_shard_bounds(numels, N)
+    assert any(tb[r] == tb[r + 1] for r in range(N))
+    c = SgdCase(abi, cuda, n, N, prec, "nesterov_wd", seed=51, bounds=tb)
+    for _ in range(3):
+        c.step()
+        c.compare()
+    z = SgdCase(abi, cuda, 0, 2, prec, "momentum", seed=52)
+    z.abi.zero_step_sgd(z.reps, z.grads, z.st, 1, **z.kw())
+    torch.cuda.synchronize()

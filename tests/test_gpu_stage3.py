@@ -170,3 +170,48 @@ def test_gather_rejects_bad_arguments(abi, cuda):
         abi.zero_gather([c.reps[0], c.reps[0], c.reps[2]], c.st)
     assert e.value.code == abi.ZERO_EINVAL
     abi.zero_gather(c.reps, c.st, 500, 500)  # empty range: nothing to do
+
+
+@pytest.mark.parametrize("prec", [oracle.FP32, oracle.BF16_MIXED])
+def test_owner_only_with_empty_shards(abi, cuda, prec):
+    """Fewer tensors than ranks: whole-tensor shards leave some ranks empty; the
+    owner-only step and the gather skip them."""
+    numels = [40_003, 17, 90_000]
+    n, N = int(sum(numels)), 5
+    tb = abi.zero_tensor_shard_bounds(numels, N)
+    assert tb == oracle.tensor_shard_bounds(numels, N)
+    assert any(tb[r] == tb[r + 1] for r in range(N))
+    c = Case(abi, cuda, n, N, prec, seed=41)
+    init = host_of(c.master) if c.mixed else host_of(c.reps[0])
+    c.st = abi.zero_init_states(n, N, prec, c.m, c.v, c.master,
+                                c.master.clone() if c.mixed else None, bounds=tb)
+    c.o_states = oracle.init_states(n, N, prec, master_init=init, mode="fp32", bounds=tb)
+    c.bounds = tb
+    for _ in range(2):
+        before = [host_of(x) for x in c.reps]
+        hg = c.new_grads()
+        c.t += 1
+        shards, c.o_states = oracle.zero_step(c.o_reps, hg, c.o_states, c.t, precision=prec,
+                                              mode="fp32", bounds=tb, all_gather=False, **HP)
+        abi.zero_step_ex(c.reps, c.grads, c.st, c.t, owner_only=True, **HP)
+        torch.cuda.synchronize()
+        check_owner_only(c, shards, before)
+        gather_and_check(c, shards)
+
+
+def test_owner_only_and_gather_degenerate(abi, cuda):
+    # one rank: the owner-only step is the full step, the gather has nothing to do
+    a = Case(abi, cuda, 10_007, 1, oracle.FP32, seed=42)
+    b = Case(abi, cuda, 10_007, 1, oracle.FP32, seed=42)
+    a.new_grads()
+    b.grads[0].copy_(a.grads[0])
+    abi.zero_step_ex(a.reps, a.grads, a.st, 1, owner_only=True, **HP)
+    abi.zero_step(b.reps, b.grads, b.st, 1, **HP)
+    abi.zero_gather(a.reps, a.st)
+    torch.cuda.synchronize()
+    assert torch.equal(a.reps[0], b.reps[0]) and torch.equal(a.m, b.m)
+    # n = 0: both calls accept empty buffers and do nothing
+    z = Case(abi, cuda, 0, 3, oracle.FP32, seed=43)
+    abi.zero_step_ex(z.reps, z.grads, z.st, 1, owner_only=True, **HP)
+    abi.zero_gather(z.reps, z.st)
+    torch.cuda.synchronize()
