@@ -143,10 +143,13 @@ struct PipeCfg {
 
 using DefaultPipe = PipeCfg<512, 3, 2, 224 * 1024>;
 // Shapes of the warp-specialised pipeline (compute threads, stages, output
-// buffers), measured per optimizer: three stages for the owner-only AdamW step,
-// two stages and three output buffers for SGD (5 % faster than three stages on
-// gpt2_small and fp32_320m; the shape changed the owner-only step by 1 % or less).
-using WsPipeAdamW = PipeCfg<512, 3, 2, 224 * 1024>;
+// buffers), measured per optimizer. The owner-only AdamW step computes in place
+// in three stages (no output buffers, so all of shared memory holds loads):
+// 0.253 -> 0.222 ms per stage-3 step on fp32_25m against three stages and two
+// output buffers; four in-place stages measured slower. SGD keeps two stages
+// and three output buffers (5 % faster than three stages on gpt2_small and
+// fp32_320m; its in-place shapes measured 2-6 % slower).
+using WsPipeAdamW = PipeCfg<512, 3, 0, 224 * 1024>;
 using WsPipeSgd = PipeCfg<512, 2, 3, 224 * 1024>;
 
 // KS fp32 state streams besides the parameter / master (AdamW 2, momentum
@@ -259,15 +262,20 @@ __device__ __forceinline__ void run_pipeline(PipeState<Cfg::kStages>& ps, int64_
 
 // ------------------------------------------------- warp-specialised pipeline --
 //
-// Used by the kernels with output buffers. Thread 0 issues the bulk loads,
-// thread 32 issues the bulk stores, and warps 2.. (Cfg::kThreads threads)
-// compute. The roles hand tiles over through mbarriers instead of block-wide
-// barriers, so neither the issue of copies nor the wait for stores to drain
-// holds up the arithmetic of the next tile:
+// Thread 0 issues the bulk loads, thread 32 issues the bulk stores, and warps
+// 2.. (Cfg::kThreads threads) compute. The roles hand tiles over through
+// mbarriers instead of block-wide barriers, so neither the issue of copies nor
+// the wait for stores to drain holds up the arithmetic of the next tile.
+// With output buffers (OB >= 2):
 //   full[s]   the loads of stage s landed           (producer's arrive + bytes)
 //   empty[s]  the compute threads are done with s   (one arrival per warp)
 //   ready[o]  output buffer o is written            (one arrival per warp)
 //   free_[o]  the stores of buffer o have read it   (storer)
+// In place (OB == 0: results overwrite the stage, so all of shared memory can
+// hold loads):
+//   full[s]   as above
+//   ready[s]  the results in stage s are written    (one arrival per warp)
+//   empty[s]  the stores of stage s have read it    (storer)
 // Tile k uses stage k % S and output buffer k % OB; each barrier completes one
 // phase per use, so the parity of use u is u & 1.
 constexpr int kWsExtraThreads = 64;
@@ -276,8 +284,8 @@ template <int S, int OB>
 struct PipeStateWS {
   uint64_t full[S];
   uint64_t empty[S];
-  uint64_t ready[OB];
-  uint64_t free_[OB];
+  uint64_t ready[OB > 0 ? OB : S];
+  uint64_t free_[OB > 0 ? OB : 1];  // unused in place
   int owner[S];  // fp32 step: owner of the whole tile, -1 if it straddles
   volatile int abort;
 };
@@ -317,13 +325,15 @@ __device__ __forceinline__ void run_pipeline_ws(PipeStateWS<Cfg::kStages, Cfg::k
   constexpr int S = Cfg::kStages;
   constexpr int OB = Cfg::kOutBufs;
   constexpr int C = Cfg::kThreads;  // compute threads
-  static_assert(OB >= 2, "the warp-specialised pipeline needs two output buffers");
+  constexpr bool kInPlace = OB == 0;
+  static_assert(OB == 0 || OB >= 2, "in place, or at least two output buffers");
   static_assert(C % 32 == 0, "whole compute warps");
   const int tid = threadIdx.x;
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&ps.full[s], 1);
-      mbar_init(&ps.empty[s], C / 32);
+      mbar_init(&ps.empty[s], kInPlace ? 1 : C / 32);
+      if constexpr (kInPlace) mbar_init(&ps.ready[s], C / 32);
     }
     for (int o = 0; o < OB; ++o) {
       mbar_init(&ps.ready[o], C / 32);
@@ -352,30 +362,46 @@ __device__ __forceinline__ void run_pipeline_ws(PipeStateWS<Cfg::kStages, Cfg::k
     }
   } else if (warp == 1) {
     for (int64_t k = 0; k < my_tiles; ++k) {
-      const int s = int(k % S), o = int(k % OB);
+      const int s = int(k % S);
+      const int o = kInPlace ? 0 : int(k % (OB > 0 ? OB : 1));
       int ok = 1;
       if (lane == 0) {
-        ok = role_wait(ps, &ps.ready[o], uint32_t((k / OB) & 1), wait_ns);
-        if (ok) {
-          issue_store(k, s, o);
-          bulk_wait_read_keep<OB - 1>();  // tile k - OB + 1 has been read out
-          if (k - OB + 1 >= 0) mbar_arrive(&ps.free_[(k - OB + 1) % OB]);
+        if constexpr (kInPlace) {
+          ok = role_wait(ps, &ps.ready[s], uint32_t((k / S) & 1), wait_ns);
+          if (ok) {
+            issue_store(k, s, o);
+            bulk_wait_read_keep<0>();  // the stores have read the stage: reload it
+            mbar_arrive(&ps.empty[s]);
+          }
+        } else {
+          ok = role_wait(ps, &ps.ready[o], uint32_t((k / OB) & 1), wait_ns);
+          if (ok) {
+            issue_store(k, s, o);
+            bulk_wait_read_keep<(OB > 0 ? OB - 1 : 0)>();  // tile k - OB + 1 read out
+            if (k - OB + 1 >= 0) mbar_arrive(&ps.free_[(k - OB + 1) % OB]);
+          }
         }
       }
       if (!__shfl_sync(0xffffffffu, ok, 0)) break;
     }
   } else {
     for (int64_t k = 0; k < my_tiles; ++k) {
-      const int s = int(k % S), o = int(k % OB);
+      const int s = int(k % S);
+      const int o = kInPlace ? 0 : int(k % (OB > 0 ? OB : 1));
       int ok = role_wait(ps, &ps.full[s], uint32_t((k / S) & 1), wait_ns);
-      if (ok && k >= OB) ok = role_wait(ps, &ps.free_[o], uint32_t((k / OB - 1) & 1), wait_ns);
+      if (!kInPlace && ok && k >= OB)
+        ok = role_wait(ps, &ps.free_[o], uint32_t((k / (OB > 0 ? OB : 1) - 1) & 1), wait_ns);
       if (!__all_sync(0xffffffffu, ok)) break;
       compute(k, s, o);
-      fence_proxy_async_smem();  // this thread's writes to buffer o, seen by the bulk stores
+      fence_proxy_async_smem();  // this thread's results, seen by the bulk stores
       __syncwarp();              // the warp's reads of stage s and writes are done
       if (lane == 0) {
-        mbar_arrive(&ps.empty[s]);
-        mbar_arrive(&ps.ready[o]);
+        if constexpr (kInPlace) {
+          mbar_arrive(&ps.ready[s]);
+        } else {
+          mbar_arrive(&ps.empty[s]);
+          mbar_arrive(&ps.ready[o]);
+        }
       }
     }
   }
