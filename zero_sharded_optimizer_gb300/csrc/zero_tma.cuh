@@ -699,14 +699,16 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
 
 // ------------------------------------------------------- stage-3 all-gather --
 
-// Tiles of 32 KB (8192 fp32 or 16384 bf16 elements), six stages, results
-// stored straight from the stage (no compute on the data).
-using GatherPipe = PipeCfg<128, 6, 0, 192 * 1024>;
+// Tiles of 16 KB (4096 fp32 or 8192 bf16 elements), twelve stages, results
+// stored straight from the stage (no compute on the data). Measured against
+// 32 KB x 6 and 64 KB x 3: the same on fp32_25m, 9 % and 25 % faster on
+// gpt2_small (seven replicas written per tile).
+using GatherPipe = PipeCfg<128, 12, 0, 192 * 1024>;
 
 template <bool BF16>
 struct GatherTile {
   static constexpr int kEB = BF16 ? 2 : 4;
-  static constexpr uint32_t kTileBytes = 32768;
+  static constexpr uint32_t kTileBytes = 16384;
   static constexpr int T = int(kTileBytes) / kEB;
   static constexpr uint32_t kSmem = GatherPipe::kStages * kTileBytes;
 };
