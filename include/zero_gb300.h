@@ -334,9 +334,14 @@ int zero_step_bucketed(void *const *params, const void *const *grads, zero_state
  *   on `d2h`     (host_params_out not NULL) the copy of the updated
  *                params[0][lo:hi] -> host_params_out[lo:hi].
  * Copies in both directions overlap the step of other chunks. The copies start
- * after everything already queued on `compute`, and `compute` completes only
- * after the last chunk reached host_params_out, so synchronizing `compute`
- * covers the whole call.
+ * after everything already queued on `compute`; but when the step launches on
+ * this handle since the previous call of this function were only that call's
+ * own, with the same chunk size and staging buffers, the copy of chunk k waits
+ * only for that call's step on chunk k, so back-to-back calls overlap. (The
+ * staging buffers belong to these calls: nothing else may use them between
+ * two such calls except through a step on this handle.) `compute` completes
+ * only after the last chunk reached host_params_out, so synchronizing
+ * `compute` covers the whole call.
  *   host_grads      : N HOST buffers of n elements, read-only (pinned memory
  *                     for asynchronous copies).
  *   staging         : N DEVICE buffers of n elements; they receive the

@@ -424,6 +424,41 @@ def test_step_from_host_mixed_matches_device(abi, cuda):
 
 
 @pytest.mark.parametrize("prec", [oracle.FP32, oracle.BF16_MIXED])
+def test_host_steps_back_to_back_match_device(abi, cuda, prec):
+    """Host-input steps queued without synchronizing: each chunk's copy of the
+    next call overlaps the previous call's tail, waiting only for that call's
+    step on the chunk. A device step in between breaks the chain (the copies
+    then wait for everything on the stream). Bitwise equal to device steps."""
+    from zero_sharded_optimizer_gb300.optimizer import ZeroOptimizer
+    n, N = 300_007, 4
+    mixed = prec == oracle.BF16_MIXED
+    dt = torch.bfloat16 if mixed else torch.float32
+    rng = np.random.default_rng(24)
+    init = torch.from_numpy(rng.normal(0, 0.02, n).astype(np.float32))
+    kw = dict(precision=prec, lr=1e-3, weight_decay=0.01, master_init=init if mixed else None)
+    a, b = ZeroOptimizer(n, N, **kw), ZeroOptimizer(n, N, **kw)
+    pa = [init.to(cuda).to(dt) for _ in range(N)]
+    pb = [p.clone() for p in pa]
+    hosts = [[torch.from_numpy(rng.normal(0, 1e-3, n).astype(np.float32)).to(dt).pin_memory()
+              for _ in range(N)] for _ in range(6)]
+    outs = [torch.empty(n, dtype=dt).pin_memory() for _ in range(6)]
+    for k, host in enumerate(hosts):
+        if k == 3:  # a device step between host steps
+            a.step(pa, [h.to(cuda) for h in host])
+        else:
+            a.step(pa, host, host_params_out=outs[k], chunk_bytes=64 * 1024)
+        b.step(pb, [h.to(cuda) for h in host])
+        if k != 3:
+            outs[k] = (outs[k], pb[0].clone())  # expected value, kept on the device
+    torch.cuda.synchronize()
+    assert all(torch.equal(x, y) for x, y in zip(pa, pb))
+    for k in range(6):
+        if k != 3:
+            got, ref = outs[k]
+            assert torch.equal(got, ref.cpu()), f"host copy of step {k}"
+
+
+@pytest.mark.parametrize("prec", [oracle.FP32, oracle.BF16_MIXED])
 def test_pipeline_wait_timeout_is_reported_and_recoverable(abi, cuda, prec):
     """A 1 ns bound on the bulk-copy waits makes every pipeline give up at its
     first wait: the kernel records ZERO_STATUS_WAIT_TIMEOUT, drains its own

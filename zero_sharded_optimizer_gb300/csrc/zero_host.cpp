@@ -30,6 +30,15 @@ struct zero_states {
   // Events of the host-input pipeline (created on first use, reused by later
   // calls, destroyed with the handle).
   std::vector<cudaEvent_t> events;
+  // Step launches on this handle so far, and the chunking of the last
+  // host-input call with the launch count right after it: when nothing else
+  // was launched since, the next host-input call with the same chunking and
+  // staging buffers may start copying a chunk as soon as the previous call's
+  // step on that chunk is done.
+  uint64_t launches = 0;
+  uint64_t host_launches = ~uint64_t(0);
+  int64_t host_B = 0;
+  std::vector<void*> host_staging;
 };
 
 namespace {
@@ -192,9 +201,10 @@ int prepare_step(void* const* params, const void* const* grads, const zero_state
   return ZERO_OK;
 }
 
-int launch_range(zk::StepArgs& a, const zero_states* st, bool vector_ok, int phase, int64_t lo,
+int launch_range(zk::StepArgs& a, zero_states* st, bool vector_ok, int phase, int64_t lo,
                  int64_t hi, cudaStream_t s, zk::Opt opt = zk::Opt::AdamW) {
   if (hi <= lo) return ZERO_OK;
+  ++st->launches;
   const bool mixed = st->precision == ZERO_BF16_MIXED;
   a.sp = make_split(lo, hi, vector_ok, phase, mixed ? 8 : 4);
   cudaError_t e = zk::launch_step(a, mixed, opt, s);
@@ -802,28 +812,37 @@ int zero_step_from_host(void* const* params, const void* const* host_grads, void
   cudaStream_t ds = reinterpret_cast<cudaStream_t>(d2h);
   cudaEvent_t* ev = st->events.data();
   auto ck = [&](cudaError_t ce, const char* what) { return ce == cudaSuccess ? 0 : cuda_fail(ce, what); };
-  // Copies start after everything already queued on `compute` (the previous
-  // step may still read the staging buffers or write the replicas).
-  if (int e = ck(cudaEventRecord(ev[0], cs), "cudaEventRecord")) return e;
-  if (int e = ck(cudaStreamWaitEvent(hs, ev[0], 0), "cudaStreamWaitEvent")) return e;
-  if (host_params_out)
-    if (int e = ck(cudaStreamWaitEvent(ds, ev[0], 0), "cudaStreamWaitEvent")) return e;
+  // Chained: the previous step launches on this handle were the previous call
+  // of this kind, with the same chunks and staging buffers. Then the copy of
+  // chunk k only has to wait for that call's step on chunk k (event done[k]),
+  // and the copies overlap the tail of that call (its last steps and its
+  // copies back). Otherwise the copies start after everything already queued
+  // on `compute`.
+  const bool chained = st->host_launches == st->launches && st->host_B == B &&
+                       st->host_staging.size() == size_t(N) &&
+                       std::equal(staging, staging + N, st->host_staging.begin());
+  if (!chained) {
+    if (int e = ck(cudaEventRecord(ev[0], cs), "cudaEventRecord")) return e;
+    if (int e = ck(cudaStreamWaitEvent(hs, ev[0], 0), "cudaStreamWaitEvent")) return e;
+  }
   for (int64_t k = 0; k < count; ++k) {
     const int64_t lo = k * B, hi = std::min<int64_t>(n, lo + B);
     const size_t off = size_t(lo) * es, bytes = size_t(hi - lo) * es;
+    cudaEvent_t in_ready = ev[2 + 2 * k], done = ev[3 + 2 * k];
+    if (chained)  // the previous call's step on this chunk has read its staging
+      if (int e = ck(cudaStreamWaitEvent(hs, done, 0), "cudaStreamWaitEvent")) return e;
     for (int32_t r = 0; r < N; ++r) {
       cudaError_t ce = cudaMemcpyAsync(static_cast<char*>(staging[r]) + off,
                                        static_cast<const char*>(host_grads[r]) + off, bytes,
                                        cudaMemcpyHostToDevice, hs);
       if (ce != cudaSuccess) return cuda_fail(ce, "host-to-device copy of a gradient chunk");
     }
-    cudaEvent_t in_ready = ev[2 + 2 * k], out_ready = ev[3 + 2 * k];
     if (int e = ck(cudaEventRecord(in_ready, hs), "cudaEventRecord")) return e;
     if (int e = ck(cudaStreamWaitEvent(cs, in_ready, 0), "cudaStreamWaitEvent")) return e;
     if (int e = launch_range(a, st, vec, phase, lo, hi, cs)) return e;
+    if (int e = ck(cudaEventRecord(done, cs), "cudaEventRecord")) return e;
     if (host_params_out) {
-      if (int e = ck(cudaEventRecord(out_ready, cs), "cudaEventRecord")) return e;
-      if (int e = ck(cudaStreamWaitEvent(ds, out_ready, 0), "cudaStreamWaitEvent")) return e;
+      if (int e = ck(cudaStreamWaitEvent(ds, done, 0), "cudaStreamWaitEvent")) return e;
       cudaError_t ce = cudaMemcpyAsync(static_cast<char*>(host_params_out) + off,
                                        static_cast<const char*>(params[0]) + off, bytes,
                                        cudaMemcpyDeviceToHost, ds);
@@ -835,6 +854,9 @@ int zero_step_from_host(void* const* params, const void* const* host_grads, void
     if (int e = ck(cudaEventRecord(ev[1], ds), "cudaEventRecord")) return e;
     if (int e = ck(cudaStreamWaitEvent(cs, ev[1], 0), "cudaStreamWaitEvent")) return e;
   }
+  st->host_launches = st->launches;
+  st->host_B = B;
+  st->host_staging.assign(staging, staging + N);
   return ZERO_OK;
 }
 
