@@ -35,6 +35,7 @@ import numpy as np  # noqa: E402
 from zero_sharded_optimizer_gb300 import inputs  # noqa: E402
 
 METRIC = "ZeRO step params/s at N ranks on 1 GB300; achieved HBM GB/s vs peak"
+METRIC_DDP = "DDP all_reduce(mean) params/s at N ranks on 1 GB300; achieved HBM GB/s vs peak"
 UNIT = "params/s"
 DEFAULT_WORKLOAD = "fp32_25m"
 KERNEL_SRCS = [os.path.join(ROOT, "zero_sharded_optimizer_gb300", "csrc", f)
@@ -189,8 +190,10 @@ class ClockSampler:
 
 # ------------------------------------------------------------ cpu baseline --
 
-def oracle_sample_rate(wl, seconds: float, sample_n: int | None = None, steps: int | None = None):
-    """Time the fp32-mirror oracle's ZeRO step on a sample of the workload.
+def oracle_sample_rate(wl, seconds: float, sample_n: int | None = None, steps: int | None = None,
+                       op: str = "step"):
+    """Time the fp32-mirror oracle's ZeRO step (or, with op "ddp_mean", its DDP
+    gradient mean) on a sample of the workload.
 
     The sample is `sample_n` consecutive parameters with all N ranks (the step
     is elementwise, so any slice is a faithful sub-problem). Returns
@@ -211,18 +214,22 @@ def oracle_sample_rate(wl, seconds: float, sample_n: int | None = None, steps: i
     t = 0
     while True:
         t += 1
-        reps, states = oracle.zero_step(reps, grads, states, t, **hp)
+        if op == "ddp_mean":
+            oracle.allreduce_mean(grads, wl.precision, mode="fp32")
+        else:
+            reps, states = oracle.zero_step(reps, grads, states, t, **hp)
         el = time.perf_counter() - t0
         if (steps is not None and t >= steps) or (steps is None and el >= seconds):
             break
     return k * t / el, t, k, el
 
 
-def cpu_baseline(wl, seconds: float = 12.0) -> dict:
-    rate, steps, k, el = oracle_sample_rate(wl, seconds)
+def cpu_baseline(wl, seconds: float = 12.0, op: str = "step") -> dict:
+    rate, steps, k, el = oracle_sample_rate(wl, seconds, op=op)
+    what = "DDP means" if op == "ddp_mean" else "steps"
     return {"value": rate, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"{steps} oracle steps (fp32-mirror numpy, one thread) on {k:,} consecutive "
-                      f"parameters x {wl.N} ranks of {wl.name}; {el:.1f} s"}
+            "sample": f"{steps} oracle {what} (fp32-mirror numpy, one thread) on {k:,} "
+                      f"consecutive parameters x {wl.N} ranks of {wl.name}; {el:.1f} s"}
 
 
 # --------------------------------------------------------------- GPU arm --
@@ -256,7 +263,8 @@ def run_gpu(args, wl, rank: int, world: int, local_rank: int) -> dict | None:
                         momentum=0.9 if args.optimizer == "sgd" else 0.0)
     del init
     stage3 = args.stage == 3
-    bucketed = wl.bucket_bytes > 0
+    ddp = args.op == "ddp_mean"
+    bucketed = wl.bucket_bytes > 0 and not ddp
     launches_per_step = len(opt.bucket_ranges(wl.bucket_bytes)) if bucketed else 1
     if clip:
         launches_per_step = 3       # norm partials, norm total, clipped step
@@ -265,7 +273,9 @@ def run_gpu(args, wl, rank: int, world: int, local_rank: int) -> dict | None:
     stream = torch.cuda.current_stream()
 
     def one_step():
-        if bucketed:
+        if ddp:
+            abi.ddp_allreduce_mean(grads, wl.precision, n)
+        elif bucketed:
             opt.step_bucketed(reps, grads, None, stream, wl.bucket_bytes)
         else:
             opt.step(reps, grads)
@@ -309,14 +319,26 @@ def run_gpu(args, wl, rank: int, world: int, local_rank: int) -> dict | None:
         h.copy_(g)
         host_grads.append(h)
     host_out = torch.empty(n, dtype=reps[0].dtype, pin_memory=True)
+    if ddp:
+        host_out = torch.empty(n, dtype=grads[0].dtype, pin_memory=True)
+
+    def e2e_step():
+        if ddp:  # gradients in, the mean gradient out
+            for g, h in zip(grads, host_grads):
+                g.copy_(h, non_blocking=True)
+            abi.ddp_allreduce_mean(grads, wl.precision, n)
+            host_out.copy_(grads[0], non_blocking=True)
+        else:
+            opt.step(reps, host_grads, host_params_out=host_out)
+
     for _ in range(2):
-        opt.step(reps, host_grads, host_params_out=host_out)
+        e2e_step()
     barrier()
     e_begin = torch.cuda.Event(enable_timing=True)
     e_end = torch.cuda.Event(enable_timing=True)
     e_begin.record(stream)
     for _ in range(K_e):
-        opt.step(reps, host_grads, host_params_out=host_out)
+        e2e_step()
     e_end.record(stream)
     barrier()
     e_ms = max_over_ranks([e_begin.elapsed_time(e_end) / K_e], dev, world)[0]
@@ -324,14 +346,18 @@ def run_gpu(args, wl, rank: int, world: int, local_rank: int) -> dict | None:
     e2e = {"value": whole_job_rate(n, world, e_ms), "unit": UNIT,
            "h2d_bytes_per_step": N * n * es, "d2h_bytes_per_step": n * es,
            "ms_per_step": e_ms, "steps": K_e,
-           "path": "ZeroOptimizer.step with pinned host gradients -> zero_step_from_host: "
-                   "25 MiB chunks, H2D on a copy stream, the step per chunk on the compute "
-                   "stream, D2H of one updated replica on a second copy stream"}
+           "path": ("pinned host gradients copied in, ddp_allreduce_mean, the mean of rank 0 "
+                    "copied out, all on the current stream") if ddp else
+                   ("ZeroOptimizer.step with pinned host gradients -> zero_step_from_host: "
+                    "25 MiB chunks, H2D on a copy stream, the step per chunk on the compute "
+                    "stream, D2H of one updated replica on a second copy stream")}
 
     if rank != 0:
         return None
     peak, peak_kind = load_peaks()
     step_bytes = n * bytes_per_param(wl)
+    if ddp:  # read and write every rank's gradient once
+        step_bytes = 2 * N * n * (2 if mixed else 4)
     sgd = args.optimizer == "sgd"
     if sgd:  # one fp32 buffer (read + write) instead of m and v
         step_bytes -= n * 8
@@ -341,12 +367,12 @@ def run_gpu(args, wl, rank: int, world: int, local_rank: int) -> dict | None:
         step_bytes += n * (2 if mixed else 4)
     achieved = step_bytes / (kernel_ms / 1e3) / 1e9
     traffic = traffic_per_launch(wl.name)
-    if traffic is not None and (bucketed or clip or stage3 or sgd):
+    if traffic is not None and (bucketed or clip or stage3 or sgd or ddp):
         traffic = None
     whole = clip or stage3  # the roofline covers the whole step (several kernels)
     per = 1 if whole else launches_per_step
     line = {
-        "metric": METRIC,
+        "metric": METRIC_DDP if ddp else METRIC,
         "value": whole_job_rate(n, world, ms_step),
         "unit": UNIT,
         "n_gpus": world,
@@ -363,6 +389,8 @@ def run_gpu(args, wl, rank: int, world: int, local_rank: int) -> dict | None:
                                  **({"max_grad_norm": args.max_grad_norm} if clip else {}),
                                  **({"zero_stage": 3} if stage3 else {}),
                                  **({"optimizer": "momentum SGD (0.9)"} if sgd else {}),
+                                 **({"op": "ddp_allreduce_mean (no optimizer step)"} if ddp
+                                    else {}),
                                  "partition": ("whole tensors (" + ", ".join(
                                      str(int(b2 - b1)) for b1, b2 in zip(bounds, bounds[1:])) +
                                      " params per rank)") if bounds else "np.array_split"}),
@@ -372,7 +400,9 @@ def run_gpu(args, wl, rank: int, world: int, local_rank: int) -> dict | None:
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs, copy "
                                     f"bandwidth)" if peak_kind == "measured" else "fallback",
                      "algorithmic_bytes_per_launch": step_bytes // per,
-                     "kernel": ("grad_norm_partials_kernel + grad_norm_total_kernel + "
+                     "kernel": ("allreduce_mean_tma_kernel" if wl.N <= 8 else
+                                "allreduce_mean_kernel") if ddp else
+                               ("grad_norm_partials_kernel + grad_norm_total_kernel + "
                                 "zero_step_tma_kernel (whole clipped step)") if clip else
                                ("zero_step_tma_kernel (owner-only) + gather_tma_kernel "
                                 "(whole stage-3 step)") if stage3 else
@@ -383,7 +413,7 @@ def run_gpu(args, wl, rank: int, world: int, local_rank: int) -> dict | None:
         "e2e": e2e,
     }
     if args.cpu_baseline and world == 1:
-        line["cpu_baseline"] = cpu_baseline(wl)
+        line["cpu_baseline"] = cpu_baseline(wl, op=args.op)
     return line
 
 
@@ -392,18 +422,20 @@ def run_gpu(args, wl, rank: int, world: int, local_rank: int) -> dict | None:
 def run_reference(args, wl, world: int) -> dict:
     K, W = args.steps, args.warmup
     # calibrate, then size each step's sample so the whole run stays near a minute
-    rate, _, _, _ = oracle_sample_rate(wl, 0.0, sample_n=min(wl.n, 1 << 18), steps=3)
+    op = args.op
+    rate, _, _, _ = oracle_sample_rate(wl, 0.0, sample_n=min(wl.n, 1 << 18), steps=3, op=op)
     budget_s = 60.0
     k = int(min(wl.n, max(4096, rate * budget_s / max(K + W, 1))))
     if W:
-        oracle_sample_rate(wl, 0.0, sample_n=k, steps=W)
-    rate, steps, k, el = oracle_sample_rate(wl, 0.0, sample_n=k, steps=K)
+        oracle_sample_rate(wl, 0.0, sample_n=k, steps=W, op=op)
+    rate, steps, k, el = oracle_sample_rate(wl, 0.0, sample_n=k, steps=K, op=op)
     ms = el / steps * 1e3
     sample = (f"each step: the fp32-mirror oracle (numpy, one thread) on {k:,} consecutive "
-              f"parameters x {wl.N} ranks of {wl.name}")
+              f"parameters x {wl.N} ranks of {wl.name}"
+              + ("; the DDP mean only" if op == "ddp_mean" else ""))
     return {
         "impl": "reference",
-        "metric": METRIC,
+        "metric": METRIC_DDP if op == "ddp_mean" else METRIC,
         "value": rate,
         "unit": UNIT,
         "n_gpus": world,
@@ -438,6 +470,8 @@ def main(argv=None):
                     help="> 0: sharded global-norm clipping before every step (norm pass + step)")
     ap.add_argument("--optimizer", default="adamw", choices=["adamw", "sgd"],
                     help="sgd: momentum SGD (momentum 0.9, the workload's lr and decay)")
+    ap.add_argument("--op", default="step", choices=["step", "ddp_mean"],
+                    help="ddp_mean: time ddp_allreduce_mean on the workload's gradients instead")
     ap.add_argument("--stage", type=int, default=2, choices=[2, 3],
                     help="3: owner-only step, then the gather of the full parameters (2 launches)")
     args = ap.parse_args(argv)
