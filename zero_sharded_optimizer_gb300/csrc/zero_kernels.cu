@@ -825,7 +825,7 @@ cudaError_t launch_step_tma(const StepArgs& a, cudaStream_t s) {
   return launch_step_cfg<NR, MIXED, O, true, Ws>(a, s);
 }
 
-template <int NR, bool BF16, class Cfg = DefaultPipe>
+template <int NR, bool BF16, class Cfg = MeanPipe>
 cudaError_t launch_mean_tma(const AllreduceArgs& a, cudaStream_t s) {
   using G = MeanTile<NR, BF16, Cfg>;
   const int64_t nelem = a.sp.nvec * (BF16 ? 8 : 4);
