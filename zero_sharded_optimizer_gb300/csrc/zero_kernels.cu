@@ -816,10 +816,24 @@ cudaError_t launch_step_cfg(const StepArgs& a, cudaStream_t s) {
       a, G::kSmem, (nelem + G::T - 1) / G::T, s, a.dependent != 0);
 }
 
+// Measured choice for the AdamW step with its all-gather. bf16-mixed: three
+// stages and two output buffers (1-1.3 % faster than in place at N = 4 and 8).
+// fp32: in place (InPlacePipe) where it measured faster -- N >= 5, where output
+// buffers would shrink the tile (N = 8: 16 % faster), and ranges of at least
+// kInPlaceMinElems elements (N = 4: 3-8 % faster at 50M-480M); at 25M elements
+// and N <= 4 the output buffers measured 0-1.5 % faster.
+constexpr int64_t kInPlaceMinElems = 48 * 1000 * 1000;
+
 template <int NR, bool MIXED, Opt O>
 cudaError_t launch_step_tma(const StepArgs& a, cudaStream_t s) {
   if constexpr (O == Opt::AdamW) {
-    if (!a.owner_only) return launch_step_cfg<NR, MIXED, O, false, DefaultPipe>(a, s);
+    if (!a.owner_only) {
+      if constexpr (!MIXED) {
+        if (NR >= 5 || a.sp.nvec * 4 >= kInPlaceMinElems)
+          return launch_step_cfg<NR, MIXED, O, false, InPlacePipe>(a, s);
+      }
+      return launch_step_cfg<NR, MIXED, O, false, DefaultPipe>(a, s);
+    }
   }
   using Ws = typename std::conditional<O == Opt::AdamW, WsPipeAdamW, WsPipeSgd>::type;
   return launch_step_cfg<NR, MIXED, O, true, Ws>(a, s);

@@ -142,6 +142,10 @@ struct PipeCfg {
 };
 
 using DefaultPipe = PipeCfg<512, 3, 2, 224 * 1024>;
+// The same loop computing in place in three stages: for the fp32 step with its
+// all-gather when the output buffers would cost tile size (N >= 5) or the range
+// is large (see launch_step_tma).
+using InPlacePipe = PipeCfg<512, 3, 0, 224 * 1024>;
 // Shapes of the warp-specialised pipeline (compute threads, stages, output
 // buffers), measured per optimizer. The owner-only AdamW step computes in place
 // in three stages (no output buffers, so all of shared memory holds loads):
