@@ -816,18 +816,27 @@ cudaError_t launch_step_cfg(const StepArgs& a, cudaStream_t s) {
       a, G::kSmem, (nelem + G::T - 1) / G::T, s, a.dependent != 0);
 }
 
-// Measured choice for the AdamW step with its all-gather. bf16-mixed: three
-// stages and two output buffers (1-1.3 % faster than in place at N = 4 and 8).
-// fp32: in place (InPlacePipe) where it measured faster -- N >= 5, where output
-// buffers would shrink the tile (N = 8: 16 % faster), and ranges of at least
-// kInPlaceMinElems elements (N = 4: 3-8 % faster at 50M-480M); at 25M elements
-// and N <= 4 the output buffers measured 0-1.5 % faster.
+// Measured choice for the AdamW step with its all-gather (GB/s over N = 1..8
+// at 25M and 100M elements, both precisions):
+//  * N = 1 runs the register-streaming kernel (launch_step_t), 35-44 % faster
+//    than either bulk-copy loop: a tile of two gradient streams is too little
+//    work per tile;
+//  * fp32 N = 2-3 and bf16-mixed N = 2-7: the warp-specialised loop in place,
+//    2-20 % faster than lock-step (most at N = 2);
+//  * fp32 N >= 4: lock-step, in place (InPlacePipe) for N >= 5, where output
+//    buffers would shrink the tile (N = 8: 16 % faster), and for ranges of at
+//    least kInPlaceMinElems elements (N = 4: 3-8 % faster at 50M-480M); with
+//    output buffers (DefaultPipe) at N = 4 below that, 0-1.5 % faster at 25M;
+//  * bf16-mixed N = 8: lock-step with output buffers (4-6 % faster
+//    than the warp-specialised loop, 1-1.3 % faster than lock-step in place).
 constexpr int64_t kInPlaceMinElems = 48 * 1000 * 1000;
 
 template <int NR, bool MIXED, Opt O>
 cudaError_t launch_step_tma(const StepArgs& a, cudaStream_t s) {
   if constexpr (O == Opt::AdamW) {
     if (!a.owner_only) {
+      if constexpr (MIXED ? NR <= 7 : NR <= 3)
+        return launch_step_cfg<NR, MIXED, O, true, WsPipeAdamW>(a, s);
       if constexpr (!MIXED) {
         if (NR >= 5 || a.sp.nvec * 4 >= kInPlaceMinElems)
           return launch_step_cfg<NR, MIXED, O, false, InPlacePipe>(a, s);
@@ -851,7 +860,10 @@ cudaError_t launch_mean_tma(const AllreduceArgs& a, cudaStream_t s) {
 // is a vector body); the register-streaming kernel for any other case.
 template <bool MIXED, Opt O>
 cudaError_t launch_step_t(const StepArgs& a, cudaStream_t s) {
-  if (a.sp.nvec > 0) {
+  // one rank's AdamW step with all-gather streams through registers (measured
+  // faster there; see launch_step_tma)
+  const bool one_rank_full = O == Opt::AdamW && a.N == 1 && !a.owner_only;
+  if (a.sp.nvec > 0 && !one_rank_full) {
     switch (a.N) {
       case 1: return launch_step_tma<1, MIXED, O>(a, s);
       case 2: return launch_step_tma<2, MIXED, O>(a, s);
