@@ -939,11 +939,13 @@ cudaError_t launch_init(const InitArgs& a, cudaStream_t s) {
 namespace {
 template <bool BF16>
 cudaError_t launch_gather_t(const GatherArgs& a, cudaStream_t s) {
-  // The bulk-copy pipeline when the replicas share a 16-byte phase and N >= 4.
-  // With two or three replicas a tile carries only one or two stores, and
-  // register streaming measured faster: 0.96 vs 0.81 of the copy peak (fp32
-  // N = 2), 0.93 vs 0.69 (bf16 N = 2), 0.86 vs 0.68 (bf16 N = 3).
-  if (a.sp.nvec > 0 && a.N >= 4) {
+  // The bulk-copy pipeline when the replicas share a 16-byte phase and N >= 4
+  // (bf16: N >= 5). With fewer replicas a tile carries few stores, and register
+  // streaming measured faster: 0.96 vs 0.81 of the copy peak (fp32 N = 2), 0.93
+  // vs 0.69 (bf16 N = 2), 0.86 vs 0.68 (bf16 N = 3), 0.84 vs 0.80-0.83 (bf16
+  // N = 4). Deeper store queues (2-6 tiles of stores reading their stage at
+  // once) changed nothing.
+  if (a.sp.nvec > 0 && a.N >= (BF16 ? 5 : 4)) {
     using G = GatherTile<BF16>;
     const int64_t tiles = (a.sp.nvec * (16 / G::kEB) + G::T - 1) / G::T;
     return launch_tma<gather_tma_kernel<BF16>, GatherPipe::kThreads>(a, G::kSmem, tiles, s);
