@@ -10,7 +10,11 @@
  *   3. all-gather: every rank's parameter replica receives all updated shards.
  * Shard i is np.array_split(np.arange(n), N)[i] (same page, "The shards").
  * The three steps run fused in one pass over memory; the mean gradient is
- * never stored.
+ * never stored. Around that step: whole-tensor shards, gradient-norm clipping
+ * and an accumulation factor (zero_grad_norm_sq, zero_step_ex), momentum SGD
+ * as the optimizer (zero_step_sgd), ZeRO stage 3 (owner-only steps and
+ * zero_gather), 25 MiB bucket streaming, host-memory gradients
+ * (zero_step_from_host), the DDP mean and per-stage memory accounting.
  *
  * Conventions for every call:
  *  - Return value: ZERO_OK (0) or a negative ZERO_E* code. zero_strerror()
