@@ -551,3 +551,30 @@ def test_whole_tensor_shards(abi, cuda, prec):
         a.compare(exact=True)
         for x, y in [(a.m, b.m), (a.v, b.v)] + list(zip(a.reps, b.reps)):
             assert torch.equal(x, y)
+
+
+@pytest.mark.parametrize("prec", [oracle.FP32, oracle.BF16_MIXED])
+def test_maximum_rank_count(abi, cuda, prec):
+    """N = ZERO_MAX_RANKS (64): the step, the owner-only step with its gather,
+    and the DDP mean, each against the oracle."""
+    n, N = 10_007, abi.ZERO_MAX_RANKS
+    c = Case(abi, cuda, n, N, prec, seed=64)
+    for _ in range(2):
+        c.step()
+        c.compare(exact=True)
+    hg = c.new_grads()
+    c.t += 1
+    shards, c.o_states = oracle.zero_step(c.o_reps, hg, c.o_states, c.t, precision=prec,
+                                          mode="fp32", all_gather=False, **c.hp)
+    abi.zero_step_ex(c.reps, c.grads, c.st, c.t, owner_only=True, **c.hp)
+    abi.zero_gather(c.reps, c.st)
+    torch.cuda.synchronize()
+    full = oracle.gather(shards, prec)
+    for r in range(N):
+        assert np.array_equal(host_of(c.reps[r]), full[r])
+    g = [x.clone() for x in c.grads]
+    abi.ddp_allreduce_mean(g, prec)
+    torch.cuda.synchronize()
+    ref = oracle.allreduce_mean(hg, prec, mode="fp32")
+    for r in range(N):
+        assert np.array_equal(host_of(g[r]), ref[r])
