@@ -75,7 +75,8 @@ Readings taken where the pages are silent (each is listed in the design notes):
 
 Parity status: every function here is pinned by a CPU test against values the
 pages print, closed forms, invariants or library routines (np.array_split,
-np.mean, torch.optim.Adam/AdamW, torch's bf16 cast); none is "parity unpinned".
+np.mean, torch.optim.Adam/AdamW/SGD, torch.nn.utils.clip_grad_norm_, torch's
+bf16 cast); none is "parity unpinned".
 """
 
 from __future__ import annotations
