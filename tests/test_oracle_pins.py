@@ -836,3 +836,93 @@ def test_mutant_sgd_first_step_damped(monkeypatch):
         return real(p, g, buf, t, lr, momentum, dampening, weight_decay, nesterov, mode)
     monkeypatch.setattr(zo, "_sgd", mutant)
     assert _fails(lambda: test_sgd_fp64_matches_torch_sgd(4, 0.9, 0.1, 0.01, False))
+
+
+# ---------------------------------------------------------------------------
+# Brute force on tiny inputs: one entry at a time in Python scalars
+# ---------------------------------------------------------------------------
+
+def _brute_adamw(p, gs, m, v, t, lr, b1, b2, eps, wd):
+    """One entry, Python floats (IEEE double): mean in rank order, then AdamW."""
+    g = 0.0
+    for x in gs:
+        g = g + x
+    g = g / len(gs)
+    p = p * (1.0 - lr * wd)
+    m = b1 * m + (1.0 - b1) * g
+    v = b2 * v + (1.0 - b2) * (g * g)
+    m_hat = m / (1.0 - b1 ** t)
+    v_hat = v / (1.0 - b2 ** t)
+    return p - lr * m_hat / (math.sqrt(v_hat) + eps), m, v
+
+
+def _brute_adamw_f32(p, gs, m, v, c):
+    """One entry in float32 scalars, one rounding per written operation."""
+    f = np.float32
+    g = f(gs[0])
+    for x in gs[1:]:
+        g = f(g + f(x))
+    g = f(g / f(len(gs)))
+    p = f(p * c["decay"])
+    m = f(f(c["b1"] * m) + f(c["omb1"] * g))
+    v = f(f(c["b2"] * v) + f(c["omb2"] * f(g * g)))
+    d = f(f(np.sqrt(v) / c["bc2s"]) + c["eps"])
+    return f(p - f(c["step"] * f(m / d))), m, v
+
+
+@pytest.mark.parametrize("n,N", [(1, 1), (2, 3), (5, 2), (7, 5), (8, 4)])
+def test_brute_force_tiny_adamw(n, N):
+    rng = np.random.default_rng(500 + 10 * n + N)
+    lr, b1, b2, eps, wd = 3e-3, 0.9, 0.95, 1e-8, 0.05
+    p0 = rng.normal(size=n)
+    params64 = [p0.copy() for _ in range(N)]
+    params32 = [p0.astype(np.float32) for _ in range(N)]
+    s64 = oracle.init_states(n, N, mode="fp64")
+    s32 = oracle.init_states(n, N, mode="fp32")
+    bp64 = [(float(x), 0.0, 0.0) for x in p0]
+    bp32 = [(np.float32(x), np.float32(0), np.float32(0)) for x in p0.astype(np.float32)]
+    for t in range(1, 5):
+        grads = [rng.normal(size=n).astype(np.float32) for _ in range(N)]
+        params64, s64 = oracle.zero_step(params64, grads, s64, t, lr=lr, beta1=b1, beta2=b2,
+                                         eps=eps, weight_decay=wd, mode="fp64")
+        params32, s32 = oracle.zero_step(params32, grads, s32, t, lr=lr, beta1=b1, beta2=b2,
+                                         eps=eps, weight_decay=wd, mode="fp32")
+        c = oracle.mirror_scalars(t, lr, b1, b2, eps, wd)
+        bp64 = [_brute_adamw(p, [float(g[j]) for g in grads], m, v, t, lr, b1, b2, eps, wd)
+                for j, (p, m, v) in enumerate(bp64)]
+        bp32 = [_brute_adamw_f32(p, [g[j] for g in grads], m, v, c)
+                for j, (p, m, v) in enumerate(bp32)]
+        for rep in params64:   # double: the same values up to the order of the last ops
+            np.testing.assert_allclose(rep, [x[0] for x in bp64], rtol=1e-13, atol=1e-15)
+        np.testing.assert_allclose(flat_state(s64, "m"), [x[1] for x in bp64], rtol=1e-13,
+                                   atol=1e-16)
+        for rep in params32:   # fp32-mirror: bit for bit
+            assert np.array_equal(rep, np.array([x[0] for x in bp32], np.float32))
+        assert np.array_equal(flat_state(s32, "v"), np.array([x[2] for x in bp32], np.float32))
+
+
+@pytest.mark.parametrize("n,N", [(1, 1), (3, 2), (8, 5)])
+def test_brute_force_tiny_sgd(n, N):
+    rng = np.random.default_rng(600 + 10 * n + N)
+    lr, mu, damp, wd = 0.05, 0.9, 0.1, 0.01
+    p0 = rng.normal(size=n)
+    params = [p0.copy() for _ in range(N)]
+    states = oracle.init_states_sgd(n, N, mode="fp64")
+    brute = [(float(x), 0.0) for x in p0]
+    for t in range(1, 5):
+        grads = [rng.normal(size=n) for _ in range(N)]
+        params, states = oracle.zero_step_sgd(params, grads, states, t, lr=lr, momentum=mu,
+                                              dampening=damp, weight_decay=wd, mode="fp64")
+        nxt = []
+        for j, (p, b) in enumerate(brute):
+            g = 0.0
+            for gr in grads:
+                g = g + float(gr[j])
+            g = g / N + wd * p
+            b = g if t == 1 else mu * b + (1.0 - damp) * g
+            nxt.append((p - lr * b, b))
+        brute = nxt
+        for rep in params:
+            np.testing.assert_allclose(rep, [x[0] for x in brute], rtol=1e-13, atol=1e-15)
+        np.testing.assert_allclose(flat_state(states, "buf"), [x[1] for x in brute], rtol=1e-13,
+                                   atol=1e-15)
