@@ -7,22 +7,25 @@
 // ("ZeRO-Sharded Adam Step", section "The step"; "Data parallelism and ZeRO
 // stages 1 to 3", section 2, stages 1 and 2). The state is flat in global
 // index order, so the shard structure only decides whose replica holds the
-// authoritative fp32 parameter (the owner's) -- never the arithmetic.
+// authoritative fp32 parameter (the owner's) -- never the arithmetic. Variants:
+// momentum SGD in place of AdamW, and the stage-3 owner-only step (no
+// all-gather; gather_kernel / gather_tma_kernel bring the replicas back).
 //
 // The step moves 8N+20 bytes per parameter in fp32 (4N+24 in mixed precision)
-// and does ~20 flops per parameter: it is bound by HBM bandwidth. Design:
-//  * 16-byte vector loads/stores, one V-element unit per thread per iteration
-//    (V = 4 fp32, V = 8 mixed: one uint4 of bf16 + two float4 of state);
-//  * every load of a unit is issued before any arithmetic, so a thread keeps
-//    (N+3) 16-byte requests in flight; streaming cache hints (ld/st .cs) since
-//    every byte is touched exactly once per step;
-//  * grid-stride loop over units with a grid of (SMs x resident blocks);
-//  * a scalar head/tail for ranges whose ends are not on a unit boundary, and
-//    a scalar path for buffers that do not share a 16-byte phase;
-//  * arithmetic with explicitly rounded IEEE fp32 intrinsics (__fadd_rn,
-//    __fmul_rn, __fdiv_rn, __fsqrt_rn): no contraction, so the result is
-//    independent of compiler scheduling and bit-reproducible.
-// No tensor cores: there is no contraction in this step.
+// and does ~20 flops per parameter: it is bound by HBM bandwidth. Two kinds of
+// kernel run it, chosen per call in launch_step_tma / launch_step_t:
+//  * the bulk-copy (TMA) pipelines of zero_tma.cuh, for most N <= 8;
+//  * the register-streaming kernel here (zero_step_kernel), for N = 1, N > 8
+//    and buffers of mixed 16-byte phase: 16-byte vector loads/stores, one
+//    V-element unit per thread per iteration (V = 4 fp32, V = 8 mixed), every
+//    load of a unit issued before any arithmetic, streaming cache hints
+//    (ld/st .cs), a grid-stride loop over units with a grid of (SMs x resident
+//    blocks), and a scalar head/tail for ranges whose ends are not on a unit
+//    boundary.
+// Both use explicitly rounded IEEE fp32 intrinsics (__fadd_rn, __fmul_rn,
+// __fdiv_rn, __fsqrt_rn): no contraction, so the result is independent of
+// compiler scheduling and bit-reproducible, and the two kinds agree bit for
+// bit. No tensor cores: there is no contraction in this step.
 
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
