@@ -14,7 +14,7 @@
  * and an accumulation factor (zero_grad_norm_sq, zero_step_ex), momentum SGD
  * as the optimizer (zero_step_sgd), ZeRO stage 3 (owner-only steps and
  * zero_gather), 25 MiB bucket streaming, host-memory gradients
- * (zero_step_from_host), the DDP mean and per-stage memory accounting.
+ * (zero_step_from_host, zero_step_from_host_ex), the DDP mean and per-stage memory accounting.
  *
  * Conventions for every call:
  *  - Return value: ZERO_OK (0) or a negative ZERO_E* code. zero_strerror()
@@ -363,6 +363,25 @@ int zero_step_from_host(void *const *params, const void *const *host_grads,
                         double beta1, double beta2, double eps, double weight_decay,
                         void *host_params_out, int64_t chunk_bytes, zero_stream_t compute,
                         zero_stream_t h2d, zero_stream_t d2h);
+
+/* zero_step_from_host with the options of zero_step_ex (AdamW) or of
+ * zero_step_sgd (momentum SGD): exactly one of `adamw` and `sgd` is non-NULL.
+ * Their step number, hyperparameters, grad_scale and owner_only are used. The
+ * range must be the whole vector (lo = 0, hi = -1 or n) and max_grad_norm <= 0:
+ * chunks are stepped before the whole gradient has arrived, so global-norm
+ * clipping cannot run in this pipeline (copy the gradients to the device, then
+ * zero_grad_norm_sq and zero_step_ex). With owner_only (ZeRO stage 3) the
+ * replicas stay released, and host_params_out still receives the full updated
+ * parameters: each piece of a chunk is copied from its owner's replica.
+ * Otherwise as zero_step_from_host. SGD needs a state initialised for it
+ * (zero_init_states with v = NULL).
+ * Errors: as zero_step_from_host, plus EINVAL for no or both option sets, a
+ * partial range, clipping, or bad options. */
+int zero_step_from_host_ex(void *const *params, const void *const *host_grads,
+                           void *const *staging, zero_states_t *st,
+                           const zero_step_opts_t *adamw, const zero_sgd_opts_t *sgd,
+                           void *host_params_out, int64_t chunk_bytes, zero_stream_t compute,
+                           zero_stream_t h2d, zero_stream_t d2h);
 
 /* ------------------------------------------------------------------- DDP -- */
 

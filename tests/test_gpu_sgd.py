@@ -256,16 +256,21 @@ def test_sgd_empty_shards_and_empty_vector(abi, cuda, prec):
 
 @pytest.mark.parametrize("prec", [oracle.FP32, oracle.BF16_MIXED])
 def test_optimizer_sgd_and_stage3_with_host_gradients(abi, cuda, prec):
-    """ZeroOptimizer with host gradients (copied in first) equals the same
-    optimizer fed device gradients, bit for bit: momentum SGD, and stage 3
-    (owner-only step; the host copy of the parameters comes after a gather)."""
+    """ZeroOptimizer with host gradients (the chunk-pipelined host-input step)
+    equals the same optimizer fed device gradients, bit for bit: momentum SGD,
+    stage 3 (owner-only step; the host copy of the parameters takes each shard
+    from its owner and the other replica elements stay as they were), both
+    together, and AdamW with a gradient scale."""
     from zero_sharded_optimizer_gb300.optimizer import ZeroOptimizer
     n, N = 200_003, 4
     mixed = prec == oracle.BF16_MIXED
     dt = torch.bfloat16 if mixed else torch.float32
     rng = np.random.default_rng(61)
     init = torch.from_numpy(rng.normal(0, 0.02, n).astype(np.float32))
-    for kw in (dict(optimizer="sgd", momentum=0.9, nesterov=True), dict(stage=3)):
+    bounds = oracle.shard_bounds(n, N)
+    for kw in (dict(optimizer="sgd", momentum=0.9, nesterov=True), dict(stage=3),
+               dict(stage=3, optimizer="sgd", momentum=0.9), dict(grad_scale=0.25)):
+        stage3 = kw.get("stage") == 3
         common = dict(precision=prec, lr=1e-3, weight_decay=0.01,
                       master_init=init if mixed else None, **kw)
         a, b = ZeroOptimizer(n, N, **common), ZeroOptimizer(n, N, **common)
@@ -275,16 +280,21 @@ def test_optimizer_sgd_and_stage3_with_host_gradients(abi, cuda, prec):
         for _ in range(3):
             host = [torch.from_numpy(rng.normal(0, 1e-3, n).astype(np.float32)).to(dt)
                     .pin_memory() for _ in range(N)]
-            a.step(pa, host, host_params_out=out)
+            before = [p.clone() for p in pa]
+            a.step(pa, host, host_params_out=out, chunk_bytes=1 << 18)
             b.step(pb, [h.to(cuda) for h in host])
-            if kw.get("stage") == 3:
+            if stage3:
                 b.gather(pb)
             torch.cuda.synchronize()
-            assert torch.equal(out, pb[0].cpu())
-        if kw.get("stage") == 3:
-            a.gather(pa)
+            assert torch.equal(out, pb[0].cpu()), kw
+            if stage3:
+                for r in range(N):
+                    lo, hi = bounds[r], bounds[r + 1]
+                    assert torch.equal(pa[r][:lo], before[r][:lo]), (kw, r)
+                    assert torch.equal(pa[r][hi:], before[r][hi:]), (kw, r)
+                a.gather(pa)
         torch.cuda.synchronize()
-        assert all(torch.equal(x, y) for x, y in zip(pa, pb))
+        assert all(torch.equal(x, y) for x, y in zip(pa, pb)), kw
         for key in ("m", "v", "master"):
             x, y = getattr(a, key), getattr(b, key)
             assert (x is None and y is None) or torch.equal(x, y)

@@ -71,6 +71,8 @@ _SIGNATURES = {
                                           _dbl, _i64, _P(_vp), _i64, _vp, _vp, _i64]),
     "zero_step_from_host": (ctypes.c_int, [_P(_vp), _P(_vp), _P(_vp), _vp, _i64, _dbl, _dbl, _dbl,
                                            _dbl, _dbl, _vp, _i64, _vp, _vp, _vp]),
+    "zero_step_from_host_ex": (ctypes.c_int, [_P(_vp), _P(_vp), _P(_vp), _vp, _vp, _vp, _vp,
+                                              _i64, _vp, _vp, _vp]),
     "ddp_allreduce_mean": (ctypes.c_int, [_P(_vp), _i64, _i32, _i32, _vp]),
     "zero_memory_bytes": (ctypes.c_int, [_i64, _i32, _i32, _i32, _P(_u64)]),
     "zero_memory_breakdown": (ctypes.c_int, [_i64, _i32, _i32, _i32, _i32, _P(_u64)]),
@@ -445,6 +447,26 @@ def zero_step_from_host(params, host_grads, staging, st: ZeroStates, t: int, lr:
     _check(_lib.zero_step_from_host(pp, hp, sp, st.handle, t, lr, beta1, beta2, eps, weight_decay,
                                     out, chunk_bytes, _stream(compute), _stream(h2d), _stream(d2h)),
            "zero_step_from_host")
+
+
+def zero_step_from_host_ex(params, host_grads, staging, st: ZeroStates, adamw=None, sgd=None,
+                           host_params_out=None, chunk_bytes: int = 25 * 1024 * 1024,
+                           compute=None, h2d=None, d2h=None):
+    """zero_step_from_host with AdamW options (a StepOpts) or SGD options (an
+    SgdOpts): exactly one of ``adamw`` and ``sgd``."""
+    dt = _storage_dtype(st.precision)
+    if len(host_grads) != st.N or len(staging) != st.N or len(params) != st.N:
+        raise ValueError(f"need {st.N} params, host gradients and staging buffers")
+    pp = _ptr_array(params, st.n, dt, "params")
+    sp = _ptr_array(staging, st.n, dt, "staging")
+    hp = _host_ptr_array(host_grads, st.n, dt, "host_grads")
+    out = None
+    if host_params_out is not None:
+        out = _host_ptr_array([host_params_out], st.n, dt, "host_params_out")[0]
+    _check(_lib.zero_step_from_host_ex(
+        pp, hp, sp, st.handle, None if adamw is None else ctypes.byref(adamw),
+        None if sgd is None else ctypes.byref(sgd), out, chunk_bytes, _stream(compute),
+        _stream(h2d), _stream(d2h)), "zero_step_from_host_ex")
 
 
 def ddp_allreduce_mean(grads, precision: int, n: int | None = None, stream=None):

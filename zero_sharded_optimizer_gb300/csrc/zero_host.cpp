@@ -371,6 +371,65 @@ int breakdown(int64_t n, int32_t stage, int32_t precision, uint64_t s, uint64_t 
   return ZERO_OK;
 }
 
+// The multiplier of the mean gradient and, when max_grad_norm > 0, clipping.
+int fill_scale_clip(double grad_scale, double max_grad_norm, const double* norm_sq,
+                    zk::StepArgs* a) {
+  if (!std::isfinite(grad_scale) || !(grad_scale > 0.0))
+    return fail(ZERO_EINVAL, "grad_scale must be finite and > 0");
+  a->gscale = grad_scale;
+  if (max_grad_norm > 0.0) {
+    if (!std::isfinite(max_grad_norm)) return fail(ZERO_EINVAL, "max_grad_norm must be finite");
+    if (!norm_sq) return fail(ZERO_EINVAL, "clipping needs the squared norm (norm_sq)");
+    a->norm_sq = norm_sq;
+    a->max_norm = max_grad_norm;
+  }
+  return ZERO_OK;
+}
+
+// zero_step_opts_t -> StepArgs (after prepare_step).
+int fill_adamw(const zero_step_opts_t* o, zk::StepArgs* a) {
+  if (int e = adam_consts(o->t, o->lr, o->beta1, o->beta2, o->eps, o->weight_decay, &a->c))
+    return e;
+  if (int e = fill_scale_clip(o->grad_scale, o->max_grad_norm, o->norm_sq, a)) return e;
+  a->owner_only = o->owner_only != 0;
+  return ZERO_OK;
+}
+
+// Checks zero_sgd_opts_t; the kernel variant it needs.
+int sgd_opt(const zero_sgd_opts_t* o, zk::Opt* opt) {
+  if (o->t < 1) return fail(ZERO_EINVAL, "step number t=%lld must be >= 1", (long long)o->t);
+  if (!std::isfinite(o->lr) || o->lr < 0.0) return fail(ZERO_EINVAL, "lr must be finite and >= 0");
+  if (!std::isfinite(o->momentum) || o->momentum < 0.0)
+    return fail(ZERO_EINVAL, "momentum must be finite and >= 0");
+  if (!std::isfinite(o->dampening)) return fail(ZERO_EINVAL, "dampening must be finite");
+  if (!std::isfinite(o->weight_decay)) return fail(ZERO_EINVAL, "weight_decay must be finite");
+  if (o->nesterov && (o->momentum <= 0.0 || o->dampening != 0.0))
+    return fail(ZERO_EINVAL, "Nesterov momentum needs momentum > 0 and zero dampening");
+  *opt = o->momentum != 0.0 ? zk::Opt::SgdMomentum : zk::Opt::Sgd;
+  return ZERO_OK;
+}
+
+// zero_sgd_opts_t -> StepArgs (after prepare_step).
+int fill_sgd(const zero_sgd_opts_t* o, zk::StepArgs* a) {
+  a->sgd.lr = float(o->lr);
+  a->sgd.wd = float(o->weight_decay);
+  a->sgd.mu = float(o->momentum);
+  a->sgd.omd = float(1.0 - o->dampening);
+  a->sgd.wd_on = o->weight_decay != 0.0;
+  a->sgd.first = o->t == 1;
+  a->sgd.nesterov = o->nesterov != 0;
+  if (int e = fill_scale_clip(o->grad_scale, o->max_grad_norm, o->norm_sq, a)) return e;
+  a->owner_only = o->owner_only != 0;
+  return ZERO_OK;
+}
+
+int check_range(int64_t lo, int64_t hi, int64_t n) {
+  if (lo < 0 || hi < lo || hi > n)
+    return fail(ZERO_EINVAL, "range [%lld, %lld) outside [0, %lld)", (long long)lo, (long long)hi,
+                (long long)n);
+  return ZERO_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -531,20 +590,8 @@ int zero_step_ex(void* const* params, const void* const* grads, zero_states_t* s
   int phase = 0;
   if (int e = prepare_step(params, grads, st, zk::Opt::AdamW, &a, &vec, &phase)) return e;
   const int64_t lo = o->lo, hi = o->hi < 0 ? st->n : o->hi;
-  if (lo < 0 || hi < lo || hi > st->n)
-    return fail(ZERO_EINVAL, "range [%lld, %lld) outside [0, %lld)", (long long)lo, (long long)hi,
-                (long long)st->n);
-  if (int e = adam_consts(o->t, o->lr, o->beta1, o->beta2, o->eps, o->weight_decay, &a.c)) return e;
-  if (!std::isfinite(o->grad_scale) || !(o->grad_scale > 0.0))
-    return fail(ZERO_EINVAL, "grad_scale must be finite and > 0");
-  a.gscale = o->grad_scale;
-  if (o->max_grad_norm > 0.0) {
-    if (!std::isfinite(o->max_grad_norm)) return fail(ZERO_EINVAL, "max_grad_norm must be finite");
-    if (!o->norm_sq) return fail(ZERO_EINVAL, "clipping needs the squared norm (norm_sq)");
-    a.norm_sq = o->norm_sq;
-    a.max_norm = o->max_grad_norm;
-  }
-  a.owner_only = o->owner_only != 0;
+  if (int e = check_range(lo, hi, st->n)) return e;
+  if (int e = fill_adamw(o, &a)) return e;
   return launch_range(a, st, vec, phase, lo, hi, reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -590,40 +637,15 @@ int zero_step_sgd(void* const* params, const void* const* grads, zero_states_t* 
                   const zero_sgd_opts_t* o, zero_stream_t stream) {
   if (!st) return fail(ZERO_EINVAL, "state handle is NULL");
   if (!o) return fail(ZERO_EINVAL, "options are NULL");
-  if (o->t < 1) return fail(ZERO_EINVAL, "step number t=%lld must be >= 1", (long long)o->t);
-  if (!std::isfinite(o->lr) || o->lr < 0.0) return fail(ZERO_EINVAL, "lr must be finite and >= 0");
-  if (!std::isfinite(o->momentum) || o->momentum < 0.0)
-    return fail(ZERO_EINVAL, "momentum must be finite and >= 0");
-  if (!std::isfinite(o->dampening)) return fail(ZERO_EINVAL, "dampening must be finite");
-  if (!std::isfinite(o->weight_decay)) return fail(ZERO_EINVAL, "weight_decay must be finite");
-  if (o->nesterov && (o->momentum <= 0.0 || o->dampening != 0.0))
-    return fail(ZERO_EINVAL, "Nesterov momentum needs momentum > 0 and zero dampening");
-  const zk::Opt opt = o->momentum != 0.0 ? zk::Opt::SgdMomentum : zk::Opt::Sgd;
+  zk::Opt opt;
+  if (int e = sgd_opt(o, &opt)) return e;
   zk::StepArgs a;
   bool vec = false;
   int phase = 0;
   if (int e = prepare_step(params, grads, st, opt, &a, &vec, &phase)) return e;
   const int64_t lo = o->lo, hi = o->hi < 0 ? st->n : o->hi;
-  if (lo < 0 || hi < lo || hi > st->n)
-    return fail(ZERO_EINVAL, "range [%lld, %lld) outside [0, %lld)", (long long)lo, (long long)hi,
-                (long long)st->n);
-  a.sgd.lr = float(o->lr);
-  a.sgd.wd = float(o->weight_decay);
-  a.sgd.mu = float(o->momentum);
-  a.sgd.omd = float(1.0 - o->dampening);
-  a.sgd.wd_on = o->weight_decay != 0.0;
-  a.sgd.first = o->t == 1;
-  a.sgd.nesterov = o->nesterov != 0;
-  if (!std::isfinite(o->grad_scale) || !(o->grad_scale > 0.0))
-    return fail(ZERO_EINVAL, "grad_scale must be finite and > 0");
-  a.gscale = o->grad_scale;
-  if (o->max_grad_norm > 0.0) {
-    if (!std::isfinite(o->max_grad_norm)) return fail(ZERO_EINVAL, "max_grad_norm must be finite");
-    if (!o->norm_sq) return fail(ZERO_EINVAL, "clipping needs the squared norm (norm_sq)");
-    a.norm_sq = o->norm_sq;
-    a.max_norm = o->max_grad_norm;
-  }
-  a.owner_only = o->owner_only != 0;
+  if (int e = check_range(lo, hi, st->n)) return e;
+  if (int e = fill_sgd(o, &a)) return e;
   return launch_range(a, st, vec, phase, lo, hi, reinterpret_cast<cudaStream_t>(stream), opt);
 }
 
@@ -783,8 +805,40 @@ int zero_step_from_host(void* const* params, const void* const* host_grads, void
                         double eps, double weight_decay, void* host_params_out,
                         int64_t chunk_bytes, zero_stream_t compute, zero_stream_t h2d,
                         zero_stream_t d2h) {
+  zero_step_opts_t o;
+  std::memset(&o, 0, sizeof(o));
+  o.t = t;
+  o.lr = lr;
+  o.beta1 = beta1;
+  o.beta2 = beta2;
+  o.eps = eps;
+  o.weight_decay = weight_decay;
+  o.grad_scale = 1.0;
+  o.hi = -1;
+  return zero_step_from_host_ex(params, host_grads, staging, st, &o, nullptr, host_params_out,
+                                chunk_bytes, compute, h2d, d2h);
+}
+
+int zero_step_from_host_ex(void* const* params, const void* const* host_grads,
+                           void* const* staging, zero_states_t* st, const zero_step_opts_t* adamw,
+                           const zero_sgd_opts_t* sgd, void* host_params_out, int64_t chunk_bytes,
+                           zero_stream_t compute, zero_stream_t h2d, zero_stream_t d2h) {
   if (!st) return fail(ZERO_EINVAL, "state handle is NULL");
   if (!host_grads) return fail(ZERO_EINVAL, "host_grads array is NULL");
+  if ((adamw == nullptr) == (sgd == nullptr))
+    return fail(ZERO_EINVAL, "give exactly one of the AdamW and the SGD options");
+  const int64_t o_lo = adamw ? adamw->lo : sgd->lo, o_hi = adamw ? adamw->hi : sgd->hi;
+  const double o_clip = adamw ? adamw->max_grad_norm : sgd->max_grad_norm;
+  if (o_lo != 0 || (o_hi >= 0 && o_hi != st->n))
+    return fail(ZERO_EINVAL, "the host-input step covers the whole vector (lo = 0, hi = -1 or n)");
+  if (o_clip > 0.0)
+    return fail(ZERO_EINVAL,
+                "no clipping in the chunked host-input step: chunks are stepped before the "
+                "whole gradient has arrived (copy the gradients, then zero_grad_norm_sq and "
+                "zero_step_ex)");
+  zk::Opt opt = zk::Opt::AdamW;
+  if (sgd)
+    if (int e = sgd_opt(sgd, &opt)) return e;
   const int32_t N = st->N;
   const int64_t n = st->n;
   for (int32_t r = 0; r < N; ++r)
@@ -795,8 +849,8 @@ int zero_step_from_host(void* const* params, const void* const* host_grads, void
   bool vec = false;
   int phase = 0;
   // the staging buffers are the kernel's gradient buffers
-  if (int e = prepare_step(params, staging, st, zk::Opt::AdamW, &a, &vec, &phase)) return e;
-  if (int e = adam_consts(t, lr, beta1, beta2, eps, weight_decay, &a.c)) return e;
+  if (int e = prepare_step(params, staging, st, opt, &a, &vec, &phase)) return e;
+  if (int e = adamw ? fill_adamw(adamw, &a) : fill_sgd(sgd, &a)) return e;
   if (n == 0) return ZERO_OK;
   const size_t es = st->precision == ZERO_BF16_MIXED ? 2 : 4;
   const int64_t count = (n + B - 1) / B;
@@ -839,14 +893,21 @@ int zero_step_from_host(void* const* params, const void* const* host_grads, void
     }
     if (int e = ck(cudaEventRecord(in_ready, hs), "cudaEventRecord")) return e;
     if (int e = ck(cudaStreamWaitEvent(cs, in_ready, 0), "cudaStreamWaitEvent")) return e;
-    if (int e = launch_range(a, st, vec, phase, lo, hi, cs)) return e;
+    if (int e = launch_range(a, st, vec, phase, lo, hi, cs, opt)) return e;
     if (int e = ck(cudaEventRecord(done, cs), "cudaEventRecord")) return e;
     if (host_params_out) {
       if (int e = ck(cudaStreamWaitEvent(ds, done, 0), "cudaStreamWaitEvent")) return e;
-      cudaError_t ce = cudaMemcpyAsync(static_cast<char*>(host_params_out) + off,
-                                       static_cast<const char*>(params[0]) + off, bytes,
-                                       cudaMemcpyDeviceToHost, ds);
-      if (ce != cudaSuccess) return cuda_fail(ce, "device-to-host copy of a parameter chunk");
+      // the chunk from replica 0, or (owner-only) each piece from its owner's replica
+      for (int32_t r = 0; r < (a.owner_only ? N : 1); ++r) {
+        const int64_t p_lo = a.owner_only ? std::max(lo, st->bounds[r]) : lo;
+        const int64_t p_hi = a.owner_only ? std::min(hi, st->bounds[r + 1]) : hi;
+        if (p_hi <= p_lo) continue;
+        const size_t p_off = size_t(p_lo) * es;
+        cudaError_t ce = cudaMemcpyAsync(static_cast<char*>(host_params_out) + p_off,
+                                         static_cast<const char*>(params[r]) + p_off,
+                                         size_t(p_hi - p_lo) * es, cudaMemcpyDeviceToHost, ds);
+        if (ce != cudaSuccess) return cuda_fail(ce, "device-to-host copy of a parameter chunk");
+      }
     }
   }
   if (host_params_out) {

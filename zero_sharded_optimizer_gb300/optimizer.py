@@ -86,17 +86,18 @@ class ZeroOptimizer:
              chunk_bytes: int = BUCKET_BYTES_25MIB) -> int:
         """One ZeRO step; returns the new step number t.
 
-        With host gradients the copies are pipelined with the step; when
+        With host gradients the copies are pipelined with the step (with
+        clipping they are copied in first: the norm needs every gradient). When
         ``host_params_out`` (a host tensor of n elements) is given, the updated
-        parameters are copied into it as well. Synchronize ``stream`` (the
-        current stream by default) before reading it.
+        parameters are copied into it as well; at stage 3 each shard comes from
+        its owner's replica and the replicas stay released. Synchronize
+        ``stream`` (the current stream by default) before reading it.
         """
         clipping = self.max_grad_norm > 0
         owner_only = self.stage == 3
         sgd = self.optimizer == "sgd"
-        if (clipping or owner_only or sgd) and not all(g.is_cuda for g in grads):
-            # the global norm needs every gradient before any update, and the
-            # chunked host pipeline runs the stage-1/2 AdamW step: copy first
+        if clipping and not all(g.is_cuda for g in grads):
+            # the global norm needs every gradient before any update: copy first
             staging = self._staging_buffers()
             s = stream if stream is not None else torch.cuda.current_stream(self.device)
             with torch.cuda.stream(s):
@@ -129,18 +130,44 @@ class ZeroOptimizer:
                 abi.zero_step(params, grads, self.states, self.t + 1, self.lr, self.beta1,
                               self.beta2, self.eps, self.weight_decay, stream)
             if host_params_out is not None:
-                if owner_only:
-                    self.gather(params, stream=stream)
                 s = stream if stream is not None else torch.cuda.current_stream(self.device)
                 with torch.cuda.stream(s):
-                    host_params_out.copy_(params[0], non_blocking=True)
+                    if owner_only:  # each shard from its owner's replica (no gather)
+                        for r, (lo, hi) in enumerate(self._bounds_pairs()):
+                            if hi > lo:
+                                host_params_out[lo:hi].copy_(params[r][lo:hi], non_blocking=True)
+                    else:
+                        host_params_out.copy_(params[0], non_blocking=True)
         else:
             staging = self._staging_buffers()
-            abi.zero_step_from_host(params, grads, staging, self.states, self.t + 1, self.lr,
-                                    self.beta1, self.beta2, self.eps, self.weight_decay,
-                                    host_params_out, chunk_bytes, stream, self._h2d, self._d2h)
+            if sgd:
+                o = abi.SgdOpts(self.t + 1, self.lr, self.momentum, self.dampening,
+                                self.weight_decay, 1 if self.nesterov else 0, self.grad_scale,
+                                0.0, None, 0, -1, 1 if owner_only else 0)
+                abi.zero_step_from_host_ex(params, grads, staging, self.states, sgd=o,
+                                           host_params_out=host_params_out,
+                                           chunk_bytes=chunk_bytes, compute=stream, h2d=self._h2d,
+                                           d2h=self._d2h)
+            elif owner_only or self.grad_scale != 1.0:
+                o = abi.StepOpts(self.t + 1, self.lr, self.beta1, self.beta2, self.eps,
+                                 self.weight_decay, self.grad_scale, 0.0, None, 0, -1,
+                                 1 if owner_only else 0)
+                abi.zero_step_from_host_ex(params, grads, staging, self.states, adamw=o,
+                                           host_params_out=host_params_out,
+                                           chunk_bytes=chunk_bytes, compute=stream, h2d=self._h2d,
+                                           d2h=self._d2h)
+            else:
+                abi.zero_step_from_host(params, grads, staging, self.states, self.t + 1, self.lr,
+                                        self.beta1, self.beta2, self.eps, self.weight_decay,
+                                        host_params_out, chunk_bytes, stream, self._h2d,
+                                        self._d2h)
         self.t += 1
         return self.t
+
+    def _bounds_pairs(self):
+        b = self.shard_bounds if self.shard_bounds is not None else \
+            abi.zero_shard_bounds(self.n, self.N)
+        return list(zip(b[:-1], b[1:]))
 
     def gather(self, params, lo: int = 0, hi: int = -1, stream=None) -> None:
         """ZeRO-3 gather: every replica receives each shard from its owner's
