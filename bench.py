@@ -17,6 +17,7 @@ bounded sample of the same workload on the host cores.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import os
@@ -79,9 +80,11 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def traffic_per_launch(workload: str):
+def traffic_per_launch(workload: str, elems_per_launch: float):
     """DRAM bytes per launch from the committed ncu summary, or None when absent
-    or taken on a different kernel source."""
+    or taken on a different kernel source. A record taken on a launch of another
+    size (one full 25 MiB bucket, against the mean bucket of a step whose last
+    bucket is short) is scaled to ``elems_per_launch`` by the elements processed."""
     try:
         with open(TRAFFIC_FILE) as f:
             entry = json.load(f).get(workload)
@@ -89,7 +92,11 @@ def traffic_per_launch(workload: str):
         return None
     if not entry or entry.get("kernel_source_sha256_16") != kernel_source_hash():
         return None
-    return entry.get("dram_bytes_per_launch")
+    t = entry.get("dram_bytes_per_launch")
+    e = entry.get("elements_per_launch")
+    if t is not None and e and e != elems_per_launch:
+        t = int(round(t * elems_per_launch / e))
+    return t
 
 
 def config_of(wl, extra=None) -> dict:
@@ -131,7 +138,78 @@ def whole_job_rate(units_per_rank: int, world: int, ms_per_step: float) -> float
 
 # ------------------------------------------------------------------- clocks --
 
+class _NvmlPoller:
+    """Reads the SM clock, its maximum, the power draw and the clock-event
+    reasons through NVML (read-only queries) every millisecond on a thread, so
+    that a timed region of a few milliseconds still gets samples."""
+
+    REASON_BITS = {0x8: "hw_slowdown", 0x40: "hw_thermal_slowdown",
+                   0x20: "sw_thermal_slowdown", 0x4: "sw_power_cap"}
+
+    def __init__(self, uuid: str):
+        import ctypes
+        import threading
+        self.ct = ctypes
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit_v2 failed")
+        self.lib = lib
+        self.dev = ctypes.c_void_p()
+        if lib.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(self.dev)) != 0:
+            lib.nvmlShutdown()
+            raise RuntimeError("nvmlDeviceGetHandleByUUID failed")
+        try:
+            self.reasons_fn = lib.nvmlDeviceGetCurrentClocksEventReasons
+        except AttributeError:
+            self.reasons_fn = lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        mx = ctypes.c_uint()
+        lib.nvmlDeviceGetMaxClockInfo(self.dev, 1, ctypes.byref(mx))  # 1 = SM clock
+        self.max_mhz = float(mx.value)
+        self.samples, self.power = [], []
+        self.halt = threading.Event()
+        self.thread = threading.Thread(target=self._run, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        ct = self.ct
+        clk, bits = ct.c_uint(), ct.c_ulonglong()
+        if self.lib.nvmlDeviceGetClockInfo(self.dev, 1, ct.byref(clk)) != 0:
+            return None
+        self.reasons_fn(self.dev, ct.byref(bits))
+        return float(clk.value), int(bits.value)
+
+    def _run(self):
+        # the clock and its reasons every millisecond; the power reading is
+        # slower to answer, so every 50 ms
+        next_power = 0.0
+        while not self.halt.is_set():
+            r = self._read()
+            if r is not None:
+                self.samples.append(r)
+            if time.monotonic() >= next_power:
+                mw = self.ct.c_uint()
+                if self.lib.nvmlDeviceGetPowerUsage(self.dev, self.ct.byref(mw)) == 0:
+                    self.power.append(mw.value / 1000.0)
+                next_power = time.monotonic() + 0.05
+            self.halt.wait(0.001)
+
+    def stop(self) -> dict:
+        self.halt.set()
+        self.thread.join(timeout=5)
+        self.lib.nvmlShutdown()
+        sm = [x[0] for x in self.samples]
+        reasons = {name for x in self.samples for bit, name in self.REASON_BITS.items()
+                   if x[1] & bit}
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": self.max_mhz,
+                "power_w_max": max(self.power) if self.power else None,
+                "reasons": sorted(reasons), "samples": len(sm), "source": "nvml, 1 ms"}
+
+
 class ClockSampler:
+    """Clocks during the timed region: NVML polled on a thread when the
+    library loads, else nvidia-smi's own 100 ms loop."""
+
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -139,12 +217,20 @@ class ClockSampler:
     def __init__(self, device_index: int):
         self.proc = None
         self.path = None
+        self.nvml = None
         try:
             import torch
             uuid = str(torch.cuda.get_device_properties(device_index).uuid)
-            target = ["-i", uuid if uuid.startswith("GPU-") else f"GPU-{uuid}"]
+            uuid = uuid if uuid.startswith("GPU-") else f"GPU-{uuid}"
+            target = ["-i", uuid]
         except Exception:
-            target = []
+            uuid, target = None, []
+        if uuid is not None:
+            try:
+                self.nvml = _NvmlPoller(uuid)
+                return
+            except Exception:
+                self.nvml = None
         fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
         os.close(fd)
         try:
@@ -156,6 +242,8 @@ class ClockSampler:
             self.proc = None
 
     def stop(self) -> dict:
+        if self.nvml is not None:
+            return self.nvml.stop()
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"],
                     "samples": 0}
@@ -185,7 +273,7 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(smax) if smax else None,
                 "power_w_max": max(power) if power else None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": sorted(reasons), "samples": len(sm), "source": "nvidia-smi, 100 ms"}
 
 
 # ------------------------------------------------------------ cpu baseline --
@@ -322,6 +410,19 @@ def run_gpu(args, wl, rank: int, world: int, local_rank: int) -> dict | None:
     if ddp:
         host_out = torch.empty(n, dtype=grads[0].dtype, pin_memory=True)
 
+    def e2e_path(o):
+        if o.max_grad_norm > 0:
+            return ("ZeroOptimizer.step with pinned host gradients: all copied in first (the "
+                    "norm needs every gradient), then zero_grad_norm_sq and the clipped step, "
+                    "D2H of the updated parameters")
+        entry = ("zero_step_from_host_ex" if o.stage == 3 or o.optimizer == "sgd"
+                 or o.grad_scale != 1.0 else "zero_step_from_host")
+        out = ("each shard from its owner's replica" if o.stage == 3
+               else "one updated replica")
+        return (f"ZeroOptimizer.step with pinned host gradients -> {entry}: 25 MiB chunks, "
+                "H2D on a copy stream, the step per chunk on the compute stream, D2H of "
+                f"{out} on a second copy stream")
+
     def e2e_step():
         if ddp:  # gradients in, the mean gradient out
             for g, h in zip(grads, host_grads):
@@ -348,9 +449,7 @@ def run_gpu(args, wl, rank: int, world: int, local_rank: int) -> dict | None:
            "ms_per_step": e_ms, "steps": K_e,
            "path": ("pinned host gradients copied in, ddp_allreduce_mean, the mean of rank 0 "
                     "copied out, all on the current stream") if ddp else
-                   ("ZeroOptimizer.step with pinned host gradients -> zero_step_from_host: "
-                    "25 MiB chunks, H2D on a copy stream, the step per chunk on the compute "
-                    "stream, D2H of one updated replica on a second copy stream")}
+                   e2e_path(opt)}
 
     if rank != 0:
         return None
@@ -366,11 +465,11 @@ def run_gpu(args, wl, rank: int, world: int, local_rank: int) -> dict | None:
     if stage3:  # the step writes 1 replica, not N; the gather reads 1 and writes N-1
         step_bytes += n * (2 if mixed else 4)
     achieved = step_bytes / (kernel_ms / 1e3) / 1e9
-    traffic = traffic_per_launch(wl.name)
-    if traffic is not None and (bucketed or clip or stage3 or sgd or ddp):
-        traffic = None
     whole = clip or stage3  # the roofline covers the whole step (several kernels)
     per = 1 if whole else launches_per_step
+    # the committed records cover the plain step of each workload (bucketed
+    # for the bucket-streamed one); the variants run other kernels
+    traffic = None if (clip or stage3 or sgd or ddp) else traffic_per_launch(wl.name, n / per)
     line = {
         "metric": METRIC_DDP if ddp else METRIC,
         "value": whole_job_rate(n, world, ms_step),
@@ -474,8 +573,15 @@ def main(argv=None):
                     help="ddp_mean: time ddp_allreduce_mean on the workload's gradients instead")
     ap.add_argument("--stage", type=int, default=2, choices=[2, 3],
                     help="3: owner-only step, then the gather of the full parameters (2 launches)")
+    ap.add_argument("--n", type=int, default=None,
+                    help="override the parameter count: a smaller case of the same kernels for "
+                         "ncu captures (named <workload>_n<count>; not a bench line)")
     args = ap.parse_args(argv)
     wl = inputs.WORKLOADS[args.workload]
+    if args.n is not None:
+        if args.n <= 0 or args.partition == "tensor":
+            ap.error("--n needs a positive count and the np.array_split partition")
+        wl = dataclasses.replace(wl, n=args.n, name=f"{wl.name}_n{args.n}")
     if args.steps is None:
         args.steps = default_steps(wl)
     if args.warmup < 3:
