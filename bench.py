@@ -165,6 +165,11 @@ class _NvmlPoller:
         mx = ctypes.c_uint()
         lib.nvmlDeviceGetMaxClockInfo(self.dev, 1, ctypes.byref(mx))  # 1 = SM clock
         self.max_mhz = float(mx.value)
+        # the first queries of a process are slow to answer: make them here,
+        # before the timed region, and keep no sample from them
+        self._read()
+        mw = ctypes.c_uint()
+        lib.nvmlDeviceGetPowerUsage(self.dev, ctypes.byref(mw))
         self.samples, self.power = [], []
         self.halt = threading.Event()
         self.thread = threading.Thread(target=self._run, daemon=True)
@@ -206,9 +211,30 @@ class _NvmlPoller:
                 "reasons": sorted(reasons), "samples": len(sm), "source": "nvml, 1 ms"}
 
 
+def _poller_child(uuid: str) -> None:
+    """Body of the clock-poller child process: poll until a line arrives on
+    stdin, then print the record as one JSON line. A process of its own, so
+    that the benchmark's launch loop, which holds the interpreter lock, does
+    not delay the samples."""
+    try:
+        p = _NvmlPoller(uuid)
+    except Exception as e:
+        print(f"unavailable {e}", flush=True)
+        return
+    print("ready", flush=True)
+    sys.stdin.readline()
+    print(json.dumps(p.stop()), flush=True)
+
+
+def _readline(proc, timeout_s: float) -> str:
+    import select
+    ready, _, _ = select.select([proc.stdout], [], [], timeout_s)
+    return proc.stdout.readline() if ready else ""
+
+
 class ClockSampler:
-    """Clocks during the timed region: NVML polled on a thread when the
-    library loads, else nvidia-smi's own 100 ms loop."""
+    """Clocks during the timed region: NVML polled every millisecond in a
+    child process when the library loads, else nvidia-smi's own 100 ms loop."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -227,8 +253,16 @@ class ClockSampler:
             uuid, target = None, []
         if uuid is not None:
             try:
-                self.nvml = _NvmlPoller(uuid)
-                return
+                child = subprocess.Popen(
+                    [sys.executable, "-c", f"import sys; sys.path.insert(0, {ROOT!r}); "
+                     f"import bench; bench._poller_child({uuid!r})"],
+                    stdin=subprocess.PIPE, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                    text=True)
+                if _readline(child, 60.0).strip() == "ready":
+                    self.nvml = child
+                    return
+                child.kill()
+                child.wait(timeout=5)
             except Exception:
                 self.nvml = None
         fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
@@ -243,7 +277,19 @@ class ClockSampler:
 
     def stop(self) -> dict:
         if self.nvml is not None:
-            return self.nvml.stop()
+            child, rec = self.nvml, None
+            try:
+                child.stdin.write("stop\n")
+                child.stdin.flush()
+                rec = json.loads(_readline(child, 30.0))
+            except Exception:
+                rec = None
+            try:
+                child.wait(timeout=5)
+            except Exception:
+                child.kill()
+            return rec or {"sm_mhz": None, "sm_max_mhz": None,
+                           "reasons": ["clock poller gave no record"], "samples": 0}
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"],
                     "samples": 0}
@@ -321,6 +367,32 @@ def cpu_baseline(wl, seconds: float = 12.0, op: str = "step") -> dict:
 
 
 # --------------------------------------------------------------- GPU arm --
+
+def host_link_ms(dev_in, host_in, host_out, dev_out, stream, reps: int = 5) -> float:
+    """Median time of the e2e step's copies alone: every host input copied to
+    its device buffer on one stream while the output is copied back on another,
+    both released at once. Overwrites ``dev_in`` (run after the timed legs)."""
+    import torch
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    times = []
+    for _ in range(reps + 1):
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        t0.record(stream)
+        s_in.wait_event(t0)
+        s_out.wait_event(t0)
+        with torch.cuda.stream(s_in):
+            for d, h in zip(dev_in, host_in):
+                d.copy_(h, non_blocking=True)
+        with torch.cuda.stream(s_out):
+            host_out.copy_(dev_out, non_blocking=True)
+        stream.wait_stream(s_in)
+        stream.wait_stream(s_out)
+        t1.record(stream)
+        torch.cuda.synchronize()
+        times.append(t0.elapsed_time(t1))
+    return statistics.median(times[1:])
+
 
 def run_gpu(args, wl, rank: int, world: int, local_rank: int) -> dict | None:
     import torch
@@ -444,9 +516,14 @@ def run_gpu(args, wl, rank: int, world: int, local_rank: int) -> dict | None:
     barrier()
     e_ms = max_over_ranks([e_begin.elapsed_time(e_end) / K_e], dev, world)[0]
     es = 2 if mixed else 4
+    link_ms = max_over_ranks([host_link_ms(grads, host_grads, host_out,
+                                           reps[0], stream)], dev, world)[0]
     e2e = {"value": whole_job_rate(n, world, e_ms), "unit": UNIT,
            "h2d_bytes_per_step": N * n * es, "d2h_bytes_per_step": n * es,
            "ms_per_step": e_ms, "steps": K_e,
+           "host_link_ms": link_ms, "frac_of_host_link": link_ms / e_ms,
+           "host_link": "the same H2D and D2H bytes alone, started together on two streams "
+                        "(no step): the e2e lower bound on this host link",
            "path": ("pinned host gradients copied in, ddp_allreduce_mean, the mean of rank 0 "
                     "copied out, all on the current stream") if ddp else
                    e2e_path(opt)}

@@ -120,3 +120,26 @@ def test_committed_traffic_records_cover_the_bench_workloads():
         e = rec[name]
         assert e["dram_bytes_per_launch"] == e["dram_bytes_read"] + e["dram_bytes_write"]
         assert os.path.exists(os.path.join(ROOT, e["summary"]))
+
+
+def test_poller_child_protocol(monkeypatch, capsys):
+    """The child prints ``ready``, polls until a line arrives on stdin, then
+    prints its record as one JSON line; without NVML it says so and stops."""
+    import io
+    import json
+    import bench
+    fake = FakeNvml([2070] * 3, [0x0] * 3)
+    monkeypatch.setattr(ctypes, "CDLL", lambda name: fake)
+    monkeypatch.setattr(sys, "stdin", io.StringIO("stop\n"))
+    bench._poller_child("GPU-0000")
+    out = capsys.readouterr().out.splitlines()
+    assert out[0] == "ready"
+    rec = json.loads(out[1])
+    assert rec["sm_max_mhz"] == 2070.0 and rec["source"] == "nvml, 1 ms"
+    assert fake.calls[-1] == "shutdown"
+
+    def missing(name):
+        raise OSError("no such library")
+    monkeypatch.setattr(ctypes, "CDLL", missing)
+    bench._poller_child("GPU-0000")
+    assert capsys.readouterr().out.startswith("unavailable")
