@@ -366,32 +366,92 @@ def cpu_baseline(wl, seconds: float = 12.0, op: str = "step") -> dict:
                       f"consecutive parameters x {wl.N} ranks of {wl.name}; {el:.1f} s"}
 
 
+def _oracle_worker(job):
+    """One process of the all-cores oracle run: wait for the common start, then
+    time the oracle on its own sample for ``seconds``."""
+    wl, seconds, op, start_at = job
+    while time.time() < start_at:
+        time.sleep(0.005)
+    rate, steps, k, el = oracle_sample_rate(wl, seconds, op=op)
+    return k * steps, el, k
+
+
+def cpu_baseline_all_cores(wl, seconds: float = 8.0, op: str = "step",
+                           procs: int | None = None) -> dict:
+    """The same oracle chunked over every core this process may run on: one
+    spawned process per core, each stepping its own sample of the workload (the
+    step is elementwise, so the samples are independent chunks), all started
+    together. Throughput = parameters stepped by all ÷ the longest process's
+    time. A pool that breaks or overruns gives a record saying so, not a hang."""
+    import concurrent.futures as cf
+    import multiprocessing as mp
+    cores = procs or len(os.sched_getaffinity(0))
+    ctx = mp.get_context("spawn")
+    ex = cf.ProcessPoolExecutor(max_workers=cores, mp_context=ctx)
+    try:
+        start_at = time.time() + 5.0  # after every process has imported numpy
+        futs = [ex.submit(_oracle_worker, (wl, seconds, op, start_at)) for _ in range(cores)]
+        res = [f.result(timeout=seconds + 120.0) for f in futs]
+    except Exception as e:  # broken pool, timeout
+        ex.shutdown(wait=False, cancel_futures=True)
+        return {"value": None, "unit": UNIT, "cores": cores,
+                "kind": "oracle, one spawned process per core",
+                "unavailable": f"{type(e).__name__}: {e}"[:200]}
+    ex.shutdown(wait=True)
+    done = sum(r[0] for r in res)
+    el = max(r[1] for r in res)
+    return {"value": done / el, "unit": UNIT, "cores": cores,
+            "kind": "oracle, one spawned process per core",
+            "sample": f"{cores} processes x about {seconds:.0f} s, each on {res[0][2]:,} "
+                      f"consecutive parameters x {wl.N} ranks of {wl.name} (fp32-mirror numpy)"}
+
+
+def percentile(sorted_vals, q: float) -> float:
+    """Linear-interpolation percentile of an ascending list."""
+    if not sorted_vals:
+        return float("nan")
+    x = (len(sorted_vals) - 1) * q / 100.0
+    lo = int(x)
+    hi = min(lo + 1, len(sorted_vals) - 1)
+    return sorted_vals[lo] + (sorted_vals[hi] - sorted_vals[lo]) * (x - lo)
+
+
 # --------------------------------------------------------------- GPU arm --
 
-def host_link_ms(dev_in, host_in, host_out, dev_out, stream, reps: int = 5) -> float:
-    """Median time of the e2e step's copies alone: every host input copied to
-    its device buffer on one stream while the output is copied back on another,
-    both released at once. Overwrites ``dev_in`` (run after the timed legs)."""
+def host_link_timer(dev_in, host_in, host_out, dev_out, stream, chunk: int):
+    """A timer of the e2e step's copies alone, in the host-input step's own
+    schedule: per chunk of ``chunk`` elements, every host input's piece is
+    copied to its device buffer on one stream, then (after an event) the
+    output's piece is copied back on another. ``run(k)`` does k such steps back
+    to back and returns the milliseconds. Overwrites ``dev_in``."""
     import torch
     s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
-    times = []
-    for _ in range(reps + 1):
+    n = dev_out.numel()
+    pieces = [(lo, min(n, lo + chunk)) for lo in range(0, n, chunk)]
+
+    def run(k: int) -> float:
         t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         torch.cuda.synchronize()
         t0.record(stream)
         s_in.wait_event(t0)
         s_out.wait_event(t0)
-        with torch.cuda.stream(s_in):
-            for d, h in zip(dev_in, host_in):
-                d.copy_(h, non_blocking=True)
-        with torch.cuda.stream(s_out):
-            host_out.copy_(dev_out, non_blocking=True)
+        for _ in range(k):
+            for lo, hi in pieces:
+                with torch.cuda.stream(s_in):
+                    for d, h in zip(dev_in, host_in):
+                        d[lo:hi].copy_(h[lo:hi], non_blocking=True)
+                    ready = torch.cuda.Event()
+                    ready.record(s_in)
+                s_out.wait_event(ready)
+                with torch.cuda.stream(s_out):
+                    host_out[lo:hi].copy_(dev_out[lo:hi], non_blocking=True)
         stream.wait_stream(s_in)
         stream.wait_stream(s_out)
         t1.record(stream)
         torch.cuda.synchronize()
-        times.append(t0.elapsed_time(t1))
-    return statistics.median(times[1:])
+        return t0.elapsed_time(t1)
+
+    return run
 
 
 def run_gpu(args, wl, rank: int, world: int, local_rank: int) -> dict | None:
@@ -399,7 +459,7 @@ def run_gpu(args, wl, rank: int, world: int, local_rank: int) -> dict | None:
     import torch.distributed as dist
 
     from zero_sharded_optimizer_gb300 import abi
-    from zero_sharded_optimizer_gb300.optimizer import ZeroOptimizer
+    from zero_sharded_optimizer_gb300.optimizer import BUCKET_BYTES_25MIB, ZeroOptimizer
 
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
@@ -466,13 +526,16 @@ def run_gpu(args, wl, rank: int, world: int, local_rank: int) -> dict | None:
     barrier()
     clocks = sampler.stop() if sampler else None
     ms_total = t_begin.elapsed_time(t_end)
-    kernel_ms = sum(s.elapsed_time(e) for s, e in zip(starts, ends)) / K
+    step_times = sorted(s.elapsed_time(e) for s, e in zip(starts, ends))
+    kernel_ms = sum(step_times) / K
     ms_step = ms_total / K
+    dist_ms = [percentile(step_times, q) for q in (10, 50, 90)]
 
     ms_step, kernel_ms = max_over_ranks([ms_step, kernel_ms], dev, world)
 
     # ---- end to end through the public API: host gradients in, parameters out
-    K_e = max(3, min(K, 30))
+    E2E_BLOCK = 5
+    K_e = E2E_BLOCK * max(1, min(K, 30) // E2E_BLOCK)
     host_grads = []
     for g in grads:
         h = torch.empty(n, dtype=g.dtype, pin_memory=True)
@@ -504,26 +567,42 @@ def run_gpu(args, wl, rank: int, world: int, local_rank: int) -> dict | None:
         else:
             opt.step(reps, host_grads, host_params_out=host_out)
 
+    # The host link's rate drifts by tens of percent over seconds (the host is
+    # shared), so the e2e steps and the copies-alone bound alternate in blocks
+    # of E2E_BLOCK back-to-back steps and each side sums its blocks.
+    link = host_link_timer(grads, host_grads, host_out, reps[0], stream,
+                           BUCKET_BYTES_25MIB // (2 if mixed else 4))
+
+    def e2e_block(k: int) -> float:
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        t0.record(stream)
+        for _ in range(k):
+            e2e_step()
+        t1.record(stream)
+        torch.cuda.synchronize()
+        return t0.elapsed_time(t1)
+
     for _ in range(2):
         e2e_step()
+    link(1)
     barrier()
-    e_begin = torch.cuda.Event(enable_timing=True)
-    e_end = torch.cuda.Event(enable_timing=True)
-    e_begin.record(stream)
-    for _ in range(K_e):
-        e2e_step()
-    e_end.record(stream)
+    e_total = l_total = 0.0
+    for _ in range(K_e // E2E_BLOCK):
+        e_total += e2e_block(E2E_BLOCK)
+        l_total += link(E2E_BLOCK)
     barrier()
-    e_ms = max_over_ranks([e_begin.elapsed_time(e_end) / K_e], dev, world)[0]
+    e_ms, link_ms = max_over_ranks([e_total / K_e, l_total / K_e], dev, world)
     es = 2 if mixed else 4
-    link_ms = max_over_ranks([host_link_ms(grads, host_grads, host_out,
-                                           reps[0], stream)], dev, world)[0]
     e2e = {"value": whole_job_rate(n, world, e_ms), "unit": UNIT,
            "h2d_bytes_per_step": N * n * es, "d2h_bytes_per_step": n * es,
            "ms_per_step": e_ms, "steps": K_e,
            "host_link_ms": link_ms, "frac_of_host_link": link_ms / e_ms,
-           "host_link": "the same H2D and D2H bytes alone, started together on two streams "
-                        "(no step): the e2e lower bound on this host link",
+           "host_link": f"the same H2D and D2H copies alone in the host-input step's "
+                        f"schedule (25 MiB chunks: H2D on one stream, then that chunk's D2H on "
+                        f"another), no step: the e2e lower bound on this host link; timed in "
+                        f"blocks of {E2E_BLOCK} back-to-back steps alternating with the e2e "
+                        f"blocks",
            "path": ("pinned host gradients copied in, ddp_allreduce_mean, the mean of rank 0 "
                     "copied out, all on the current stream") if ddp else
                    e2e_path(opt)}
@@ -583,13 +662,15 @@ def run_gpu(args, wl, rank: int, world: int, local_rank: int) -> dict | None:
                                ("zero_step_tma_kernel (owner-only) + gather_tma_kernel "
                                 "(whole stage-3 step)") if stage3 else
                                ("zero_step_tma_kernel" if wl.N <= 8 else "zero_step_kernel"),
-                     "kernel_ms": kernel_ms / per},
+                     "kernel_ms": kernel_ms / per,
+                     "step_ms_p10_median_p90": dist_ms},
         "gpu_launches": K * launches_per_step,
         "clocks": clocks,
         "e2e": e2e,
     }
     if args.cpu_baseline and world == 1:
         line["cpu_baseline"] = cpu_baseline(wl, op=args.op)
+        line["cpu_baseline"]["all_cores"] = cpu_baseline_all_cores(wl, op=args.op)
     return line
 
 

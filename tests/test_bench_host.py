@@ -68,7 +68,7 @@ def run_poller(monkeypatch, clocks, reasons):
     monkeypatch.setattr(ctypes, "CDLL", lambda name: fake)
     p = bench._NvmlPoller("GPU-0000")
     deadline = time.time() + 5
-    while fake.i < len(clocks) and time.time() < deadline:
+    while len(p.samples) < len(clocks) and time.time() < deadline:
         time.sleep(0.002)
     rec = p.stop()
     return fake, rec
@@ -143,3 +143,22 @@ def test_poller_child_protocol(monkeypatch, capsys):
     monkeypatch.setattr(ctypes, "CDLL", missing)
     bench._poller_child("GPU-0000")
     assert capsys.readouterr().out.startswith("unavailable")
+
+
+def test_step_time_percentiles():
+    import numpy as np
+    import bench
+    v = sorted(np.random.default_rng(3).random(37).tolist())
+    for q in (10, 50, 90):
+        assert abs(bench.percentile(v, q) - np.percentile(v, q)) < 1e-12
+    assert bench.percentile([2.0], 90) == 2.0
+
+
+def test_all_cores_oracle_baseline_runs_on_spawned_processes():
+    """The all-cores oracle leg starts its processes with spawn and adds up
+    what they stepped; two processes on the small parity workload."""
+    import bench
+    from zero_sharded_optimizer_gb300 import inputs
+    rec = bench.cpu_baseline_all_cores(inputs.WORKLOADS["tiny_adam"], seconds=0.3, procs=2)
+    assert rec["cores"] == 2 and "unavailable" not in rec, rec
+    assert rec["value"] > 0
