@@ -50,8 +50,8 @@ Arithmetic modes:
 
 Readings taken where the pages are silent (each is listed in the design notes):
 
-1. The Adam update itself is not printed on the pages (the scratchllm problem
-   says ``adam_update`` "is given"). Reading: Adam with bias correction and eps
+1. The Adam update itself is not printed on the pages (the problem page
+   treats ``adam_update`` as supplied and never shows its body). Reading: Adam with bias correction and eps
    added outside the square root; AdamW's weight decay is decoupled and scaled
    by lr, applied before the moment update. The course page fixes the t=1
    behaviour (m = (1-b1) g, v = (1-b2) g^2, m_hat = g, sqrt(v_hat) = |g|).
