@@ -558,12 +558,12 @@ def run_gpu(args, wl, rank: int, world: int, local_rank: int) -> dict | None:
                 "H2D on a copy stream, the step per chunk on the compute stream, D2H of "
                 f"{out} on a second copy stream")
 
+    ddp_h2d, ddp_d2h = (torch.cuda.Stream(), torch.cuda.Stream()) if ddp else (None, None)
+
     def e2e_step():
-        if ddp:  # gradients in, the mean gradient out
-            for g, h in zip(grads, host_grads):
-                g.copy_(h, non_blocking=True)
-            abi.ddp_allreduce_mean(grads, wl.precision, n)
-            host_out.copy_(grads[0], non_blocking=True)
+        if ddp:  # gradients in, the mean gradient out, chunk-pipelined
+            abi.ddp_allreduce_mean_from_host(host_grads, grads, wl.precision, n, host_out,
+                                             BUCKET_BYTES_25MIB, None, ddp_h2d, ddp_d2h)
         else:
             opt.step(reps, host_grads, host_params_out=host_out)
 
@@ -603,8 +603,9 @@ def run_gpu(args, wl, rank: int, world: int, local_rank: int) -> dict | None:
                         f"another), no step: the e2e lower bound on this host link; timed in "
                         f"blocks of {E2E_BLOCK} back-to-back steps alternating with the e2e "
                         f"blocks",
-           "path": ("pinned host gradients copied in, ddp_allreduce_mean, the mean of rank 0 "
-                    "copied out, all on the current stream") if ddp else
+           "path": ("ddp_allreduce_mean_from_host with pinned host gradients: 25 MiB chunks, "
+                    "H2D on a copy stream, the mean per chunk on the compute stream, D2H of "
+                    "the mean on a second copy stream") if ddp else
                    e2e_path(opt)}
 
     if rank != 0:

@@ -395,6 +395,33 @@ int zero_step_from_host_ex(void *const *params, const void *const *host_grads,
 int ddp_allreduce_mean(void *const *grads, int64_t n, int32_t N, int32_t precision,
                        zero_stream_t stream);
 
+/* ddp_allreduce_mean with the gradients in HOST memory, pipelined chunk by
+ * chunk like zero_step_from_host. For every chunk [lo, hi) of B = chunk_bytes /
+ * element_size elements, in index order, this queues:
+ *   on `h2d`     the copies host_grads[r][lo:hi] -> staging[r][lo:hi], all r;
+ *   on `compute` the mean of that chunk in place in the staging buffers, once
+ *                it has arrived;
+ *   on `d2h`     (host_mean_out not NULL) the copy of the mean
+ *                staging[0][lo:hi] -> host_mean_out[lo:hi].
+ * The copies start after everything already queued on `compute`, and
+ * `compute` completes only after the last copy in either direction, so
+ * synchronizing `compute` covers the whole call.
+ *   host_grads    : N HOST buffers of n elements, read-only (pinned memory for
+ *                   asynchronous copies).
+ *   staging       : N DEVICE buffers of n elements, distinct and with the same
+ *                   alignment rules as ddp_allreduce_mean; each ends holding
+ *                   the mean, identical on every rank.
+ *   host_mean_out : NULL, or a HOST buffer of n elements.
+ * The staging buffers end bit for bit as ddp_allreduce_mean leaves device
+ * buffers holding the same gradients. The library keeps a pool of CUDA events
+ * per device for these calls (ceil(n/B)+2 at most), created on first use.
+ * Errors: as ddp_allreduce_mean, plus EINVAL for a NULL host or staging
+ * buffer or a chunk smaller than one element, ECUDA for a failed copy. */
+int ddp_allreduce_mean_from_host(const void *const *host_grads, void *const *staging, int64_t n,
+                                 int32_t N, int32_t precision, void *host_mean_out,
+                                 int64_t chunk_bytes, zero_stream_t compute, zero_stream_t h2d,
+                                 zero_stream_t d2h);
+
 /* ---------------------------------------------------------------- memory -- */
 
 /* Model-state bytes per rank after a step, by stage: 0 = plain DDP, 1 = shard

@@ -258,3 +258,26 @@ def test_host_input_step_option_checks(abi):
     assert abi.raw_call("zero_step_from_host_ex", empty, empty, empty, h, ctypes.byref(ad), None,
                         None, 0, None, None, None) == abi.ZERO_EINVAL
     assert abi.raw_call("zero_free_states", h) == abi.ZERO_OK
+
+
+def test_ddp_mean_from_host_argument_checks(abi):
+    """Every refusal of ddp_allreduce_mean_from_host comes before device work."""
+    vp = ctypes.c_void_p
+    host = (vp * 2)(16, 32)
+    stg = (vp * 2)(64, 128)
+    mib = 25 << 20
+
+    def call(h, s, n, N, prec, chunk):
+        return abi.raw_call("ddp_allreduce_mean_from_host", h, s, n, N, prec, None, chunk,
+                            None, None, None)
+
+    assert call(host, stg, -1, 2, abi.ZERO_FP32, mib) == abi.ZERO_EINVAL          # n < 0
+    assert call(host, stg, 10, 0, abi.ZERO_FP32, mib) == abi.ZERO_EINVAL          # N = 0
+    assert call(None, stg, 10, 2, abi.ZERO_FP32, mib) == abi.ZERO_EINVAL          # no host array
+    assert call(host, None, 10, 2, abi.ZERO_FP32, mib) == abi.ZERO_EINVAL         # no staging
+    assert call(host, stg, 10, 2, abi.ZERO_FP64_EMU, mib) == abi.ZERO_EINVAL      # precision
+    assert call(host, stg, 10, 2, abi.ZERO_FP32, 3) == abi.ZERO_EINVAL            # chunk < 1 elem
+    assert call((vp * 2)(16, None), stg, 10, 2, abi.ZERO_FP32, mib) == abi.ZERO_EINVAL
+    assert call(host, (vp * 2)(64, 18), 10, 2, abi.ZERO_FP32, mib) == abi.ZERO_EALIGN
+    assert call(host, (vp * 2)(64, 64), 10, 2, abi.ZERO_FP32, mib) == abi.ZERO_EINVAL  # same
+    assert call(host, (vp * 2)(64, 96), 10, 2, abi.ZERO_FP32, mib) == abi.ZERO_EINVAL  # overlap

@@ -353,6 +353,88 @@ def test_ddp_allreduce_mean(abi, cuda, n, N, prec):
         assert np.array_equal(host_of(dev[r]), ref[r])
 
 
+def _pinned_host(h, dt):
+    """A pinned host tensor holding `h` (float32, or bf16 bits as uint16)."""
+    if dt == torch.bfloat16:
+        t = torch.from_numpy(h.view(np.int16).copy()).view(torch.bfloat16)
+    else:
+        t = torch.from_numpy(h.copy())
+    return t.pin_memory()
+
+
+@pytest.mark.parametrize("prec", [oracle.FP32, oracle.BF16_MIXED])
+@pytest.mark.parametrize("n,N,chunk_bytes", [(1, 1, 64), (4099, 3, 1000), (100_003, 4, 1 << 16),
+                                             (100_003, 8, 25 << 20), (1_000_003, 5, 1 << 20),
+                                             (65_537, 13, 4094)])
+def test_ddp_mean_from_host(abi, cuda, n, N, chunk_bytes, prec):
+    """The chunk-pipelined DDP mean of host gradients: every staging buffer and
+    the host copy equal the oracle's mean bit for bit, with chunks that split
+    vectors (1000 and 4094 bytes) and a staging offset that shifts the phase."""
+    rng = np.random.default_rng(n * 3 + N)
+    mixed = prec == oracle.BF16_MIXED
+    dt = torch.bfloat16 if mixed else torch.float32
+    hs = []
+    for _ in range(N):
+        g = rng.normal(0, 1, n).astype(np.float32)
+        hs.append(oracle.f32_to_bf16_rne(g) if mixed else g)
+    host = [_pinned_host(h, dt) for h in hs]
+    staging = [to_dev(np.zeros(n, np.uint16 if mixed else np.float32), dt, cuda,
+                      offset=1 if n % 2 else 0) for _ in range(N)]
+    out = torch.empty(n, dtype=dt).pin_memory()
+    h2d, d2h = torch.cuda.Stream(), torch.cuda.Stream()
+    abi.ddp_allreduce_mean_from_host(host, staging, prec, n, out, chunk_bytes, None, h2d, d2h)
+    torch.cuda.synchronize()
+    ref = oracle.allreduce_mean(hs, precision=prec, mode="fp32")
+    for r in range(N):
+        assert np.array_equal(host_of(staging[r]), ref[r]), f"staging {r}"
+    assert np.array_equal(inputs.to_numpy_storage(out), ref[0])
+
+
+@pytest.mark.parametrize("prec", [oracle.FP32, oracle.BF16_MIXED])
+def test_ddp_mean_from_host_back_to_back(abi, cuda, prec):
+    """Calls queued back to back on the same buffers, with no synchronisation
+    between them: each host copy holds its own call's mean."""
+    n, N = 300_007, 4
+    mixed = prec == oracle.BF16_MIXED
+    dt = torch.bfloat16 if mixed else torch.float32
+    rng = np.random.default_rng(77)
+    staging = [torch.empty(n, dtype=dt, device=cuda) for _ in range(N)]
+    h2d, d2h = torch.cuda.Stream(), torch.cuda.Stream()
+    calls = []
+    for _ in range(3):
+        hs = []
+        for _ in range(N):
+            g = rng.normal(0, 1, n).astype(np.float32)
+            hs.append(oracle.f32_to_bf16_rne(g) if mixed else g)
+        host = [_pinned_host(h, dt) for h in hs]
+        out = torch.empty(n, dtype=dt).pin_memory()
+        abi.ddp_allreduce_mean_from_host(host, staging, prec, n, out, 1 << 18, None, h2d, d2h)
+        calls.append((hs, host, out))
+    torch.cuda.synchronize()
+    for hs, _, out in calls:
+        ref = oracle.allreduce_mean(hs, precision=prec, mode="fp32")
+        assert np.array_equal(inputs.to_numpy_storage(out), ref[0])
+    for r in range(N):
+        assert np.array_equal(host_of(staging[r]), ref[r])
+
+
+def test_ddp_mean_from_host_rejects_bad_arguments(abi, cuda):
+    n, N = 1000, 3
+    staging = [torch.empty(n, device=cuda) for _ in range(N)]
+    host = [torch.zeros(n).pin_memory() for _ in range(N)]
+    with pytest.raises(abi.ZeroError) as e:  # the same staging buffer twice
+        abi.ddp_allreduce_mean_from_host(host, [staging[0], staging[0], staging[2]], abi.ZERO_FP32)
+    assert e.value.code == abi.ZERO_EINVAL
+    with pytest.raises(abi.ZeroError) as e:  # a chunk below one element
+        abi.ddp_allreduce_mean_from_host(host, staging, abi.ZERO_FP32, chunk_bytes=2)
+    assert e.value.code == abi.ZERO_EINVAL
+    with pytest.raises(TypeError):  # device tensors where host ones are expected
+        abi.ddp_allreduce_mean_from_host(staging, staging, abi.ZERO_FP32)
+    abi.ddp_allreduce_mean_from_host([h[:0] for h in host], [s[:0] for s in staging],
+                                     abi.ZERO_FP32, 0)  # n = 0: nothing to do
+    torch.cuda.synchronize()
+
+
 def test_checkpoint_resume_is_bitwise(abi, cuda):
     from zero_sharded_optimizer_gb300.optimizer import ZeroOptimizer
     n, N = 123_457, 4

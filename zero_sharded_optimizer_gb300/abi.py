@@ -74,6 +74,8 @@ _SIGNATURES = {
     "zero_step_from_host_ex": (ctypes.c_int, [_P(_vp), _P(_vp), _P(_vp), _vp, _vp, _vp, _vp,
                                               _i64, _vp, _vp, _vp]),
     "ddp_allreduce_mean": (ctypes.c_int, [_P(_vp), _i64, _i32, _i32, _vp]),
+    "ddp_allreduce_mean_from_host": (ctypes.c_int, [_P(_vp), _P(_vp), _i64, _i32, _i32, _vp,
+                                                    _i64, _vp, _vp, _vp]),
     "zero_memory_bytes": (ctypes.c_int, [_i64, _i32, _i32, _i32, _P(_u64)]),
     "zero_memory_breakdown": (ctypes.c_int, [_i64, _i32, _i32, _i32, _i32, _P(_u64)]),
     "zero_grad_norm_scratch_count": (ctypes.c_int, [_i64, _i32, _P(_i64)]),
@@ -474,6 +476,26 @@ def ddp_allreduce_mean(grads, precision: int, n: int | None = None, stream=None)
     gp = _ptr_array(grads, n, _storage_dtype(precision), "grads")
     _check(_lib.ddp_allreduce_mean(gp, n, len(grads), precision, _stream(stream)),
            "ddp_allreduce_mean")
+
+
+def ddp_allreduce_mean_from_host(host_grads, staging, precision: int, n: int | None = None,
+                                 host_mean_out=None, chunk_bytes: int = 25 * 1024 * 1024,
+                                 compute=None, h2d=None, d2h=None):
+    """The DDP mean of host gradients, chunk-pipelined into the ``staging``
+    CUDA buffers (which end holding the mean); ``host_mean_out`` (a host
+    tensor) receives it too when given."""
+    n = staging[0].numel() if n is None else n
+    if len(host_grads) != len(staging):
+        raise ValueError("need one staging buffer per host gradient")
+    dt = _storage_dtype(precision)
+    hp = _host_ptr_array(host_grads, n, dt, "host_grads")
+    sp = _ptr_array(staging, n, dt, "staging")
+    out = None
+    if host_mean_out is not None:
+        out = _host_ptr_array([host_mean_out], n, dt, "host_mean_out")[0]
+    _check(_lib.ddp_allreduce_mean_from_host(hp, sp, n, len(staging), precision, out, chunk_bytes,
+                                             _stream(compute), _stream(h2d), _stream(d2h)),
+           "ddp_allreduce_mean_from_host")
 
 
 def zero_device_status(clear: bool = False) -> int:

@@ -13,6 +13,7 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <mutex>
 #include <new>
 #include <thread>
 #include <vector>
@@ -951,6 +952,94 @@ int ddp_allreduce_mean(void* const* grads, int64_t n, int32_t N, int32_t precisi
   a.sp = make_split(0, n, same, ph, es == 2 ? 8 : 4);
   cudaError_t e = zk::launch_allreduce(a, es == 2, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "ddp_allreduce_mean kernel launch");
+  return ZERO_OK;
+}
+
+int ddp_allreduce_mean_from_host(const void* const* host_grads, void* const* staging, int64_t n,
+                                 int32_t N, int32_t precision, void* host_mean_out,
+                                 int64_t chunk_bytes, zero_stream_t compute, zero_stream_t h2d,
+                                 zero_stream_t d2h) {
+  if (n < 0) return fail(ZERO_EINVAL, "n=%lld must be >= 0", (long long)n);
+  if (!valid_ranks(N)) return fail(ZERO_EINVAL, "N=%d outside [1, %d]", N, ZERO_MAX_RANKS);
+  if (!host_grads || !staging) return fail(ZERO_EINVAL, "host_grads or staging array is NULL");
+  int64_t B;
+  if (int e = bucket_elems(precision, chunk_bytes, &B)) return e;
+  const size_t es = precision == ZERO_BF16_MIXED ? 2 : 4;
+  for (int32_t r = 0; r < N; ++r)
+    if (n > 0 && (!host_grads[r] || !staging[r]))
+      return fail(ZERO_EINVAL, "host_grads[%d] or staging[%d] is NULL", r, r);
+  // the whole-vector checks (alignment, distinct buffers) before anything is queued
+  if (int e = ddp_allreduce_mean(staging, 0, N, precision, compute)) return e;
+  {
+    std::vector<Range> rs;
+    for (int32_t r = 0; r < N && n > 0; ++r)
+      rs.push_back({uintptr_t(staging[r]), uintptr_t(staging[r]) + uintptr_t(n) * es,
+                    "a staging buffer"});
+    if (int e = check_disjoint(rs)) return e;
+  }
+  if (n == 0) return ZERO_OK;
+  const int64_t count = (n + B - 1) / B;
+  // Events come from a process-wide pool per device, grown on demand. A wait
+  // takes the state of an event when it is queued, so re-recording an event in
+  // a later call is safe; the mutex keeps two host threads from interleaving
+  // their record/wait pairs on one event.
+  static std::mutex mu;
+  static std::vector<cudaEvent_t> pools[256];
+  int dev = 0;
+  {
+    cudaError_t ce = cudaGetDevice(&dev);
+    if (ce != cudaSuccess) return cuda_fail(ce, "cudaGetDevice");
+    if (dev < 0 || dev >= 256) return fail(ZERO_EINVAL, "device %d outside the event pools", dev);
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  std::vector<cudaEvent_t>& pool = pools[dev];
+  const size_t need = size_t(count + 2);
+  while (pool.size() < need) {
+    cudaEvent_t ev;
+    cudaError_t ce = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
+    if (ce != cudaSuccess) return cuda_fail(ce, "cudaEventCreateWithFlags");
+    pool.push_back(ev);
+  }
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(compute);
+  cudaStream_t hs = reinterpret_cast<cudaStream_t>(h2d);
+  cudaStream_t ds = reinterpret_cast<cudaStream_t>(d2h);
+  auto ck = [&](cudaError_t ce, const char* what) { return ce == cudaSuccess ? 0 : cuda_fail(ce, what); };
+  // the copies start after everything already queued on `compute`
+  if (int e = ck(cudaEventRecord(pool[0], cs), "cudaEventRecord")) return e;
+  if (int e = ck(cudaStreamWaitEvent(hs, pool[0], 0), "cudaStreamWaitEvent")) return e;
+  if (host_mean_out)
+    if (int e = ck(cudaStreamWaitEvent(ds, pool[0], 0), "cudaStreamWaitEvent")) return e;
+  std::vector<void*> chunk(size_t(N), nullptr);
+  for (int64_t k = 0; k < count; ++k) {
+    const int64_t lo = k * B, hi = std::min<int64_t>(n, lo + B);
+    const size_t off = size_t(lo) * es, bytes = size_t(hi - lo) * es;
+    for (int32_t r = 0; r < N; ++r) {
+      cudaError_t ce = cudaMemcpyAsync(static_cast<char*>(staging[r]) + off,
+                                       static_cast<const char*>(host_grads[r]) + off, bytes,
+                                       cudaMemcpyHostToDevice, hs);
+      if (ce != cudaSuccess) return cuda_fail(ce, "host-to-device copy of a gradient chunk");
+      chunk[size_t(r)] = static_cast<char*>(staging[r]) + off;
+    }
+    cudaEvent_t landed = pool[size_t(2 + k)];
+    if (int e = ck(cudaEventRecord(landed, hs), "cudaEventRecord")) return e;
+    if (int e = ck(cudaStreamWaitEvent(cs, landed, 0), "cudaStreamWaitEvent")) return e;
+    if (int e = ddp_allreduce_mean(chunk.data(), hi - lo, N, precision, compute)) return e;
+    if (host_mean_out) {
+      // the event is re-recorded on `compute` after the mean of this chunk
+      if (int e = ck(cudaEventRecord(landed, cs), "cudaEventRecord")) return e;
+      if (int e = ck(cudaStreamWaitEvent(ds, landed, 0), "cudaStreamWaitEvent")) return e;
+      cudaError_t ce = cudaMemcpyAsync(static_cast<char*>(host_mean_out) + off, chunk[0], bytes,
+                                       cudaMemcpyDeviceToHost, ds);
+      if (ce != cudaSuccess) return cuda_fail(ce, "device-to-host copy of a mean chunk");
+    }
+  }
+  // `compute` completes only after the last copy in either direction
+  if (int e = ck(cudaEventRecord(pool[1], hs), "cudaEventRecord")) return e;
+  if (int e = ck(cudaStreamWaitEvent(cs, pool[1], 0), "cudaStreamWaitEvent")) return e;
+  if (host_mean_out) {
+    if (int e = ck(cudaEventRecord(pool[1], ds), "cudaEventRecord")) return e;
+    if (int e = ck(cudaStreamWaitEvent(cs, pool[1], 0), "cudaStreamWaitEvent")) return e;
+  }
   return ZERO_OK;
 }
 
