@@ -776,7 +776,7 @@ cudaError_t launch(K kernel, const A& args, int64_t work, cudaStream_t s) {
 // whose data is disjoint from that kernel's (the next bucket of one step).
 template <auto kernel, int THREADS, typename A>
 cudaError_t launch_tma(const A& args, uint32_t smem, int64_t tiles, cudaStream_t s,
-                       bool dependent = false) {
+                       bool dependent = false, int ctas_per_sm = 1) {
   static bool configured[256] = {false};  // per device ordinal; one array per kernel
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -788,7 +788,8 @@ cudaError_t launch_tma(const A& args, uint32_t smem, int64_t tiles, cudaStream_t
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
-  const int blocks = int(tiles < 1 ? 1 : (tiles < sms ? tiles : sms));
+  const int64_t slots = int64_t(sms) * ctas_per_sm;
+  const int blocks = int(tiles < 1 ? 1 : (tiles < slots ? tiles : slots));
   if (!dependent) {
     kernel<<<blocks, THREADS, smem, s>>>(args);
     return cudaGetLastError();
@@ -951,7 +952,8 @@ cudaError_t launch_gather_t(const GatherArgs& a, cudaStream_t s) {
   if (a.sp.nvec > 0 && a.N >= (BF16 ? 5 : 4)) {
     using G = GatherTile<BF16>;
     const int64_t tiles = (a.sp.nvec * (16 / G::kEB) + G::T - 1) / G::T;
-    return launch_tma<gather_tma_kernel<BF16>, GatherPipe::kThreads>(a, G::kSmem, tiles, s);
+    return launch_tma<gather_tma_kernel<BF16>, GatherPipe::kThreads>(a, G::kSmem, tiles, s, false,
+                                                                      kGatherCtasPerSm);
   }
   const int64_t work = a.sp.nvec > a.sp.head + a.sp.tail ? a.sp.nvec : a.sp.head + a.sp.tail;
   return launch(gather_kernel<BF16>, a, work, s);

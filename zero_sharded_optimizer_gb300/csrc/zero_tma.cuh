@@ -708,11 +708,16 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
 
 // ------------------------------------------------------- stage-3 all-gather --
 
-// Tiles of 16 KB (4096 fp32 or 8192 bf16 elements), twelve stages, results
-// stored straight from the stage (no compute on the data). Measured against
-// 32 KB x 6 and 64 KB x 3: the same on fp32_25m, 9 % and 25 % faster on
-// gpt2_small (seven replicas written per tile).
-using GatherPipe = PipeCfg<128, 12, 0, 192 * 1024>;
+// Tiles of 16 KB (4096 fp32 or 8192 bf16 elements), stored straight from the
+// stage (no compute on the data), in two CTAs per SM of six stages each. One
+// CTA of twelve stages measured the same on fp32_25m and 9 % and 25 % faster
+// than 32 KB x 6 and 64 KB x 3 on gpt2_small (seven replicas written per
+// tile); splitting it into two CTAs per SM took another 2-5 % (329.8 against
+// 342.6 us on gpt2_small, 172.2 against 182.0 us for bf16 N = 5 at 100M; fp32
+// N = 4 at 100M unchanged at 6.0 TB/s). Storing from shared memory with
+// register stores measured 2-7 % slower, and 4 KB bulk stores the same.
+using GatherPipe = PipeCfg<128, 6, 0, 96 * 1024>;
+constexpr int kGatherCtasPerSm = 2;
 
 template <bool BF16>
 struct GatherTile {
@@ -728,7 +733,7 @@ struct GatherTile {
 // later owners are then read from their owners' replicas into the tile, and
 // each replica receives the tile minus its own shard (store_slice).
 template <bool BF16>
-__global__ void __launch_bounds__(GatherPipe::kThreads, 1)
+__global__ void __launch_bounds__(GatherPipe::kThreads, kGatherCtasPerSm)
     gather_tma_kernel(const __grid_constant__ GatherArgs P) {
   using G = GatherTile<BF16>;
   using E = typename std::conditional<BF16, uint16_t, float>::type;
