@@ -14,7 +14,8 @@
  * and an accumulation factor (zero_grad_norm_sq, zero_step_ex), momentum SGD
  * as the optimizer (zero_step_sgd), ZeRO stage 3 (owner-only steps and
  * zero_gather), 25 MiB bucket streaming, host-memory gradients
- * (zero_step_from_host, zero_step_from_host_ex), the DDP mean and per-stage memory accounting.
+ * (zero_step_from_host, zero_step_from_host_ex), the DDP mean (also from host
+ * memory: ddp_allreduce_mean_from_host) and per-stage memory accounting.
  *
  * Conventions for every call:
  *  - Return value: ZERO_OK (0) or a negative ZERO_E* code. zero_strerror()
