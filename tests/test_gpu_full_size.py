@@ -176,3 +176,36 @@ def test_full_size_sampled_sgd_and_stage3(abi, cuda, name, variant):
                 assert_fp32_close(take(reps[r]), ref_p, f"{name} t={t} rep {r}")
         for r in range(1, N):
             assert torch.equal(reps[r], reps[0])
+
+
+def test_indices_beyond_int32(abi, cuda):
+    """The largest single buffer: n = 2^31 + 12,345 fp32 parameters over two
+    ranks (about 60 GB on the device at the peak), one step, sampled around
+    the 2^31 element boundary, the shard edge and both ends."""
+    import dataclasses
+    from zero_sharded_optimizer_gb300.optimizer import ZeroOptimizer
+    wl = dataclasses.replace(inputs.WORKLOADS["fp32_320m"], name="fp32_2g", n=(1 << 31) + 12_345,
+                             N=2, steps=1)
+    assert wl.zero_frac == 0  # keeps the generator's scratch to one buffer
+    n, N = wl.n, wl.N
+    init = inputs.init_params_fp32(n, wl, seed=3, device=cuda)
+    reps = inputs.make_replicas(init, N, wl.precision)
+    del init
+    grads = inputs.make_grads(n, N, wl.precision, device=cuda)
+    inputs.fill_grads(grads, wl, step=1, seed=3)
+    opt = ZeroOptimizer(n, N, wl.precision, lr=wl.lr, betas=(wl.beta1, wl.beta2), eps=wl.eps,
+                        weight_decay=wl.weight_decay)
+    idx = sample_indices(n, N, [(0, 1 << 31), (1 << 31, n)], k=1 << 14, seed=31)
+    idx_d = torch.from_numpy(idx).to(cuda)
+    take = lambda x: inputs.to_numpy_storage(x[idx_d])  # noqa: E731
+    p_before, m_before, v_before = take(reps[0]), take(opt.m), take(opt.v)
+    opt.step(reps, grads)
+    torch.cuda.synchronize()
+    ref_p, ref_m, ref_v, _ = oracle_on_sample(wl, 1, [take(g) for g in grads], p_before,
+                                              m_before, v_before, None)
+    assert_fp32_close(take(opt.m), ref_m, "2^31+ m")
+    assert_fp32_close(take(opt.v), ref_v, "2^31+ v")
+    for r in range(N):
+        assert_fp32_close(take(reps[r]), ref_p, f"2^31+ rep {r}")
+    assert torch.equal(reps[1], reps[0])
+    assert ((1 << 31) + 5) in set(idx.tolist())
