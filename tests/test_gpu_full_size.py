@@ -209,3 +209,19 @@ def test_indices_beyond_int32(abi, cuda):
         assert_fp32_close(take(reps[r]), ref_p, f"2^31+ rep {r}")
     assert torch.equal(reps[1], reps[0])
     assert ((1 << 31) + 5) in set(idx.tolist())
+    # the gather past 2^31: clear what each replica does not own, then gather
+    half = n // 2 + (n % 2)
+    want = reps[0].clone()
+    reps[0][half:].zero_()
+    reps[1][:half].zero_()
+    abi.zero_gather(reps, opt.states)
+    torch.cuda.synchronize()
+    assert torch.equal(reps[0], want) and torch.equal(reps[1], want)
+    del want
+    # the DDP mean past 2^31, bit for bit on the samples
+    g_s = [take(g) for g in grads]
+    abi.ddp_allreduce_mean(grads, wl.precision)
+    torch.cuda.synchronize()
+    ref = oracle.allreduce_mean(g_s, wl.precision, mode="fp32")
+    for r in range(N):
+        assert np.array_equal(take(grads[r]), ref[r])
