@@ -547,9 +547,10 @@ def run_gpu(args, wl, rank: int, world: int, local_rank: int) -> dict | None:
 
     def e2e_path(o):
         if o.max_grad_norm > 0:
-            return ("ZeroOptimizer.step with pinned host gradients: all copied in first (the "
-                    "norm needs every gradient), then zero_grad_norm_sq and the clipped step, "
-                    "D2H of the updated parameters")
+            return ("ZeroOptimizer.step with pinned host gradients -> zero_step_from_host_ex "
+                    "with clipping: every 25 MiB chunk copied in on a copy stream, the norm "
+                    "once all have arrived, then the clipped step chunk by chunk, each chunk's "
+                    "D2H on a second copy stream while the next is stepped")
         entry = ("zero_step_from_host_ex" if o.stage == 3 or o.optimizer == "sgd"
                  or o.grad_scale != 1.0 else "zero_step_from_host")
         out = ("each shard from its owner's replica" if o.stage == 3

@@ -367,17 +367,23 @@ int zero_step_from_host(void *const *params, const void *const *host_grads,
 
 /* zero_step_from_host with the options of zero_step_ex (AdamW) or of
  * zero_step_sgd (momentum SGD): exactly one of `adamw` and `sgd` is non-NULL.
- * Their step number, hyperparameters, grad_scale and owner_only are used. The
- * range must be the whole vector (lo = 0, hi = -1 or n) and max_grad_norm <= 0:
- * chunks are stepped before the whole gradient has arrived, so global-norm
- * clipping cannot run in this pipeline (copy the gradients to the device, then
- * zero_grad_norm_sq and zero_step_ex). With owner_only (ZeRO stage 3) the
- * replicas stay released, and host_params_out still receives the full updated
- * parameters: each piece of a chunk is copied from its owner's replica.
- * Otherwise as zero_step_from_host. SGD needs a state initialised for it
- * (zero_init_states with v = NULL).
+ * Their step number, hyperparameters, grad_scale, clipping and owner_only are
+ * used; the range must be the whole vector (lo = 0, hi = -1 or n).
+ * Clipping (max_grad_norm > 0): the global norm needs the whole gradient, so
+ * every chunk is copied in first; then the call itself computes the squared
+ * norm, as zero_grad_norm_sq_noalloc does (bit for bit what zero_grad_norm_sq
+ * gives), into *norm_sq. Here norm_sq is an OUTPUT: a DEVICE double the caller
+ * provides. The chunks are then stepped in order, each copied back while the
+ * next is stepped. This uses the library's own norm scratch, so n <=
+ * ZERO_NOALLOC_MAX_N, and calls whose norms overlap on the GPU must not
+ * share it (see zero_grad_norm_sq_noalloc).
+ * With owner_only (ZeRO stage 3) the replicas stay released, and
+ * host_params_out still receives the full updated parameters: each piece of a
+ * chunk is copied from its owner's replica. Otherwise as zero_step_from_host.
+ * SGD needs a state initialised for it (zero_init_states with v = NULL).
  * Errors: as zero_step_from_host, plus EINVAL for no or both option sets, a
- * partial range, clipping, or bad options. */
+ * partial range, bad options, clipping without norm_sq or with n >
+ * ZERO_NOALLOC_MAX_N; EALIGN for a misaligned norm_sq. */
 int zero_step_from_host_ex(void *const *params, const void *const *host_grads,
                            void *const *staging, zero_states_t *st,
                            const zero_step_opts_t *adamw, const zero_sgd_opts_t *sgd,

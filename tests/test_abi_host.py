@@ -219,8 +219,9 @@ def test_sgd_and_gather_argument_checks(abi):
 
 
 def test_host_input_step_option_checks(abi):
-    """zero_step_from_host_ex takes exactly one option set, the whole vector and
-    no clipping; each refusal comes before any device work."""
+    """zero_step_from_host_ex takes exactly one option set and the whole vector,
+    and clipping only with a norm_sq output; each refusal comes before any
+    device work."""
     vp = ctypes.c_void_p
     h = vp()
     assert abi.raw_call("zero_init_states", 0, 2, 0, None, None, None, None, None,
@@ -242,18 +243,21 @@ def test_host_input_step_option_checks(abi):
     assert call(ad, None, grads=None) == abi.ZERO_EINVAL      # no host gradients
     bad_adamw = [abi.StepOpts(1, 1e-3, 0.9, 0.999, 1e-8, 0.01, 1.0, 0.0, None, 1, -1, 0),  # lo
                  abi.StepOpts(1, 1e-3, 0.9, 0.999, 1e-8, 0.01, 1.0, 0.0, None, 0, 5, 0),   # hi
-                 abi.StepOpts(1, 1e-3, 0.9, 0.999, 1e-8, 0.01, 1.0, 1.0, None, 0, -1, 0),  # clip
+                 abi.StepOpts(1, 1e-3, 0.9, 0.999, 1e-8, 0.01, 1.0, 1.0, None, 0, -1, 0),  # no norm
                  abi.StepOpts(0, 1e-3, 0.9, 0.999, 1e-8, 0.01, 1.0, 0.0, None, 0, -1, 0),  # t = 0
                  abi.StepOpts(1, 1e-3, 1.0, 0.999, 1e-8, 0.01, 1.0, 0.0, None, 0, -1, 0),  # beta1
                  abi.StepOpts(1, 1e-3, 0.9, 0.999, 1e-8, 0.01, 0.0, 0.0, None, 0, -1, 0)]  # scale
     for o in bad_adamw:
         assert call(o, None) == abi.ZERO_EINVAL
     bad_sgd = [abi.SgdOpts(1, 0.1, 0.9, 0.0, 0.0, 0, 1.0, 0.0, None, 3, -1, 0),   # lo
-               abi.SgdOpts(1, 0.1, 0.9, 0.0, 0.0, 0, 1.0, 2.0, None, 0, -1, 0),   # clip
+               abi.SgdOpts(1, 0.1, 0.9, 0.0, 0.0, 0, 1.0, 2.0, None, 0, -1, 0),   # no norm
                abi.SgdOpts(1, 0.1, 0.9, 0.1, 0.0, 1, 1.0, 0.0, None, 0, -1, 0),   # nesterov+damp
                abi.SgdOpts(1, -0.1, 0.9, 0.0, 0.0, 0, 1.0, 0.0, None, 0, -1, 0)]  # lr < 0
     for o in bad_sgd:
         assert call(None, o) == abi.ZERO_EINVAL
+    # clipping with a norm_sq output is accepted (n = 0: nothing to queue)
+    clip_ok = abi.StepOpts(1, 1e-3, 0.9, 0.999, 1e-8, 0.01, 1.0, 1.0, 4096, 0, -1, 0)
+    assert call(clip_ok, None) == abi.ZERO_OK
     # chunk size below one vector of elements is refused too
     assert abi.raw_call("zero_step_from_host_ex", empty, empty, empty, h, ctypes.byref(ad), None,
                         None, 0, None, None, None) == abi.ZERO_EINVAL

@@ -260,7 +260,9 @@ def test_optimizer_sgd_and_stage3_with_host_gradients(abi, cuda, prec):
     equals the same optimizer fed device gradients, bit for bit: momentum SGD,
     stage 3 (owner-only step; the host copy of the parameters takes each shard
     from its owner and the other replica elements stay as they were), both
-    together, and AdamW with a gradient scale."""
+    together, AdamW with a gradient scale, and clipping (the host-input call
+    computes the norm after every chunk has arrived; the device path uses
+    zero_grad_norm_sq with its own scratch)."""
     from zero_sharded_optimizer_gb300.optimizer import ZeroOptimizer
     n, N = 200_003, 4
     mixed = prec == oracle.BF16_MIXED
@@ -269,7 +271,9 @@ def test_optimizer_sgd_and_stage3_with_host_gradients(abi, cuda, prec):
     init = torch.from_numpy(rng.normal(0, 0.02, n).astype(np.float32))
     bounds = oracle.shard_bounds(n, N)
     for kw in (dict(optimizer="sgd", momentum=0.9, nesterov=True), dict(stage=3),
-               dict(stage=3, optimizer="sgd", momentum=0.9), dict(grad_scale=0.25)):
+               dict(stage=3, optimizer="sgd", momentum=0.9), dict(grad_scale=0.25),
+               dict(max_grad_norm=0.05), dict(max_grad_norm=0.05, grad_scale=0.5, stage=3),
+               dict(optimizer="sgd", momentum=0.9, max_grad_norm=0.05)):
         stage3 = kw.get("stage") == 3
         common = dict(precision=prec, lr=1e-3, weight_decay=0.01,
                       master_init=init if mixed else None, **kw)
@@ -298,3 +302,6 @@ def test_optimizer_sgd_and_stage3_with_host_gradients(abi, cuda, prec):
         for key in ("m", "v", "master"):
             x, y = getattr(a, key), getattr(b, key)
             assert (x is None and y is None) or torch.equal(x, y)
+        if kw.get("max_grad_norm"):
+            assert torch.equal(a._norm, b._norm), kw
+            assert float(a._norm) > 0.05 ** 2, "the case must clip"

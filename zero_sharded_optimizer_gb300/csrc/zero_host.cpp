@@ -829,14 +829,13 @@ int zero_step_from_host_ex(void* const* params, const void* const* host_grads,
   if ((adamw == nullptr) == (sgd == nullptr))
     return fail(ZERO_EINVAL, "give exactly one of the AdamW and the SGD options");
   const int64_t o_lo = adamw ? adamw->lo : sgd->lo, o_hi = adamw ? adamw->hi : sgd->hi;
-  const double o_clip = adamw ? adamw->max_grad_norm : sgd->max_grad_norm;
+  const bool clip = (adamw ? adamw->max_grad_norm : sgd->max_grad_norm) > 0.0;
+  double* norm_out = const_cast<double*>(adamw ? adamw->norm_sq : sgd->norm_sq);
   if (o_lo != 0 || (o_hi >= 0 && o_hi != st->n))
     return fail(ZERO_EINVAL, "the host-input step covers the whole vector (lo = 0, hi = -1 or n)");
-  if (o_clip > 0.0)
-    return fail(ZERO_EINVAL,
-                "no clipping in the chunked host-input step: chunks are stepped before the "
-                "whole gradient has arrived (copy the gradients, then zero_grad_norm_sq and "
-                "zero_step_ex)");
+  if (clip && st->n > ZERO_NOALLOC_MAX_N)
+    return fail(ZERO_EINVAL, "clipping in the host-input step covers n <= %lld (the library's "
+                "own norm scratch)", (long long)ZERO_NOALLOC_MAX_N);
   zk::Opt opt = zk::Opt::AdamW;
   if (sgd)
     if (int e = sgd_opt(sgd, &opt)) return e;
@@ -880,36 +879,57 @@ int zero_step_from_host_ex(void* const* params, const void* const* host_grads,
     if (int e = ck(cudaEventRecord(ev[0], cs), "cudaEventRecord")) return e;
     if (int e = ck(cudaStreamWaitEvent(hs, ev[0], 0), "cudaStreamWaitEvent")) return e;
   }
-  for (int64_t k = 0; k < count; ++k) {
+  auto copy_in = [&](int64_t k) -> int {  // on `h2d`: chunk k of every rank's gradient
     const int64_t lo = k * B, hi = std::min<int64_t>(n, lo + B);
     const size_t off = size_t(lo) * es, bytes = size_t(hi - lo) * es;
-    cudaEvent_t in_ready = ev[2 + 2 * k], done = ev[3 + 2 * k];
     if (chained)  // the previous call's step on this chunk has read its staging
-      if (int e = ck(cudaStreamWaitEvent(hs, done, 0), "cudaStreamWaitEvent")) return e;
+      if (int e = ck(cudaStreamWaitEvent(hs, ev[3 + 2 * k], 0), "cudaStreamWaitEvent")) return e;
     for (int32_t r = 0; r < N; ++r) {
       cudaError_t ce = cudaMemcpyAsync(static_cast<char*>(staging[r]) + off,
                                        static_cast<const char*>(host_grads[r]) + off, bytes,
                                        cudaMemcpyHostToDevice, hs);
       if (ce != cudaSuccess) return cuda_fail(ce, "host-to-device copy of a gradient chunk");
     }
-    if (int e = ck(cudaEventRecord(in_ready, hs), "cudaEventRecord")) return e;
-    if (int e = ck(cudaStreamWaitEvent(cs, in_ready, 0), "cudaStreamWaitEvent")) return e;
+    return ck(cudaEventRecord(ev[2 + 2 * k], hs), "cudaEventRecord");
+  };
+  auto step_out = [&](int64_t k) -> int {  // on `compute`, then `d2h`: step and copy back
+    const int64_t lo = k * B, hi = std::min<int64_t>(n, lo + B);
+    cudaEvent_t done = ev[3 + 2 * k];
     if (int e = launch_range(a, st, vec, phase, lo, hi, cs, opt)) return e;
     if (int e = ck(cudaEventRecord(done, cs), "cudaEventRecord")) return e;
-    if (host_params_out) {
-      if (int e = ck(cudaStreamWaitEvent(ds, done, 0), "cudaStreamWaitEvent")) return e;
-      // the chunk from replica 0, or (owner-only) each piece from its owner's replica
-      for (int32_t r = 0; r < (a.owner_only ? N : 1); ++r) {
-        const int64_t p_lo = a.owner_only ? std::max(lo, st->bounds[r]) : lo;
-        const int64_t p_hi = a.owner_only ? std::min(hi, st->bounds[r + 1]) : hi;
-        if (p_hi <= p_lo) continue;
-        const size_t p_off = size_t(p_lo) * es;
-        cudaError_t ce = cudaMemcpyAsync(static_cast<char*>(host_params_out) + p_off,
-                                         static_cast<const char*>(params[r]) + p_off,
-                                         size_t(p_hi - p_lo) * es, cudaMemcpyDeviceToHost, ds);
-        if (ce != cudaSuccess) return cuda_fail(ce, "device-to-host copy of a parameter chunk");
-      }
+    if (!host_params_out) return ZERO_OK;
+    if (int e = ck(cudaStreamWaitEvent(ds, done, 0), "cudaStreamWaitEvent")) return e;
+    // the chunk from replica 0, or (owner-only) each piece from its owner's replica
+    for (int32_t r = 0; r < (a.owner_only ? N : 1); ++r) {
+      const int64_t p_lo = a.owner_only ? std::max(lo, st->bounds[r]) : lo;
+      const int64_t p_hi = a.owner_only ? std::min(hi, st->bounds[r + 1]) : hi;
+      if (p_hi <= p_lo) continue;
+      const size_t p_off = size_t(p_lo) * es;
+      cudaError_t ce = cudaMemcpyAsync(static_cast<char*>(host_params_out) + p_off,
+                                       static_cast<const char*>(params[r]) + p_off,
+                                       size_t(p_hi - p_lo) * es, cudaMemcpyDeviceToHost, ds);
+      if (ce != cudaSuccess) return cuda_fail(ce, "device-to-host copy of a parameter chunk");
     }
+    return ZERO_OK;
+  };
+  if (!clip) {
+    // each chunk is stepped as soon as it has arrived
+    for (int64_t k = 0; k < count; ++k) {
+      if (int e = copy_in(k)) return e;
+      if (int e = ck(cudaStreamWaitEvent(cs, ev[2 + 2 * k], 0), "cudaStreamWaitEvent")) return e;
+      if (int e = step_out(k)) return e;
+    }
+  } else {
+    // the global norm needs the whole gradient: every chunk in, the norm, then
+    // the steps (their copies back overlapping the later steps)
+    for (int64_t k = 0; k < count; ++k)
+      if (int e = copy_in(k)) return e;
+    if (int e = ck(cudaStreamWaitEvent(cs, ev[2 + 2 * (count - 1)], 0), "cudaStreamWaitEvent"))
+      return e;
+    if (int e = zero_grad_norm_sq_noalloc(staging, n, N, st->precision, norm_out, compute))
+      return e;
+    for (int64_t k = 0; k < count; ++k)
+      if (int e = step_out(k)) return e;
   }
   if (host_params_out) {
     // `compute` completes only after the last parameter chunk reached the host

@@ -86,8 +86,9 @@ class ZeroOptimizer:
              chunk_bytes: int = BUCKET_BYTES_25MIB) -> int:
         """One ZeRO step; returns the new step number t.
 
-        With host gradients the copies are pipelined with the step (with
-        clipping they are copied in first: the norm needs every gradient). When
+        With host gradients the copies are pipelined with the step; with
+        clipping every chunk comes in first, then the norm, then the chunks
+        are stepped and copied back one after another. When
         ``host_params_out`` (a host tensor of n elements) is given, the updated
         parameters are copied into it as well; at stage 3 each shard comes from
         its owner's replica and the replicas stay released. Synchronize
@@ -96,8 +97,8 @@ class ZeroOptimizer:
         clipping = self.max_grad_norm > 0
         owner_only = self.stage == 3
         sgd = self.optimizer == "sgd"
-        if clipping and not all(g.is_cuda for g in grads):
-            # the global norm needs every gradient before any update: copy first
+        if clipping and not all(g.is_cuda for g in grads) and self.n > abi.ZERO_NOALLOC_MAX_N:
+            # past the library's own norm scratch: copy first, then the device path
             staging = self._staging_buffers()
             s = stream if stream is not None else torch.cuda.current_stream(self.device)
             with torch.cuda.stream(s):
@@ -108,10 +109,11 @@ class ZeroOptimizer:
             if clipping or owner_only or sgd or self.grad_scale != 1.0:
                 norm = None
                 if clipping:
-                    if self._norm is None:
+                    f64 = dict(dtype=torch.float64, device=self.device)
+                    if self._norm_scratch is None:
                         count = abi.zero_grad_norm_scratch_count(self.n, self.precision)
-                        f64 = dict(dtype=torch.float64, device=self.device)
                         self._norm_scratch = torch.empty(count, **f64)
+                    if self._norm is None:
                         self._norm = torch.empty(1, **f64)
                     abi.zero_grad_norm_sq(grads, self.precision, self._norm_scratch, self._norm,
                                           self.n, stream)
@@ -140,18 +142,23 @@ class ZeroOptimizer:
                         host_params_out.copy_(params[0], non_blocking=True)
         else:
             staging = self._staging_buffers()
+            norm = None
+            if clipping:  # the host-input step computes the norm into this scalar
+                if self._norm is None:
+                    self._norm = torch.empty(1, dtype=torch.float64, device=self.device)
+                norm = self._norm.data_ptr()
             if sgd:
                 o = abi.SgdOpts(self.t + 1, self.lr, self.momentum, self.dampening,
                                 self.weight_decay, 1 if self.nesterov else 0, self.grad_scale,
-                                0.0, None, 0, -1, 1 if owner_only else 0)
+                                self.max_grad_norm, norm, 0, -1, 1 if owner_only else 0)
                 abi.zero_step_from_host_ex(params, grads, staging, self.states, sgd=o,
                                            host_params_out=host_params_out,
                                            chunk_bytes=chunk_bytes, compute=stream, h2d=self._h2d,
                                            d2h=self._d2h)
-            elif owner_only or self.grad_scale != 1.0:
+            elif clipping or owner_only or self.grad_scale != 1.0:
                 o = abi.StepOpts(self.t + 1, self.lr, self.beta1, self.beta2, self.eps,
-                                 self.weight_decay, self.grad_scale, 0.0, None, 0, -1,
-                                 1 if owner_only else 0)
+                                 self.weight_decay, self.grad_scale, self.max_grad_norm, norm,
+                                 0, -1, 1 if owner_only else 0)
                 abi.zero_step_from_host_ex(params, grads, staging, self.states, adamw=o,
                                            host_params_out=host_params_out,
                                            chunk_bytes=chunk_bytes, compute=stream, h2d=self._h2d,
