@@ -455,7 +455,9 @@ def zero_step_from_host_ex(params, host_grads, staging, st: ZeroStates, adamw=No
                            host_params_out=None, chunk_bytes: int = 25 * 1024 * 1024,
                            compute=None, h2d=None, d2h=None):
     """zero_step_from_host with AdamW options (a StepOpts) or SGD options (an
-    SgdOpts): exactly one of ``adamw`` and ``sgd``."""
+    SgdOpts): exactly one of ``adamw`` and ``sgd``. With max_grad_norm > 0 the
+    options' norm_sq is the device address of a float64 scalar that the call
+    fills with the squared norm before the clipped step."""
     dt = _storage_dtype(st.precision)
     if len(host_grads) != st.N or len(staging) != st.N or len(params) != st.N:
         raise ValueError(f"need {st.N} params, host gradients and staging buffers")
