@@ -305,3 +305,24 @@ def test_optimizer_sgd_and_stage3_with_host_gradients(abi, cuda, prec):
         if kw.get("max_grad_norm"):
             assert torch.equal(a._norm, b._norm), kw
             assert float(a._norm) > 0.05 ** 2, "the case must clip"
+
+
+def test_clipped_host_step_checks_norm_sq_before_queuing(abi, cuda):
+    """The clipped host-input step refuses a misaligned or overlapping norm_sq
+    before any copy is queued: the staging buffers keep their contents."""
+    n, N = 50_000, 2
+    reps = [torch.zeros(n, device=cuda) for _ in range(N)]
+    m, v = torch.empty(n, device=cuda), torch.empty(n, device=cuda)
+    st = abi.zero_init_states(n, N, abi.ZERO_FP32, m, v, None, None)
+    staging = [torch.full((n,), 7.0, device=cuda) for _ in range(N)]
+    host = [torch.ones(n).pin_memory() for _ in range(N)]
+    scalar = torch.empty(2, dtype=torch.float64, device=cuda)
+    for ptr, code in ((scalar.data_ptr() + 4, abi.ZERO_EALIGN),
+                      (staging[1].data_ptr() + 800, abi.ZERO_EINVAL)):
+        o = abi.StepOpts(1, 1e-3, 0.9, 0.999, 1e-8, 0.0, 1.0, 1.0, ptr, 0, -1, 0)
+        with pytest.raises(abi.ZeroError) as e:
+            abi.zero_step_from_host_ex(reps, host, staging, st, adamw=o)
+        assert e.value.code == code
+    torch.cuda.synchronize()
+    assert all(bool((s == 7.0).all()) for s in staging)
+    st.close()

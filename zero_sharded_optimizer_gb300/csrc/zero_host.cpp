@@ -853,6 +853,16 @@ int zero_step_from_host_ex(void* const* params, const void* const* host_grads,
   if (int e = adamw ? fill_adamw(adamw, &a) : fill_sgd(sgd, &a)) return e;
   if (n == 0) return ZERO_OK;
   const size_t es = st->precision == ZERO_BF16_MIXED ? 2 : 4;
+  if (clip) {  // the norm's own checks, before anything is queued
+    if (reinterpret_cast<uintptr_t>(norm_out) % 8)
+      return fail(ZERO_EALIGN, "norm_sq not 8-byte aligned");
+    std::vector<Range> rs;
+    for (int32_t r = 0; r < N; ++r)
+      rs.push_back({uintptr_t(staging[r]), uintptr_t(staging[r]) + uintptr_t(n) * es,
+                    "a staging buffer"});
+    rs.push_back({uintptr_t(norm_out), uintptr_t(norm_out) + 8, "norm_sq"});
+    if (int e = check_disjoint(rs)) return e;
+  }
   const int64_t count = (n + B - 1) / B;
   const size_t need = size_t(2 * count + 2);
   while (st->events.size() < need) {
