@@ -38,7 +38,7 @@ from zero_sharded_optimizer_gb300 import inputs  # noqa: E402
 METRIC = "ZeRO step params/s at N ranks on 1 GB300; achieved HBM GB/s vs peak"
 METRIC_DDP = "DDP all_reduce(mean) params/s at N ranks on 1 GB300; achieved HBM GB/s vs peak"
 UNIT = "params/s"
-DEFAULT_WORKLOAD = "fp32_25m"
+DEFAULT_WORKLOAD = "mixed_1p3b"
 KERNEL_SRCS = [os.path.join(ROOT, "zero_sharded_optimizer_gb300", "csrc", f)
                for f in ("zero_kernels.cu", "zero_tma.cuh")]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
@@ -53,6 +53,14 @@ def bytes_per_param(wl) -> int:
     if wl.precision == inputs.BF16_MIXED:
         return 4 * wl.N + 24
     return 8 * wl.N + 20
+
+
+def dtype_of(wl) -> str:
+    """Storage and arithmetic of the workload's step: mixed precision stores
+    bf16 replicas and gradients and computes in fp32 on the fp32 master, m, v."""
+    if wl.precision == inputs.BF16_MIXED:
+        return "bf16 storage (params, grads), f32 arithmetic (master, m, v)"
+    return "f32"
 
 
 def default_steps(wl) -> int:
@@ -639,7 +647,7 @@ def run_gpu(args, wl, rank: int, world: int, local_rank: int) -> dict | None:
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "f32",
+        "dtype": dtype_of(wl),
         "data": "synthetic (seeded device draws; inputs resident in HBM)",
         "config": config_of(wl, {"parallelism": f"{N} simulated ranks per GPU; "
                                                 f"{world} independent GPU replica(s)",
@@ -704,7 +712,7 @@ def run_reference(args, wl, world: int) -> dict:
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "f32",
+        "dtype": dtype_of(wl),
         "data": "synthetic (seeded numpy draws)",
         "config": config_of(wl, {"parallelism": f"{wl.N} simulated ranks; host cores"}),
         "cpu_baseline": {"value": rate, "unit": UNIT, "cores": 1, "kind": "oracle",

@@ -30,3 +30,16 @@ def cuda(abi):
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     return torch.device("cuda:0")
+
+
+@pytest.fixture(autouse=True)
+def _guard_regions():
+    """After every test, the sentinels around every buffer made with
+    parity_util.guarded_empty are unchanged (no out-of-range device write)."""
+    yield
+    import parity_util
+    try:
+        if parity_util.guard_count():
+            parity_util.check_guards()
+    finally:
+        parity_util.forget_guards()

@@ -57,3 +57,61 @@ def exact_fraction(got, ref):
 
 def flat(states, key):
     return np.concatenate([s[key] for s in states]) if states else np.zeros(0, np.float32)
+
+
+# ---------------------------------------------------------------------------
+# Guard regions. compute-sanitizer is not available on the GPU pool, so every
+# device buffer of the small parity tests sits inside a larger allocation whose
+# other elements hold a sentinel bit pattern (a NaN in both float formats, so a
+# kernel that read it as data would also show). A kernel that writes past
+# either end of its range -- a bulk store rounded up to 16 bytes, a tile past
+# `hi`, a head written before a non-zero offset -- changes a sentinel, and
+# check_guards() reports it. Buffers register themselves; the conftest checks
+# and forgets them after every test.
+# ---------------------------------------------------------------------------
+
+GUARD = 4096          # sentinel elements on each side of a buffer (two full tiles)
+_SENTINEL_BITS = {4: 0x7FA5A5A5, 2: 0x7FA5, 8: 0x7FF5A5A5A5A5A5A5}
+_guarded = []
+
+
+def _bits_dtype(elem_size):
+    import torch
+    return {4: torch.int32, 2: torch.int16, 8: torch.int64}[elem_size]
+
+
+def guarded_empty(n, dtype, device, offset=0, what="buffer"):
+    """A device view of n elements, ``GUARD + offset`` elements into an
+    allocation of ``n + 2*GUARD + offset`` whose elements outside the view
+    hold the sentinel. The view's own elements hold the sentinel too until
+    written."""
+    import torch
+    es = torch.empty(0, dtype=dtype).element_size()
+    buf = torch.empty(n + 2 * GUARD + offset, dtype=dtype, device=device)
+    buf.view(_bits_dtype(es)).fill_(_SENTINEL_BITS[es])
+    lo = GUARD + offset
+    _guarded.append((buf, lo, lo + n, what))
+    return buf[lo:lo + n]
+
+
+def check_guards():
+    """Every registered buffer's elements outside its view still hold the
+    sentinel, bit for bit."""
+    for buf, lo, hi, what in _guarded:
+        es = buf.element_size()
+        bits = buf.view(_bits_dtype(es))
+        s = _SENTINEL_BITS[es]
+        before = int((bits[:lo] != s).sum())
+        after = int((bits[hi:] != s).sum())
+        if before or after:
+            raise AssertionError(f"{what}: {before} element(s) written before the buffer and "
+                                 f"{after} after it (guard regions of {lo} and "
+                                 f"{bits.numel() - hi} elements)")
+
+
+def forget_guards():
+    _guarded.clear()
+
+
+def guard_count():
+    return len(_guarded)

@@ -11,7 +11,8 @@ import pytest
 import torch
 
 import oracle
-from parity_util import (assert_bf16_within_one_ulp, assert_fp32_close, exact_fraction, flat)
+from parity_util import (assert_bf16_within_one_ulp, assert_fp32_close, check_guards,
+                         exact_fraction, flat, guarded_empty)
 from zero_sharded_optimizer_gb300 import inputs
 
 pytestmark = pytest.mark.gpu
@@ -19,17 +20,19 @@ pytestmark = pytest.mark.gpu
 HP = dict(lr=3e-3, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.01)
 
 
-def to_dev(host, dtype, device, offset=0):
-    """Device view of `host` (float32, or bf16 bits as uint16) starting `offset`
-    elements into a padded allocation."""
-    n = host.shape[0]
-    buf = torch.zeros(n + 16, dtype=dtype, device=device)
-    view = buf[offset:offset + n]
+def host_tensor(host, dtype):
+    """CPU tensor of `host` (float32, or bf16 bits as uint16) in `dtype`."""
     if dtype == torch.bfloat16:
-        src = torch.from_numpy(host.view(np.int16).copy()).view(torch.bfloat16)
-    else:
-        src = torch.from_numpy(host.copy())
-    view.copy_(src)
+        return torch.from_numpy(host.view(np.int16).copy()).view(torch.bfloat16)
+    return torch.from_numpy(host.copy())
+
+
+def to_dev(host, dtype, device, offset=0, what="buffer"):
+    """Device view of `host` (float32, or bf16 bits as uint16) starting `offset`
+    elements into a guarded allocation: every element around the view holds a
+    sentinel that the conftest checks after the test (parity_util.GUARD)."""
+    view = guarded_empty(host.shape[0], dtype, device, offset, what)
+    view.copy_(host_tensor(host, dtype))
     return view
 
 
@@ -54,17 +57,18 @@ class Case:
             rep_host = oracle.f32_to_bf16_rne(init)    # replicas hold RNE(init)
         else:
             rep_host = init
-        self.reps = [to_dev(rep_host, self.dt, device, rep_off[r]) for r in range(N)]
+        self.reps = [to_dev(rep_host, self.dt, device, rep_off[r], f"replica {r}")
+                     for r in range(N)]
         self.grads = [to_dev(np.zeros(n, np.uint16 if self.mixed else np.float32), self.dt,
-                             device, self.grad_off[r]) for r in range(N)]
-        f32 = dict(dtype=torch.float32, device=device)
-        self.m = torch.full((n + 16,), 7.0, **f32)[state_off:state_off + n]
-        self.v = torch.full((n + 16,), 7.0, **f32)[state_off:state_off + n]
+                             device, self.grad_off[r], f"gradient {r}") for r in range(N)]
+        f32 = torch.float32
+        self.m = guarded_empty(n, f32, device, state_off, "m").fill_(7.0)
+        self.v = guarded_empty(n, f32, device, state_off, "v").fill_(7.0)
         self.master = None
         master_init = None
         if self.mixed:
-            self.master = torch.zeros(n + 16, **f32)[state_off:state_off + n]
-            master_init = to_dev(init, torch.float32, device, state_off)
+            self.master = guarded_empty(n, f32, device, state_off, "master").zero_()
+            master_init = to_dev(init, torch.float32, device, state_off, "master_init")
         self.st = abi.zero_init_states(n, N, prec, self.m, self.v, self.master, master_init)
         self.o_reps = [rep_host.copy() for _ in range(N)]
         self.o_states = oracle.init_states(n, N, prec, master_init=init, mode="fp32")
@@ -77,7 +81,7 @@ class Case:
             if self.mixed:
                 g = oracle.f32_to_bf16_rne(g)
             hs.append(g)
-            self.grads[r].copy_(to_dev(g, self.dt, self.device))
+            self.grads[r].copy_(host_tensor(g, self.dt))
         return hs
 
     def oracle_step(self, host_grads):
@@ -96,6 +100,7 @@ class Case:
         torch.cuda.synchronize()
 
     def compare(self, exact=False):
+        check_guards()  # nothing written outside any buffer
         om, ov = flat(self.o_states, "m"), flat(self.o_states, "v")
         gm, gv = host_of(self.m), host_of(self.v)
         assert_fp32_close(gm, om, "m")
@@ -398,7 +403,7 @@ def test_ddp_mean_from_host_back_to_back(abi, cuda, prec):
     mixed = prec == oracle.BF16_MIXED
     dt = torch.bfloat16 if mixed else torch.float32
     rng = np.random.default_rng(77)
-    staging = [torch.empty(n, dtype=dt, device=cuda) for _ in range(N)]
+    staging = [guarded_empty(n, dt, cuda, 1 + r, f"staging {r}") for r in range(N)]
     h2d, d2h = torch.cuda.Stream(), torch.cuda.Stream()
     calls = []
     for _ in range(3):
@@ -595,7 +600,7 @@ def test_zero_and_subnormal_state_bitwise(abi, cuda, prec):
             if c.mixed:
                 g = oracle.f32_to_bf16_rne(g)
             hs.append(g)
-            c.grads[r].copy_(to_dev(g, c.dt, cuda))
+            c.grads[r].copy_(host_tensor(g, c.dt))
         c.oracle_step(hs)
         c.gpu_step()
         torch.cuda.synchronize()

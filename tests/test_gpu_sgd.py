@@ -12,8 +12,9 @@ import pytest
 import torch
 
 import oracle
-from parity_util import assert_bf16_within_one_ulp, assert_fp32_close, exact_fraction, flat
-from test_gpu_parity import host_of, to_dev
+from parity_util import (assert_bf16_within_one_ulp, assert_fp32_close, check_guards,
+                         exact_fraction, flat, guarded_empty)
+from test_gpu_parity import host_of, host_tensor, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -39,18 +40,19 @@ class SgdCase:
         grad_off = grad_off or [0] * N
         init = self.rng.normal(0, 0.5, n).astype(np.float32)
         rep_host = oracle.f32_to_bf16_rne(init) if self.mixed else init
-        self.reps = [to_dev(rep_host, self.dt, device, rep_off[r]) for r in range(N)]
+        self.reps = [to_dev(rep_host, self.dt, device, rep_off[r], f"replica {r}")
+                     for r in range(N)]
         self.grads = [to_dev(np.zeros(n, np.uint16 if self.mixed else np.float32), self.dt,
-                             device, grad_off[r]) for r in range(N)]
-        f32 = dict(dtype=torch.float32, device=device)
+                             device, grad_off[r], f"gradient {r}") for r in range(N)]
+        f32 = torch.float32
         self.buf = None
         if self.mu:
-            self.buf = torch.full((n + 16,), 7.0, **f32)[state_off:state_off + n]
+            self.buf = guarded_empty(n, f32, device, state_off, "momentum buffer").fill_(7.0)
         self.master = None
         master_init = None
         if self.mixed:
-            self.master = torch.zeros(n + 16, **f32)[state_off:state_off + n]
-            master_init = to_dev(init, torch.float32, device, state_off)
+            self.master = guarded_empty(n, f32, device, state_off, "master").zero_()
+            master_init = to_dev(init, torch.float32, device, state_off, "master_init")
         self.st = abi.zero_init_states(n, N, prec, self.buf, None, self.master, master_init,
                                        bounds=bounds)
         self.bounds = bounds
@@ -66,7 +68,7 @@ class SgdCase:
             if self.mixed:
                 g = oracle.f32_to_bf16_rne(g)
             hs.append(g)
-            self.grads[r].copy_(to_dev(g, self.dt, self.device))
+            self.grads[r].copy_(host_tensor(g, self.dt))
         return hs
 
     def kw(self):
@@ -87,6 +89,7 @@ class SgdCase:
         return out
 
     def compare(self):
+        check_guards()  # nothing written outside any buffer
         if self.mu:
             ob = flat(self.o_states, "buf")
             gb = host_of(self.buf)
@@ -197,7 +200,7 @@ def test_sgd_clipped_and_scaled(abi, cuda, prec):
         if c.mixed:
             c.master.copy_(torch.from_numpy(flat(c.o_states, "master")))
         for r in range(N):
-            c.reps[r].copy_(to_dev(c.o_reps[r], c.dt, cuda))
+            c.reps[r].copy_(host_tensor(c.o_reps[r], c.dt))
 
 
 def test_sgd_range_partition_is_bitwise_full_step(abi, cuda):
