@@ -462,6 +462,106 @@ def host_link_timer(dev_in, host_in, host_out, dev_out, stream, chunk: int):
     return run
 
 
+def producer_report(opt, reps, grads, wl, stream, iters: int, gaps_us=(0, 200)) -> dict:
+    """The bucket streamer against a gradient producer, as in a backward pass:
+    a producer stream writes each 25 MiB bucket of every rank's gradient in
+    reverse index order (a copy from a second set of gradient buffers, 2 bytes
+    read and written per element and rank) and records that bucket's ready
+    event; the step runs each bucket on a side stream once its event fires.
+    ``gap_us`` > 0 puts a bounded single-thread busy wait of that length on the
+    producer stream before every bucket, standing in for the backward compute
+    that produces it (it uses no memory bandwidth). Reported per mode, in ms
+    per step (mean over ``iters`` steps, each bracketed by synchronisation):
+      producer_ms   the producer alone;
+      overlapped_ms producer start to the last bucket stepped;
+      tail_ms       the last bucket's ready event to the last bucket stepped
+                    (what of the step is exposed after the gradients are in);
+    and once, the bucketed step whose ready events have all fired before it
+    is queued (the waits stay on the stream), against the same step with no
+    waits: whether the programmatic chaining of bucket launches survives the
+    event waits between them."""
+    import torch
+    ranges = opt.bucket_ranges(wl.bucket_bytes)
+    src = [g.clone() for g in grads]
+    producer, side = torch.cuda.Stream(), torch.cuda.Stream()
+    T = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    # the busy wait counts SM clock cycles: calibrate cycles per microsecond
+    a, b = T(), T()
+    torch.cuda.synchronize()
+    a.record(producer)
+    with torch.cuda.stream(producer):
+        torch.cuda._sleep(4_000_000)
+    b.record(producer)
+    torch.cuda.synchronize()
+    clock_mhz = 4_000_000 / (a.elapsed_time(b) * 1e3)
+
+    def produce(ready, gap_us):
+        with torch.cuda.stream(producer):
+            for k, (lo, hi) in enumerate(ranges):
+                if gap_us:
+                    torch.cuda._sleep(int(gap_us * clock_mhz))
+                for d, s_ in zip(grads, src):
+                    d[lo:hi].copy_(s_[lo:hi])
+                ready[k].record(producer)
+
+    def one(gap_us, with_step):
+        ready = [T() for _ in ranges]
+        t0, t1, done = T(), T(), T()
+        torch.cuda.synchronize()
+        t0.record(stream)
+        producer.wait_event(t0)
+        side.wait_event(t0)
+        produce(ready, gap_us)
+        if with_step:
+            opt.step_bucketed(reps, grads, ready, side, wl.bucket_bytes, done=done)
+            stream.wait_event(done)
+        stream.wait_stream(producer)
+        t1.record(stream)
+        torch.cuda.synchronize()
+        tail = ready[-1].elapsed_time(done) if with_step else None
+        return t0.elapsed_time(t1), tail
+
+    modes = []
+    for gap in gaps_us:
+        one(gap, True)  # warm-up of this mode
+        alone = [one(gap, False)[0] for _ in range(iters)]
+        both = [one(gap, True) for _ in range(iters)]
+        modes.append({"gap_us_per_bucket": gap,
+                      "producer_ms": statistics.mean(alone),
+                      "overlapped_ms": statistics.mean(x[0] for x in both),
+                      "tail_ms": statistics.mean(x[1] for x in both),
+                      "tail_ms_max": max(x[1] for x in both)})
+
+    def bucketed_ms(with_events):
+        ready = [T() for _ in ranges]
+        if with_events:
+            produce(ready, 0)
+        torch.cuda.synchronize()
+        t0, t1 = T(), T()
+        side.wait_stream(stream)
+        t0.record(side)
+        opt.step_bucketed(reps, grads, ready if with_events else None, side, wl.bucket_bytes)
+        t1.record(side)
+        torch.cuda.synchronize()
+        return t0.elapsed_time(t1)
+
+    bucketed_ms(True)
+    fired = statistics.median(bucketed_ms(True) for _ in range(iters))
+    no_waits = statistics.median(bucketed_ms(False) for _ in range(iters))
+    del src
+    full_bucket = max(hi - lo for lo, hi in ranges)
+    return {"what": "the bucket streamer against a producer stream writing 25 MiB buckets of "
+                    "every rank's gradient in reverse index order (a copy, HBM-bound), optionally "
+                    "after a bounded busy wait per bucket standing in for backward compute",
+            "buckets": len(ranges), "full_bucket_params": full_bucket,
+            "last_bucket_params": ranges[-1][1] - ranges[-1][0],
+            "modes": modes,
+            "step_with_fired_events_ms": fired,
+            "step_without_events_ms": no_waits,
+            "busy_wait_cycles_per_us": clock_mhz,
+            "iters": iters}
+
+
 def run_gpu(args, wl, rank: int, world: int, local_rank: int) -> dict | None:
     import torch
     import torch.distributed as dist
@@ -495,7 +595,7 @@ def run_gpu(args, wl, rank: int, world: int, local_rank: int) -> dict | None:
     bucketed = wl.bucket_bytes > 0 and not ddp
     launches_per_step = len(opt.bucket_ranges(wl.bucket_bytes)) if bucketed else 1
     if clip:
-        launches_per_step = 3       # norm partials, norm total, clipped step
+        launches_per_step = 2       # norm partials, then the step that adds them
     if stage3:
         launches_per_step += 1      # the gather after the owner-only step
     stream = torch.cuda.current_stream()
@@ -540,6 +640,9 @@ def run_gpu(args, wl, rank: int, world: int, local_rank: int) -> dict | None:
     dist_ms = [percentile(step_times, q) for q in (10, 50, 90)]
 
     ms_step, kernel_ms = max_over_ranks([ms_step, kernel_ms], dev, world)
+    producer = None
+    if bucketed and args.producer:
+        producer = producer_report(opt, reps, grads, wl, stream, iters=10)
 
     # ---- end to end through the public API: host gradients in, parameters out
     E2E_BLOCK = 5
@@ -556,8 +659,9 @@ def run_gpu(args, wl, rank: int, world: int, local_rank: int) -> dict | None:
     def e2e_path(o):
         if o.max_grad_norm > 0:
             return ("ZeroOptimizer.step with pinned host gradients -> zero_step_from_host_ex "
-                    "with clipping: every 25 MiB chunk copied in on a copy stream, the norm "
-                    "once all have arrived, then the clipped step chunk by chunk, each chunk's "
+                    "with clipping: every 25 MiB chunk copied in on a copy stream, its part of "
+                    "the norm summed once it has arrived, the norm's total once all have, then "
+                    "the clipped step chunk by chunk, each chunk's "
                     "D2H on a second copy stream while the next is stepped")
         entry = ("zero_step_from_host_ex" if o.stage == 3 or o.optimizer == "sgd"
                  or o.grad_scale != 1.0 else "zero_step_from_host")
@@ -568,11 +672,12 @@ def run_gpu(args, wl, rank: int, world: int, local_rank: int) -> dict | None:
                 f"{out} on a second copy stream")
 
     ddp_h2d, ddp_d2h = (torch.cuda.Stream(), torch.cuda.Stream()) if ddp else (None, None)
+    ddp_host = abi.DdpHost() if ddp else None
 
     def e2e_step():
-        if ddp:  # gradients in, the mean gradient out, chunk-pipelined
-            abi.ddp_allreduce_mean_from_host(host_grads, grads, wl.precision, n, host_out,
-                                             BUCKET_BYTES_25MIB, None, ddp_h2d, ddp_d2h)
+        if ddp:  # gradients in, the mean gradient out, chunk-pipelined and chained
+            ddp_host.mean_from_host(host_grads, grads, wl.precision, n, host_out,
+                                    BUCKET_BYTES_25MIB, None, ddp_h2d, ddp_d2h)
         else:
             opt.step(reps, host_grads, host_params_out=host_out)
 
@@ -612,9 +717,10 @@ def run_gpu(args, wl, rank: int, world: int, local_rank: int) -> dict | None:
                         f"another), no step: the e2e lower bound on this host link; timed in "
                         f"blocks of {E2E_BLOCK} back-to-back steps alternating with the e2e "
                         f"blocks",
-           "path": ("ddp_allreduce_mean_from_host with pinned host gradients: 25 MiB chunks, "
-                    "H2D on a copy stream, the mean per chunk on the compute stream, D2H of "
-                    "the mean on a second copy stream") if ddp else
+           "path": ("ddp_allreduce_mean_from_host_h with pinned host gradients: 25 MiB "
+                    "chunks, H2D on a copy stream, the mean per chunk on the compute stream, "
+                    "D2H of the mean on a second copy stream; back-to-back calls on one handle "
+                    "chained chunk by chunk") if ddp else
                    e2e_path(opt)}
 
     if rank != 0:
@@ -667,8 +773,8 @@ def run_gpu(args, wl, rank: int, world: int, local_rank: int) -> dict | None:
                      "algorithmic_bytes_per_launch": step_bytes // per,
                      "kernel": ("allreduce_mean_tma_kernel" if wl.N <= 8 else
                                 "allreduce_mean_kernel") if ddp else
-                               ("grad_norm_partials_kernel + grad_norm_total_kernel + "
-                                "zero_step_tma_kernel (whole clipped step)") if clip else
+                               ("grad_norm_partials_kernel + zero_step_tma_kernel adding "
+                                "the partials (whole clipped step)") if clip else
                                ("zero_step_tma_kernel (owner-only) + gather_tma_kernel "
                                 "(whole stage-3 step)") if stage3 else
                                ("zero_step_tma_kernel" if wl.N <= 8 else "zero_step_kernel"),
@@ -678,6 +784,8 @@ def run_gpu(args, wl, rank: int, world: int, local_rank: int) -> dict | None:
         "clocks": clocks,
         "e2e": e2e,
     }
+    if producer is not None:
+        line["producer"] = producer
     if args.cpu_baseline and world == 1:
         line["cpu_baseline"] = cpu_baseline(wl, op=args.op)
         line["cpu_baseline"]["all_cores"] = cpu_baseline_all_cores(wl, op=args.op)
@@ -731,6 +839,8 @@ def main(argv=None):
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(inputs.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    ap.add_argument("--no-producer", dest="producer", action="store_false",
+                    help="bucket-streamed workloads: skip the step-against-a-producer report")
     ap.add_argument("--partition", default="array_split", choices=["array_split", "tensor"],
                     help="tensor: shards of whole tensors (workloads with a tensor list)")
     ap.add_argument("--max-grad-norm", type=float, default=0.0,

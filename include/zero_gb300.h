@@ -193,11 +193,13 @@ int zero_grad_norm_sq(const void *const *grads, int64_t n, int32_t N, int32_t pr
  *   grads, n, N, precision, stream : as zero_grad_norm_sq.
  *   norm_sq : DEVICE scalar receiving ||(1/N) sum_r g_r||^2 (caller-owned).
  * The first call on a device, with that device current, looks up the device
- * address of the array (a host-side runtime call); make that first call
- * before any stream capture. Every call shares the one array: calls whose
- * work can overlap on the GPU (other streams, other host threads) race and
- * must be ordered by the caller. Each call writes every partial it reads, so
- * nothing needs clearing between calls.
+ * address of the array (a host-side runtime call) and keeps it for the life
+ * of the process; make that first call before any stream capture, and do not
+ * use this entry point on a device after cudaDeviceReset (the kept address
+ * would be stale). Every call shares the one array: calls whose work can
+ * overlap on the GPU (other streams, other host threads) race and must be
+ * ordered by the caller. No other entry point uses the array. Each call
+ * writes every partial it reads, so nothing needs clearing between calls.
  * Errors: as zero_grad_norm_sq, plus EINVAL when n > ZERO_NOALLOC_MAX_N
  * (use zero_grad_norm_sq with your own scratch above that). */
 #define ZERO_NOALLOC_MAX_N 2147450880LL /* 65,535 partials x 32,768 elements */
@@ -216,9 +218,10 @@ typedef struct zero_step_opts {
    * coefficient min(1, max_grad_norm / (grad_scale * sqrt(*norm_sq) + 1e-6));
    * <= 0: no clipping. */
   double max_grad_norm;
-  /* DEVICE scalar from zero_grad_norm_sq on the same gradients, read on the
-   * device when the step runs (no host synchronisation); required when
-   * clipping, ignored otherwise. */
+  /* DEVICE scalar, required when clipping, ignored otherwise. Without
+   * norm_scratch it is an INPUT: the squared norm from zero_grad_norm_sq on
+   * the same gradients, read on the device when the step runs (no host
+   * synchronisation). With norm_scratch it is an OUTPUT (see below). */
   const double *norm_sq;
   int64_t lo, hi;        /* index range of the step; hi < 0 means n */
   /* Nonzero: ZeRO stage 3 ("Data parallelism and ZeRO stages 1 to 3",
@@ -227,6 +230,17 @@ typedef struct zero_step_opts {
    * other replica element is left as it was (released). zero_gather brings the
    * replicas back to the full parameters. 0: the stage-1/2 step. */
   int32_t owner_only;
+  /* NULL, or (when clipping) a DEVICE buffer of at least norm_scratch_count
+   * >= zero_grad_norm_scratch_count(n) doubles, caller-owned, overwritten,
+   * 8-byte aligned and disjoint from every other buffer of the call. Given,
+   * the call computes the squared norm of the whole gradient [0, n) itself,
+   * exactly as zero_grad_norm_sq on the same buffers (bit for bit), writes it
+   * to *norm_sq and clips with it: the partial sums in one launch, then the
+   * step, which starts while that launch finishes, adds the partials in the
+   * same fixed order while its first loads are in flight, and so saves the
+   * separate total launch. The host-input step requires it when clipping. */
+  double *norm_scratch;
+  int64_t norm_scratch_count;
 } zero_step_opts_t;
 
 /* zero_step with the options above. The multiplier grad_scale * coefficient
@@ -234,7 +248,9 @@ typedef struct zero_step_opts {
  * gradient is multiplied by it (one IEEE fp32 multiply) before the update.
  * With grad_scale = 1 and no clipping the result equals zero_step bit for bit.
  * Errors: as zero_step_range, plus EINVAL for a bad grad_scale or
- * max_grad_norm, or clipping without norm_sq. */
+ * max_grad_norm, clipping without norm_sq, a norm_scratch that is too small
+ * or overlaps another buffer; EALIGN for a misaligned norm_scratch or
+ * norm_sq. */
 int zero_step_ex(void *const *params, const void *const *grads, zero_states_t *st,
                  const zero_step_opts_t *opts, zero_stream_t stream);
 
@@ -255,6 +271,8 @@ typedef struct zero_sgd_opts {
   const double *norm_sq; /* as zero_step_opts_t */
   int64_t lo, hi;        /* index range of the step; hi < 0 means n */
   int32_t owner_only;    /* as zero_step_opts_t: ZeRO stage 3 */
+  double *norm_scratch;  /* as zero_step_opts_t */
+  int64_t norm_scratch_count;
 } zero_sgd_opts_t;
 
 /* The fused ZeRO step with momentum SGD on each shard: reduce-scatter-mean
@@ -369,21 +387,20 @@ int zero_step_from_host(void *const *params, const void *const *host_grads,
  * zero_step_sgd (momentum SGD): exactly one of `adamw` and `sgd` is non-NULL.
  * Their step number, hyperparameters, grad_scale, clipping and owner_only are
  * used; the range must be the whole vector (lo = 0, hi = -1 or n).
- * Clipping (max_grad_norm > 0): the global norm needs the whole gradient, so
- * every chunk is copied in first; then the call itself computes the squared
- * norm, as zero_grad_norm_sq_noalloc does (bit for bit what zero_grad_norm_sq
- * gives), into *norm_sq. Here norm_sq is an OUTPUT: a DEVICE double the caller
- * provides. The chunks are then stepped in order, each copied back while the
- * next is stepped. This uses the library's own norm scratch, so n <=
- * ZERO_NOALLOC_MAX_N, and calls whose norms overlap on the GPU must not
- * share it (see zero_grad_norm_sq_noalloc).
+ * Clipping (max_grad_norm > 0) needs norm_scratch (see zero_step_opts_t) and
+ * norm_sq, an OUTPUT here: the global norm needs the whole gradient, so the
+ * partial sums of each chunk's part of the norm run as soon as that chunk has
+ * arrived, the fixed-order total once every chunk is in (bit for bit what
+ * zero_grad_norm_sq gives on the staging buffers), and only then are the
+ * chunks stepped in order, each copied back while the next is stepped.
  * With owner_only (ZeRO stage 3) the replicas stay released, and
  * host_params_out still receives the full updated parameters: each piece of a
  * chunk is copied from its owner's replica. Otherwise as zero_step_from_host.
  * SGD needs a state initialised for it (zero_init_states with v = NULL).
  * Errors: as zero_step_from_host, plus EINVAL for no or both option sets, a
- * partial range, bad options, clipping without norm_sq or with n >
- * ZERO_NOALLOC_MAX_N; EALIGN for a misaligned norm_sq. */
+ * partial range, bad options, clipping without norm_sq or norm_scratch, a
+ * norm_scratch that is too small or overlaps a staging buffer; EALIGN for a
+ * misaligned norm_sq or norm_scratch. */
 int zero_step_from_host_ex(void *const *params, const void *const *host_grads,
                            void *const *staging, zero_states_t *st,
                            const zero_step_opts_t *adamw, const zero_sgd_opts_t *sgd,
@@ -428,6 +445,34 @@ int ddp_allreduce_mean_from_host(const void *const *host_grads, void *const *sta
                                  int32_t N, int32_t precision, void *host_mean_out,
                                  int64_t chunk_bytes, zero_stream_t compute, zero_stream_t h2d,
                                  zero_stream_t d2h);
+
+/* A host handle for back-to-back DDP means of host gradients. Consecutive
+ * ddp_allreduce_mean_from_host_h calls on one handle with the same staging
+ * buffers, n, N, precision and chunk size are chained chunk by chunk: the copy
+ * of chunk k waits only for the previous call's mean of chunk k and its copy
+ * back to the host, not for everything queued on `compute`, so the next call's
+ * copies overlap the previous call's tail (the pipeline of "Data parallelism
+ * and ZeRO stages 1 to 3", section 2, "DDP", over a stream of steps). The
+ * staging buffers then belong to the handle's calls: device work that reads
+ * or writes them between two calls (using the mean on the device, say) is not
+ * waited for by the next call's copies unless the caller orders it on `h2d`,
+ * or calls zero_ddp_host_reset first (the next call then waits for
+ * everything queued on `compute`, as ddp_allreduce_mean_from_host always
+ * does). A handle serves one device and one host thread at a time; it keeps
+ * 2*ceil(n/B)+2 CUDA events, created on first use.
+ * Errors: EINVAL (NULL), ENOMEM. */
+typedef struct zero_ddp_host zero_ddp_host_t;
+int zero_ddp_host_create(zero_ddp_host_t **out);
+int zero_ddp_host_reset(zero_ddp_host_t *h);
+int zero_ddp_host_free(zero_ddp_host_t *h); /* NULL is a no-op */
+
+/* ddp_allreduce_mean_from_host on a handle (chained as described above); the
+ * results are the same bits. Errors: as ddp_allreduce_mean_from_host, plus
+ * EINVAL for a NULL handle or a handle used before on another device. */
+int ddp_allreduce_mean_from_host_h(zero_ddp_host_t *h, const void *const *host_grads,
+                                   void *const *staging, int64_t n, int32_t N, int32_t precision,
+                                   void *host_mean_out, int64_t chunk_bytes, zero_stream_t compute,
+                                   zero_stream_t h2d, zero_stream_t d2h);
 
 /* ---------------------------------------------------------------- memory -- */
 

@@ -127,7 +127,7 @@ def test_raw_argument_checks_before_any_device_work(abi):
     assert abi.raw_call("ddp_allreduce_mean", same, 10, 2, 0, None) == abi.ZERO_EINVAL
     odd = (vp * 2)(4097, 8192)
     assert abi.raw_call("ddp_allreduce_mean", odd, 10, 2, 1, None) == abi.ZERO_EALIGN
-    assert "overlap" in abi.raw_call.__globals__["_lib"].zero_last_error().decode() or True
+    assert "aligned" in abi.zero_last_error()
     assert abi.raw_call("zero_free_states", None) == abi.ZERO_OK
 
 
@@ -158,7 +158,7 @@ def test_init_states_rejects_bad_bounds_before_device_work(abi):
         code = abi.raw_call("zero_init_states_ex", 10, N, 0, 4096, 8192, None, None, arr, None,
                             ctypes.byref(h))
         assert code == abi.ZERO_EINVAL
-        assert "bounds" in abi.raw_call.__globals__["_lib"].zero_last_error().decode()
+        assert "bounds" in abi.zero_last_error()
 
 
 def test_option_structs_match_the_header(abi, tmp_path):
@@ -220,8 +220,8 @@ def test_sgd_and_gather_argument_checks(abi):
 
 def test_host_input_step_option_checks(abi):
     """zero_step_from_host_ex takes exactly one option set and the whole vector,
-    and clipping only with a norm_sq output; each refusal comes before any
-    device work."""
+    and clipping only with a norm_sq output and the caller's norm scratch; each
+    refusal comes before any device work."""
     vp = ctypes.c_void_p
     h = vp()
     assert abi.raw_call("zero_init_states", 0, 2, 0, None, None, None, None, None,
@@ -255,8 +255,12 @@ def test_host_input_step_option_checks(abi):
                abi.SgdOpts(1, -0.1, 0.9, 0.0, 0.0, 0, 1.0, 0.0, None, 0, -1, 0)]  # lr < 0
     for o in bad_sgd:
         assert call(None, o) == abi.ZERO_EINVAL
-    # clipping with a norm_sq output is accepted (n = 0: nothing to queue)
-    clip_ok = abi.StepOpts(1, 1e-3, 0.9, 0.999, 1e-8, 0.01, 1.0, 1.0, 4096, 0, -1, 0)
+    # clipping needs the caller's norm scratch as well as the norm_sq output
+    no_scratch = abi.StepOpts(1, 1e-3, 0.9, 0.999, 1e-8, 0.01, 1.0, 1.0, 4096, 0, -1, 0)
+    assert call(no_scratch, None) == abi.ZERO_EINVAL
+    assert "norm_scratch" in abi.zero_last_error()
+    # with both it is accepted (n = 0: nothing to queue)
+    clip_ok = abi.StepOpts(1, 1e-3, 0.9, 0.999, 1e-8, 0.01, 1.0, 1.0, 4096, 0, -1, 0, 8192, 1)
     assert call(clip_ok, None) == abi.ZERO_OK
     # chunk size below one vector of elements is refused too
     assert abi.raw_call("zero_step_from_host_ex", empty, empty, empty, h, ctypes.byref(ad), None,
@@ -285,3 +289,28 @@ def test_ddp_mean_from_host_argument_checks(abi):
     assert call(host, (vp * 2)(64, 18), 10, 2, abi.ZERO_FP32, mib) == abi.ZERO_EALIGN
     assert call(host, (vp * 2)(64, 64), 10, 2, abi.ZERO_FP32, mib) == abi.ZERO_EINVAL  # same
     assert call(host, (vp * 2)(64, 96), 10, 2, abi.ZERO_FP32, mib) == abi.ZERO_EINVAL  # overlap
+
+
+def test_ddp_host_handle_checks(abi):
+    """The DDP host-input handle: create, reset and free; a NULL handle and
+    the whole-vector argument checks are refused before any device work."""
+    vp = ctypes.c_void_p
+    h = vp()
+    assert abi.raw_call("zero_ddp_host_create", ctypes.byref(h)) == abi.ZERO_OK
+    assert h.value
+    assert abi.raw_call("zero_ddp_host_create", None) == abi.ZERO_EINVAL
+    assert abi.raw_call("zero_ddp_host_reset", h) == abi.ZERO_OK
+    assert abi.raw_call("zero_ddp_host_reset", None) == abi.ZERO_EINVAL
+    host = (vp * 2)(4096, 8192)
+    staging = (vp * 2)(1 << 20, 1 << 21)
+    same = (vp * 2)(1 << 20, 1 << 20)
+    call = lambda hh, st, n=100, N=2, prec=0, chunk=1 << 20: abi.raw_call(  # noqa: E731
+        "ddp_allreduce_mean_from_host_h", hh, host, st, n, N, prec, None, chunk, None, None, None)
+    assert call(None, staging) == abi.ZERO_EINVAL            # no handle
+    assert call(h, same) == abi.ZERO_EINVAL                  # the same staging buffer twice
+    assert call(h, staging, N=0) == abi.ZERO_EINVAL          # no ranks
+    assert call(h, staging, chunk=2) == abi.ZERO_EINVAL      # a chunk below one element
+    assert call(h, staging, prec=2) == abi.ZERO_EINVAL       # not a gradient precision
+    assert call(h, staging, n=0) == abi.ZERO_OK              # nothing to do
+    assert abi.raw_call("zero_ddp_host_free", h) == abi.ZERO_OK
+    assert abi.raw_call("zero_ddp_host_free", None) == abi.ZERO_OK

@@ -151,13 +151,16 @@ def test_host_input_step_stays_in_bounds(abi, cuda, prec, clip):
     count = abi.zero_grad_norm_scratch_count(n, prec)
     scratch = guarded_empty(count, torch.float64, cuda, 0, "norm scratch")
     ref_norm = guarded_empty(1, torch.float64, cuda, 0, "reference norm_sq")
+    host_scratch = guarded_empty(count, torch.float64, cuda, 0, "host-input norm scratch")
     for t in (1, 2):
         o = abi.StepOpts(t, HP["lr"], HP["beta1"], HP["beta2"], HP["eps"], HP["weight_decay"],
-                         1.0, 0.05 if clip else 0.0, norm.data_ptr() if clip else None, 0, -1, 0)
+                         1.0, 0.05 if clip else 0.0, norm.data_ptr() if clip else None, 0, -1, 0,
+                         host_scratch.data_ptr() if clip else None, count if clip else 0)
         abi.zero_step_from_host_ex(a.reps, host, staging, a.st, adamw=o, host_params_out=out,
                                    chunk_bytes=40_006, h2d=h2d, d2h=d2h)
         if clip:
-            abi.zero_grad_norm_sq(b.grads, prec, scratch, ref_norm, n)
+            # the norm of the same buffers (its chunking follows their 16-byte phase)
+            abi.zero_grad_norm_sq(staging, prec, scratch, ref_norm, n)
         abi.zero_step_ex(b.reps, b.grads, b.st, t, max_grad_norm=0.05 if clip else 0.0,
                          norm_sq=ref_norm if clip else None, **HP)
         torch.cuda.synchronize()

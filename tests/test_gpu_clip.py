@@ -127,3 +127,83 @@ def test_optimizer_clipping_host_and_device_agree(abi, cuda):
         assert all(torch.equal(x, y) for x, y in zip(pa, pb))
         assert_fp32_close(host_of(pa[0]), o_reps[0], f"t={t}")
         assert_fp32_close(host_of(a.m), flat(o_st, "m"), f"t={t} m")
+
+
+@pytest.mark.parametrize("prec", [oracle.FP32, oracle.BF16_MIXED])
+@pytest.mark.parametrize("n,N,kind", [(1_000_003, 4, "adamw"), (1_000_003, 8, "adamw"),
+                                      (300_007, 2, "adamw"), (300_007, 3, "owner_only"),
+                                      (300_007, 1, "adamw"), (65_537, 13, "adamw"),
+                                      (500_009, 4, "sgd"), (50_011, 4, "mixed_phase"),
+                                      (4099, 3, "adamw"), (2000, 4, "empty_range")])
+def test_step_computing_its_own_norm_equals_two_calls(abi, cuda, prec, n, N, kind):
+    """zero_step_ex / zero_step_sgd given norm_scratch: the norm's partial sums
+    in one launch, the step adding them itself. Bitwise the same as
+    zero_grad_norm_sq followed by the step that reads the norm, in every
+    kernel shape (lock-step and warp-specialised bulk-copy loops, register
+    streaming for N = 1, N > 8 and mixed 16-byte phases), the norm scalar
+    included; for an empty range only the norm is written."""
+    from test_gpu_sgd import SgdCase
+    kw = {}
+    if kind == "mixed_phase":
+        kw = dict(rep_off=[1, 2, 3, 0], grad_off=[0, 0, 0, 1], state_off=0)
+    if kind == "sgd":
+        a = SgdCase(abi, cuda, n, N, prec, "damped_wd", seed=81)
+        b = SgdCase(abi, cuda, n, N, prec, "damped_wd", seed=81)
+    else:
+        a = Case(abi, cuda, n, N, prec, seed=81, **kw)
+        b = Case(abi, cuda, n, N, prec, seed=81, **kw)
+    count = abi.zero_grad_norm_scratch_count(n, prec)
+    scratch = torch.empty(count, dtype=torch.float64, device=cuda)
+    norm_a = torch.full((1,), -1.0, dtype=torch.float64, device=cuda)
+    ref_scratch = torch.empty(count, dtype=torch.float64, device=cuda)
+    norm_b = torch.empty(1, dtype=torch.float64, device=cuda)
+    lo, hi = (700, 700) if kind == "empty_range" else (0, -1)
+    for t in (1, 2):
+        a.new_grads(scale=1e-2)
+        for r in range(N):
+            b.grads[r].copy_(a.grads[r])
+        abi.zero_grad_norm_sq(b.grads, prec, ref_scratch, norm_b, n)
+        if kind == "sgd":
+            abi.zero_step_sgd(a.reps, a.grads, a.st, t, max_grad_norm=0.05, norm_sq=norm_a,
+                              norm_scratch=scratch, lo=lo, hi=hi, **a.kw())
+            abi.zero_step_sgd(b.reps, b.grads, b.st, t, max_grad_norm=0.05, norm_sq=norm_b,
+                              lo=lo, hi=hi, **b.kw())
+        else:
+            own = kind == "owner_only"
+            abi.zero_step_ex(a.reps, a.grads, a.st, t, max_grad_norm=0.05, norm_sq=norm_a,
+                             norm_scratch=scratch, grad_scale=0.5, lo=lo, hi=hi, owner_only=own,
+                             **HP)
+            abi.zero_step_ex(b.reps, b.grads, b.st, t, max_grad_norm=0.05, norm_sq=norm_b,
+                             grad_scale=0.5, lo=lo, hi=hi, owner_only=own, **HP)
+        torch.cuda.synchronize()
+        assert torch.equal(norm_a, norm_b), (float(norm_a), float(norm_b))
+        assert float(norm_a) > 0.05 ** 2  # the case clips
+        pairs = list(zip(a.reps, b.reps))
+        if kind == "sgd":
+            pairs.append((a.buf, b.buf))
+        else:
+            pairs += [(a.m, b.m), (a.v, b.v)]
+        if a.mixed:
+            pairs.append((a.master, b.master))
+        for x, y in pairs:
+            assert torch.equal(x, y)
+
+
+def test_step_computing_its_own_norm_rejects_bad_scratch(abi, cuda):
+    n, N = 100_000, 2
+    c = Case(abi, cuda, n, N, oracle.FP32, seed=82)
+    count = abi.zero_grad_norm_scratch_count(n, oracle.FP32)
+    scratch = torch.empty(count, dtype=torch.float64, device=cuda)
+    norm = torch.empty(1, dtype=torch.float64, device=cuda)
+    with pytest.raises(abi.ZeroError) as e:  # too small
+        abi.zero_step_ex(c.reps, c.grads, c.st, 1, max_grad_norm=1.0, norm_sq=norm,
+                         norm_scratch=scratch[:count - 1], **HP)
+    assert e.value.code == abi.ZERO_EINVAL
+    with pytest.raises(abi.ZeroError) as e:  # no output scalar
+        abi.zero_step_ex(c.reps, c.grads, c.st, 1, max_grad_norm=1.0, norm_scratch=scratch, **HP)
+    assert e.value.code == abi.ZERO_EINVAL
+    with pytest.raises(abi.ZeroError) as e:  # the scalar inside the scratch
+        abi.zero_step_ex(c.reps, c.grads, c.st, 1, max_grad_norm=1.0, norm_sq=scratch[3:4],
+                         norm_scratch=scratch, **HP)
+    assert e.value.code == abi.ZERO_EINVAL
+    torch.cuda.synchronize()

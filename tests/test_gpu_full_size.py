@@ -30,8 +30,10 @@ def sample_indices(n, N, bucket_ranges=(), k=1 << 15, seed=0):
     return np.array(sorted(idx), dtype=np.int64)
 
 
-def oracle_on_sample(wl, t, g_s, p_s, m_s, v_s, master_s):
-    """The oracle's step on the sampled sub-problem (k indices, N ranks)."""
+def oracle_on_sample(wl, t, g_s, p_s, m_s, v_s, master_s, grad_scale=1.0):
+    """The oracle's step on the sampled sub-problem (k indices, N ranks);
+    ``grad_scale`` multiplies the mean gradient (a clip multiplier formed from
+    the whole vector's norm, since the sample's own norm is not that)."""
     N, k = wl.N, len(m_s)
     b = oracle.shard_bounds(k, N)
     states = []
@@ -42,7 +44,7 @@ def oracle_on_sample(wl, t, g_s, p_s, m_s, v_s, master_s):
         states.append(st)
     reps, new = oracle.zero_step([p_s] * N, g_s, states, t, lr=wl.lr, beta1=wl.beta1,
                                  beta2=wl.beta2, eps=wl.eps, weight_decay=wl.weight_decay,
-                                 precision=wl.precision, mode="fp32")
+                                 precision=wl.precision, mode="fp32", grad_scale=grad_scale)
     cat = lambda key: np.concatenate([s[key] for s in new])  # noqa: E731
     return reps[0], cat("m"), cat("v"), (cat("master") if master_s is not None else None)
 
@@ -225,3 +227,68 @@ def test_indices_beyond_int32(abi, cuda):
     ref = oracle.allreduce_mean(g_s, wl.precision, mode="fp32")
     for r in range(N):
         assert np.array_equal(take(grads[r]), ref[r])
+
+
+def oracle_norm_sq(grads, precision, chunk=1 << 23):
+    """The oracle's squared norm of the whole mean gradient, from host copies
+    of the device gradients taken chunk by chunk (squared norms add over
+    disjoint chunks)."""
+    n = grads[0].numel()
+    total = 0.0
+    for lo in range(0, n, chunk):
+        hi = min(n, lo + chunk)
+        part = [inputs.to_numpy_storage(g[lo:hi]) for g in grads]
+        total += oracle.grad_norm(part, precision=precision, mode="fp32") ** 2
+    return total
+
+
+@pytest.mark.parametrize("name", ["gpt2_small", "fp32_320m"])
+def test_full_size_sampled_clipped(abi, cuda, name):
+    """Sharded global-norm clipping at full size, as the bench's clipped line
+    runs it: ZeroOptimizer with max_grad_norm and device gradients, so
+    zero_step_ex forms the norm itself (thousands of 32,768-element partial
+    sums, added in the step's prologue). The norm against the oracle's, over
+    the whole vector; the sampled outputs against the oracle's step with the
+    clip multiplier formed from that whole-vector norm."""
+    import math
+    from zero_sharded_optimizer_gb300.optimizer import ZeroOptimizer
+    wl = inputs.WORKLOADS[name]
+    n, N = wl.n, wl.N
+    mixed = wl.precision == inputs.BF16_MIXED
+    max_norm = 1.0
+    init = inputs.init_params_fp32(n, wl, seed=2, device=cuda)
+    reps = inputs.make_replicas(init, N, wl.precision)
+    grads = inputs.make_grads(n, N, wl.precision, device=cuda)
+    opt = ZeroOptimizer(n, N, wl.precision, lr=wl.lr, betas=(wl.beta1, wl.beta2), eps=wl.eps,
+                        weight_decay=wl.weight_decay, master_init=init if mixed else None,
+                        max_grad_norm=max_norm)
+    del init
+    idx = sample_indices(n, N, seed=11 + len(name))
+    idx_d = torch.from_numpy(idx).to(cuda)
+    take = lambda x: inputs.to_numpy_storage(x[idx_d])  # noqa: E731
+    assert abi.zero_grad_norm_scratch_count(n, wl.precision) > 3000  # thousands of partials
+    for t in (1, 2):
+        p_before = take(opt.master) if mixed else take(reps[0])
+        m_before, v_before = take(opt.m), take(opt.v)
+        inputs.fill_grads(grads, wl, step=t, seed=2)
+        opt.step(reps, grads)
+        torch.cuda.synchronize()
+        ref_nsq = oracle_norm_sq(grads, wl.precision)
+        assert float(opt._norm.item()) == pytest.approx(ref_nsq, rel=1e-9)
+        mult = oracle.grad_multiplier(math.sqrt(ref_nsq), 1.0, max_norm)
+        assert mult < 0.5, "the case must clip"
+        g_s = [take(g) for g in grads]
+        ref_p, ref_m, ref_v, ref_master = oracle_on_sample(
+            wl, t, g_s, p_before, m_before, v_before, p_before if mixed else None,
+            grad_scale=mult)
+        assert_fp32_close(take(opt.m), ref_m, f"{name} t={t} m")
+        assert_fp32_close(take(opt.v), ref_v, f"{name} t={t} v")
+        if mixed:
+            assert_fp32_close(take(opt.master), ref_master, f"{name} t={t} master")
+            for r in range(N):
+                assert_bf16_within_one_ulp(take(reps[r]), ref_master, f"{name} t={t} rep {r}")
+        else:
+            for r in range(N):
+                assert_fp32_close(take(reps[r]), ref_p, f"{name} t={t} rep {r}")
+        for r in range(1, N):
+            assert torch.equal(reps[r], reps[0])

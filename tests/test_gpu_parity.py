@@ -423,6 +423,51 @@ def test_ddp_mean_from_host_back_to_back(abi, cuda, prec):
         assert np.array_equal(host_of(staging[r]), ref[r])
 
 
+@pytest.mark.parametrize("prec", [oracle.FP32, oracle.BF16_MIXED])
+def test_ddp_mean_from_host_chained_on_a_handle(abi, cuda, prec):
+    """Calls on a DdpHost handle, queued back to back with no synchronisation:
+    chunk k of each call waits only for the previous call's mean and copy back
+    of chunk k. Every host copy holds its own call's mean, bit for bit; a reset
+    in the middle (after device work that reads the staging buffers) and a
+    change of chunk size both fall back to waiting for the compute stream. The
+    staging buffers sit between guard regions."""
+    n, N = 300_007, 4
+    mixed = prec == oracle.BF16_MIXED
+    dt = torch.bfloat16 if mixed else torch.float32
+    rng = np.random.default_rng(78)
+    staging = [guarded_empty(n, dt, cuda, 1 + r, f"staging {r}") for r in range(N)]
+    h2d, d2h = torch.cuda.Stream(), torch.cuda.Stream()
+    ddp = abi.DdpHost()
+    calls = []
+    for i in range(6):
+        hs = []
+        for _ in range(N):
+            g = rng.normal(0, 1, n).astype(np.float32)
+            hs.append(oracle.f32_to_bf16_rne(g) if mixed else g)
+        host = [_pinned_host(h, dt) for h in hs]
+        out = torch.empty(n, dtype=dt).pin_memory()
+        if i == 3:  # device work on the staging buffers between calls, then a reset
+            seen = staging[0].clone()
+            ddp.reset()
+        chunk = 1 << 18 if i != 4 else 3 * (1 << 16) + 6
+        ddp.mean_from_host(host, staging, prec, n, out, chunk, None, h2d, d2h)
+        calls.append((hs, out))
+        if i == 3:
+            calls.append(("seen", seen))
+    torch.cuda.synchronize()
+    last_ref = None
+    for entry in calls:
+        if entry[0] == "seen":  # the clone saw the mean of the call before it
+            assert np.array_equal(host_of(entry[1]), last_ref[0])
+            continue
+        hs, out = entry
+        last_ref = oracle.allreduce_mean(hs, precision=prec, mode="fp32")
+        assert np.array_equal(inputs.to_numpy_storage(out), last_ref[0])
+    for r in range(N):
+        assert np.array_equal(host_of(staging[r]), last_ref[r])
+    ddp.close()
+
+
 def test_ddp_mean_from_host_rejects_bad_arguments(abi, cuda):
     n, N = 1000, 3
     staging = [torch.empty(n, device=cuda) for _ in range(N)]

@@ -311,8 +311,9 @@ def test_optimizer_sgd_and_stage3_with_host_gradients(abi, cuda, prec):
 
 
 def test_clipped_host_step_checks_norm_sq_before_queuing(abi, cuda):
-    """The clipped host-input step refuses a misaligned or overlapping norm_sq
-    before any copy is queued: the staging buffers keep their contents."""
+    """The clipped host-input step refuses a misaligned or overlapping norm_sq,
+    and a missing, short, misaligned or overlapping norm scratch, before any
+    copy is queued: the staging buffers keep their contents."""
     n, N = 50_000, 2
     reps = [torch.zeros(n, device=cuda) for _ in range(N)]
     m, v = torch.empty(n, device=cuda), torch.empty(n, device=cuda)
@@ -320,9 +321,16 @@ def test_clipped_host_step_checks_norm_sq_before_queuing(abi, cuda):
     staging = [torch.full((n,), 7.0, device=cuda) for _ in range(N)]
     host = [torch.ones(n).pin_memory() for _ in range(N)]
     scalar = torch.empty(2, dtype=torch.float64, device=cuda)
-    for ptr, code in ((scalar.data_ptr() + 4, abi.ZERO_EALIGN),
-                      (staging[1].data_ptr() + 800, abi.ZERO_EINVAL)):
-        o = abi.StepOpts(1, 1e-3, 0.9, 0.999, 1e-8, 0.0, 1.0, 1.0, ptr, 0, -1, 0)
+    count = abi.zero_grad_norm_scratch_count(n, abi.ZERO_FP32)
+    scratch = torch.empty(count, dtype=torch.float64, device=cuda)
+    sp = scratch.data_ptr()
+    for ptr, sc, cnt, code in ((scalar.data_ptr() + 4, sp, count, abi.ZERO_EALIGN),
+                               (staging[1].data_ptr() + 800, sp, count, abi.ZERO_EINVAL),
+                               (scalar.data_ptr(), None, 0, abi.ZERO_EINVAL),      # no scratch
+                               (scalar.data_ptr(), sp, count - 1, abi.ZERO_EINVAL),  # too small
+                               (scalar.data_ptr(), sp + 4, count - 1, abi.ZERO_EALIGN),
+                               (scalar.data_ptr(), staging[0].data_ptr(), count, abi.ZERO_EINVAL)):
+        o = abi.StepOpts(1, 1e-3, 0.9, 0.999, 1e-8, 0.0, 1.0, 1.0, ptr, 0, -1, 0, sc, cnt)
         with pytest.raises(abi.ZeroError) as e:
             abi.zero_step_from_host_ex(reps, host, staging, st, adamw=o)
         assert e.value.code == code

@@ -76,6 +76,11 @@ _SIGNATURES = {
     "ddp_allreduce_mean": (ctypes.c_int, [_P(_vp), _i64, _i32, _i32, _vp]),
     "ddp_allreduce_mean_from_host": (ctypes.c_int, [_P(_vp), _P(_vp), _i64, _i32, _i32, _vp,
                                                     _i64, _vp, _vp, _vp]),
+    "zero_ddp_host_create": (ctypes.c_int, [_P(_vp)]),
+    "zero_ddp_host_reset": (ctypes.c_int, [_vp]),
+    "zero_ddp_host_free": (ctypes.c_int, [_vp]),
+    "ddp_allreduce_mean_from_host_h": (ctypes.c_int, [_vp, _P(_vp), _P(_vp), _i64, _i32, _i32,
+                                                      _vp, _i64, _vp, _vp, _vp]),
     "zero_memory_bytes": (ctypes.c_int, [_i64, _i32, _i32, _i32, _P(_u64)]),
     "zero_memory_breakdown": (ctypes.c_int, [_i64, _i32, _i32, _i32, _i32, _P(_u64)]),
     "zero_grad_norm_scratch_count": (ctypes.c_int, [_i64, _i32, _P(_i64)]),
@@ -334,7 +339,8 @@ class StepOpts(ctypes.Structure):
     """zero_step_opts_t."""
     _fields_ = [("t", _i64), ("lr", _dbl), ("beta1", _dbl), ("beta2", _dbl), ("eps", _dbl),
                 ("weight_decay", _dbl), ("grad_scale", _dbl), ("max_grad_norm", _dbl),
-                ("norm_sq", _vp), ("lo", _i64), ("hi", _i64), ("owner_only", _i32)]
+                ("norm_sq", _vp), ("lo", _i64), ("hi", _i64), ("owner_only", _i32),
+                ("norm_scratch", _vp), ("norm_scratch_count", _i64)]
 
 
 def _f64_device_ptr(t, count: int, what: str):
@@ -377,16 +383,27 @@ def zero_grad_norm_sq_noalloc(grads, precision: int, norm_sq, n: int | None = No
            "zero_grad_norm_sq_noalloc")
 
 
+def _scratch_args(norm_scratch):
+    if norm_scratch is None:
+        return None, 0
+    return _f64_device_ptr(norm_scratch, 1, "norm_scratch"), norm_scratch.numel()
+
+
 def zero_step_ex(params, grads, st: ZeroStates, t: int, lr: float, beta1: float = 0.9,
                  beta2: float = 0.999, eps: float = 1e-8, weight_decay: float = 0.0,
                  grad_scale: float = 1.0, max_grad_norm: float = 0.0, norm_sq=None,
-                 lo: int = 0, hi: int = -1, stream=None, owner_only: bool = False):
+                 lo: int = 0, hi: int = -1, stream=None, owner_only: bool = False,
+                 norm_scratch=None):
     """``owner_only`` (ZeRO-3): write the new parameters into the owner's
-    replica over its own shard only; ``zero_gather`` restores the replicas."""
+    replica over its own shard only; ``zero_gather`` restores the replicas.
+    Clipping: ``norm_sq`` is the squared norm from zero_grad_norm_sq, or, with
+    ``norm_scratch`` (a float64 CUDA tensor of zero_grad_norm_scratch_count
+    elements), the scalar this call computes the norm into itself."""
     pp, gp = _step_ptrs(params, grads, st)
     nq = None if norm_sq is None else _f64_device_ptr(norm_sq, 1, "norm_sq")
+    sc, count = _scratch_args(norm_scratch)
     o = StepOpts(t, lr, beta1, beta2, eps, weight_decay, grad_scale, max_grad_norm, nq, lo, hi,
-                 1 if owner_only else 0)
+                 1 if owner_only else 0, sc, count)
     _check(_lib.zero_step_ex(pp, gp, st.handle, ctypes.byref(o), _stream(stream)), "zero_step_ex")
 
 
@@ -395,19 +412,21 @@ class SgdOpts(ctypes.Structure):
     _fields_ = [("t", _i64), ("lr", _dbl), ("momentum", _dbl), ("dampening", _dbl),
                 ("weight_decay", _dbl), ("nesterov", _i32), ("grad_scale", _dbl),
                 ("max_grad_norm", _dbl), ("norm_sq", _vp), ("lo", _i64), ("hi", _i64),
-                ("owner_only", _i32)]
+                ("owner_only", _i32), ("norm_scratch", _vp), ("norm_scratch_count", _i64)]
 
 
 def zero_step_sgd(params, grads, st: ZeroStates, t: int, lr: float, momentum: float = 0.0,
                   dampening: float = 0.0, weight_decay: float = 0.0, nesterov: bool = False,
                   grad_scale: float = 1.0, max_grad_norm: float = 0.0, norm_sq=None,
-                  lo: int = 0, hi: int = -1, stream=None, owner_only: bool = False):
+                  lo: int = 0, hi: int = -1, stream=None, owner_only: bool = False,
+                  norm_scratch=None):
     """The fused ZeRO step with momentum SGD (torch.optim.SGD semantics); the
-    state's m is the momentum buffer."""
+    state's m is the momentum buffer. Clipping as in zero_step_ex."""
     pp, gp = _step_ptrs(params, grads, st)
     nq = None if norm_sq is None else _f64_device_ptr(norm_sq, 1, "norm_sq")
+    sc, count = _scratch_args(norm_scratch)
     o = SgdOpts(t, lr, momentum, dampening, weight_decay, 1 if nesterov else 0, grad_scale,
-                max_grad_norm, nq, lo, hi, 1 if owner_only else 0)
+                max_grad_norm, nq, lo, hi, 1 if owner_only else 0, sc, count)
     _check(_lib.zero_step_sgd(pp, gp, st.handle, ctypes.byref(o), _stream(stream)),
            "zero_step_sgd")
 
@@ -457,7 +476,9 @@ def zero_step_from_host_ex(params, host_grads, staging, st: ZeroStates, adamw=No
     """zero_step_from_host with AdamW options (a StepOpts) or SGD options (an
     SgdOpts): exactly one of ``adamw`` and ``sgd``. With max_grad_norm > 0 the
     options' norm_sq is the device address of a float64 scalar that the call
-    fills with the squared norm before the clipped step."""
+    fills with the squared norm before the clipped step, and norm_scratch /
+    norm_scratch_count the caller's float64 device buffer for its partial
+    sums (zero_grad_norm_scratch_count elements)."""
     dt = _storage_dtype(st.precision)
     if len(host_grads) != st.N or len(staging) != st.N or len(params) != st.N:
         raise ValueError(f"need {st.N} params, host gradients and staging buffers")
@@ -500,6 +521,47 @@ def ddp_allreduce_mean_from_host(host_grads, staging, precision: int, n: int | N
            "ddp_allreduce_mean_from_host")
 
 
+class DdpHost:
+    """A zero_ddp_host_t handle: back-to-back DDP means of host gradients on it
+    chain chunk by chunk (see ddp_allreduce_mean_from_host_h)."""
+
+    def __init__(self):
+        h = _vp()
+        _check(_lib.zero_ddp_host_create(ctypes.byref(h)), "zero_ddp_host_create")
+        self.handle = h.value
+
+    def reset(self):
+        """The next call waits for everything queued on its compute stream."""
+        _check(_lib.zero_ddp_host_reset(self.handle), "zero_ddp_host_reset")
+
+    def mean_from_host(self, host_grads, staging, precision: int, n: int | None = None,
+                       host_mean_out=None, chunk_bytes: int = 25 * 1024 * 1024, compute=None,
+                       h2d=None, d2h=None):
+        n = staging[0].numel() if n is None else n
+        if len(host_grads) != len(staging):
+            raise ValueError("need one staging buffer per host gradient")
+        dt = _storage_dtype(precision)
+        hp = _host_ptr_array(host_grads, n, dt, "host_grads")
+        sp = _ptr_array(staging, n, dt, "staging")
+        out = None
+        if host_mean_out is not None:
+            out = _host_ptr_array([host_mean_out], n, dt, "host_mean_out")[0]
+        _check(_lib.ddp_allreduce_mean_from_host_h(
+            self.handle, hp, sp, n, len(staging), precision, out, chunk_bytes, _stream(compute),
+            _stream(h2d), _stream(d2h)), "ddp_allreduce_mean_from_host_h")
+
+    def close(self):
+        if self.handle:
+            _lib.zero_ddp_host_free(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
 def zero_device_status(clear: bool = False) -> int:
     out = ctypes.c_uint32()
     _check(_lib.zero_device_status(ctypes.byref(out), 1 if clear else 0), "zero_device_status")
@@ -508,6 +570,11 @@ def zero_device_status(clear: bool = False) -> int:
 
 def zero_debug_set_wait_timeout_ns(ns: int) -> None:
     _check(_lib.zero_debug_set_wait_timeout_ns(ns), "zero_debug_set_wait_timeout_ns")
+
+
+def zero_last_error() -> str:
+    """The calling thread's most recent error message from the library."""
+    return _lib.zero_last_error().decode(errors="replace")
 
 
 def raw_call(name: str, *args) -> int:

@@ -135,7 +135,8 @@ int adam_consts(int64_t t, double lr, double beta1, double beta2, double eps, do
 // Checks the buffers of a step with optimizer `opt` and fills everything in
 // StepArgs except the split and the constants.
 int prepare_step(void* const* params, const void* const* grads, const zero_states* st,
-                 zk::Opt opt, zk::StepArgs* a, bool* vector_ok, int* phase) {
+                 zk::Opt opt, zk::StepArgs* a, bool* vector_ok, int* phase,
+                 std::vector<Range>* ranges = nullptr) {
   if (!st) return fail(ZERO_EINVAL, "state handle is NULL");
   if (!params || !grads) return fail(ZERO_EINVAL, "params/grads array is NULL");
   const int nstates = opt == zk::Opt::AdamW ? 2 : (opt == zk::Opt::SgdMomentum ? 1 : 0);
@@ -190,6 +191,7 @@ int prepare_step(void* const* params, const void* const* grads, const zero_state
     if (st->n > 0) rs.push_back({uintptr_t(sbufs[k]), uintptr_t(sbufs[k]) + sbytes, "a state buffer"});
   }
   if (int e = check_disjoint(rs)) return e;
+  if (ranges) *ranges = rs;
   if (mixed) {
     // 8-element units: bf16 buffers 16-byte aligned at j = -ph16 (mod 8), fp32
     // buffers at j = -ph32 (mod 4); both hold when ph16 = ph32 (mod 4).
@@ -266,7 +268,38 @@ int prepare_norm(const void* const* grads, int64_t n, int32_t N, int32_t precisi
   a->sp = make_split(0, n, same, ph, V);
   a->chunk = zk::kNormChunk;
   a->nchunks = (a->sp.nvec * V + a->chunk - 1) / a->chunk;
+  a->c_begin = 0;
+  a->c_end = a->nchunks + 1;
   return ZERO_OK;
+}
+
+// A norm pass into caller scratch: after prepare_norm, checks the scratch and
+// the output scalar (aligned, large enough, disjoint from each other and from
+// `others`, the call's other buffers) and sets them in `a`.
+int attach_norm_buffers(double* scratch, int64_t scratch_count, double* norm_sq,
+                        std::vector<Range> others, zk::NormArgs* a) {
+  if (!scratch || !norm_sq) return fail(ZERO_EINVAL, "norm scratch or norm_sq is NULL");
+  if (reinterpret_cast<uintptr_t>(scratch) % 8 || reinterpret_cast<uintptr_t>(norm_sq) % 8)
+    return fail(ZERO_EALIGN, "norm scratch and norm_sq must be 8-byte aligned");
+  if (scratch_count < a->nchunks + 1)
+    return fail(ZERO_EINVAL, "norm scratch holds %lld doubles, %lld needed",
+                (long long)scratch_count, (long long)(a->nchunks + 1));
+  others.push_back({uintptr_t(scratch), uintptr_t(scratch) + uintptr_t(a->nchunks + 1) * 8,
+                    "the norm scratch"});
+  others.push_back({uintptr_t(norm_sq), uintptr_t(norm_sq) + 8, "norm_sq"});
+  if (int e = check_disjoint(others)) return e;
+  a->partials = scratch;
+  a->out = norm_sq;
+  return ZERO_OK;
+}
+
+// The gradients' buffer ranges of a norm pass.
+std::vector<Range> grad_ranges(const void* const* grads, int64_t n, int32_t N, int es) {
+  std::vector<Range> rs;
+  if (n > 0)
+    for (int32_t r = 0; r < N; ++r)
+      rs.push_back({uintptr_t(grads[r]), uintptr_t(grads[r]) + uintptr_t(n) * es, "a gradient"});
+  return rs;
 }
 
 }  // namespace
@@ -372,17 +405,25 @@ int breakdown(int64_t n, int32_t stage, int32_t precision, uint64_t s, uint64_t 
   return ZERO_OK;
 }
 
-// The multiplier of the mean gradient and, when max_grad_norm > 0, clipping.
+// The multiplier of the mean gradient and, when max_grad_norm > 0, clipping:
+// with the squared norm read from norm_sq, or (norm_scratch given) formed by
+// the call itself -- then norm_partials marks it, the caller runs the norm
+// pass into norm_scratch, and norm_sq receives the total.
 int fill_scale_clip(double grad_scale, double max_grad_norm, const double* norm_sq,
-                    zk::StepArgs* a) {
+                    double* norm_scratch, zk::StepArgs* a) {
   if (!std::isfinite(grad_scale) || !(grad_scale > 0.0))
     return fail(ZERO_EINVAL, "grad_scale must be finite and > 0");
   a->gscale = grad_scale;
   if (max_grad_norm > 0.0) {
     if (!std::isfinite(max_grad_norm)) return fail(ZERO_EINVAL, "max_grad_norm must be finite");
     if (!norm_sq) return fail(ZERO_EINVAL, "clipping needs the squared norm (norm_sq)");
-    a->norm_sq = norm_sq;
     a->max_norm = max_grad_norm;
+    if (norm_scratch) {
+      a->norm_partials = norm_scratch;
+      a->norm_out = const_cast<double*>(norm_sq);
+    } else {
+      a->norm_sq = norm_sq;
+    }
   }
   return ZERO_OK;
 }
@@ -391,7 +432,8 @@ int fill_scale_clip(double grad_scale, double max_grad_norm, const double* norm_
 int fill_adamw(const zero_step_opts_t* o, zk::StepArgs* a) {
   if (int e = adam_consts(o->t, o->lr, o->beta1, o->beta2, o->eps, o->weight_decay, &a->c))
     return e;
-  if (int e = fill_scale_clip(o->grad_scale, o->max_grad_norm, o->norm_sq, a)) return e;
+  if (int e = fill_scale_clip(o->grad_scale, o->max_grad_norm, o->norm_sq, o->norm_scratch, a))
+    return e;
   a->owner_only = o->owner_only != 0;
   return ZERO_OK;
 }
@@ -419,7 +461,8 @@ int fill_sgd(const zero_sgd_opts_t* o, zk::StepArgs* a) {
   a->sgd.wd_on = o->weight_decay != 0.0;
   a->sgd.first = o->t == 1;
   a->sgd.nesterov = o->nesterov != 0;
-  if (int e = fill_scale_clip(o->grad_scale, o->max_grad_norm, o->norm_sq, a)) return e;
+  if (int e = fill_scale_clip(o->grad_scale, o->max_grad_norm, o->norm_sq, o->norm_scratch, a))
+    return e;
   a->owner_only = o->owner_only != 0;
   return ZERO_OK;
 }
@@ -429,6 +472,33 @@ int check_range(int64_t lo, int64_t hi, int64_t n) {
     return fail(ZERO_EINVAL, "range [%lld, %lld) outside [0, %lld)", (long long)lo, (long long)hi,
                 (long long)n);
   return ZERO_OK;
+}
+
+// The step of zero_step_ex / zero_step_sgd over [lo, hi), after the options
+// are filled in. When the call forms the norm itself (a.norm_partials), the
+// partial sums of the whole gradient go into the caller's scratch first, and
+// the step follows as a programmatic dependent that adds them in its prologue
+// (for an empty range a separate total launch writes norm_sq instead).
+int run_step(zk::StepArgs& a, zero_states* st, const void* const* grads, bool vec, int phase,
+             int64_t lo, int64_t hi, int64_t scratch_count, const std::vector<Range>& bufs,
+             cudaStream_t s, zk::Opt opt) {
+  if (a.norm_partials) {
+    zk::NormArgs na;
+    if (int e = prepare_norm(grads, st->n, st->N, st->precision, &na)) return e;
+    if (int e = attach_norm_buffers(const_cast<double*>(a.norm_partials), scratch_count,
+                                    a.norm_out, bufs, &na))
+      return e;
+    const bool bf16 = st->precision == ZERO_BF16_MIXED;
+    cudaError_t ce = zk::launch_norm_partials(na, bf16, s);
+    if (ce != cudaSuccess) return cuda_fail(ce, "gradient norm kernel launch");
+    if (hi <= lo) {
+      ce = zk::launch_norm_total(na, s);
+      return ce == cudaSuccess ? ZERO_OK : cuda_fail(ce, "gradient norm kernel launch");
+    }
+    a.npartials = na.nchunks + 1;
+    a.dependent = 1;
+  }
+  return launch_range(a, st, vec, phase, lo, hi, s, opt);
 }
 
 }  // namespace
@@ -589,11 +659,13 @@ int zero_step_ex(void* const* params, const void* const* grads, zero_states_t* s
   zk::StepArgs a;
   bool vec = false;
   int phase = 0;
-  if (int e = prepare_step(params, grads, st, zk::Opt::AdamW, &a, &vec, &phase)) return e;
+  std::vector<Range> bufs;
+  if (int e = prepare_step(params, grads, st, zk::Opt::AdamW, &a, &vec, &phase, &bufs)) return e;
   const int64_t lo = o->lo, hi = o->hi < 0 ? st->n : o->hi;
   if (int e = check_range(lo, hi, st->n)) return e;
   if (int e = fill_adamw(o, &a)) return e;
-  return launch_range(a, st, vec, phase, lo, hi, reinterpret_cast<cudaStream_t>(stream));
+  return run_step(a, st, grads, vec, phase, lo, hi, o->norm_scratch_count, bufs,
+                  reinterpret_cast<cudaStream_t>(stream), zk::Opt::AdamW);
 }
 
 int zero_gather(void* const* params, zero_states_t* st, int64_t lo, int64_t hi,
@@ -643,11 +715,13 @@ int zero_step_sgd(void* const* params, const void* const* grads, zero_states_t* 
   zk::StepArgs a;
   bool vec = false;
   int phase = 0;
-  if (int e = prepare_step(params, grads, st, opt, &a, &vec, &phase)) return e;
+  std::vector<Range> bufs;
+  if (int e = prepare_step(params, grads, st, opt, &a, &vec, &phase, &bufs)) return e;
   const int64_t lo = o->lo, hi = o->hi < 0 ? st->n : o->hi;
   if (int e = check_range(lo, hi, st->n)) return e;
   if (int e = fill_sgd(o, &a)) return e;
-  return launch_range(a, st, vec, phase, lo, hi, reinterpret_cast<cudaStream_t>(stream), opt);
+  return run_step(a, st, grads, vec, phase, lo, hi, o->norm_scratch_count, bufs,
+                  reinterpret_cast<cudaStream_t>(stream), opt);
 }
 
 int zero_grad_norm_scratch_count(int64_t n, int32_t precision, int64_t* count) {
@@ -664,22 +738,10 @@ int zero_grad_norm_sq(const void* const* grads, int64_t n, int32_t N, int32_t pr
                       zero_stream_t stream) {
   zk::NormArgs a;
   if (int e = prepare_norm(grads, n, N, precision, &a)) return e;
-  if (!scratch || !norm_sq) return fail(ZERO_EINVAL, "scratch or norm_sq is NULL");
-  if (reinterpret_cast<uintptr_t>(scratch) % 8 || reinterpret_cast<uintptr_t>(norm_sq) % 8)
-    return fail(ZERO_EALIGN, "scratch and norm_sq must be 8-byte aligned");
-  if (scratch_count < a.nchunks + 1)
-    return fail(ZERO_EINVAL, "scratch holds %lld doubles, %lld needed", (long long)scratch_count,
-                (long long)(a.nchunks + 1));
   const int es = precision == ZERO_BF16_MIXED ? 2 : 4;
-  std::vector<Range> rs;
-  if (n > 0)
-    for (int32_t r = 0; r < N; ++r)
-      rs.push_back({uintptr_t(grads[r]), uintptr_t(grads[r]) + uintptr_t(n) * es, "a gradient"});
-  rs.push_back({uintptr_t(scratch), uintptr_t(scratch) + uintptr_t(a.nchunks + 1) * 8, "the scratch"});
-  rs.push_back({uintptr_t(norm_sq), uintptr_t(norm_sq) + 8, "norm_sq"});
-  if (int e = check_disjoint(rs)) return e;
-  a.partials = scratch;
-  a.out = norm_sq;
+  if (int e = attach_norm_buffers(scratch, scratch_count, norm_sq, grad_ranges(grads, n, N, es),
+                                  &a))
+    return e;
   cudaError_t e = zk::launch_norm(a, es == 2, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "gradient norm kernel launch");
   return ZERO_OK;
@@ -831,11 +893,13 @@ int zero_step_from_host_ex(void* const* params, const void* const* host_grads,
   const int64_t o_lo = adamw ? adamw->lo : sgd->lo, o_hi = adamw ? adamw->hi : sgd->hi;
   const bool clip = (adamw ? adamw->max_grad_norm : sgd->max_grad_norm) > 0.0;
   double* norm_out = const_cast<double*>(adamw ? adamw->norm_sq : sgd->norm_sq);
+  double* norm_scratch = adamw ? adamw->norm_scratch : sgd->norm_scratch;
+  const int64_t norm_count = adamw ? adamw->norm_scratch_count : sgd->norm_scratch_count;
   if (o_lo != 0 || (o_hi >= 0 && o_hi != st->n))
     return fail(ZERO_EINVAL, "the host-input step covers the whole vector (lo = 0, hi = -1 or n)");
-  if (clip && st->n > ZERO_NOALLOC_MAX_N)
-    return fail(ZERO_EINVAL, "clipping in the host-input step covers n <= %lld (the library's "
-                "own norm scratch)", (long long)ZERO_NOALLOC_MAX_N);
+  if (clip && !norm_scratch)
+    return fail(ZERO_EINVAL, "clipping in the host-input step needs norm_scratch (the norm's "
+                "partial sums)");
   zk::Opt opt = zk::Opt::AdamW;
   if (sgd)
     if (int e = sgd_opt(sgd, &opt)) return e;
@@ -848,20 +912,21 @@ int zero_step_from_host_ex(void* const* params, const void* const* host_grads,
   zk::StepArgs a;
   bool vec = false;
   int phase = 0;
+  std::vector<Range> bufs;
   // the staging buffers are the kernel's gradient buffers
-  if (int e = prepare_step(params, staging, st, opt, &a, &vec, &phase)) return e;
+  if (int e = prepare_step(params, staging, st, opt, &a, &vec, &phase, &bufs)) return e;
   if (int e = adamw ? fill_adamw(adamw, &a) : fill_sgd(sgd, &a)) return e;
   if (n == 0) return ZERO_OK;
   const size_t es = st->precision == ZERO_BF16_MIXED ? 2 : 4;
-  if (clip) {  // the norm's own checks, before anything is queued
-    if (reinterpret_cast<uintptr_t>(norm_out) % 8)
-      return fail(ZERO_EALIGN, "norm_sq not 8-byte aligned");
-    std::vector<Range> rs;
-    for (int32_t r = 0; r < N; ++r)
-      rs.push_back({uintptr_t(staging[r]), uintptr_t(staging[r]) + uintptr_t(n) * es,
-                    "a staging buffer"});
-    rs.push_back({uintptr_t(norm_out), uintptr_t(norm_out) + 8, "norm_sq"});
-    if (int e = check_disjoint(rs)) return e;
+  zk::NormArgs na;
+  if (clip) {
+    // the norm's own checks, before anything is queued; the steps then read
+    // the total from norm_sq (one total launch, not one per chunk's step)
+    if (int e = prepare_norm(staging, n, N, st->precision, &na)) return e;
+    if (int e = attach_norm_buffers(norm_scratch, norm_count, norm_out, bufs, &na)) return e;
+    a.norm_partials = nullptr;
+    a.norm_out = nullptr;
+    a.norm_sq = norm_out;
   }
   const int64_t count = (n + B - 1) / B;
   const size_t need = size_t(2 * count + 2);
@@ -930,14 +995,36 @@ int zero_step_from_host_ex(void* const* params, const void* const* host_grads,
       if (int e = step_out(k)) return e;
     }
   } else {
-    // the global norm needs the whole gradient: every chunk in, the norm, then
-    // the steps (their copies back overlapping the later steps)
-    for (int64_t k = 0; k < count; ++k)
+    // The global norm needs the whole gradient. Its partial sums cover fixed
+    // runs of kNormChunk vector elements after the scalar head, so each run
+    // whose elements have all arrived is summed as soon as they have: after
+    // chunk k, the runs ending at or before its end (all of them once the
+    // vector body is in). The last launch adds the scalar head and tail's
+    // partial; then the fixed-order total, then the steps (their copies back
+    // overlapping the later steps).
+    const bool bf16 = st->precision == ZERO_BF16_MIXED;
+    const int V = bf16 ? 8 : 4;
+    const int64_t body_lo = na.sp.lo + na.sp.head, body_hi = body_lo + na.sp.nvec * V;
+    int64_t c_done = 0;
+    for (int64_t k = 0; k < count; ++k) {
       if (int e = copy_in(k)) return e;
+      const int64_t hi = std::min<int64_t>(n, (k + 1) * B);
+      const int64_t c_ready = k + 1 == count ? na.nchunks + 1
+                              : hi >= body_hi ? na.nchunks
+                              : hi > body_lo  ? (hi - body_lo) / na.chunk
+                                              : 0;
+      if (c_ready <= c_done) continue;
+      if (int e = ck(cudaStreamWaitEvent(cs, ev[2 + 2 * k], 0), "cudaStreamWaitEvent")) return e;
+      zk::NormArgs part = na;
+      part.c_begin = c_done;
+      part.c_end = c_ready;
+      if (int e = ck(zk::launch_norm_partials(part, bf16, cs), "gradient norm kernel launch"))
+        return e;
+      c_done = c_ready;
+    }
     if (int e = ck(cudaStreamWaitEvent(cs, ev[2 + 2 * (count - 1)], 0), "cudaStreamWaitEvent"))
       return e;
-    if (int e = zero_grad_norm_sq_noalloc(staging, n, N, st->precision, norm_out, compute))
-      return e;
+    if (int e = ck(zk::launch_norm_total(na, cs), "gradient norm kernel launch")) return e;
     for (int64_t k = 0; k < count; ++k)
       if (int e = step_out(k)) return e;
   }
@@ -985,34 +1072,128 @@ int ddp_allreduce_mean(void* const* grads, int64_t n, int32_t N, int32_t precisi
   return ZERO_OK;
 }
 
-int ddp_allreduce_mean_from_host(const void* const* host_grads, void* const* staging, int64_t n,
-                                 int32_t N, int32_t precision, void* host_mean_out,
-                                 int64_t chunk_bytes, zero_stream_t compute, zero_stream_t h2d,
-                                 zero_stream_t d2h) {
+}  // extern "C"
+
+// Chained DDP host-input calls (ddp_allreduce_mean_from_host_h): the events
+// of the last call and the configuration they belong to.
+struct zero_ddp_host {
+  int device = -1;
+  std::vector<cudaEvent_t> events;  // [0] start, [1] end, [2+2k] landed k, [3+2k] released k
+  bool have_last = false;           // the last call queued completely
+  int64_t n = 0, B = 0;
+  int32_t N = 0, precision = 0;
+  std::vector<void*> staging;
+};
+
+namespace {
+
+// Checks of a DDP host-input call, before anything is queued; the chunk size
+// in elements.
+int ddp_host_checks(const void* const* host_grads, void* const* staging, int64_t n, int32_t N,
+                    int32_t precision, int64_t chunk_bytes, zero_stream_t compute, int64_t* B) {
   if (n < 0) return fail(ZERO_EINVAL, "n=%lld must be >= 0", (long long)n);
   if (!valid_ranks(N)) return fail(ZERO_EINVAL, "N=%d outside [1, %d]", N, ZERO_MAX_RANKS);
   if (!host_grads || !staging) return fail(ZERO_EINVAL, "host_grads or staging array is NULL");
-  int64_t B;
-  if (int e = bucket_elems(precision, chunk_bytes, &B)) return e;
+  if (int e = bucket_elems(precision, chunk_bytes, B)) return e;
   const size_t es = precision == ZERO_BF16_MIXED ? 2 : 4;
   for (int32_t r = 0; r < N; ++r)
     if (n > 0 && (!host_grads[r] || !staging[r]))
       return fail(ZERO_EINVAL, "host_grads[%d] or staging[%d] is NULL", r, r);
   // the whole-vector checks (alignment, distinct buffers) before anything is queued
   if (int e = ddp_allreduce_mean(staging, 0, N, precision, compute)) return e;
-  {
-    std::vector<Range> rs;
-    for (int32_t r = 0; r < N && n > 0; ++r)
-      rs.push_back({uintptr_t(staging[r]), uintptr_t(staging[r]) + uintptr_t(n) * es,
-                    "a staging buffer"});
-    if (int e = check_disjoint(rs)) return e;
+  std::vector<Range> rs;
+  for (int32_t r = 0; r < N && n > 0; ++r)
+    rs.push_back({uintptr_t(staging[r]), uintptr_t(staging[r]) + uintptr_t(n) * es,
+                  "a staging buffer"});
+  return check_disjoint(rs);
+}
+
+// Grows `pool` to `need` events of the current device.
+int grow_events(std::vector<cudaEvent_t>& pool, size_t need) {
+  while (pool.size() < need) {
+    cudaEvent_t ev;
+    cudaError_t ce = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
+    if (ce != cudaSuccess) return cuda_fail(ce, "cudaEventCreateWithFlags");
+    pool.push_back(ev);
   }
+  return ZERO_OK;
+}
+
+// The chunk pipeline of the DDP mean from host memory, on events
+// ev[0 .. 2 + 2*count). Unchained, the copies start after everything queued
+// on `compute`; chained (the previous call on the same events had the same
+// buffers and chunks), the copy of chunk k waits only for that call's
+// release of chunk k: its mean and its copy back.
+int ddp_host_pipeline(cudaEvent_t* ev, bool chained, const void* const* host_grads,
+                      void* const* staging, int64_t n, int32_t N, int32_t precision,
+                      void* host_mean_out, int64_t B, zero_stream_t compute, zero_stream_t h2d,
+                      zero_stream_t d2h) {
+  const size_t es = precision == ZERO_BF16_MIXED ? 2 : 4;
+  const int64_t count = (n + B - 1) / B;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(compute);
+  cudaStream_t hs = reinterpret_cast<cudaStream_t>(h2d);
+  cudaStream_t ds = reinterpret_cast<cudaStream_t>(d2h);
+  auto ck = [&](cudaError_t ce, const char* what) { return ce == cudaSuccess ? 0 : cuda_fail(ce, what); };
+  if (!chained) {  // the copies start after everything already queued on `compute`
+    if (int e = ck(cudaEventRecord(ev[0], cs), "cudaEventRecord")) return e;
+    if (int e = ck(cudaStreamWaitEvent(hs, ev[0], 0), "cudaStreamWaitEvent")) return e;
+    if (host_mean_out)
+      if (int e = ck(cudaStreamWaitEvent(ds, ev[0], 0), "cudaStreamWaitEvent")) return e;
+  }
+  std::vector<void*> chunk(size_t(N), nullptr);
+  for (int64_t k = 0; k < count; ++k) {
+    const int64_t lo = k * B, hi = std::min<int64_t>(n, lo + B);
+    const size_t off = size_t(lo) * es, bytes = size_t(hi - lo) * es;
+    cudaEvent_t landed = ev[2 + 2 * k], released = ev[3 + 2 * k];
+    if (chained)  // the previous call's mean and copy back of this chunk are done
+      if (int e = ck(cudaStreamWaitEvent(hs, released, 0), "cudaStreamWaitEvent")) return e;
+    for (int32_t r = 0; r < N; ++r) {
+      cudaError_t ce = cudaMemcpyAsync(static_cast<char*>(staging[r]) + off,
+                                       static_cast<const char*>(host_grads[r]) + off, bytes,
+                                       cudaMemcpyHostToDevice, hs);
+      if (ce != cudaSuccess) return cuda_fail(ce, "host-to-device copy of a gradient chunk");
+      chunk[size_t(r)] = static_cast<char*>(staging[r]) + off;
+    }
+    if (int e = ck(cudaEventRecord(landed, hs), "cudaEventRecord")) return e;
+    if (int e = ck(cudaStreamWaitEvent(cs, landed, 0), "cudaStreamWaitEvent")) return e;
+    if (int e = ddp_allreduce_mean(chunk.data(), hi - lo, N, precision, compute)) return e;
+    if (int e = ck(cudaEventRecord(released, cs), "cudaEventRecord")) return e;
+    if (host_mean_out) {
+      if (int e = ck(cudaStreamWaitEvent(ds, released, 0), "cudaStreamWaitEvent")) return e;
+      cudaError_t ce = cudaMemcpyAsync(static_cast<char*>(host_mean_out) + off, chunk[0], bytes,
+                                       cudaMemcpyDeviceToHost, ds);
+      if (ce != cudaSuccess) return cuda_fail(ce, "device-to-host copy of a mean chunk");
+      // released again once the copy back has read the chunk
+      if (int e = ck(cudaEventRecord(released, ds), "cudaEventRecord")) return e;
+    }
+  }
+  // `compute` completes only after the last copy in either direction
+  if (int e = ck(cudaEventRecord(ev[1], hs), "cudaEventRecord")) return e;
+  if (int e = ck(cudaStreamWaitEvent(cs, ev[1], 0), "cudaStreamWaitEvent")) return e;
+  if (host_mean_out) {
+    if (int e = ck(cudaEventRecord(ev[1], ds), "cudaEventRecord")) return e;
+    if (int e = ck(cudaStreamWaitEvent(cs, ev[1], 0), "cudaStreamWaitEvent")) return e;
+  }
+  return ZERO_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int ddp_allreduce_mean_from_host(const void* const* host_grads, void* const* staging, int64_t n,
+                                 int32_t N, int32_t precision, void* host_mean_out,
+                                 int64_t chunk_bytes, zero_stream_t compute, zero_stream_t h2d,
+                                 zero_stream_t d2h) {
+  int64_t B;
+  if (int e = ddp_host_checks(host_grads, staging, n, N, precision, chunk_bytes, compute, &B))
+    return e;
   if (n == 0) return ZERO_OK;
   const int64_t count = (n + B - 1) / B;
   // Events come from a process-wide pool per device, grown on demand. A wait
   // takes the state of an event when it is queued, so re-recording an event in
   // a later call is safe; the mutex keeps two host threads from interleaving
-  // their record/wait pairs on one event.
+  // their record/wait pairs on one event. These calls never chain.
   static std::mutex mu;
   static std::vector<cudaEvent_t> pools[256];
   int dev = 0;
@@ -1023,53 +1204,64 @@ int ddp_allreduce_mean_from_host(const void* const* host_grads, void* const* sta
   }
   std::lock_guard<std::mutex> lock(mu);
   std::vector<cudaEvent_t>& pool = pools[dev];
-  const size_t need = size_t(count + 2);
-  while (pool.size() < need) {
-    cudaEvent_t ev;
-    cudaError_t ce = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
-    if (ce != cudaSuccess) return cuda_fail(ce, "cudaEventCreateWithFlags");
-    pool.push_back(ev);
+  if (int e = grow_events(pool, size_t(2 + 2 * count))) return e;
+  return ddp_host_pipeline(pool.data(), false, host_grads, staging, n, N, precision,
+                           host_mean_out, B, compute, h2d, d2h);
+}
+
+int zero_ddp_host_create(zero_ddp_host_t** out) {
+  if (!out) return fail(ZERO_EINVAL, "out is NULL");
+  *out = new (std::nothrow) zero_ddp_host;
+  if (!*out) return fail(ZERO_ENOMEM, "cannot allocate the DDP host-input handle");
+  return ZERO_OK;
+}
+
+int zero_ddp_host_reset(zero_ddp_host_t* h) {
+  if (!h) return fail(ZERO_EINVAL, "handle is NULL");
+  h->have_last = false;
+  return ZERO_OK;
+}
+
+int zero_ddp_host_free(zero_ddp_host_t* h) {
+  if (h)
+    for (cudaEvent_t e : h->events) cudaEventDestroy(e);
+  delete h;
+  return ZERO_OK;
+}
+
+int ddp_allreduce_mean_from_host_h(zero_ddp_host_t* h, const void* const* host_grads,
+                                   void* const* staging, int64_t n, int32_t N, int32_t precision,
+                                   void* host_mean_out, int64_t chunk_bytes, zero_stream_t compute,
+                                   zero_stream_t h2d, zero_stream_t d2h) {
+  if (!h) return fail(ZERO_EINVAL, "handle is NULL");
+  int64_t B;
+  if (int e = ddp_host_checks(host_grads, staging, n, N, precision, chunk_bytes, compute, &B))
+    return e;
+  if (n == 0) return ZERO_OK;
+  int dev = 0;
+  {
+    cudaError_t ce = cudaGetDevice(&dev);
+    if (ce != cudaSuccess) return cuda_fail(ce, "cudaGetDevice");
   }
-  cudaStream_t cs = reinterpret_cast<cudaStream_t>(compute);
-  cudaStream_t hs = reinterpret_cast<cudaStream_t>(h2d);
-  cudaStream_t ds = reinterpret_cast<cudaStream_t>(d2h);
-  auto ck = [&](cudaError_t ce, const char* what) { return ce == cudaSuccess ? 0 : cuda_fail(ce, what); };
-  // the copies start after everything already queued on `compute`
-  if (int e = ck(cudaEventRecord(pool[0], cs), "cudaEventRecord")) return e;
-  if (int e = ck(cudaStreamWaitEvent(hs, pool[0], 0), "cudaStreamWaitEvent")) return e;
-  if (host_mean_out)
-    if (int e = ck(cudaStreamWaitEvent(ds, pool[0], 0), "cudaStreamWaitEvent")) return e;
-  std::vector<void*> chunk(size_t(N), nullptr);
-  for (int64_t k = 0; k < count; ++k) {
-    const int64_t lo = k * B, hi = std::min<int64_t>(n, lo + B);
-    const size_t off = size_t(lo) * es, bytes = size_t(hi - lo) * es;
-    for (int32_t r = 0; r < N; ++r) {
-      cudaError_t ce = cudaMemcpyAsync(static_cast<char*>(staging[r]) + off,
-                                       static_cast<const char*>(host_grads[r]) + off, bytes,
-                                       cudaMemcpyHostToDevice, hs);
-      if (ce != cudaSuccess) return cuda_fail(ce, "host-to-device copy of a gradient chunk");
-      chunk[size_t(r)] = static_cast<char*>(staging[r]) + off;
-    }
-    cudaEvent_t landed = pool[size_t(2 + k)];
-    if (int e = ck(cudaEventRecord(landed, hs), "cudaEventRecord")) return e;
-    if (int e = ck(cudaStreamWaitEvent(cs, landed, 0), "cudaStreamWaitEvent")) return e;
-    if (int e = ddp_allreduce_mean(chunk.data(), hi - lo, N, precision, compute)) return e;
-    if (host_mean_out) {
-      // the event is re-recorded on `compute` after the mean of this chunk
-      if (int e = ck(cudaEventRecord(landed, cs), "cudaEventRecord")) return e;
-      if (int e = ck(cudaStreamWaitEvent(ds, landed, 0), "cudaStreamWaitEvent")) return e;
-      cudaError_t ce = cudaMemcpyAsync(static_cast<char*>(host_mean_out) + off, chunk[0], bytes,
-                                       cudaMemcpyDeviceToHost, ds);
-      if (ce != cudaSuccess) return cuda_fail(ce, "device-to-host copy of a mean chunk");
-    }
-  }
-  // `compute` completes only after the last copy in either direction
-  if (int e = ck(cudaEventRecord(pool[1], hs), "cudaEventRecord")) return e;
-  if (int e = ck(cudaStreamWaitEvent(cs, pool[1], 0), "cudaStreamWaitEvent")) return e;
-  if (host_mean_out) {
-    if (int e = ck(cudaEventRecord(pool[1], ds), "cudaEventRecord")) return e;
-    if (int e = ck(cudaStreamWaitEvent(cs, pool[1], 0), "cudaStreamWaitEvent")) return e;
-  }
+  if (h->device >= 0 && h->device != dev)
+    return fail(ZERO_EINVAL, "the handle belongs to device %d, not the current device %d",
+                h->device, dev);
+  const int64_t count = (n + B - 1) / B;
+  if (int e = grow_events(h->events, size_t(2 + 2 * count))) return e;
+  h->device = dev;
+  const bool chained = h->have_last && h->n == n && h->N == N && h->precision == precision &&
+                       h->B == B && h->staging.size() == size_t(N) &&
+                       std::equal(staging, staging + N, h->staging.begin());
+  h->have_last = false;  // until this call has queued completely
+  if (int e = ddp_host_pipeline(h->events.data(), chained, host_grads, staging, n, N, precision,
+                                host_mean_out, B, compute, h2d, d2h))
+    return e;
+  h->have_last = true;
+  h->n = n;
+  h->N = N;
+  h->precision = precision;
+  h->B = B;
+  h->staging.assign(staging, staging + N);
   return ZERO_OK;
 }
 

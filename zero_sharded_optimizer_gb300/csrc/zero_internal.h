@@ -65,6 +65,13 @@ struct StepArgs {
   // min(1, max_norm / (gscale * sqrt(*norm_sq) + 1e-6)) when norm_sq is set
   // (formed on the device, in double, rounded to float once).
   const double* norm_sq;         // device scalar, or NULL (no clipping)
+  // Clipping with the norm's fixed-order total formed in this kernel: the
+  // partial sums of a norm pass launched just before (npartials of them, the
+  // kernel waits for that pass first); the total is written to norm_out by
+  // block 0. NULL: the multiplier comes from norm_sq (or there is none).
+  const double* norm_partials;
+  int64_t npartials;
+  double* norm_out;
   double gscale;
   double max_norm;
   // Stage 3: write the new parameters only into the owner's replica, over the
@@ -89,6 +96,11 @@ struct NormArgs {
   // 2,048-16,384 elements, for a more even spread over the SMs, slower still).
   int64_t chunk;
   int64_t nchunks;   // vector chunks (chunk / V units each); partial nchunks = scalars
+  // The partials this launch computes: [c_begin, c_end) within [0, nchunks]
+  // (index nchunks is the scalar head and tail). The whole pass is
+  // [0, nchunks + 1); the host-input step launches the chunks of each piece of
+  // the gradient as soon as it has arrived.
+  int64_t c_begin, c_end;
   double* partials;  // nchunks + 1 doubles
   double* out;       // device scalar receiving the sum of the partials
 };
@@ -131,6 +143,10 @@ cudaError_t launch_init(const InitArgs& a, cudaStream_t s);
 cudaError_t launch_gather(const GatherArgs& a, bool bf16, cudaStream_t s);
 // Partial sums then their fixed-order total (two launches, deterministic).
 cudaError_t launch_norm(const NormArgs& a, bool bf16, cudaStream_t s);
+// The partials [a.c_begin, a.c_end) only (one launch; its blocks let a
+// programmatic dependent start early), and the fixed-order total only.
+cudaError_t launch_norm_partials(const NormArgs& a, bool bf16, cudaStream_t s);
+cudaError_t launch_norm_total(const NormArgs& a, cudaStream_t s);
 
 // Capacity of the library's own partial-sum array (zero_grad_norm_sq_noalloc),
 // and the device address of that array on the current device (looked up on

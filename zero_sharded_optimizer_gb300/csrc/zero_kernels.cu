@@ -86,6 +86,64 @@ __device__ __forceinline__ uint2 pack4(float4 f) {
   return make_uint2(pack_bf2(f.x, f.y), pack_bf2(f.z, f.w));
 }
 
+// Programmatic dependent launch: let the next kernel on the stream start
+// (once every CTA here has said so), and wait for the kernel before this one
+// to complete with its memory visible (a no-op when this kernel was launched
+// without the attribute).
+__device__ __forceinline__ void pdl_allow_next() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait_previous() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Barrier over `nthreads` threads (whole warps): the block barrier for id 0,
+// else the named barrier `id`.
+__device__ __forceinline__ void sync_group(int id, int nthreads) {
+  if (id == 0) {
+    __syncthreads();
+  } else {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+  }
+}
+
+// The fixed-order total of `count` non-negative doubles (partial sums of
+// squares), the same bits for any caller: local thread lt < 256 adds p[lt],
+// p[lt + 256], ... in that order; each warp
+// folds its 32 sums by one fixed shuffle tree; then one thread adds the warp
+// sums in warp order, starting from zero (warps past the eighth contribute
+// +0.0, which leaves the sum unchanged). Called by `nthreads` threads (local
+// indices 0..nthreads-1, whole warps, nthreads <= 1024) that meet at barrier
+// `bar` (0: the whole block); every caller gets the total.
+__device__ __forceinline__ double fixed_order_total(const double* p, int64_t count, int lt,
+                                                    int nthreads, int bar) {
+  __shared__ double warp_sums[33];
+  double acc = 0.0;
+  if (lt < 256) {
+    // eight loads in flight before their sums; past the end they read as +0.0,
+    // which leaves the (non-negative) running sum unchanged
+    for (int64_t c = lt; c < count; c += 8 * 256) {
+      double x[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) x[u] = c + u * 256 < count ? p[c + u * 256] : 0.0;
+#pragma unroll
+      for (int u = 0; u < 8; ++u) acc += x[u];
+    }
+  }
+  for (int off = 16; off > 0; off >>= 1) acc += __shfl_down_sync(0xffffffffu, acc, off);
+  if ((lt & 31) == 0) warp_sums[lt >> 5] = acc;
+  sync_group(bar, nthreads);
+  if (lt == 0) {
+    double t = 0.0;
+    for (int w = 0; w < nthreads / 32; ++w) t += warp_sums[w];
+    warp_sums[32] = t;
+  }
+  sync_group(bar, nthreads);
+  const double total = warp_sums[32];
+  sync_group(bar, nthreads);  // the slots may be reused after this
+  return total;
+}
+
 // ----------------------------------------------------------------- the math --
 
 // Divide the rank-ordered sum by N. For a power-of-two N the product with 1/N
@@ -147,16 +205,35 @@ __device__ __forceinline__ int ranks(const StepArgs& P) {
 }
 
 // Multiplier of the mean gradient: the accumulation factor gscale, times the
-// clip coefficient min(1, max_norm / (gscale * sqrt(norm_sq) + 1e-6)) when a
-// squared global norm is given. Formed in double with separately rounded
-// operations (no contraction), rounded to float once; 1.0f when neither is set.
-__device__ __forceinline__ float grad_multiplier(const StepArgs& P) {
+// clip coefficient min(1, max_norm / (gscale * sqrt(norm_sq) + 1e-6)) when
+// clipping. Formed in double with separately rounded operations (no
+// contraction), rounded to float once; 1.0f when neither is set.
+__device__ __forceinline__ float multiplier_of(const StepArgs& P, bool clip, double norm_sq) {
   double c = 1.0;
-  if (P.norm_sq) {
-    const double denom = __dadd_rn(__dmul_rn(P.gscale, __dsqrt_rn(*P.norm_sq)), 1e-6);
+  if (clip) {
+    const double denom = __dadd_rn(__dmul_rn(P.gscale, __dsqrt_rn(norm_sq)), 1e-6);
     c = fmin(1.0, __ddiv_rn(P.max_norm, denom));
   }
   return __double2float_rn(__dmul_rn(P.gscale, c));
+}
+
+// The multiplier from the squared norm in memory (per thread).
+__device__ __forceinline__ float grad_multiplier(const StepArgs& P) {
+  return multiplier_of(P, P.norm_sq != nullptr, P.norm_sq ? *P.norm_sq : 0.0);
+}
+
+// The multiplier, for a group of `nthreads` threads meeting at barrier `bar`
+// (local index lt). When the kernel forms the norm's total itself, the group
+// waits for the norm pass launched before it, adds its partials in the fixed
+// order of grad_norm_total_kernel (so the total is that kernel's, bit for
+// bit), and block 0 stores the total in norm_out.
+__device__ __forceinline__ float group_grad_multiplier(const StepArgs& P, int lt, int nthreads,
+                                                       int bar) {
+  if (!P.norm_partials) return grad_multiplier(P);
+  pdl_wait_previous();
+  const double total = fixed_order_total(P.norm_partials, P.npartials, lt, nthreads, bar);
+  if (lt == 0 && blockIdx.x == 0 && P.norm_out) *P.norm_out = total;
+  return multiplier_of(P, true, total);
 }
 
 // The mean of the rank-ordered sum, times the gradient multiplier.
@@ -399,7 +476,7 @@ __global__ void __launch_bounds__(kThreads) zero_step_kernel(const __grid_consta
   const int64_t tid = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
   const int64_t stride = int64_t(gridDim.x) * blockDim.x;
   const Split& sp = P.sp;
-  const float gm = grad_multiplier(P);
+  const float gm = group_grad_multiplier(P, threadIdx.x, blockDim.x, 0);
 
   // Scalar head and tail (a handful of elements, or the whole range when the
   // buffers do not share a 16-byte phase). j grows with s, so the owner scan
@@ -561,17 +638,18 @@ __device__ __forceinline__ double norm_chunk_sum(const NormArgs& P, int64_t c) {
 template <int NR, bool BF16>
 __global__ void __launch_bounds__(kThreads)
     grad_norm_partials_kernel(const __grid_constant__ NormArgs P) {
-  for (int64_t c = blockIdx.x; c <= P.nchunks; c += gridDim.x) {
+  // a step that forms the total itself may start now: it waits for this
+  // kernel to complete before it reads a partial
+  pdl_allow_next();
+  for (int64_t c = P.c_begin + blockIdx.x; c < P.c_end; c += gridDim.x) {
     const double total = norm_chunk_sum<NR, BF16>(P, c);
     if (threadIdx.x == 0) P.partials[c] = total;
   }
 }
 
-// The partials added in a fixed order by one block.
+// The partials added in a fixed order by one block (fixed_order_total).
 __global__ void __launch_bounds__(kThreads) grad_norm_total_kernel(const __grid_constant__ NormArgs P) {
-  double acc = 0.0;
-  for (int64_t c = threadIdx.x; c <= P.nchunks; c += blockDim.x) acc += P.partials[c];
-  const double total = block_sum(acc);
+  const double total = fixed_order_total(P.partials, P.nchunks + 1, threadIdx.x, blockDim.x, 0);
   if (threadIdx.x == 0) *P.out = total;
 }
 
@@ -966,24 +1044,35 @@ cudaError_t launch_gather(const GatherArgs& a, bool bf16, cudaStream_t s) {
 
 namespace {
 template <bool BF16>
-cudaError_t launch_norm_t(const NormArgs& a, cudaStream_t s) {
-  const int64_t work = (a.nchunks + 1) * kThreads;  // one block per partial at most
-  cudaError_t e;
+cudaError_t launch_partials_t(const NormArgs& a, cudaStream_t s) {
+  if (a.c_end <= a.c_begin) return cudaSuccess;
+  const int64_t work = (a.c_end - a.c_begin) * kThreads;  // one block per partial at most
   switch (a.N) {
-    case 1: e = launch(grad_norm_partials_kernel<1, BF16>, a, work, s); break;
-    case 2: e = launch(grad_norm_partials_kernel<2, BF16>, a, work, s); break;
-    case 4: e = launch(grad_norm_partials_kernel<4, BF16>, a, work, s); break;
-    case 8: e = launch(grad_norm_partials_kernel<8, BF16>, a, work, s); break;
-    default: e = launch(grad_norm_partials_kernel<0, BF16>, a, work, s); break;
+    case 1: return launch(grad_norm_partials_kernel<1, BF16>, a, work, s);
+    case 2: return launch(grad_norm_partials_kernel<2, BF16>, a, work, s);
+    case 4: return launch(grad_norm_partials_kernel<4, BF16>, a, work, s);
+    case 8: return launch(grad_norm_partials_kernel<8, BF16>, a, work, s);
+    default: return launch(grad_norm_partials_kernel<0, BF16>, a, work, s);
   }
-  if (e != cudaSuccess) return e;
-  grad_norm_total_kernel<<<1, kThreads, 0, s>>>(a);
-  return cudaGetLastError();
 }
 }  // namespace
 
+cudaError_t launch_norm_partials(const NormArgs& a, bool bf16, cudaStream_t s) {
+  return bf16 ? launch_partials_t<true>(a, s) : launch_partials_t<false>(a, s);
+}
+
+cudaError_t launch_norm_total(const NormArgs& a, cudaStream_t s) {
+  grad_norm_total_kernel<<<1, kThreads, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_norm(const NormArgs& a, bool bf16, cudaStream_t s) {
-  return bf16 ? launch_norm_t<true>(a, s) : launch_norm_t<false>(a, s);
+  NormArgs all = a;
+  all.c_begin = 0;
+  all.c_end = a.nchunks + 1;
+  cudaError_t e = launch_norm_partials(all, bf16, s);
+  if (e != cudaSuccess) return e;
+  return launch_norm_total(all, s);
 }
 
 // ---------------------------------------------- partial sums without allocation

@@ -112,15 +112,6 @@ __device__ __forceinline__ void bulk_wait_all() {
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
-// Programmatic dependent launch: let the next kernel on the stream start
-// (once every CTA here has said so), and wait for the kernel before this one
-// to complete (a no-op when this kernel was launched without the attribute).
-__device__ __forceinline__ void pdl_allow_next() {
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-__device__ __forceinline__ void pdl_wait_previous() {
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-}
 
 // ------------------------------------------------------------ pipeline shape --
 
@@ -218,17 +209,25 @@ __device__ __forceinline__ void drain_after_timeout(PipeState<S>& ps, int64_t co
     mbar_wait(&ps.full[t % S], uint32_t((t / S) & 1), kDrainNs);
 }
 
+// A pipeline prologue that does nothing.
+struct NoPrologue {
+  __device__ __forceinline__ void operator()() const {}
+};
+
 // The lock-step loop: every thread computes, thread 0 also issues the copies,
 // and block barriers separate the phases. `issue_load(local)` queues the bulk
 // loads of local tile `local` into stage local % kStages;
 // `compute(local, stage, out)` turns stage `stage` into output
 // buffer `out` (or back into the stage when there are no output buffers);
 // `issue_store(local, stage, out)` queues and commits the bulk stores of the
-// results.
-template <class Cfg, typename Load, typename Compute, typename Store>
+// results. `prologue()` runs on every thread once the first loads are issued,
+// before the first tile is computed (work that can overlap those loads).
+template <class Cfg, typename Load, typename Compute, typename Store,
+          typename Prologue = NoPrologue>
 __device__ __forceinline__ void run_pipeline(PipeState<Cfg::kStages>& ps, int64_t my_tiles,
                                              uint64_t wait_ns, Load issue_load,
-                                             Compute compute, Store issue_store) {
+                                             Compute compute, Store issue_store,
+                                             Prologue prologue = Prologue()) {
   constexpr int S = Cfg::kStages;
   constexpr int OB = Cfg::kOutBufs > 0 ? Cfg::kOutBufs : 1;
   const int tid = threadIdx.x;
@@ -242,6 +241,7 @@ __device__ __forceinline__ void run_pipeline(PipeState<Cfg::kStages>& ps, int64_
   if (tid == 0) {
     for (; issued < S && issued < my_tiles; ++issued) issue_load(issued);
   }
+  prologue();
   for (int64_t k = 0; k < my_tiles; ++k) {
     const int s = int(k % S);
     const int o = int(k % OB);
@@ -325,12 +325,16 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
 // on full[local % S]); `compute(local, s, o)`, run by the Cfg::kThreads
 // compute threads (thread index minus kWsExtraThreads), turns stage s into
 // output buffer o; `issue_store(local, s, o)`
-// queues and commits the stores of buffer o.
-template <class Cfg, typename Load, typename Compute, typename Store>
+// queues and commits the stores of buffer o. `prologue()` runs on the compute
+// threads only, before their first tile, while the load warp issues the first
+// loads (it may synchronize them with named barrier 1).
+template <class Cfg, typename Load, typename Compute, typename Store,
+          typename Prologue = NoPrologue>
 __device__ __forceinline__ void run_pipeline_ws(PipeStateWS<Cfg::kStages, Cfg::kOutBufs>& ps,
                                                 int64_t my_tiles, uint64_t wait_ns,
                                                 Load issue_load, Compute compute,
-                                                Store issue_store) {
+                                                Store issue_store,
+                                                Prologue prologue = Prologue()) {
   constexpr int S = Cfg::kStages;
   constexpr int OB = Cfg::kOutBufs;
   constexpr int C = Cfg::kThreads;  // compute threads
@@ -394,6 +398,7 @@ __device__ __forceinline__ void run_pipeline_ws(PipeStateWS<Cfg::kStages, Cfg::k
       if (!__shfl_sync(0xffffffffu, ok, 0)) break;
     }
   } else {
+    prologue();
     for (int64_t k = 0; k < my_tiles; ++k) {
       const int s = int(k % S);
       const int o = kInPlace ? 0 : int(k % (OB > 0 ? OB : 1));
@@ -444,23 +449,24 @@ __global__ void __launch_bounds__(Cfg::kThreads + (WS ? kWsExtraThreads : 0), 1)
   // (a runtime index or stride measured 1-2 % slower on the whole step)
   const int ct = WS ? tid - kWsExtraThreads : tid;
   const Split& sp = P.sp;
-  const float gm = grad_multiplier(P);
   // Buckets of one step touch disjoint indices: the next one may start now.
   // This kernel still completes only after the one before it (the wait at the
   // end), so completion on the stream keeps its order.
   pdl_allow_next();
 
-  // Scalar head and tail (fewer than 2V elements) by block 0.
-  if (blockIdx.x == 0) {
+  // Scalar head and tail (fewer than 2V elements) by block 0, after the tiles
+  // (the multiplier gm may come from a norm pass that is still finishing).
+  auto head_and_tail = [&](int first, int stride, float gm) {
+    if (blockIdx.x != 0) return;
     const int64_t nscalar = sp.head + sp.tail;
     const int64_t body_end = sp.lo + sp.head + sp.nvec * V;
     int owner = 0;
-    for (int64_t s = tid; s < nscalar; s += blockDim.x) {
+    for (int64_t s = first; s < nscalar; s += stride) {
       const int64_t j = s < sp.head ? sp.lo + s : body_end + (s - sp.head);
       owner = advance_owner(P, owner, j);
       step_scalar<NR, MIXED, O>(P, j, owner, gm);
     }
-  }
+  };
 
   const int64_t base = sp.lo + sp.head;
   const int64_t nelem = sp.nvec * V;
@@ -468,9 +474,18 @@ __global__ void __launch_bounds__(Cfg::kThreads + (WS ? kWsExtraThreads : 0), 1)
   const int64_t my_tiles =
       ntiles > int64_t(blockIdx.x) ? (ntiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
   if (my_tiles == 0) {
+    const float gm = group_grad_multiplier(P, tid, blockDim.x, 0);
+    head_and_tail(tid, blockDim.x, gm);
     pdl_wait_previous();
     return;
   }
+  // Set by the pipeline's prologue in every thread that computes: in the
+  // lock-step loop all threads (block barrier), in the warp-specialised loop
+  // the compute warps (named barrier 1), while the first loads are in flight.
+  float gm = 1.0f;
+  auto prologue = [&]() {
+    gm = WS ? group_grad_multiplier(P, ct, TH, 1) : group_grad_multiplier(P, tid, blockDim.x, 0);
+  };
 
   auto stage = [&](int s) { return smem + size_t(s) * G::kStage; };
   auto grad_slot = [&](int s, int r) { return stage(s) + r * G::kGradTile; };
@@ -607,9 +622,11 @@ __global__ void __launch_bounds__(Cfg::kThreads + (WS ? kWsExtraThreads : 0), 1)
   };
 
   if constexpr (WS) {
-    run_pipeline_ws<Cfg>(ps, my_tiles, P.wait_ns, issue_load, compute, issue_store);
+    run_pipeline_ws<Cfg>(ps, my_tiles, P.wait_ns, issue_load, compute, issue_store, prologue);
+    if (ct >= 0) head_and_tail(ct, TH, gm);
   } else {
-    run_pipeline<Cfg>(ps, my_tiles, P.wait_ns, issue_load, compute, issue_store);
+    run_pipeline<Cfg>(ps, my_tiles, P.wait_ns, issue_load, compute, issue_store, prologue);
+    head_and_tail(tid, blockDim.x, gm);
   }
   pdl_wait_previous();
 }

@@ -87,8 +87,10 @@ class ZeroOptimizer:
         """One ZeRO step; returns the new step number t.
 
         With host gradients the copies are pipelined with the step; with
-        clipping every chunk comes in first, then the norm, then the chunks
-        are stepped and copied back one after another. When
+        clipping each chunk's part of the norm is summed as soon as the chunk
+        has arrived, and once all are in the chunks are stepped and copied back
+        one after another. Clipping uses this optimizer's own norm buffers
+        (``_norm`` receives the squared norm). When
         ``host_params_out`` (a host tensor of n elements) is given, the updated
         parameters are copied into it as well; at stage 3 each shard comes from
         its owner's replica and the replicas stay released. Synchronize
@@ -97,37 +99,21 @@ class ZeroOptimizer:
         clipping = self.max_grad_norm > 0
         owner_only = self.stage == 3
         sgd = self.optimizer == "sgd"
-        if clipping and not all(g.is_cuda for g in grads) and self.n > abi.ZERO_NOALLOC_MAX_N:
-            # past the library's own norm scratch: copy first, then the device path
-            staging = self._staging_buffers()
-            s = stream if stream is not None else torch.cuda.current_stream(self.device)
-            with torch.cuda.stream(s):
-                for dst, src in zip(staging, grads):
-                    dst.copy_(src, non_blocking=True)
-            grads = staging
+        norm = scratch = None
+        if clipping:  # the step computes the norm into self._norm itself
+            norm, scratch = self._norm_buffers()
         if all(g.is_cuda for g in grads):
             if clipping or owner_only or sgd or self.grad_scale != 1.0:
-                norm = None
-                if clipping:
-                    f64 = dict(dtype=torch.float64, device=self.device)
-                    if self._norm_scratch is None:
-                        count = abi.zero_grad_norm_scratch_count(self.n, self.precision)
-                        self._norm_scratch = torch.empty(count, **f64)
-                    if self._norm is None:
-                        self._norm = torch.empty(1, **f64)
-                    abi.zero_grad_norm_sq(grads, self.precision, self._norm_scratch, self._norm,
-                                          self.n, stream)
-                    norm = self._norm
                 if sgd:
                     abi.zero_step_sgd(params, grads, self.states, self.t + 1, self.lr,
                                       self.momentum, self.dampening, self.weight_decay,
                                       self.nesterov, self.grad_scale, self.max_grad_norm, norm,
-                                      0, -1, stream, owner_only)
+                                      0, -1, stream, owner_only, norm_scratch=scratch)
                 else:
                     abi.zero_step_ex(params, grads, self.states, self.t + 1, self.lr,
                                      self.beta1, self.beta2, self.eps, self.weight_decay,
                                      self.grad_scale, self.max_grad_norm, norm, 0, -1, stream,
-                                     owner_only)
+                                     owner_only, norm_scratch=scratch)
             else:
                 abi.zero_step(params, grads, self.states, self.t + 1, self.lr, self.beta1,
                               self.beta2, self.eps, self.weight_decay, stream)
@@ -142,23 +128,20 @@ class ZeroOptimizer:
                         host_params_out.copy_(params[0], non_blocking=True)
         else:
             staging = self._staging_buffers()
-            norm = None
-            if clipping:  # the host-input step computes the norm into this scalar
-                if self._norm is None:
-                    self._norm = torch.empty(1, dtype=torch.float64, device=self.device)
-                norm = self._norm.data_ptr()
+            nq = None if norm is None else norm.data_ptr()
+            sq, count = (None, 0) if scratch is None else (scratch.data_ptr(), scratch.numel())
             if sgd:
                 o = abi.SgdOpts(self.t + 1, self.lr, self.momentum, self.dampening,
                                 self.weight_decay, 1 if self.nesterov else 0, self.grad_scale,
-                                self.max_grad_norm, norm, 0, -1, 1 if owner_only else 0)
+                                self.max_grad_norm, nq, 0, -1, 1 if owner_only else 0, sq, count)
                 abi.zero_step_from_host_ex(params, grads, staging, self.states, sgd=o,
                                            host_params_out=host_params_out,
                                            chunk_bytes=chunk_bytes, compute=stream, h2d=self._h2d,
                                            d2h=self._d2h)
             elif clipping or owner_only or self.grad_scale != 1.0:
                 o = abi.StepOpts(self.t + 1, self.lr, self.beta1, self.beta2, self.eps,
-                                 self.weight_decay, self.grad_scale, self.max_grad_norm, norm,
-                                 0, -1, 1 if owner_only else 0)
+                                 self.weight_decay, self.grad_scale, self.max_grad_norm, nq,
+                                 0, -1, 1 if owner_only else 0, sq, count)
                 abi.zero_step_from_host_ex(params, grads, staging, self.states, adamw=o,
                                            host_params_out=host_params_out,
                                            chunk_bytes=chunk_bytes, compute=stream, h2d=self._h2d,
@@ -170,6 +153,18 @@ class ZeroOptimizer:
                                         self._d2h)
         self.t += 1
         return self.t
+
+    def _norm_buffers(self):
+        """This optimizer's own device buffers for the clipping norm: the
+        squared norm and the scratch of its partial sums (never shared with
+        another optimizer, so optimizers on different streams do not race)."""
+        f64 = dict(dtype=torch.float64, device=self.device)
+        if self._norm_scratch is None:
+            count = abi.zero_grad_norm_scratch_count(self.n, self.precision)
+            self._norm_scratch = torch.empty(count, **f64)
+        if self._norm is None:
+            self._norm = torch.empty(1, **f64)
+        return self._norm, self._norm_scratch
 
     def _bounds_pairs(self):
         b = self.shard_bounds if self.shard_bounds is not None else \
