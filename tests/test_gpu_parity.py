@@ -447,17 +447,15 @@ def test_ddp_mean_from_host_chained_on_a_handle(abi, cuda, prec):
         host = [_pinned_host(h, dt) for h in hs]
         out = torch.empty(n, dtype=dt).pin_memory()
         if i == 3:  # device work on the staging buffers between calls, then a reset
-            seen = staging[0].clone()
+            calls.append(("seen", staging[0].clone()))
             ddp.reset()
         chunk = 1 << 18 if i != 4 else 3 * (1 << 16) + 6
         ddp.mean_from_host(host, staging, prec, n, out, chunk, None, h2d, d2h)
         calls.append((hs, out))
-        if i == 3:
-            calls.append(("seen", seen))
     torch.cuda.synchronize()
     last_ref = None
     for entry in calls:
-        if entry[0] == "seen":  # the clone saw the mean of the call before it
+        if isinstance(entry[0], str):  # the clone saw the mean of the call before it
             assert np.array_equal(host_of(entry[1]), last_ref[0])
             continue
         hs, out = entry

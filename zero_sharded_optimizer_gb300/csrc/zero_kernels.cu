@@ -893,9 +893,13 @@ template <int NR, bool MIXED, Opt O, bool WS, class Cfg>
 cudaError_t launch_step_cfg(const StepArgs& a, cudaStream_t s) {
   using G = StepTile<NR, MIXED, kStates<O>, Cfg>;
   const int64_t nelem = a.sp.nvec * (MIXED ? 8 : 4);
-  return launch_tma<zero_step_tma_kernel<NR, MIXED, O, WS, Cfg>,
-                    Cfg::kThreads + (WS ? kWsExtraThreads : 0)>(
-      a, G::kSmem, (nelem + G::T - 1) / G::T, s, a.dependent != 0);
+  const int64_t tiles = (nelem + G::T - 1) / G::T;
+  constexpr int kTh = Cfg::kThreads + (WS ? kWsExtraThreads : 0);
+  if (a.norm_partials)
+    return launch_tma<zero_step_tma_kernel<NR, MIXED, O, WS, Cfg, true>, kTh>(
+        a, G::kSmem, tiles, s, a.dependent != 0);
+  return launch_tma<zero_step_tma_kernel<NR, MIXED, O, WS, Cfg, false>, kTh>(
+      a, G::kSmem, tiles, s, a.dependent != 0);
 }
 
 // Measured choice for the AdamW step with its all-gather (GB/s over N = 1..8
