@@ -600,7 +600,7 @@ def run_gpu(args, wl, rank: int, world: int, local_rank: int) -> dict | None:
         launches_per_step += 1      # the gather after the owner-only step
     stream = torch.cuda.current_stream()
 
-    def one_step():
+    def one_step(mid=None):
         if ddp:
             abi.ddp_allreduce_mean(grads, wl.precision, n)
         elif bucketed:
@@ -608,6 +608,8 @@ def run_gpu(args, wl, rank: int, world: int, local_rank: int) -> dict | None:
         else:
             opt.step(reps, grads)
             if stage3:
+                if mid is not None:  # between the owner-only step and the gather
+                    mid.record(stream)
                 opt.gather(reps)
 
     def barrier():
@@ -622,13 +624,14 @@ def run_gpu(args, wl, rank: int, world: int, local_rank: int) -> dict | None:
     sampler = ClockSampler(local_rank) if rank == 0 else None
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    mids = [torch.cuda.Event(enable_timing=True) for _ in range(K)] if stage3 else None
     t_begin = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     barrier()
     t_begin.record(stream)
     for k in range(K):
         starts[k].record(stream)
-        one_step()
+        one_step(mids[k] if mids else None)
         ends[k].record(stream)
     t_end.record(stream)
     barrier()
@@ -638,6 +641,14 @@ def run_gpu(args, wl, rank: int, world: int, local_rank: int) -> dict | None:
     kernel_ms = sum(step_times) / K
     ms_step = ms_total / K
     dist_ms = [percentile(step_times, q) for q in (10, 50, 90)]
+    split = None
+    if stage3:  # each kernel of the stage-3 step on its own (CUDA events between them)
+        es_ = 2 if wl.precision == inputs.BF16_MIXED else 4
+        step_part = sum(s.elapsed_time(m) for s, m in zip(starts, mids)) / K
+        gather_part = sum(m.elapsed_time(e) for m, e in zip(mids, ends)) / K
+        split = {"owner_only_step_ms": step_part, "gather_ms": gather_part,
+                 "gather_gbs": n * wl.N * es_ / (gather_part / 1e3) / 1e9,
+                 "gather_bytes": "n x N x element size (read the owner's element, write N-1)"}
 
     ms_step, kernel_ms = max_over_ranks([ms_step, kernel_ms], dev, world)
     producer = None
@@ -775,11 +786,12 @@ def run_gpu(args, wl, rank: int, world: int, local_rank: int) -> dict | None:
                                 "allreduce_mean_kernel") if ddp else
                                ("grad_norm_partials_kernel + zero_step_tma_kernel adding "
                                 "the partials (whole clipped step)") if clip else
-                               ("zero_step_tma_kernel (owner-only) + gather_tma_kernel "
+                               ("zero_step_tma_kernel (owner-only) + gather_kernel "
                                 "(whole stage-3 step)") if stage3 else
-                               ("zero_step_tma_kernel" if wl.N <= 8 else "zero_step_kernel"),
+                               ("zero_step_tma_kernel" if 2 <= wl.N <= 8 else "zero_step_kernel"),
                      "kernel_ms": kernel_ms / per,
-                     "step_ms_p10_median_p90": dist_ms},
+                     "step_ms_p10_median_p90": dist_ms,
+                     **({"stage3_split": split} if split else {})},
         "gpu_launches": K * launches_per_step,
         "clocks": clocks,
         "e2e": e2e,
@@ -854,12 +866,19 @@ def main(argv=None):
     ap.add_argument("--n", type=int, default=None,
                     help="override the parameter count: a smaller case of the same kernels for "
                          "ncu captures (named <workload>_n<count>; not a bench line)")
+    ap.add_argument("--ranks", type=int, default=None,
+                    help="override the simulated rank count N (named <workload>_N<ranks>; a "
+                         "case for sweeps, not a bench line)")
     args = ap.parse_args(argv)
     wl = inputs.WORKLOADS[args.workload]
     if args.n is not None:
         if args.n <= 0 or args.partition == "tensor":
             ap.error("--n needs a positive count and the np.array_split partition")
         wl = dataclasses.replace(wl, n=args.n, name=f"{wl.name}_n{args.n}")
+    if args.ranks is not None:
+        if not 1 <= args.ranks <= 64 or args.partition == "tensor":
+            ap.error("--ranks needs 1..64 and the np.array_split partition")
+        wl = dataclasses.replace(wl, N=args.ranks, name=f"{wl.name}_N{args.ranks}")
     if args.steps is None:
         args.steps = default_steps(wl)
     if args.warmup < 3:

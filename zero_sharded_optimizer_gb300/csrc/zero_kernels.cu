@@ -9,7 +9,7 @@
 // index order, so the shard structure only decides whose replica holds the
 // authoritative fp32 parameter (the owner's) -- never the arithmetic. Variants:
 // momentum SGD in place of AdamW, and the stage-3 owner-only step (no
-// all-gather; gather_kernel / gather_tma_kernel bring the replicas back).
+// all-gather; gather_kernel brings the replicas back).
 //
 // The step moves 8N+20 bytes per parameter in fp32 (4N+24 in mixed precision)
 // and does ~20 flops per parameter: it is bound by HBM bandwidth. Two kinds of
@@ -19,9 +19,11 @@
 //    and buffers of mixed 16-byte phase: 16-byte vector loads/stores, one
 //    V-element unit per thread per iteration (V = 4 fp32, V = 8 mixed), every
 //    load of a unit issued before any arithmetic, streaming cache hints
-//    (ld/st .cs), a grid-stride loop over units with a grid of (SMs x resident
-//    blocks), and a scalar head/tail for ranges whose ends are not on a unit
-//    boundary.
+//    (ld/st .cs), and a scalar head/tail for ranges whose ends are not on a
+//    unit boundary. Its grid is one pass over the units in mixed precision and
+//    for N > 8 (a block per stretch of units, launched in waves), else a
+//    grid-stride loop over (SMs x resident blocks): each measured faster there.
+// The stage-3 gather (gather_kernel) is register streaming in one pass too.
 // Both use explicitly rounded IEEE fp32 intrinsics (__fadd_rn, __fmul_rn,
 // __fdiv_rn, __fsqrt_rn): no contraction, so the result is independent of
 // compiler scheduling and bit-reproducible, and the two kinds agree bit for
@@ -738,7 +740,12 @@ __device__ __forceinline__ void gather_one(const GatherArgs& P, int owner, int64
     if (r != owner) __stcs(static_cast<E*>(P.reps[r]) + j, x);
 }
 
-template <bool BF16>
+// U units per thread per iteration, block-interleaved (unit u of a thread is
+// u * blockDim.x units after its first, so each warp-wide access covers 512
+// contiguous bytes): the loads of all U units, each from its unit's owner, are
+// issued before any store, then each unit goes to the N-1 other replicas. The
+// owner scan only moves forward along a thread's units.
+template <bool BF16, int U>
 __global__ void __launch_bounds__(kThreads) gather_kernel(const __grid_constant__ GatherArgs P) {
   using E = typename std::conditional<BF16, uint16_t, float>::type;
   constexpr int V = 16 / int(sizeof(E));
@@ -756,19 +763,40 @@ __global__ void __launch_bounds__(kThreads) gather_kernel(const __grid_constant_
   }
 
   const int64_t base = sp.lo + sp.head;
+  const int64_t span = int64_t(blockDim.x) * U;  // units per block and iteration
   owner = 0;
-  for (int64_t u = tid; u < sp.nvec; u += stride) {
-    const int64_t j = base + u * V;
-    owner = gather_owner(P, owner, j);
-    if (j + V - 1 < P.bounds[owner + 1]) {
-      const uint4 x = __ldcs(reinterpret_cast<const uint4*>(static_cast<const E*>(P.reps[owner]) + j));
-      for (int r = 0; r < P.N; ++r)
-        if (r != owner) __stcs(reinterpret_cast<uint4*>(static_cast<E*>(P.reps[r]) + j), x);
-    } else {
-      int o = owner;
-      for (int k = 0; k < V; ++k) {
-        o = gather_owner(P, o, j + k);
-        gather_one<E>(P, o, j + k);
+  for (int64_t b0 = int64_t(blockIdx.x) * span; b0 < sp.nvec; b0 += int64_t(gridDim.x) * span) {
+    uint4 x[U];
+    int o[U];
+    bool whole[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t uv = b0 + threadIdx.x + int64_t(u) * blockDim.x;
+      whole[u] = false;
+      o[u] = owner;
+      if (uv < sp.nvec) {
+        const int64_t j = base + uv * V;
+        owner = gather_owner(P, owner, j);
+        o[u] = owner;
+        whole[u] = j + V - 1 < P.bounds[owner + 1];
+        if (whole[u])
+          x[u] = __ldcs(reinterpret_cast<const uint4*>(static_cast<const E*>(P.reps[owner]) + j));
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t uv = b0 + threadIdx.x + int64_t(u) * blockDim.x;
+      if (uv >= sp.nvec) continue;
+      const int64_t j = base + uv * V;
+      if (whole[u]) {
+        for (int r = 0; r < P.N; ++r)
+          if (r != o[u]) __stcs(reinterpret_cast<uint4*>(static_cast<E*>(P.reps[r]) + j), x[u]);
+      } else {  // the unit straddles a shard boundary: element by element
+        int e = o[u];
+        for (int k = 0; k < V; ++k) {
+          e = gather_owner(P, e, j + k);
+          gather_one<E>(P, e, j + k);
+        }
       }
     }
   }
@@ -843,6 +871,20 @@ cudaError_t launch(K kernel, const A& args, int64_t work, cudaStream_t s) {
   cudaError_t e = grid_for(kernel, work, &blocks);
   if (e != cudaSuccess) return e;
   kernel<<<blocks, kThreads, 0, s>>>(args);
+  return cudaGetLastError();
+}
+
+// One pass: blocks for all the work, launched in waves, each block taking
+// one stretch of units and exiting (no grid-stride loop). For the gather
+// (1 read, N-1 writes) this measured 6-13 % faster than a persistent
+// grid-stride grid of the same kernel, and than the bulk-copy pipeline it
+// replaced, at N = 2, 4, 8 on 25M-320M elements.
+template <typename K, typename A>
+cudaError_t launch_one_pass(K kernel, const A& args, int64_t threads_needed, cudaStream_t s) {
+  int64_t blocks = (threads_needed + kThreads - 1) / kThreads;
+  if (blocks < 1) blocks = 1;
+  if (blocks > 0x7fffffff) return cudaErrorInvalidValue;
+  kernel<<<unsigned(blocks), kThreads, 0, s>>>(args);
   return cudaGetLastError();
 }
 
@@ -963,6 +1005,19 @@ cudaError_t launch_step_t(const StepArgs& a, cudaStream_t s) {
     }
   }
   const int64_t work = a.sp.nvec > a.sp.head + a.sp.tail ? a.sp.nvec : a.sp.head + a.sp.tail;
+  // A vector body in mixed precision, or for N > 8, runs in one pass (a
+  // block per stretch of units, no grid-stride loop): bf16 N = 1 on 124M
+  // 0.61 -> 0.52 ms, fp32 N = 13 on 25M 0.50 -> 0.45 ms. fp32 N = 1 measured 2 %
+  // faster persistent, and keeps that grid.
+  if (a.sp.nvec > 0 && (MIXED || a.N > 8)) {
+    switch (a.N) {
+      case 1: return launch_one_pass(zero_step_kernel<1, MIXED, O>, a, work, s);
+      case 2: return launch_one_pass(zero_step_kernel<2, MIXED, O>, a, work, s);
+      case 4: return launch_one_pass(zero_step_kernel<4, MIXED, O>, a, work, s);
+      case 8: return launch_one_pass(zero_step_kernel<8, MIXED, O>, a, work, s);
+      default: return launch_one_pass(zero_step_kernel<0, MIXED, O>, a, work, s);
+    }
+  }
   switch (a.N) {
     case 1: return launch(zero_step_kernel<1, MIXED, O>, a, work, s);
     case 2: return launch(zero_step_kernel<2, MIXED, O>, a, work, s);
@@ -1025,20 +1080,15 @@ cudaError_t launch_init(const InitArgs& a, cudaStream_t s) {
 namespace {
 template <bool BF16>
 cudaError_t launch_gather_t(const GatherArgs& a, cudaStream_t s) {
-  // The bulk-copy pipeline when the replicas share a 16-byte phase and N >= 4
-  // (bf16: N >= 5). With fewer replicas a tile carries few stores, and register
-  // streaming measured faster: 0.96 vs 0.81 of the copy peak (fp32 N = 2), 0.93
-  // vs 0.69 (bf16 N = 2), 0.86 vs 0.68 (bf16 N = 3), 0.84 vs 0.80-0.83 (bf16
-  // N = 4). Deeper store queues (2-6 tiles of stores reading their stage at
-  // once) changed nothing.
-  if (a.sp.nvec > 0 && a.N >= (BF16 ? 5 : 4)) {
-    using G = GatherTile<BF16>;
-    const int64_t tiles = (a.sp.nvec * (16 / G::kEB) + G::T - 1) / G::T;
-    return launch_tma<gather_tma_kernel<BF16>, GatherPipe::kThreads>(a, G::kSmem, tiles, s, false,
-                                                                      kGatherCtasPerSm);
+  // Units per thread: one with at least four replicas, two below (fewer
+  // stores per load); measured at N = 2, 4, 8 (6.1, 6.5, 6.7 TB/s).
+  const int64_t nscalar = a.sp.head + a.sp.tail;
+  if (a.N >= 4) {
+    const int64_t work = a.sp.nvec > nscalar ? a.sp.nvec : nscalar;
+    return launch_one_pass(gather_kernel<BF16, 1>, a, work, s);
   }
-  const int64_t work = a.sp.nvec > a.sp.head + a.sp.tail ? a.sp.nvec : a.sp.head + a.sp.tail;
-  return launch(gather_kernel<BF16>, a, work, s);
+  const int64_t units = (a.sp.nvec + 1) / 2;
+  return launch_one_pass(gather_kernel<BF16, 2>, a, units > nscalar ? units : nscalar, s);
 }
 }  // namespace
 

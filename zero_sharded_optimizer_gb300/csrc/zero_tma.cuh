@@ -1,6 +1,6 @@
 // Bulk-copy (TMA) staged kernels: the fused ZeRO step (AdamW or SGD, with the
-// all-gather or owner-only), the DDP mean for N <= 8 ranks, and the stage-3
-// gather. Included by zero_kernels.cu after the element helpers.
+// all-gather or owner-only) and the DDP mean for N <= 8 ranks. Included by
+// zero_kernels.cu after the element helpers.
 //
 // Pipeline (one CTA per SM, persistent over tiles tile = blockIdx.x + k*gridDim.x):
 //   * per tile, one cp.async.bulk global->shared copy per input stream (N
@@ -737,118 +737,6 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
       }
     }
   };
-  run_pipeline<Cfg>(ps, my_tiles, P.wait_ns, issue_load, compute, issue_store);
-}
-
-// ------------------------------------------------------- stage-3 all-gather --
-
-// Tiles of 16 KB (4096 fp32 or 8192 bf16 elements), stored straight from the
-// stage (no compute on the data), in two CTAs per SM of six stages each. One
-// CTA of twelve stages measured the same on fp32_25m and 9 % and 25 % faster
-// than 32 KB x 6 and 64 KB x 3 on gpt2_small (seven replicas written per
-// tile); splitting it into two CTAs per SM took another 2-5 % (329.8 against
-// 342.6 us on gpt2_small, 172.2 against 182.0 us for bf16 N = 5 at 100M; fp32
-// N = 4 at 100M unchanged at 6.0 TB/s). Storing from shared memory with
-// register stores measured 2-7 % slower, and 4 KB bulk stores the same.
-using GatherPipe = PipeCfg<128, 6, 0, 96 * 1024>;
-constexpr int kGatherCtasPerSm = 2;
-
-template <bool BF16>
-struct GatherTile {
-  static constexpr int kEB = BF16 ? 2 : 4;
-  static constexpr uint32_t kTileBytes = 16384;
-  static constexpr int T = int(kTileBytes) / kEB;
-  static constexpr uint32_t kSmem = GatherPipe::kStages * kTileBytes;
-};
-
-// Per tile: one bulk load of the owner's replica into shared memory, then one
-// bulk store into each of the other N-1 replicas. A tile that straddles shard
-// boundaries is loaded from its first element's owner; the elements of the
-// later owners are then read from their owners' replicas into the tile, and
-// each replica receives the tile minus its own shard (store_slice).
-template <bool BF16>
-__global__ void __launch_bounds__(GatherPipe::kThreads, kGatherCtasPerSm)
-    gather_tma_kernel(const __grid_constant__ GatherArgs P) {
-  using G = GatherTile<BF16>;
-  using E = typename std::conditional<BF16, uint16_t, float>::type;
-  using Cfg = GatherPipe;
-  constexpr int T = G::T;
-  constexpr int V = 16 / G::kEB;
-  constexpr int S = Cfg::kStages;
-  constexpr int TH = Cfg::kThreads;
-  extern __shared__ __align__(128) unsigned char smem[];
-  __shared__ PipeState<S> ps;
-  const int tid = threadIdx.x;
-  const Split& sp = P.sp;
-
-  if (blockIdx.x == 0) {
-    const int64_t nscalar = sp.head + sp.tail;
-    const int64_t body_end = sp.lo + sp.head + sp.nvec * V;
-    int owner = 0;
-    for (int64_t s = tid; s < nscalar; s += blockDim.x) {
-      const int64_t j = s < sp.head ? sp.lo + s : body_end + (s - sp.head);
-      owner = gather_owner(P, owner, j);
-      gather_one<E>(P, owner, j);
-    }
-  }
-
-  const int64_t base = sp.lo + sp.head;
-  const int64_t nelem = sp.nvec * V;
-  const int64_t ntiles = (nelem + T - 1) / T;
-  const int64_t my_tiles =
-      ntiles > int64_t(blockIdx.x) ? (ntiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
-  if (my_tiles == 0) return;
-
-  auto tile = [&](int s) { return reinterpret_cast<E*>(smem + size_t(s) * G::kTileBytes); };
-  auto tile_j0 = [&](int64_t local) { return base + (blockIdx.x + local * gridDim.x) * T; };
-  auto tile_cnt = [&](int64_t local) {
-    const int64_t rem = nelem - (blockIdx.x + local * gridDim.x) * int64_t(T);
-    return uint32_t(rem < T ? rem : T);
-  };
-
-  auto issue_load = [&](int64_t local) {
-    const int s = int(local % S);
-    const int64_t j0 = tile_j0(local);
-    const uint32_t cnt = tile_cnt(local);
-    const int owner = gather_owner(P, 0, j0);
-    ps.owner[s] = j0 + cnt - 1 >= P.bounds[owner + 1] ? -1 : owner;
-    mbar_expect_tx(&ps.full[s], cnt * G::kEB);
-    bulk_load(tile(s), static_cast<const E*>(P.reps[owner]) + j0, cnt * G::kEB, &ps.full[s]);
-  };
-
-  auto compute = [&](int64_t local, int s, int) {
-    if (ps.owner[s] >= 0) return;  // one owner: the tile is already complete
-    const int64_t j0 = tile_j0(local);
-    const int cnt = int(tile_cnt(local));
-    const int first = gather_owner(P, 0, j0);
-    E* t = tile(s);
-    for (int q = tid; q < cnt; q += TH) {
-      if (j0 + q < P.bounds[first + 1]) continue;  // loaded from the first owner
-      const int o = gather_owner(P, first, j0 + q);
-      t[q] = __ldcs(static_cast<const E*>(P.reps[o]) + j0 + q);
-    }
-  };
-
-  auto issue_store = [&](int64_t local, int s, int) {
-    const int64_t j0 = tile_j0(local);
-    const uint32_t cnt = tile_cnt(local);
-    const int owner = ps.owner[s];
-    const E* t = tile(s);
-    for (int r = 0; r < P.N; ++r) {
-      if (owner >= 0) {
-        if (r != owner) bulk_store(static_cast<E*>(P.reps[r]) + j0, t, cnt * G::kEB);
-      } else {  // the tile minus replica r's own shard: up to two slices
-        const int64_t end = j0 + cnt;
-        const int64_t a = P.bounds[r] < j0 ? j0 : (P.bounds[r] > end ? end : P.bounds[r]);
-        const int64_t b = P.bounds[r + 1] < j0 ? j0 : (P.bounds[r + 1] > end ? end : P.bounds[r + 1]);
-        E* dst = static_cast<E*>(P.reps[r]);
-        store_slice(dst, t, j0, j0, a);
-        store_slice(dst, t, j0, b, end);
-      }
-    }
-    bulk_commit();
-  };
-
   run_pipeline<Cfg>(ps, my_tiles, P.wait_ns, issue_load, compute, issue_store);
 }
 
