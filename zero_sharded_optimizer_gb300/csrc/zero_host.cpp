@@ -682,7 +682,6 @@ int zero_gather(void* const* params, zero_states_t* st, int64_t lo, int64_t hi,
   zk::GatherArgs a;
   std::memset(&a, 0, sizeof(a));
   a.N = N;
-  a.wait_ns = g_wait_ns.load(std::memory_order_relaxed);
   std::memcpy(a.bounds, st->bounds, sizeof(int64_t) * (N + 1));
   std::vector<Range> rs;
   int ph = -2;

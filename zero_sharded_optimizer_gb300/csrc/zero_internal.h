@@ -120,7 +120,6 @@ struct GatherArgs {
   int64_t bounds[kMaxRanks + 1];
   Split sp;
   int32_t N;
-  uint64_t wait_ns;  // bound of every wait on a bulk copy (TMA kernel)
 };
 
 struct InitArgs {

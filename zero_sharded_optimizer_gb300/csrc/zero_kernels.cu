@@ -896,7 +896,7 @@ cudaError_t launch_one_pass(K kernel, const A& args, int64_t threads_needed, cud
 // whose data is disjoint from that kernel's (the next bucket of one step).
 template <auto kernel, int THREADS, typename A>
 cudaError_t launch_tma(const A& args, uint32_t smem, int64_t tiles, cudaStream_t s,
-                       bool dependent = false, int ctas_per_sm = 1) {
+                       bool dependent = false) {
   static bool configured[256] = {false};  // per device ordinal; one array per kernel
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -908,8 +908,7 @@ cudaError_t launch_tma(const A& args, uint32_t smem, int64_t tiles, cudaStream_t
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
-  const int64_t slots = int64_t(sms) * ctas_per_sm;
-  const int blocks = int(tiles < 1 ? 1 : (tiles < slots ? tiles : slots));
+  const int blocks = int(tiles < 1 ? 1 : (tiles < sms ? tiles : sms));
   if (!dependent) {
     kernel<<<blocks, THREADS, smem, s>>>(args);
     return cudaGetLastError();
