@@ -139,6 +139,18 @@ def max_over_ranks(values, device, world: int):
     return [float(x) for x in t.tolist()]
 
 
+def host_memory_available() -> int | None:
+    """MemAvailable of /proc/meminfo in bytes, or None where it cannot be read."""
+    try:
+        with open("/proc/meminfo") as f:
+            for line in f:
+                if line.startswith("MemAvailable:"):
+                    return int(line.split()[1]) * 1024
+    except (OSError, ValueError, IndexError):
+        return None
+    return None
+
+
 def whole_job_rate(units_per_rank: int, world: int, ms_per_step: float) -> float:
     """Units processed by all ranks per second, over the slowest rank's time."""
     return world * units_per_rank / (ms_per_step / 1e3)
@@ -656,83 +668,105 @@ def run_gpu(args, wl, rank: int, world: int, local_rank: int) -> dict | None:
         producer = producer_report(opt, reps, grads, wl, stream, iters=10)
 
     # ---- end to end through the public API: host gradients in, parameters out
-    E2E_BLOCK = 5
-    K_e = E2E_BLOCK * max(1, min(K, 30) // E2E_BLOCK)
-    host_grads = []
-    for g in grads:
-        h = torch.empty(n, dtype=g.dtype, pin_memory=True)
-        h.copy_(g)
-        host_grads.append(h)
-    host_out = torch.empty(n, dtype=reps[0].dtype, pin_memory=True)
-    if ddp:
-        host_out = torch.empty(n, dtype=grads[0].dtype, pin_memory=True)
-
-    def e2e_path(o):
-        if o.max_grad_norm > 0:
-            return ("ZeroOptimizer.step with pinned host gradients -> zero_step_from_host_ex "
-                    "with clipping: every 25 MiB chunk copied in on a copy stream, its part of "
-                    "the norm summed once it has arrived, the norm's total once all have, then "
-                    "the clipped step chunk by chunk, each chunk's "
-                    "D2H on a second copy stream while the next is stepped")
-        entry = ("zero_step_from_host_ex" if o.stage == 3 or o.optimizer == "sgd"
-                 or o.grad_scale != 1.0 else "zero_step_from_host")
-        out = ("each shard from its owner's replica" if o.stage == 3
-               else "one updated replica")
-        return (f"ZeroOptimizer.step with pinned host gradients -> {entry}: 25 MiB chunks, "
-                "H2D on a copy stream, the step per chunk on the compute stream, D2H of "
-                f"{out} on a second copy stream")
-
-    ddp_h2d, ddp_d2h = (torch.cuda.Stream(), torch.cuda.Stream()) if ddp else (None, None)
-    ddp_host = abi.DdpHost() if ddp else None
-
-    def e2e_step():
-        if ddp:  # gradients in, the mean gradient out, chunk-pipelined and chained
-            ddp_host.mean_from_host(host_grads, grads, wl.precision, n, host_out,
-                                    BUCKET_BYTES_25MIB, None, ddp_h2d, ddp_d2h)
-        else:
-            opt.step(reps, host_grads, host_params_out=host_out)
-
-    # The host link's rate drifts by tens of percent over seconds (the host is
-    # shared), so the e2e steps and the copies-alone bound alternate in blocks
-    # of E2E_BLOCK back-to-back steps and each side sums its blocks.
-    link = host_link_timer(grads, host_grads, host_out, reps[0], stream,
-                           BUCKET_BYTES_25MIB // (2 if mixed else 4))
-
-    def e2e_block(k: int) -> float:
-        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        torch.cuda.synchronize()
-        t0.record(stream)
-        for _ in range(k):
-            e2e_step()
-        t1.record(stream)
-        torch.cuda.synchronize()
-        return t0.elapsed_time(t1)
-
-    for _ in range(2):
-        e2e_step()
-    link(1)
-    barrier()
-    e_total = l_total = 0.0
-    for _ in range(K_e // E2E_BLOCK):
-        e_total += e2e_block(E2E_BLOCK)
-        l_total += link(E2E_BLOCK)
-    barrier()
-    e_ms, link_ms = max_over_ranks([e_total / K_e, l_total / K_e], dev, world)
     es = 2 if mixed else 4
-    e2e = {"value": whole_job_rate(n, world, e_ms), "unit": UNIT,
-           "h2d_bytes_per_step": N * n * es, "d2h_bytes_per_step": n * es,
-           "ms_per_step": e_ms, "steps": K_e,
-           "host_link_ms": link_ms, "frac_of_host_link": link_ms / e_ms,
-           "host_link": f"the same H2D and D2H copies alone in the host-input step's "
-                        f"schedule (25 MiB chunks: H2D on one stream, then that chunk's D2H on "
-                        f"another), no step: the e2e lower bound on this host link; timed in "
-                        f"blocks of {E2E_BLOCK} back-to-back steps alternating with the e2e "
-                        f"blocks",
-           "path": ("ddp_allreduce_mean_from_host_h with pinned host gradients: 25 MiB "
-                    "chunks, H2D on a copy stream, the mean per chunk on the compute stream, "
-                    "D2H of the mean on a second copy stream; back-to-back calls on one handle "
-                    "chained chunk by chunk") if ddp else
-                   e2e_path(opt)}
+    h2d_bytes, d2h_bytes = N * n * es, n * es
+
+    def measure_e2e():
+        E2E_BLOCK = 5
+        K_e = E2E_BLOCK * max(1, min(K, 30) // E2E_BLOCK)
+        host_grads = []
+        for g in grads:
+            h = torch.empty(n, dtype=g.dtype, pin_memory=True)
+            h.copy_(g)
+            host_grads.append(h)
+        host_out = torch.empty(n, dtype=reps[0].dtype, pin_memory=True)
+        if ddp:
+            host_out = torch.empty(n, dtype=grads[0].dtype, pin_memory=True)
+
+        def e2e_path(o):
+            if o.max_grad_norm > 0:
+                return ("ZeroOptimizer.step with pinned host gradients -> zero_step_from_host_ex "
+                        "with clipping: every 25 MiB chunk copied in on a copy stream, its part of "
+                        "the norm summed once it has arrived, the norm's total once all have, then "
+                        "the clipped step chunk by chunk, each chunk's "
+                        "D2H on a second copy stream while the next is stepped")
+            entry = ("zero_step_from_host_ex" if o.stage == 3 or o.optimizer == "sgd"
+                     or o.grad_scale != 1.0 else "zero_step_from_host")
+            out = ("each shard from its owner's replica" if o.stage == 3
+                   else "one updated replica")
+            return (f"ZeroOptimizer.step with pinned host gradients -> {entry}: 25 MiB chunks, "
+                    "H2D on a copy stream, the step per chunk on the compute stream, D2H of "
+                    f"{out} on a second copy stream")
+
+        ddp_h2d, ddp_d2h = (torch.cuda.Stream(), torch.cuda.Stream()) if ddp else (None, None)
+        ddp_host = abi.DdpHost() if ddp else None
+
+        def e2e_step():
+            if ddp:  # gradients in, the mean gradient out, chunk-pipelined and chained
+                ddp_host.mean_from_host(host_grads, grads, wl.precision, n, host_out,
+                                        BUCKET_BYTES_25MIB, None, ddp_h2d, ddp_d2h)
+            else:
+                opt.step(reps, host_grads, host_params_out=host_out)
+
+        # The host link's rate drifts by tens of percent over seconds (the host is
+        # shared), so the e2e steps and the copies-alone bound alternate in blocks
+        # of E2E_BLOCK back-to-back steps and each side sums its blocks.
+        link = host_link_timer(grads, host_grads, host_out, reps[0], stream,
+                               BUCKET_BYTES_25MIB // (2 if mixed else 4))
+
+        def e2e_block(k: int) -> float:
+            t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            t0.record(stream)
+            for _ in range(k):
+                e2e_step()
+            t1.record(stream)
+            torch.cuda.synchronize()
+            return t0.elapsed_time(t1)
+
+        for _ in range(2):
+            e2e_step()
+        link(1)
+        barrier()
+        e_total = l_total = 0.0
+        for _ in range(K_e // E2E_BLOCK):
+            e_total += e2e_block(E2E_BLOCK)
+            l_total += link(E2E_BLOCK)
+        barrier()
+        e_ms, link_ms = max_over_ranks([e_total / K_e, l_total / K_e], dev, world)
+        e2e = {"value": whole_job_rate(n, world, e_ms), "unit": UNIT,
+               "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": d2h_bytes,
+               "ms_per_step": e_ms, "steps": K_e,
+               "host_link_ms": link_ms, "frac_of_host_link": link_ms / e_ms,
+               "host_link": f"the same H2D and D2H copies alone in the host-input step's "
+                            f"schedule (25 MiB chunks: H2D on one stream, then that chunk's D2H on "
+                            f"another), no step: the e2e lower bound on this host link; timed in "
+                            f"blocks of {E2E_BLOCK} back-to-back steps alternating with the e2e "
+                            f"blocks",
+               "path": ("ddp_allreduce_mean_from_host_h with pinned host gradients: 25 MiB "
+                        "chunks, H2D on a copy stream, the mean per chunk on the compute stream, "
+                        "D2H of the mean on a second copy stream; back-to-back calls on one handle "
+                        "chained chunk by chunk") if ddp else
+                       e2e_path(opt)}
+        return e2e
+
+    # The e2e leg pins the step's host gradients and output (N + 1 vectors per
+    # rank). All ranks decide together whether the node's free host memory
+    # holds them for every local rank; if not, the leg reports why instead of
+    # failing the run.
+    local_ranks = int(os.environ.get("LOCAL_WORLD_SIZE", str(world)))
+    pinned = h2d_bytes + d2h_bytes
+    avail = host_memory_available()
+    short = avail is not None and pinned * local_ranks > 0.7 * avail
+    short = max_over_ranks([1.0 if short else 0.0], dev, world)[0] > 0
+    if short:
+        e2e = {"value": None, "unit": UNIT, "h2d_bytes_per_step": h2d_bytes,
+               "d2h_bytes_per_step": d2h_bytes,
+               "unavailable": f"host memory: {local_ranks} local rank(s) x {pinned / 1e9:.1f} GB "
+                              f"pinned would exceed 70 % of the node's available "
+                              f"{(avail or 0) / 1e9:.1f} GB"}
+    else:
+        e2e = measure_e2e()
 
     if rank != 0:
         return None

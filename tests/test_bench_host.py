@@ -162,3 +162,17 @@ def test_all_cores_oracle_baseline_runs_on_spawned_processes():
     rec = bench.cpu_baseline_all_cores(inputs.WORKLOADS["tiny_adam"], seconds=0.3, procs=2)
     assert rec["cores"] == 2 and "unavailable" not in rec, rec
     assert rec["value"] > 0
+
+
+def test_host_memory_available_reads_meminfo():
+    """The e2e leg sizes its pinned buffers against MemAvailable: on Linux it
+    is a positive byte count below the total memory."""
+    import bench
+    avail = bench.host_memory_available()
+    if not os.path.exists("/proc/meminfo"):
+        assert avail is None
+        return
+    assert avail is not None and avail > 0
+    with open("/proc/meminfo") as f:
+        total = next(int(l.split()[1]) * 1024 for l in f if l.startswith("MemTotal:"))
+    assert avail <= total
