@@ -39,8 +39,7 @@ METRIC = "ZeRO step params/s at N ranks on 1 GB300; achieved HBM GB/s vs peak"
 METRIC_DDP = "DDP all_reduce(mean) params/s at N ranks on 1 GB300; achieved HBM GB/s vs peak"
 UNIT = "params/s"
 DEFAULT_WORKLOAD = "mixed_1p3b"
-KERNEL_SRCS = [os.path.join(ROOT, "zero_sharded_optimizer_gb300", "csrc", f)
-               for f in ("zero_kernels.cu", "zero_tma.cuh")]
+KERNEL_SRCS = [os.path.join(ROOT, "zero_sharded_optimizer_gb300", "csrc", "zero_kernels.cu")]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 L2_BYTES = 129 * 10 ** 6
 
@@ -607,7 +606,7 @@ def run_gpu(args, wl, rank: int, world: int, local_rank: int) -> dict | None:
     bucketed = wl.bucket_bytes > 0 and not ddp
     launches_per_step = len(opt.bucket_ranges(wl.bucket_bytes)) if bucketed else 1
     if clip:
-        launches_per_step = 2       # norm partials, then the step that adds them
+        launches_per_step = 3       # norm partials, norm total, the clipped step
     if stage3:
         launches_per_step += 1      # the gather after the owner-only step
     stream = torch.cuda.current_stream()
@@ -816,13 +815,11 @@ def run_gpu(args, wl, rank: int, world: int, local_rank: int) -> dict | None:
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs, copy "
                                     f"bandwidth)" if peak_kind == "measured" else "fallback",
                      "algorithmic_bytes_per_launch": step_bytes // per,
-                     "kernel": ("allreduce_mean_tma_kernel" if wl.N <= 8 else
-                                "allreduce_mean_kernel") if ddp else
-                               ("grad_norm_partials_kernel + zero_step_tma_kernel adding "
-                                "the partials (whole clipped step)") if clip else
-                               ("zero_step_tma_kernel (owner-only) + gather_kernel "
-                                "(whole stage-3 step)") if stage3 else
-                               ("zero_step_tma_kernel" if 2 <= wl.N <= 8 else "zero_step_kernel"),
+                     "kernel": "allreduce_mean_kernel" if ddp else
+                               ("grad_norm_partials_kernel + grad_norm_total_kernel + "
+                                "zero_step_kernel (whole clipped step, chained launches)") if clip else
+                               ("zero_step_kernel (owner-only) + gather_kernel "
+                                "(whole stage-3 step)") if stage3 else "zero_step_kernel",
                      "kernel_ms": kernel_ms / per,
                      "step_ms_p10_median_p90": dist_ms,
                      **({"stage3_split": split} if split else {})},

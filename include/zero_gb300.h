@@ -234,11 +234,11 @@ typedef struct zero_step_opts {
    * >= zero_grad_norm_scratch_count(n) doubles, caller-owned, overwritten,
    * 8-byte aligned and disjoint from every other buffer of the call. Given,
    * the call computes the squared norm of the whole gradient [0, n) itself,
-   * exactly as zero_grad_norm_sq on the same buffers (bit for bit), writes it
-   * to *norm_sq and clips with it: the partial sums in one launch, then the
-   * step, which starts while that launch finishes, adds the partials in the
-   * same fixed order while its first loads are in flight, and so saves the
-   * separate total launch. The host-input step requires it when clipping. */
+   * as zero_grad_norm_sq does on the same buffers (the same launches, so the
+   * same bits), writes it to *norm_sq and clips with it; the step is chained
+   * to the norm's launches as a programmatic dependent (it starts while they
+   * finish and waits for the norm before reading it). The host-input step
+   * requires it when clipping. */
   double *norm_scratch;
   int64_t norm_scratch_count;
 } zero_step_opts_t;
@@ -498,26 +498,6 @@ int zero_memory_breakdown(int64_t n, int32_t N, int32_t stage, int32_t precision
  * 0 to n; NULL: the np.array_split shards), e.g. whole-tensor shards. */
 int zero_memory_breakdown_ex(int64_t n, int32_t N, int32_t stage, int32_t precision,
                              int32_t rank, const int64_t *bounds, uint64_t out[3]);
-
-/* ---------------------------------------------------------------- health -- */
-
-/* Status bits a kernel may set on the device.
- * ZERO_STATUS_WAIT_TIMEOUT: a bounded wait of a bulk-copy pipeline on its own
- * copies ran out (after 2 s by default); that kernel stopped early, so the
- * outputs of the call that launched it are incomplete. */
-enum { ZERO_STATUS_WAIT_TIMEOUT = 1 };
-
-/* Read the sticky device status word of the current device into *status (0:
- * nothing happened) and clear it when `clear` is non-zero. Synchronizes the
- * current device. Errors: EINVAL (NULL), ECUDA. */
-int zero_device_status(uint32_t *status, int32_t clear);
-
-/* Test hook: bound of every device-side wait of later launches, in
- * nanoseconds (0 restores the default of 2 s). A tiny bound makes the
- * pipeline give up on its first wait, which exercises the timeout path
- * (status bit, bounded drain of its own copies, early return) without any
- * fault. Process-wide; not for production use. Always returns ZERO_OK. */
-int zero_debug_set_wait_timeout_ns(uint64_t ns);
 
 /* ---------------------------------------------------------------- errors -- */
 

@@ -64,7 +64,7 @@ def flat(states, key):
 # device buffer of the small parity tests sits inside a larger allocation whose
 # other elements hold a sentinel bit pattern (a NaN in both float formats, so a
 # kernel that read it as data would also show). A kernel that writes past
-# either end of its range -- a bulk store rounded up to 16 bytes, a tile past
+# either end of its range -- a vector store rounded up to 16 bytes, a unit past
 # `hi`, a head written before a non-zero offset -- changes a sentinel, and
 # check_guards() reports it. Buffers register themselves; the conftest checks
 # and forgets them after every test.

@@ -4,7 +4,7 @@ every replica, and no call may write outside its buffers.
 
 compute-sanitizer is not available on the GPU pool, so these checks stand in
 for it: the ranges are ragged (odd ends, off the 16-byte vector grid and the
-bulk-copy tile grid, across shard edges), the buffers sit between sentinel
+2048-element grid, across shard edges), the buffers sit between sentinel
 guard regions (parity_util.GUARD, checked after every call here and by the
 conftest after every test), and the values inside the range must equal those
 of the same step over the whole vector. The update is elementwise ("Data

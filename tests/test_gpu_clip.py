@@ -136,12 +136,13 @@ def test_optimizer_clipping_host_and_device_agree(abi, cuda):
                                       (500_009, 4, "sgd"), (50_011, 4, "mixed_phase"),
                                       (4099, 3, "adamw"), (2000, 4, "empty_range")])
 def test_step_computing_its_own_norm_equals_two_calls(abi, cuda, prec, n, N, kind):
-    """zero_step_ex / zero_step_sgd given norm_scratch: the norm's partial sums
-    in one launch, the step adding them itself. Bitwise the same as
-    zero_grad_norm_sq followed by the step that reads the norm, in every
-    kernel shape (lock-step and warp-specialised bulk-copy loops, register
-    streaming for N = 1, N > 8 and mixed 16-byte phases), the norm scalar
-    included; for an empty range only the norm is written."""
+    """zero_step_ex / zero_step_sgd given norm_scratch: the call forms the norm
+    itself (its partial sums, their total) and the step follows as a
+    programmatic dependent that waits for the norm. Bitwise the same as
+    zero_grad_norm_sq followed by the step that reads the norm, over rank
+    counts 1-13, both precisions, owner-only, SGD and mixed 16-byte phases
+    (the persistent grid), the norm scalar included; for an empty range only
+    the norm is written."""
     from test_gpu_sgd import SgdCase
     kw = {}
     if kind == "mixed_phase":

@@ -39,7 +39,6 @@ ZERO_ECUDA = -3
 ZERO_ETIMEDOUT = -4
 ZERO_ENOMEM = -5
 ZERO_MAX_RANKS = 64
-ZERO_STATUS_WAIT_TIMEOUT = 1
 
 _i64 = ctypes.c_int64
 _i32 = ctypes.c_int32
@@ -89,8 +88,6 @@ _SIGNATURES = {
     "zero_gather": (ctypes.c_int, [_P(_vp), _vp, _i64, _i64, _vp]),
     "zero_step_sgd": (ctypes.c_int, [_P(_vp), _P(_vp), _vp, _vp, _vp]),
     "zero_grad_norm_sq_noalloc": (ctypes.c_int, [_P(_vp), _i64, _i32, _i32, _vp, _vp]),
-    "zero_device_status": (ctypes.c_int, [_P(ctypes.c_uint32), _i32]),
-    "zero_debug_set_wait_timeout_ns": (ctypes.c_int, [_u64]),
     "zero_strerror": (ctypes.c_char_p, [ctypes.c_int]),
     "zero_last_error": (ctypes.c_char_p, []),
 }
@@ -560,16 +557,6 @@ class DdpHost:
             self.close()
         except Exception:
             pass
-
-
-def zero_device_status(clear: bool = False) -> int:
-    out = ctypes.c_uint32()
-    _check(_lib.zero_device_status(ctypes.byref(out), 1 if clear else 0), "zero_device_status")
-    return out.value
-
-
-def zero_debug_set_wait_timeout_ns(ns: int) -> None:
-    _check(_lib.zero_debug_set_wait_timeout_ns(ns), "zero_debug_set_wait_timeout_ns")
 
 
 def zero_last_error() -> str:

@@ -20,8 +20,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libzero_gb300.so")
 
 SOURCES = ["zero_kernels.cu", "zero_host.cpp"]
-HEADERS = [os.path.join(CSRC, "zero_internal.h"), os.path.join(CSRC, "zero_tma.cuh"),
-           os.path.join(INCLUDE, "zero_gb300.h")]
+HEADERS = [os.path.join(CSRC, "zero_internal.h"), os.path.join(INCLUDE, "zero_gb300.h")]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-ffp-contract=off",

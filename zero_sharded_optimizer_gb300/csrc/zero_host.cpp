@@ -6,7 +6,6 @@
 // separately rounded double operations.
 
 #include <algorithm>
-#include <atomic>
 #include <chrono>
 #include <cmath>
 #include <cstdarg>
@@ -45,10 +44,6 @@ struct zero_states {
 namespace {
 
 thread_local char g_last_error[512] = "";
-
-// Bound of every device-side wait on a bulk copy, in nanoseconds.
-constexpr uint64_t kDefaultWaitNs = 2000000000ull;
-std::atomic<uint64_t> g_wait_ns{kDefaultWaitNs};
 
 int fail(int code, const char* fmt, ...) {
   va_list ap;
@@ -150,7 +145,6 @@ int prepare_step(void* const* params, const void* const* grads, const zero_state
   std::memset(a, 0, sizeof(*a));
   a->N = N;
   a->fN = float(N);
-  a->wait_ns = g_wait_ns.load(std::memory_order_relaxed);
   a->norm_sq = nullptr;  // no clipping
   a->gscale = 1.0;       // mean gradient used as is
   a->max_norm = 0.0;
@@ -210,6 +204,8 @@ int launch_range(zk::StepArgs& a, zero_states* st, bool vector_ok, int phase, in
   ++st->launches;
   const bool mixed = st->precision == ZERO_BF16_MIXED;
   a.sp = make_split(lo, hi, vector_ok, phase, mixed ? 8 : 4);
+  // gscale * 1 rounded to float once, as the device forms it when clipping
+  a.gm = float(a.gscale);
   cudaError_t e = zk::launch_step(a, mixed, opt, s);
   if (e != cudaSuccess) return cuda_fail(e, "zero_step kernel launch");
   return ZERO_OK;
@@ -320,18 +316,6 @@ const char* zero_strerror(int code) {
 
 const char* zero_last_error(void) { return g_last_error; }
 
-int zero_device_status(uint32_t* status, int32_t clear) {
-  if (!status) return fail(ZERO_EINVAL, "status is NULL");
-  cudaError_t e = zk::read_device_status(status, clear != 0);
-  if (e != cudaSuccess) return cuda_fail(e, "reading the device status");
-  return ZERO_OK;
-}
-
-int zero_debug_set_wait_timeout_ns(uint64_t ns) {
-  g_wait_ns.store(ns == 0 ? kDefaultWaitNs : ns, std::memory_order_relaxed);
-  return ZERO_OK;
-}
-
 int zero_shard_bounds(int64_t n, int32_t N, int64_t* bounds) {
   if (n < 0) return fail(ZERO_EINVAL, "n=%lld must be >= 0", (long long)n);
   if (N < 1) return fail(ZERO_EINVAL, "N=%d must be >= 1", N);
@@ -405,12 +389,11 @@ int breakdown(int64_t n, int32_t stage, int32_t precision, uint64_t s, uint64_t 
   return ZERO_OK;
 }
 
-// The multiplier of the mean gradient and, when max_grad_norm > 0, clipping:
-// with the squared norm read from norm_sq, or (norm_scratch given) formed by
-// the call itself -- then norm_partials marks it, the caller runs the norm
-// pass into norm_scratch, and norm_sq receives the total.
+// The multiplier of the mean gradient and, when max_grad_norm > 0, clipping
+// with the squared norm at norm_sq (read on the device; with norm_scratch the
+// call writes it there first).
 int fill_scale_clip(double grad_scale, double max_grad_norm, const double* norm_sq,
-                    double* norm_scratch, zk::StepArgs* a) {
+                    zk::StepArgs* a) {
   if (!std::isfinite(grad_scale) || !(grad_scale > 0.0))
     return fail(ZERO_EINVAL, "grad_scale must be finite and > 0");
   a->gscale = grad_scale;
@@ -418,12 +401,7 @@ int fill_scale_clip(double grad_scale, double max_grad_norm, const double* norm_
     if (!std::isfinite(max_grad_norm)) return fail(ZERO_EINVAL, "max_grad_norm must be finite");
     if (!norm_sq) return fail(ZERO_EINVAL, "clipping needs the squared norm (norm_sq)");
     a->max_norm = max_grad_norm;
-    if (norm_scratch) {
-      a->norm_partials = norm_scratch;
-      a->norm_out = const_cast<double*>(norm_sq);
-    } else {
-      a->norm_sq = norm_sq;
-    }
+    a->norm_sq = norm_sq;
   }
   return ZERO_OK;
 }
@@ -432,8 +410,7 @@ int fill_scale_clip(double grad_scale, double max_grad_norm, const double* norm_
 int fill_adamw(const zero_step_opts_t* o, zk::StepArgs* a) {
   if (int e = adam_consts(o->t, o->lr, o->beta1, o->beta2, o->eps, o->weight_decay, &a->c))
     return e;
-  if (int e = fill_scale_clip(o->grad_scale, o->max_grad_norm, o->norm_sq, o->norm_scratch, a))
-    return e;
+  if (int e = fill_scale_clip(o->grad_scale, o->max_grad_norm, o->norm_sq, a)) return e;
   a->owner_only = o->owner_only != 0;
   return ZERO_OK;
 }
@@ -461,8 +438,7 @@ int fill_sgd(const zero_sgd_opts_t* o, zk::StepArgs* a) {
   a->sgd.wd_on = o->weight_decay != 0.0;
   a->sgd.first = o->t == 1;
   a->sgd.nesterov = o->nesterov != 0;
-  if (int e = fill_scale_clip(o->grad_scale, o->max_grad_norm, o->norm_sq, o->norm_scratch, a))
-    return e;
+  if (int e = fill_scale_clip(o->grad_scale, o->max_grad_norm, o->norm_sq, a)) return e;
   a->owner_only = o->owner_only != 0;
   return ZERO_OK;
 }
@@ -475,27 +451,21 @@ int check_range(int64_t lo, int64_t hi, int64_t n) {
 }
 
 // The step of zero_step_ex / zero_step_sgd over [lo, hi), after the options
-// are filled in. When the call forms the norm itself (a.norm_partials), the
-// partial sums of the whole gradient go into the caller's scratch first, and
-// the step follows as a programmatic dependent that adds them in its prologue
-// (for an empty range a separate total launch writes norm_sq instead).
+// are filled in. With clipping and norm_scratch the call forms the norm
+// itself: the partial sums of the whole gradient into the scratch, their
+// fixed-order total into norm_sq (the two launches of zero_grad_norm_sq), then
+// the step, each launch a programmatic dependent of the one before.
 int run_step(zk::StepArgs& a, zero_states* st, const void* const* grads, bool vec, int phase,
-             int64_t lo, int64_t hi, int64_t scratch_count, const std::vector<Range>& bufs,
-             cudaStream_t s, zk::Opt opt) {
-  if (a.norm_partials) {
+             int64_t lo, int64_t hi, double* norm_scratch, int64_t scratch_count,
+             const std::vector<Range>& bufs, cudaStream_t s, zk::Opt opt) {
+  if (a.norm_sq && norm_scratch) {
     zk::NormArgs na;
     if (int e = prepare_norm(grads, st->n, st->N, st->precision, &na)) return e;
-    if (int e = attach_norm_buffers(const_cast<double*>(a.norm_partials), scratch_count,
-                                    a.norm_out, bufs, &na))
+    if (int e = attach_norm_buffers(norm_scratch, scratch_count, const_cast<double*>(a.norm_sq),
+                                    bufs, &na))
       return e;
-    const bool bf16 = st->precision == ZERO_BF16_MIXED;
-    cudaError_t ce = zk::launch_norm_partials(na, bf16, s);
+    cudaError_t ce = zk::launch_norm(na, st->precision == ZERO_BF16_MIXED, s);
     if (ce != cudaSuccess) return cuda_fail(ce, "gradient norm kernel launch");
-    if (hi <= lo) {
-      ce = zk::launch_norm_total(na, s);
-      return ce == cudaSuccess ? ZERO_OK : cuda_fail(ce, "gradient norm kernel launch");
-    }
-    a.npartials = na.nchunks + 1;
     a.dependent = 1;
   }
   return launch_range(a, st, vec, phase, lo, hi, s, opt);
@@ -664,7 +634,7 @@ int zero_step_ex(void* const* params, const void* const* grads, zero_states_t* s
   const int64_t lo = o->lo, hi = o->hi < 0 ? st->n : o->hi;
   if (int e = check_range(lo, hi, st->n)) return e;
   if (int e = fill_adamw(o, &a)) return e;
-  return run_step(a, st, grads, vec, phase, lo, hi, o->norm_scratch_count, bufs,
+  return run_step(a, st, grads, vec, phase, lo, hi, o->norm_scratch, o->norm_scratch_count, bufs,
                   reinterpret_cast<cudaStream_t>(stream), zk::Opt::AdamW);
 }
 
@@ -719,7 +689,7 @@ int zero_step_sgd(void* const* params, const void* const* grads, zero_states_t* 
   const int64_t lo = o->lo, hi = o->hi < 0 ? st->n : o->hi;
   if (int e = check_range(lo, hi, st->n)) return e;
   if (int e = fill_sgd(o, &a)) return e;
-  return run_step(a, st, grads, vec, phase, lo, hi, o->norm_scratch_count, bufs,
+  return run_step(a, st, grads, vec, phase, lo, hi, o->norm_scratch, o->norm_scratch_count, bufs,
                   reinterpret_cast<cudaStream_t>(stream), opt);
 }
 
@@ -923,9 +893,6 @@ int zero_step_from_host_ex(void* const* params, const void* const* host_grads,
     // the total from norm_sq (one total launch, not one per chunk's step)
     if (int e = prepare_norm(staging, n, N, st->precision, &na)) return e;
     if (int e = attach_norm_buffers(norm_scratch, norm_count, norm_out, bufs, &na)) return e;
-    a.norm_partials = nullptr;
-    a.norm_out = nullptr;
-    a.norm_sq = norm_out;
   }
   const int64_t count = (n + B - 1) / B;
   const size_t need = size_t(2 * count + 2);
@@ -1050,7 +1017,6 @@ int ddp_allreduce_mean(void* const* grads, int64_t n, int32_t N, int32_t precisi
   std::memset(&a, 0, sizeof(a));
   a.N = N;
   a.fN = float(N);
-  a.wait_ns = g_wait_ns.load(std::memory_order_relaxed);
   int ph = -2;
   bool same = true;
   std::vector<Range> rs;

@@ -60,26 +60,25 @@ struct StepArgs {
   float fN;                      // (float)N
   AdamConsts c;                  // AdamW steps
   SgdConsts sgd;                 // momentum-SGD steps (the buffer is m)
-  uint64_t wait_ns;              // bound of every wait on a bulk copy (TMA kernels)
   // Multiplier of the mean gradient: gscale, times the clip coefficient
   // min(1, max_norm / (gscale * sqrt(*norm_sq) + 1e-6)) when norm_sq is set
   // (formed on the device, in double, rounded to float once).
-  const double* norm_sq;         // device scalar, or NULL (no clipping)
-  // Clipping with the norm's fixed-order total formed in this kernel: the
-  // partial sums of a norm pass launched just before (npartials of them, the
-  // kernel waits for that pass first); the total is written to norm_out by
-  // block 0. NULL: the multiplier comes from norm_sq (or there is none).
-  const double* norm_partials;
-  int64_t npartials;
-  double* norm_out;
+  // Device scalar, or NULL (no clipping). When the launch is a programmatic
+  // dependent, the kernel waits for the kernel before it (the norm's total)
+  // before reading it.
+  const double* norm_sq;
   double gscale;
   double max_norm;
+  // The multiplier when there is no clipping (norm_sq NULL): float(gscale),
+  // formed on the host -- the device's double pipe is slow, and a one-pass
+  // grid has millions of threads.
+  float gm;
   // Stage 3: write the new parameters only into the owner's replica, over the
   // owner's shard; the other replicas' elements are left untouched.
   int32_t owner_only;
-  // Launch as a programmatic dependent of the previous kernel on the stream,
-  // which must touch indices disjoint from this range (a later bucket of the
-  // same step). Honoured by the bulk-copy kernels.
+  // Launch as a programmatic dependent of the previous kernel on the stream:
+  // a later bucket of the same step (disjoint indices), or a clipped step
+  // after the kernel that writes norm_sq.
   int32_t dependent;
 };
 
@@ -110,7 +109,6 @@ struct AllreduceArgs {
   Split sp;
   int32_t N;
   float fN;
-  uint64_t wait_ns;
 };
 
 // Stage-3 all-gather: copy each shard [bounds[r], bounds[r+1]) of replica r
@@ -143,7 +141,9 @@ cudaError_t launch_gather(const GatherArgs& a, bool bf16, cudaStream_t s);
 // Partial sums then their fixed-order total (two launches, deterministic).
 cudaError_t launch_norm(const NormArgs& a, bool bf16, cudaStream_t s);
 // The partials [a.c_begin, a.c_end) only (one launch; its blocks let a
-// programmatic dependent start early), and the fixed-order total only.
+// programmatic dependent start early), and the fixed-order total only (one
+// block, launched as a programmatic dependent of the kernel before it, which
+// it waits for before reading the partials; it lets its own dependent start).
 cudaError_t launch_norm_partials(const NormArgs& a, bool bf16, cudaStream_t s);
 cudaError_t launch_norm_total(const NormArgs& a, cudaStream_t s);
 
@@ -153,8 +153,5 @@ cudaError_t launch_norm_total(const NormArgs& a, cudaStream_t s);
 constexpr int64_t kNoAllocPartials = 65536;
 cudaError_t noalloc_partials(double** ptr);
 
-// Sticky device status word (bit 0: a bounded wait on a bulk copy ran out).
-// Reading synchronizes the current device.
-cudaError_t read_device_status(uint32_t* status, bool clear);
 
 }  // namespace zk
