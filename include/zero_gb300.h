@@ -237,8 +237,10 @@ typedef struct zero_step_opts {
    * as zero_grad_norm_sq does on the same buffers (the same launches, so the
    * same bits), writes it to *norm_sq and clips with it; the step is chained
    * to the norm's launches as a programmatic dependent (it starts while they
-   * finish and waits for the norm before reading it). The host-input step
-   * requires it when clipping. */
+   * finish and waits for the norm before reading it). The norm's last launch
+   * also forms the clip multiplier once, into the scratch's last slot, where
+   * the step reads it (the same value the step would form from *norm_sq). The
+   * host-input step requires it when clipping. */
   double *norm_scratch;
   int64_t norm_scratch_count;
 } zero_step_opts_t;

@@ -133,7 +133,8 @@ def test_optimizer_clipping_host_and_device_agree(abi, cuda):
 @pytest.mark.parametrize("n,N,kind", [(1_000_003, 4, "adamw"), (1_000_003, 8, "adamw"),
                                       (300_007, 2, "adamw"), (300_007, 3, "owner_only"),
                                       (300_007, 1, "adamw"), (65_537, 13, "adamw"),
-                                      (500_009, 4, "sgd"), (50_011, 4, "mixed_phase"),
+                                      (500_009, 4, "sgd"), (500_009, 1, "sgd"),
+                                      (50_011, 4, "mixed_phase"),
                                       (4099, 3, "adamw"), (2000, 4, "empty_range")])
 def test_step_computing_its_own_norm_equals_two_calls(abi, cuda, prec, n, N, kind):
     """zero_step_ex / zero_step_sgd given norm_scratch: the call forms the norm

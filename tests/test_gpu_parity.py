@@ -307,6 +307,43 @@ def test_bucketed_equals_monolithic(abi, cuda, prec):
         assert torch.equal(x, y)
 
 
+@pytest.mark.parametrize("prec", [oracle.FP32, oracle.BF16_MIXED])
+def test_bucket_chain_completes_in_order(abi, cuda, prec):
+    """Bucket launches are programmatic dependents of the one before: a
+    bucket's blocks may start while the previous bucket drains, but every
+    bucket completes in stream order. Over 1,000+ tiny buckets (down to one
+    block each, ragged edges), a copy of every output queued on the side
+    stream right after the call -- and the done event -- must see all the
+    buckets: bitwise equal to the monolithic step."""
+    n, N = 100_003, 4
+    bucket_bytes = 390 if prec == oracle.FP32 else 194   # 97 elements: odd, off the vector grid
+    a = Case(abi, cuda, n, N, prec, seed=14)
+    b = Case(abi, cuda, n, N, prec, seed=14)
+    count = abi.zero_bucket_count(n, prec, bucket_bytes)
+    assert count > 1000
+    side = torch.cuda.Stream()
+    for t in (1, 2):
+        a.new_grads()
+        for r in range(N):
+            b.grads[r].copy_(a.grads[r])
+        a.t = b.t = t
+        a.gpu_step()
+        side.wait_stream(torch.cuda.current_stream())
+        done = torch.cuda.Event()
+        abi.zero_step_bucketed(b.reps, b.grads, b.st, t, HP["lr"], HP["beta1"], HP["beta2"],
+                               HP["eps"], HP["weight_decay"], bucket_bytes, None, side, done)
+        with torch.cuda.stream(side):  # queued right behind the last bucket
+            snap = [x.clone() for x in [b.m, b.v] + list(b.reps)]
+        after_done = torch.cuda.Stream()
+        after_done.wait_event(done)
+        with torch.cuda.stream(after_done):
+            snap_done = [x.clone() for x in [b.m, b.v] + list(b.reps)]
+        torch.cuda.synchronize()
+        want = [a.m, a.v] + list(a.reps)
+        for x, y, z in zip(snap, snap_done, want):
+            assert torch.equal(x, z) and torch.equal(y, z)
+
+
 def test_bucketed_deadline_reports_timeout(abi, cuda):
     """A producer that is late: the host deadline passes, the call returns
     ZERO_ETIMEDOUT, and the queued work still completes correctly."""

@@ -109,8 +109,11 @@ class SgdCase:
             assert np.array_equal(got, self.o_reps[r]), f"replica {r} not bit-exact"
 
 
-GRID = [(1, 1), (7, 3), (33, 4), (4099, 5), (100_003, 2), (100_003, 4), (100_003, 8),
-        (65_537, 13), (300_007, 6), (1_000_003, 8)]
+# One rank in fp32 takes two units per thread: 6151 elements leave 1537
+# units (one past three blocks' 512) and a 3-element tail; 100_003 and
+# 1_000_003 end inside a block's second units.
+GRID = [(1, 1), (6151, 1), (100_003, 1), (1_000_003, 1), (7, 3), (33, 4), (4099, 5),
+        (100_003, 2), (100_003, 4), (100_003, 8), (65_537, 13), (300_007, 6), (1_000_003, 8)]
 
 
 @pytest.mark.parametrize("prec", [oracle.FP32, oracle.BF16_MIXED])
@@ -170,8 +173,9 @@ def test_sgd_whole_tensor_shards(abi, cuda, prec):
 
 
 @pytest.mark.parametrize("prec", [oracle.FP32, oracle.BF16_MIXED])
-def test_sgd_clipped_and_scaled(abi, cuda, prec):
-    n, N = 200_003, 4
+@pytest.mark.parametrize("N", [4, 1])
+def test_sgd_clipped_and_scaled(abi, cuda, prec, N):
+    n = 200_003
     c = SgdCase(abi, cuda, n, N, prec, "damped_wd", seed=26)
     norm = torch.empty(1, dtype=torch.float64, device=cuda)
     count = abi.zero_grad_norm_scratch_count(n, prec)

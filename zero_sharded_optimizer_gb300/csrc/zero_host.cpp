@@ -277,16 +277,27 @@ int attach_norm_buffers(double* scratch, int64_t scratch_count, double* norm_sq,
   if (!scratch || !norm_sq) return fail(ZERO_EINVAL, "norm scratch or norm_sq is NULL");
   if (reinterpret_cast<uintptr_t>(scratch) % 8 || reinterpret_cast<uintptr_t>(norm_sq) % 8)
     return fail(ZERO_EALIGN, "norm scratch and norm_sq must be 8-byte aligned");
-  if (scratch_count < a->nchunks + 1)
+  const int64_t need = a->nchunks + zk::kNormScratchExtra;
+  if (scratch_count < need)
     return fail(ZERO_EINVAL, "norm scratch holds %lld doubles, %lld needed",
-                (long long)scratch_count, (long long)(a->nchunks + 1));
-  others.push_back({uintptr_t(scratch), uintptr_t(scratch) + uintptr_t(a->nchunks + 1) * 8,
+                (long long)scratch_count, (long long)need);
+  others.push_back({uintptr_t(scratch), uintptr_t(scratch) + uintptr_t(need) * 8,
                     "the norm scratch"});
   others.push_back({uintptr_t(norm_sq), uintptr_t(norm_sq) + 8, "norm_sq"});
   if (int e = check_disjoint(others)) return e;
   a->partials = scratch;
   a->out = norm_sq;
   return ZERO_OK;
+}
+
+// A clipped step chained to the norm of `na` (after attach_norm_buffers): the
+// norm's total kernel forms the step's multiplier into the scratch slot after
+// the partials, and the step reads it there.
+void chain_multiplier(zk::NormArgs* na, zk::StepArgs* a) {
+  na->gm_out = reinterpret_cast<float*>(na->partials + na->nchunks + 1);
+  na->gscale = a->gscale;
+  na->max_norm = a->max_norm;
+  a->gm_dev = na->gm_out;
 }
 
 // The gradients' buffer ranges of a norm pass.
@@ -464,6 +475,7 @@ int run_step(zk::StepArgs& a, zero_states* st, const void* const* grads, bool ve
     if (int e = attach_norm_buffers(norm_scratch, scratch_count, const_cast<double*>(a.norm_sq),
                                     bufs, &na))
       return e;
+    chain_multiplier(&na, &a);
     cudaError_t ce = zk::launch_norm(na, st->precision == ZERO_BF16_MIXED, s);
     if (ce != cudaSuccess) return cuda_fail(ce, "gradient norm kernel launch");
     a.dependent = 1;
@@ -698,7 +710,7 @@ int zero_grad_norm_scratch_count(int64_t n, int32_t precision, int64_t* count) {
   if (n < 0) return fail(ZERO_EINVAL, "n=%lld must be >= 0", (long long)n);
   if (precision != ZERO_FP32 && precision != ZERO_BF16_MIXED)
     return fail(ZERO_EINVAL, "gradient precision must be FP32 or BF16_MIXED");
-  *count = (n + zk::kNormChunk - 1) / zk::kNormChunk + 1;
+  *count = (n + zk::kNormChunk - 1) / zk::kNormChunk + zk::kNormScratchExtra;
   return ZERO_OK;
 }
 
@@ -893,6 +905,7 @@ int zero_step_from_host_ex(void* const* params, const void* const* host_grads,
     // the total from norm_sq (one total launch, not one per chunk's step)
     if (int e = prepare_norm(staging, n, N, st->precision, &na)) return e;
     if (int e = attach_norm_buffers(norm_scratch, norm_count, norm_out, bufs, &na)) return e;
+    chain_multiplier(&na, &a);
   }
   const int64_t count = (n + B - 1) / B;
   const size_t need = size_t(2 * count + 2);

@@ -80,6 +80,10 @@ struct StepArgs {
   // a later bucket of the same step (disjoint indices), or a clipped step
   // after the kernel that writes norm_sq.
   int32_t dependent;
+  // A clipped step whose call formed the norm itself: the multiplier, formed
+  // from norm_sq by the norm's total kernel (NormArgs::gm_out), read instead of
+  // forming it again in every block. NULL otherwise.
+  const float* gm_dev;
 };
 
 // Squared global norm of the mean gradient, as fixed-size partial sums.
@@ -102,7 +106,17 @@ struct NormArgs {
   int64_t c_begin, c_end;
   double* partials;  // nchunks + 1 doubles
   double* out;       // device scalar receiving the sum of the partials
+  // A clipped step chained to this norm: the total kernel also forms the
+  // step's gradient multiplier from the total (gscale, max_norm as in
+  // StepArgs) into *gm_out, the float slot after the partials in the caller's
+  // scratch. NULL: the norm alone.
+  float* gm_out;
+  double gscale, max_norm;
 };
+
+// The caller's norm scratch: the nchunks + 1 partial sums, then one double
+// slot holding the chained step's multiplier (a float in its first 4 bytes).
+constexpr int64_t kNormScratchExtra = 2;
 
 struct AllreduceArgs {
   void* grads[kMaxRanks];

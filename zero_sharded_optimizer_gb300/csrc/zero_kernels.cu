@@ -190,33 +190,28 @@ __device__ __forceinline__ int ranks(const StepArgs& P) {
   return NR > 0 ? NR : P.N;
 }
 
-// Multiplier of the mean gradient: the accumulation factor gscale, times the
-// clip coefficient min(1, max_norm / (gscale * sqrt(norm_sq) + 1e-6)) when
-// clipping. Formed in double with separately rounded operations (no
-// contraction), rounded to float once; 1.0f when neither is set.
-__device__ __forceinline__ float multiplier_of(const StepArgs& P, bool clip, double norm_sq) {
-  double c = 1.0;
-  if (clip) {
-    const double denom = __dadd_rn(__dmul_rn(P.gscale, __dsqrt_rn(norm_sq)), 1e-6);
-    c = fmin(1.0, __ddiv_rn(P.max_norm, denom));
-  }
-  return __double2float_rn(__dmul_rn(P.gscale, c));
+// Multiplier of the mean gradient when clipping: the accumulation factor
+// gscale times the clip coefficient
+// min(1, max_norm / (gscale * sqrt(norm_sq) + 1e-6)). Formed in double with
+// separately rounded operations (no contraction), rounded to float once.
+__device__ __forceinline__ float clip_multiplier(double gscale, double max_norm, double norm_sq) {
+  const double denom = __dadd_rn(__dmul_rn(gscale, __dsqrt_rn(norm_sq)), 1e-6);
+  const double c = fmin(1.0, __ddiv_rn(max_norm, denom));
+  return __double2float_rn(__dmul_rn(gscale, c));
 }
 
-// The multiplier: from the squared norm in memory when clipping, else the
-// host's float(gscale) (the same value: gscale * 1 rounded to float once).
-__device__ __forceinline__ float grad_multiplier(const StepArgs& P) {
-  if (!P.norm_sq) return P.gm;
-  return multiplier_of(P, true, *P.norm_sq);
-}
-
-// grad_multiplier for a whole block: with clipping, thread 0 forms it in
-// double and the block shares it (one double square root and divide per
-// block, not per thread). Every thread of the block must call it.
+// The multiplier of a block's threads. Without clipping: the host's
+// float(gscale) (the same value: gscale * 1 rounded to float once). A clipped
+// step chained to its norm: the multiplier the norm's total kernel formed,
+// read from memory by every thread (no barrier, so the unit loads are not held
+// behind it). Otherwise thread 0 forms it from the squared norm in double and
+// the block shares it: the double pipe is slow, so once per block, not per
+// thread. Every thread of the block must call it.
 __device__ __forceinline__ float block_grad_multiplier(const StepArgs& P) {
   if (!P.norm_sq) return P.gm;
+  if (P.gm_dev) return *P.gm_dev;
   __shared__ float shared_gm;
-  if (threadIdx.x == 0) shared_gm = multiplier_of(P, true, *P.norm_sq);
+  if (threadIdx.x == 0) shared_gm = clip_multiplier(P.gscale, P.max_norm, *P.norm_sq);
   __syncthreads();
   return shared_gm;
 }
@@ -388,6 +383,45 @@ __device__ __forceinline__ void step_vec_fp32(const StepArgs& P, int64_t j, int 
   }
 }
 
+// Units per thread: two for SGD in fp32 with one rank (three loads of a unit
+// are too few bytes in flight per thread), one everywhere else. AdamW with one
+// rank stays at one: two units take 69 registers (3 blocks per SM) and measured
+// 19 % slower, where SGD measured 12 % faster (fp32_25m, N = 1).
+template <int NR, bool MIXED, Opt O>
+constexpr int kUnits = !MIXED && NR == 1 && O != Opt::AdamW ? 2 : 1;
+
+// Two units of an fp32 step with one rank (kUnits): the second blockDim.x
+// units after the first (each warp-wide access still covers 512 contiguous
+// bytes), the loads of both issued before any arithmetic. One rank owns every
+// index, so no unit straddles a shard. u0 < nvec; the second unit exists when
+// u1 < nvec.
+template <Opt O>
+__device__ __forceinline__ void step_vec_fp32_one_rank(const StepArgs& P, int64_t base,
+                                                       int64_t u0, int64_t nvec, float gm) {
+  const int64_t u1 = u0 + blockDim.x;
+  const bool two = u1 < nvec;
+  const int64_t j[2] = {base + u0 * 4, base + u1 * 4};
+  const float* rep = static_cast<const float*>(P.reps[0]);
+  const float* grad = static_cast<const float*>(P.grads[0]);
+  float4 p[2], g[2], st[2][kSA<O>];
+#pragma unroll
+  for (int u = 0; u < 2; ++u) {
+    if (u == 1 && !two) break;
+    p[u] = ld4(rep + j[u]);
+#pragma unroll
+    for (int k = 0; k < kStates<O>; ++k) st[u][k] = ld4(state_ptr(P, k) + j[u]);
+    g[u] = ld4(grad + j[u]);
+  }
+#pragma unroll
+  for (int u = 0; u < 2; ++u) {
+    if (u == 1 && !two) break;
+    update4<1, O>(P, gm, g[u], p[u], st[u]);
+#pragma unroll
+    for (int k = 0; k < kStates<O>; ++k) st4(state_ptr(P, k) + j[u], st[u][k]);
+    st4(static_cast<float*>(P.reps[0]) + j[u], p[u]);
+  }
+}
+
 // ------------------------------------------------------ mixed vector path (V=8)
 
 template <int NR, Opt O>
@@ -464,8 +498,9 @@ __global__ void __launch_bounds__(kThreads) zero_step_kernel(const __grid_consta
   // A later bucket of the same step (disjoint indices) may start now; this
   // kernel still completes only after the one before it (the wait at the end).
   pdl_allow_next();
-  // The squared norm may come from the kernel just before this one (a
-  // clipped step chained to its norm): wait for it before reading.
+  // The squared norm (or the multiplier formed from it) may come from the
+  // kernel just before this one (a clipped step chained to its norm): wait
+  // for it before reading.
   if (P.norm_sq) pdl_wait_previous();
   const float gm = block_grad_multiplier(P);
 
@@ -483,17 +518,24 @@ __global__ void __launch_bounds__(kThreads) zero_step_kernel(const __grid_consta
     }
   }
 
-  // Vector body.
+  // Vector body: one unit per thread, or two (kUnits).
   const int64_t base = sp.lo + sp.head;
-  int owner = 0;
-  for (int64_t u = tid; u < sp.nvec; u += stride) {
-    const int64_t j = base + u * V;
-    if constexpr (MIXED) {
-      if (P.owner_only) owner = advance_owner(P, owner, j);
-      step_vec_mixed<NR, O>(P, j, owner, gm);
-    } else {
-      owner = advance_owner(P, owner, j);
-      step_vec_fp32<NR, O>(P, j, owner, gm);
+  if constexpr (kUnits<NR, MIXED, O> == 2) {
+    const int64_t span = 2 * int64_t(blockDim.x);  // units per block and iteration
+    for (int64_t b0 = int64_t(blockIdx.x) * span; b0 < sp.nvec; b0 += int64_t(gridDim.x) * span)
+      if (b0 + threadIdx.x < sp.nvec)
+        step_vec_fp32_one_rank<O>(P, base, b0 + threadIdx.x, sp.nvec, gm);
+  } else {
+    int owner = 0;
+    for (int64_t u = tid; u < sp.nvec; u += stride) {
+      const int64_t j = base + u * V;
+      if constexpr (MIXED) {
+        if (P.owner_only) owner = advance_owner(P, owner, j);
+        step_vec_mixed<NR, O>(P, j, owner, gm);
+      } else {
+        owner = advance_owner(P, owner, j);
+        step_vec_fp32<NR, O>(P, j, owner, gm);
+      }
     }
   }
   pdl_wait_previous();
@@ -646,7 +688,10 @@ __global__ void __launch_bounds__(kThreads) grad_norm_total_kernel(const __grid_
   pdl_allow_next();
   pdl_wait_previous();
   const double total = fixed_order_total(P.partials, P.nchunks + 1);
-  if (threadIdx.x == 0) *P.out = total;
+  if (threadIdx.x == 0) {
+    *P.out = total;
+    if (P.gm_out) *P.gm_out = clip_multiplier(P.gscale, P.max_norm, total);
+  }
 }
 
 // One element of the DDP mean, in place in every rank's buffer.
@@ -896,13 +941,17 @@ cudaError_t launch_one_pass(K kernel, const A& args, int64_t threads_needed, cud
 
 // The step: register streaming in one pass, as a programmatic dependent of the
 // kernel before it when the caller asks (a later bucket of one step, or a
-// clipped step after its norm). fp32 N = 1 without such a chain keeps a
-// persistent grid-stride grid, measured 2 % faster there.
+// clipped step after its norm). fp32 AdamW with one rank and no such chain
+// keeps a persistent grid-stride grid, measured 2 % faster there; SGD with
+// one rank takes two units per thread (kUnits).
 template <bool MIXED, Opt O>
 cudaError_t launch_step_t(const StepArgs& a, cudaStream_t s) {
-  const int64_t work = a.sp.nvec > a.sp.head + a.sp.tail ? a.sp.nvec : a.sp.head + a.sp.tail;
+  const int64_t nscalar = a.sp.head + a.sp.tail;
+  const bool two = a.N == 1 && kUnits<1, MIXED, O> == 2;
+  const int64_t body = two ? (a.sp.nvec + 1) / 2 : a.sp.nvec;
+  const int64_t work = body > nscalar ? body : nscalar;
   const bool dep = a.dependent != 0;
-  if (a.sp.nvec == 0 || (!MIXED && a.N == 1 && !dep)) {
+  if (a.sp.nvec == 0 || (!MIXED && O == Opt::AdamW && a.N == 1 && !dep)) {
     switch (a.N) {
       case 1: return launch(zero_step_kernel<1, MIXED, O>, a, work, s);
       case 2: return launch(zero_step_kernel<2, MIXED, O>, a, work, s);
