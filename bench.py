@@ -39,7 +39,8 @@ METRIC = "ZeRO step params/s at N ranks on 1 GB300; achieved HBM GB/s vs peak"
 METRIC_DDP = "DDP all_reduce(mean) params/s at N ranks on 1 GB300; achieved HBM GB/s vs peak"
 UNIT = "params/s"
 DEFAULT_WORKLOAD = "mixed_1p3b"
-KERNEL_SRCS = [os.path.join(ROOT, "zero_sharded_optimizer_gb300", "csrc", "zero_kernels.cu")]
+KERNEL_SRCS = [os.path.join(ROOT, "zero_sharded_optimizer_gb300", "csrc", name)
+               for name in ("zero_kernels.cu", "zero_internal.h")]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 L2_BYTES = 129 * 10 ** 6
 
@@ -77,13 +78,39 @@ def load_peaks() -> tuple[float, str]:
         return 6800.0, "fallback"
 
 
+def code_without_comments(text: str) -> str:
+    """C/C++/CUDA source with its // and /* */ comments removed (string and
+    character literals kept as they are) and blank lines dropped."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c in "\"'":  # a literal: copy through its closing quote
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    lines = (line.rstrip() for line in "".join(out).splitlines())
+    return "\n".join(line for line in lines if line) + "\n"
+
+
 def kernel_source_hash() -> str:
-    """sha256[:16] over the kernel sources, in order (ties a traffic record to
-    the code it was measured on)."""
+    """sha256[:16] over the code of the kernel sources (the kernels and the
+    argument structs they are compiled with), in order, comments left out:
+    ties a traffic record to the code it was measured on."""
     h = hashlib.sha256()
     for path in KERNEL_SRCS:
-        with open(path, "rb") as f:
-            h.update(f.read())
+        with open(path, encoding="utf-8") as f:
+            h.update(code_without_comments(f.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -109,6 +109,24 @@ def test_traffic_record_scaled_to_the_mean_launch(monkeypatch, tmp_path):
     assert bench.traffic_per_launch("missing", 100) is None
 
 
+def test_kernel_source_hash_ignores_comments_only(monkeypatch, tmp_path):
+    """The traffic record's source hash covers the code: comments and blank
+    lines may change, code (including inside a string literal) may not."""
+    import bench
+    src = tmp_path / "k.cu"
+    monkeypatch.setattr(bench, "KERNEL_SRCS", [str(src)])
+
+    def h(text):
+        src.write_text(text)
+        return bench.kernel_source_hash()
+
+    base = h('int a = 1;\nconst char* s = "x // y";\n')
+    assert h('// a note\nint a = 1;  /* two\nlines */\n\nconst char* s = "x // y"; // z\n') == base
+    assert h('int a = 2;\nconst char* s = "x // y";\n') != base
+    assert h('int a = 1;\nconst char* s = "x // w";\n') != base
+    assert bench.code_without_comments("char c = '\"'; // q\n") == "char c = '\"';\n"
+
+
 def test_committed_traffic_records_cover_the_bench_workloads():
     import json
     import bench

@@ -21,8 +21,9 @@
 // launched in waves, each block exiting after its stretch, so the blocks that
 // run at one time work on one contiguous window of memory. This measured 3-6 %
 // faster than a persistent bulk-copy (TMA) pipeline through shared memory and
-// than a persistent grid-stride grid of the same kernel; fp32 N = 1 alone keeps
-// the grid-stride grid. The stage-3 gather and the DDP mean are register
+// than a persistent grid-stride grid of the same kernel; fp32 AdamW with one
+// rank alone keeps the grid-stride grid, and fp32 SGD with one rank takes two
+// units per thread. The stage-3 gather and the DDP mean are register
 // streaming in one pass too. Bucket launches of one step are programmatic
 // dependents of the one before (their ramp and tail overlap); every kernel
 // still completes in stream order. No kernel waits on another block or on a
