@@ -508,6 +508,14 @@ const char *zero_strerror(int code);
 /* The calling thread's most recent error message ("" if none). */
 const char *zero_last_error(void);
 
+/* Failure injection for tests of the callers' error paths: the next `count`
+ * handle allocations made by the calling thread (zero_init_states,
+ * zero_init_states_ex, zero_ddp_host_create) fail with ZERO_ENOMEM, as if the
+ * host allocator had returned NULL; nothing is queued and *out stays NULL.
+ * count <= 0 clears a pending injection. Other threads are unaffected.
+ * Returns ZERO_OK. */
+int zero_debug_fail_host_allocs(int32_t count);
+
 #ifdef __cplusplus
 }
 #endif

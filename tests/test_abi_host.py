@@ -314,3 +314,52 @@ def test_ddp_host_handle_checks(abi):
     assert call(h, staging, n=0) == abi.ZERO_OK              # nothing to do
     assert abi.raw_call("zero_ddp_host_free", h) == abi.ZERO_OK
     assert abi.raw_call("zero_ddp_host_free", None) == abi.ZERO_OK
+
+
+def test_injected_host_allocation_failures(abi):
+    """A handle allocation that fails (injected, as if the host allocator
+    returned NULL) reports ZERO_ENOMEM with a message, leaves the output NULL
+    and queues nothing; the injection counts down, can be cleared, and stays
+    in the thread that set it."""
+    import threading
+    vp = ctypes.c_void_p
+
+    def init_states():
+        h = vp(12345)
+        rc = abi.raw_call("zero_init_states", 0, 2, abi.ZERO_FP32, None, None, None, None, None,
+                          ctypes.byref(h))
+        return rc, h
+
+    def ddp_handle():
+        h = vp(12345)
+        return abi.raw_call("zero_ddp_host_create", ctypes.byref(h)), h
+
+    abi.zero_debug_fail_host_allocs(2)
+    rc, h = init_states()
+    assert rc == abi.ZERO_ENOMEM and h.value is None
+    assert "state handle" in abi.zero_last_error()
+    rc, h = ddp_handle()
+    assert rc == abi.ZERO_ENOMEM and h.value is None
+    assert "DDP host-input handle" in abi.zero_last_error()
+    rc, h = init_states()                      # the injection is used up
+    assert rc == abi.ZERO_OK and h.value
+    assert abi.raw_call("zero_free_states", h) == abi.ZERO_OK
+    abi.zero_debug_fail_host_allocs(3)
+    abi.zero_debug_fail_host_allocs(0)         # cleared
+    rc, h = ddp_handle()
+    assert rc == abi.ZERO_OK and h.value
+    assert abi.raw_call("zero_ddp_host_free", h) == abi.ZERO_OK
+    # another thread's injection leaves this thread's allocations alone
+    seen = {}
+    t = threading.Thread(target=lambda: (abi.zero_debug_fail_host_allocs(1),
+                                         seen.update(other=init_states()[0])))
+    t.start()
+    t.join()
+    assert seen["other"] == abi.ZERO_ENOMEM
+    rc, h = init_states()
+    assert rc == abi.ZERO_OK
+    assert abi.raw_call("zero_free_states", h) == abi.ZERO_OK
+    with pytest.raises(abi.ZeroError) as e:    # through the binding's handle class
+        abi.zero_debug_fail_host_allocs(1)
+        abi.DdpHost()
+    assert e.value.code == abi.ZERO_ENOMEM

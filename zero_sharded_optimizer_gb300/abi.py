@@ -76,6 +76,7 @@ _SIGNATURES = {
     "ddp_allreduce_mean_from_host": (ctypes.c_int, [_P(_vp), _P(_vp), _i64, _i32, _i32, _vp,
                                                     _i64, _vp, _vp, _vp]),
     "zero_ddp_host_create": (ctypes.c_int, [_P(_vp)]),
+    "zero_debug_fail_host_allocs": (ctypes.c_int, [_i32]),
     "zero_ddp_host_reset": (ctypes.c_int, [_vp]),
     "zero_ddp_host_free": (ctypes.c_int, [_vp]),
     "ddp_allreduce_mean_from_host_h": (ctypes.c_int, [_vp, _P(_vp), _P(_vp), _i64, _i32, _i32,
@@ -562,6 +563,12 @@ class DdpHost:
 def zero_last_error() -> str:
     """The calling thread's most recent error message from the library."""
     return _lib.zero_last_error().decode(errors="replace")
+
+
+def zero_debug_fail_host_allocs(count: int) -> None:
+    """Failure injection: the calling thread's next ``count`` handle
+    allocations fail with ZERO_ENOMEM (count <= 0 clears it)."""
+    _check(_lib.zero_debug_fail_host_allocs(count), "zero_debug_fail_host_allocs")
 
 
 def raw_call(name: str, *args) -> int:

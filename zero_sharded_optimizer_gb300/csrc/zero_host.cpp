@@ -45,6 +45,20 @@ namespace {
 
 thread_local char g_last_error[512] = "";
 
+// Handle allocations of this thread still to fail (zero_debug_fail_host_allocs).
+thread_local int32_t g_failing_allocs = 0;
+
+// A handle from the host allocator, or NULL when it fails (or an injected
+// failure is pending for this thread).
+template <typename T>
+T* new_handle() {
+  if (g_failing_allocs > 0) {
+    --g_failing_allocs;
+    return nullptr;
+  }
+  return new (std::nothrow) T;
+}
+
 int fail(int code, const char* fmt, ...) {
   va_list ap;
   va_start(ap, fmt);
@@ -327,6 +341,11 @@ const char* zero_strerror(int code) {
 
 const char* zero_last_error(void) { return g_last_error; }
 
+int zero_debug_fail_host_allocs(int32_t count) {
+  g_failing_allocs = count > 0 ? count : 0;
+  return ZERO_OK;
+}
+
 int zero_shard_bounds(int64_t n, int32_t N, int64_t* bounds) {
   if (n < 0) return fail(ZERO_EINVAL, "n=%lld must be >= 0", (long long)n);
   if (N < 1) return fail(ZERO_EINVAL, "N=%d must be >= 1", N);
@@ -561,7 +580,7 @@ int zero_init_states_ex(int64_t n, int32_t N, int32_t precision, float* m, float
     if (n > 0) rs.push_back({uintptr_t(bufs[k]), uintptr_t(bufs[k]) + uintptr_t(n) * 4, "a state buffer"});
   }
   if (int e = check_disjoint(rs)) return e;
-  zero_states* st = new (std::nothrow) zero_states;
+  zero_states* st = new_handle<zero_states>();
   if (!st) return fail(ZERO_ENOMEM, "cannot allocate the state handle");
   st->n = n;
   st->N = N;
@@ -1189,7 +1208,7 @@ int ddp_allreduce_mean_from_host(const void* const* host_grads, void* const* sta
 
 int zero_ddp_host_create(zero_ddp_host_t** out) {
   if (!out) return fail(ZERO_EINVAL, "out is NULL");
-  *out = new (std::nothrow) zero_ddp_host;
+  *out = new_handle<zero_ddp_host>();
   if (!*out) return fail(ZERO_ENOMEM, "cannot allocate the DDP host-input handle");
   return ZERO_OK;
 }
