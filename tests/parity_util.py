@@ -55,6 +55,23 @@ def exact_fraction(got, ref):
                          ref.view(np.uint32 if ref.dtype == np.float32 else ref.dtype)))
 
 
+def assert_same_bits_or_both_nan(got, ref, what=""):
+    """Bitwise equal, except that a NaN matches any NaN (the GPU returns one
+    canonical NaN where numpy keeps an operand's payload). float32 arrays, or
+    bf16 bits as uint16."""
+    got, ref = np.asarray(got), np.asarray(ref)
+    assert got.shape == ref.shape, what
+    if got.dtype == np.uint16:
+        gn, rn = (got & 0x7FFF) > 0x7F80, (ref & 0x7FFF) > 0x7F80
+        gb, rb = got, ref
+    else:
+        gn, rn = np.isnan(got), np.isnan(ref)
+        gb, rb = got.view(np.uint32), ref.view(np.uint32)
+    assert np.array_equal(gn, rn), f"{what}: NaN positions differ ({int((gn != rn).sum())})"
+    bad = np.flatnonzero(gb[~gn] != rb[~rn])
+    assert bad.size == 0, f"{what}: {bad.size} values differ"
+
+
 def flat(states, key):
     return np.concatenate([s[key] for s in states]) if states else np.zeros(0, np.float32)
 

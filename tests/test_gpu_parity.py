@@ -11,8 +11,9 @@ import pytest
 import torch
 
 import oracle
-from parity_util import (assert_bf16_within_one_ulp, assert_fp32_close, check_guards,
-                         exact_fraction, flat, guarded_empty)
+from parity_util import (assert_bf16_within_one_ulp, assert_fp32_close,
+                         assert_same_bits_or_both_nan, check_guards, exact_fraction, flat,
+                         guarded_empty)
 from zero_sharded_optimizer_gb300 import inputs
 
 pytestmark = pytest.mark.gpu
@@ -658,6 +659,97 @@ def test_zero_and_subnormal_state_bitwise(abi, cuda, prec):
         c.gpu_step()
         torch.cuda.synchronize()
         c.compare(exact=True)
+
+
+def _special_grads(rng, n, N, mixed, idx):
+    """Gradients N(0, 1e-3) with special values at the index sets of idx: a NaN
+    in one rank, +Inf, opposite infinities (a NaN sum), a rank sum that
+    overflows float32 (3e38 in every rank) and a square that overflows
+    (1e20: v becomes +Inf)."""
+    hs = []
+    for r in range(N):
+        g = rng.normal(0, 1e-3, n).astype(np.float32)
+        if r == 1:
+            g[idx[0]] = np.nan
+        if r == 0:
+            g[idx[1]] = np.inf
+        if r == 2:
+            g[idx[2]] = -np.inf
+        if r == 3:
+            g[idx[2]] = np.inf
+        g[idx[3]] = 3e38
+        g[idx[4]] = 1e20
+        hs.append(oracle.f32_to_bf16_rne(g) if mixed else g)
+    return hs
+
+
+@pytest.mark.parametrize("prec", [oracle.FP32, oracle.BF16_MIXED])
+def test_nan_and_inf_propagate_like_the_oracle(abi, cuda, prec):
+    """NaN and Inf propagate as IEEE arithmetic gives them, nothing skipped: two
+    steps with special gradients (and the NaN and infinite state they leave),
+    then the DDP mean of special gradients, and clipping with a NaN norm (the
+    coefficient min(1, NaN) stays 1) and with an infinite one (coefficient 0).
+    Every output equals the oracle bit for bit, NaN matching NaN."""
+    n, N = 100_003, 4
+    c = Case(abi, cuda, n, N, prec, seed=61)
+    rng = np.random.default_rng(62)
+    idx = rng.permutation(n)[:5 * 700].reshape(5, 700)
+
+    def compare(case):
+        check_guards()
+        for key, buf in [("m", case.m), ("v", case.v)] + ([("master", case.master)]
+                                                         if case.mixed else []):
+            assert_same_bits_or_both_nan(host_of(buf), flat(case.o_states, key), key)
+        for r in range(N):
+            want = oracle.f32_to_bf16_rne(flat(case.o_states, "master")) if case.mixed \
+                else case.o_reps[r]
+            assert_same_bits_or_both_nan(host_of(case.reps[r]), want, f"replica {r}")
+
+    for _ in range(2):
+        hs = _special_grads(rng, n, N, c.mixed, idx)
+        for r in range(N):
+            c.grads[r].copy_(host_tensor(hs[r], c.dt))
+        with np.errstate(all="ignore"):
+            c.oracle_step(hs)
+        c.gpu_step()
+        torch.cuda.synchronize()
+        compare(c)
+    m = host_of(c.m)
+    assert np.isnan(m[idx[0]]).all() and np.isinf(host_of(c.v)[idx[4]]).all()
+
+    # the DDP mean
+    hs = _special_grads(rng, n, N, c.mixed, idx)
+    dev = [to_dev(h, c.dt, cuda) for h in hs]
+    abi.ddp_allreduce_mean(dev, prec)
+    torch.cuda.synchronize()
+    with np.errstate(all="ignore"):
+        ref = oracle.allreduce_mean(hs, precision=prec, mode="fp32")
+    for r in range(N):
+        assert_same_bits_or_both_nan(host_of(dev[r]), ref[r], f"mean {r}")
+
+    # clipping: a NaN norm, then an infinite one (no NaN gradient)
+    count = abi.zero_grad_norm_scratch_count(n, prec)
+    scratch = torch.empty(count, dtype=torch.float64, device=cuda)
+    norm = torch.empty(1, dtype=torch.float64, device=cuda)
+    for with_nan in (True, False):
+        d = Case(abi, cuda, n, N, prec, seed=63)
+        hs = _special_grads(rng, n, N, d.mixed, idx)
+        if not with_nan:
+            nan_free = [np.where(np.isin(np.arange(n), idx[0]), 0, h).astype(h.dtype)
+                        for h in hs]
+            hs = [h.copy() for h in nan_free]
+            hs[2][idx[2]] = hs[3][idx[2]]       # +Inf + +Inf: no NaN sum either
+        for r in range(N):
+            d.grads[r].copy_(host_tensor(hs[r], d.dt))
+        d.t = 1
+        with np.errstate(all="ignore"):
+            d.o_reps, d.o_states = oracle.zero_step(d.o_reps, hs, d.o_states, 1, precision=prec,
+                                                    mode="fp32", max_grad_norm=1.0, **d.hp)
+        abi.zero_step_ex(d.reps, d.grads, d.st, 1, max_grad_norm=1.0, norm_sq=norm,
+                         norm_scratch=scratch, **d.hp)
+        torch.cuda.synchronize()
+        assert np.isnan(float(norm)) if with_nan else np.isinf(float(norm))
+        compare(d)
 
 
 @pytest.mark.parametrize("prec", [oracle.FP32, oracle.BF16_MIXED])

@@ -188,6 +188,49 @@ def test_fp64_matches_torch_adamw(N, wd, scale):
                                    atol=1e-13 * np.abs(rv).max())
 
 
+def test_special_values_match_torch_adamw():
+    """Reading: NaN and Inf propagate as IEEE arithmetic gives them, nothing is
+    skipped. One step from zero state against torch.optim.AdamW in float64 on the
+    same mean gradient, with a NaN in one rank, +Inf, opposite infinities (a NaN
+    sum), a rank sum that overflows and a square that overflows in v: the NaN
+    positions of p, m and v are the same and every other value agrees,
+    infinities included. Each special value stays at its own index: the other
+    indices equal the step with those gradients zeroed. (One step only: torch
+    forms m with lerp, m + w*(g - m), which turns an infinite m into NaN on the
+    next step where beta1*m + (1 - beta1)*g keeps it infinite.)"""
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(41)
+    n, N, lr, b1, b2, eps, wd = 64, 4, 1e-3, 0.9, 0.95, 1e-8, 0.1
+    p0 = rng.normal(0, 0.02, n)
+    grads = [rng.normal(0, 1e-3, n) for _ in range(N)]
+    grads[1][0:4] = np.nan
+    grads[0][4:8] = np.inf
+    grads[2][8:12], grads[3][8:12] = -np.inf, np.inf
+    for g in grads:
+        g[12:16] = 1.7e308   # the rank sum overflows to +Inf
+        g[16:20] = 1e160     # the mean is finite, its square overflows: v = +Inf
+    special = np.zeros(n, bool)
+    special[:20] = True
+    with np.errstate(all="ignore"):
+        (rp, rm, rv), = _torch_reference(p0, [grads], lr, b1, b2, eps, wd, dtype=torch.float64)
+        params, states = oracle.zero_step([p0.copy() for _ in range(N)], grads,
+                                          oracle.init_states(n, N, mode="fp64"), 1, lr=lr,
+                                          beta1=b1, beta2=b2, eps=eps, weight_decay=wd,
+                                          mode="fp64")
+    for got, want in [(params[0], rp), (flat_state(states, "m"), rm),
+                      (flat_state(states, "v"), rv)]:
+        assert np.array_equal(np.isnan(got), np.isnan(want))
+        ok = ~np.isnan(want)
+        np.testing.assert_allclose(got[ok], want[ok], rtol=1e-12, atol=1e-18)
+    assert np.all(np.isnan(params[0][:16])) and np.all(np.isfinite(params[0][16:]))
+    assert np.all(np.isinf(flat_state(states, "v")[16:20]))
+    zeroed = [np.where(special, 0.0, g) for g in grads]
+    clean, _ = oracle.zero_step([p0.copy() for _ in range(N)], zeroed,
+                                oracle.init_states(n, N, mode="fp64"), 1, lr=lr, beta1=b1,
+                                beta2=b2, eps=eps, weight_decay=wd, mode="fp64")
+    assert np.array_equal(params[0][~special], clean[0][~special])
+
+
 def test_fp32_mirror_close_to_torch_fp32_and_fp64():
     torch = pytest.importorskip("torch")
     rng = np.random.default_rng(11)
