@@ -12,8 +12,9 @@ import pytest
 import torch
 
 import oracle
-from parity_util import (assert_bf16_within_one_ulp, assert_fp32_close, check_guards,
-                         exact_fraction, flat, guarded_empty)
+from parity_util import (assert_bf16_within_one_ulp, assert_fp32_close,
+                         assert_same_bits_or_both_nan, check_guards, exact_fraction, flat,
+                         guarded_empty)
 from test_gpu_parity import host_of, host_tensor, to_dev
 
 pytestmark = pytest.mark.gpu
@@ -205,6 +206,46 @@ def test_sgd_clipped_and_scaled(abi, cuda, prec, N):
             c.master.copy_(torch.from_numpy(flat(c.o_states, "master")))
         for r in range(N):
             c.reps[r].copy_(host_tensor(c.o_reps[r], c.dt))
+
+
+@pytest.mark.parametrize("prec", [oracle.FP32, oracle.BF16_MIXED])
+@pytest.mark.parametrize("variant,N", [("damped_wd", 4), ("nesterov_wd", 4), ("momentum", 1),
+                                       ("plain_wd", 2)])
+def test_sgd_nan_and_inf_propagate_like_the_oracle(abi, cuda, prec, variant, N):
+    """Momentum SGD with special gradients (NaN in one rank, +Inf, opposite
+    infinities, a rank sum that overflows), two steps, one rank included (two
+    units per thread): every output equals the oracle bit for bit, NaN
+    matching NaN."""
+    n = 100_003
+    c = SgdCase(abi, cuda, n, N, prec, variant, seed=71)
+    rng = np.random.default_rng(72)
+    idx = rng.permutation(n)[:4 * 600].reshape(4, 600)
+    for _ in range(2):
+        hs = []
+        for r in range(N):
+            g = rng.normal(0, 1e-3, n).astype(np.float32)
+            g[idx[0]] = np.nan if r == N - 1 else g[idx[0]]
+            g[idx[1]] = np.inf if r == 0 else g[idx[1]]
+            if N > 1:
+                g[idx[2]] = -np.inf if r == 0 else (np.inf if r == 1 else g[idx[2]])
+            g[idx[3]] = 3e38
+            hs.append(oracle.f32_to_bf16_rne(g) if c.mixed else g)
+            c.grads[r].copy_(host_tensor(hs[-1], c.dt))
+        c.t += 1
+        with np.errstate(all="ignore"):
+            c.o_reps, c.o_states = oracle.zero_step_sgd(c.o_reps, hs, c.o_states, c.t,
+                                                        precision=prec, mode="fp32", **c.kw())
+        abi.zero_step_sgd(c.reps, c.grads, c.st, c.t, **c.kw())
+        torch.cuda.synchronize()
+        check_guards()
+        if c.mu:
+            assert_same_bits_or_both_nan(host_of(c.buf), flat(c.o_states, "buf"), "buffer")
+        if c.mixed:
+            assert_same_bits_or_both_nan(host_of(c.master), flat(c.o_states, "master"),
+                                         "master")
+        for r in range(N):
+            assert_same_bits_or_both_nan(host_of(c.reps[r]), c.o_reps[r], f"replica {r}")
+    assert np.isnan(host_of(c.master if c.mixed else c.reps[0])[idx[0]]).all()
 
 
 def test_sgd_range_partition_is_bitwise_full_step(abi, cuda):
