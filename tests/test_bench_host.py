@@ -138,6 +138,8 @@ def test_committed_traffic_records_cover_the_bench_workloads():
         e = rec[name]
         assert e["dram_bytes_per_launch"] == e["dram_bytes_read"] + e["dram_bytes_write"]
         assert os.path.exists(os.path.join(ROOT, e["summary"]))
+        # taken on the kernel code as committed: the bench line carries it
+        assert e["kernel_source_sha256_16"] == bench.kernel_source_hash(), name
 
 
 def test_poller_child_protocol(monkeypatch, capsys):
