@@ -822,12 +822,13 @@ def run_gpu(args, wl, rank: int, world: int, local_rank: int) -> dict | None:
     whole = clip or stage3  # the roofline covers the whole step (several kernels)
     per = 1 if whole else launches_per_step
     # the committed records cover the plain step of each workload (bucketed
-    # for the bucket-streamed one), the momentum-SGD step and the DDP mean
-    # ("<workload>/sgd", "<workload>/ddp_mean"); the clipped and stage-3 lines
-    # run several kernels per step and report none
-    variant = "ddp_mean" if ddp else ("sgd" if sgd else None)
-    key = wl.name if variant is None else f"{wl.name}/{variant}"
-    traffic = None if (clip or stage3) else traffic_per_launch(key, n / per)
+    # for the bucket-streamed one) and single variants of it: "<workload>/sgd",
+    # "/ddp_mean", and "/clip", "/stage3" (whole steps of several launches);
+    # combined variants have none
+    variants = [v for v, on in (("sgd", sgd), ("ddp_mean", ddp), ("clip", clip),
+                                ("stage3", stage3)) if on]
+    key = wl.name + ("/" + "+".join(variants) if variants else "")
+    traffic = traffic_per_launch(key, n / per)
     line = {
         "metric": METRIC_DDP if ddp else METRIC,
         "value": whole_job_rate(n, world, ms_step),

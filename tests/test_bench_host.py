@@ -133,8 +133,13 @@ def test_committed_traffic_records_cover_the_bench_workloads():
     from zero_sharded_optimizer_gb300 import inputs
     with open(bench.TRAFFIC_FILE) as f:
         rec = json.load(f)
-    for name in ("fp32_25m", "gpt2_small", "fp32_320m", "mixed_1p3b"):
-        assert name in inputs.WORKLOADS
+    names = ("fp32_25m", "gpt2_small", "fp32_320m", "mixed_1p3b", "fp32_25m/sgd",
+             "gpt2_small/sgd", "fp32_320m/sgd", "fp32_25m/ddp_mean", "gpt2_small/ddp_mean",
+             "fp32_25m/clip", "gpt2_small/clip", "fp32_320m/clip", "fp32_25m/stage3",
+             "gpt2_small/stage3")
+    assert sorted(rec) == sorted(names)
+    for name in names:
+        assert name.split("/")[0] in inputs.WORKLOADS
         e = rec[name]
         assert e["dram_bytes_per_launch"] == e["dram_bytes_read"] + e["dram_bytes_write"]
         assert os.path.exists(os.path.join(ROOT, e["summary"]))
